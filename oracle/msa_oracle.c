@@ -1,0 +1,246 @@
+/*
+ * CPU oracle for the MSA index-branch block score (test infrastructure only).
+ *
+ * This file is the plain, slow definition that the CUDA path is checked
+ * against.  Only the test suite, the smoke check and the benchmark's CPU
+ * baseline load it; the product library never links, includes or calls it,
+ * and it includes nothing from the product.
+ *
+ * Definition followed (the feature request "MsaIndexScore",
+ * gitcode.com/cann/ops-transformer/issues/4117, section "calculation"):
+ *
+ *   for token t of request b, head h, logical block beta:
+ *     score[h,t,beta] = max over j in [beta*P, beta*P+P), j <= q_pos(t),
+ *                       j < kv_len[b]  of  < q[t,h], k~[j, h/g] >
+ *   with k~ gathered from the paged cache through block_table (or the packed
+ *   TND keys), optionally int8-dequantised by scale[page, h_kv, j mod P]
+ *   applied to the dot product before the mask ("DOT -> DEQUANT -> MASK ->
+ *   MAX"), and fill_value (-inf) where no j is visible.
+ *
+ * Then the local mask of the torch API guide "CANN ops-transformer ...
+ * msa_index_score" (sec. 2): blocks [0, init_blocks) take 1e30, the window
+ * [max(0, start_loc+1-local_blocks), start_loc] takes 1e29 and overrides the
+ * init value.  Output is fp32 [H_q, T, RoundUp(MB, 16)] (same guide, sec. 5),
+ * padding columns hold the fill value.
+ *
+ * Readings taken where the pages are silent or disagree (each one is listed
+ * with its reason in the design notes of this repository):
+ *   - visibility uses rightDownCausal: q_pos = kv_len - Lq + i (sparse_mode 3);
+ *     sparse_mode 0 has no causal bound.  start_loc is a logical block index
+ *     used only by the local mask.
+ *   - the local mask is applied to every row of a request with kv_len > 0,
+ *     columns clipped to [0, MB); a request with kv_len == 0 is all fill.
+ *   - arithmetic: products and sums in fp64 (all inputs are exact in fp64),
+ *     int8 scale multiplied in fp64, one rounding to fp32 at the end.
+ *
+ * Element types: 0 = fp16, 1 = bf16, 2 = int8 (keys only).
+ * Layouts: 0 = BBND [NP,P,H_kv,D], 1 = BNBD [NP,H_kv,P,D], 2 = TND [T2,H_kv,D].
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+typedef struct {
+    const void *query;          /* [T, H_q, D] contiguous */
+    int32_t q_dtype;            /* 0 fp16, 1 bf16 */
+    int64_t T;
+    int32_t H_q, D;
+    const void *key;            /* layout below; dim0 stride = page_stride elements */
+    int32_t k_dtype;            /* 0 fp16, 1 bf16, 2 int8 */
+    int32_t layout;             /* 0 BBND, 1 BNBD, 2 TND */
+    int64_t NP;                 /* pages (paged) or T2 rows (TND) */
+    int32_t P, H_kv;
+    int64_t page_stride;        /* elements between consecutive dim0 entries */
+    const int32_t *block_table; /* [B, MB] (paged) */
+    int32_t B, MB;
+    const int32_t *cu_q;        /* [B+1] */
+    const int32_t *kv_len;      /* [B] (paged) */
+    const int32_t *cu_k;        /* [B+1] (TND) */
+    const int32_t *start_loc;   /* [B] */
+    const float *scale;         /* int8: paged [NP, H_kv, P]; TND [T2, H_kv] */
+    int32_t sparse_mode, init_blocks, local_blocks;
+    float fill_value;
+} msa_oracle_args;
+
+/* IEEE binary16 -> double, from the format's definition (1/5/10 bits). */
+static double half_to_double(uint16_t h)
+{
+    int s = (h >> 15) & 1, e = (h >> 10) & 0x1f, m = h & 0x3ff;
+    double v;
+    if (e == 0)
+        v = ldexp((double)m, -24);               /* subnormal: m * 2^-14 / 2^10 */
+    else if (e == 31)
+        v = m ? NAN : INFINITY;
+    else
+        v = ldexp((double)(m + 1024), e - 25);   /* (1 + m/2^10) * 2^(e-15) */
+    return s ? -v : v;
+}
+
+/* bfloat16 -> double: the upper half of an IEEE binary32. */
+static double bf16_to_double(uint16_t h)
+{
+    uint32_t u = (uint32_t)h << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+static double load_elem(const void *base, int32_t dtype, int64_t idx)
+{
+    if (dtype == 2)
+        return (double)((const int8_t *)base)[idx];
+    uint16_t bits = ((const uint16_t *)base)[idx];
+    return dtype == 1 ? bf16_to_double(bits) : half_to_double(bits);
+}
+
+/* Request that owns global token t: the b with cu_q[b] <= t < cu_q[b+1]. */
+static int request_of(const msa_oracle_args *a, int64_t t)
+{
+    for (int b = 0; b < a->B; ++b)
+        if (a->cu_q[b] <= t && t < a->cu_q[b + 1])
+            return b;
+    return -1;
+}
+
+/* Element offset of key row j (logical position in request b), head hk.
+ * Returns -1 if the row cannot be addressed (bad table entry). */
+static int64_t key_offset(const msa_oracle_args *a, int b, int64_t j, int hk,
+                          int64_t *scale_idx)
+{
+    if (a->layout == 2) {                                   /* TND */
+        int64_t row = (int64_t)a->cu_k[b] + j;
+        if (row < 0 || row >= a->NP)
+            return -1;
+        *scale_idx = row * a->H_kv + hk;
+        return (row * a->H_kv + hk) * (int64_t)a->D;
+    }
+    int64_t beta = j / a->P, off = j % a->P;
+    int64_t page = a->block_table[(int64_t)b * a->MB + beta];
+    if (page < 0 || page >= a->NP)
+        return -1;
+    *scale_idx = (page * a->H_kv + hk) * (int64_t)a->P + off;
+    if (a->layout == 0)                                      /* BBND */
+        return page * a->page_stride + (off * a->H_kv + hk) * (int64_t)a->D;
+    return page * a->page_stride + ((int64_t)hk * a->P + off) * (int64_t)a->D;  /* BNBD */
+}
+
+/* One output row (h, t): MBp values. Returns 0, or 1 if a needed key row could
+ * not be addressed (the row is then left as computed from the rows that could). */
+static int oracle_row(const msa_oracle_args *a, int h, int64_t t, float *dst)
+{
+    const int64_t MBp = ((int64_t)a->MB + 15) / 16 * 16;
+    const int g = a->H_q / a->H_kv;
+    const int hk = h / g;
+    int bad = 0;
+    for (int64_t c = 0; c < MBp; ++c)
+        dst[c] = a->fill_value;
+    int b = request_of(a, t);
+    if (b < 0)
+        return 0;
+    const int64_t Lq = a->cu_q[b + 1] - a->cu_q[b];
+    const int64_t L = a->layout == 2 ? (int64_t)a->cu_k[b + 1] - a->cu_k[b]
+                                     : (int64_t)a->kv_len[b];
+    const int64_t i = t - a->cu_q[b];
+    const int64_t qpos = a->sparse_mode == 3 ? L - Lq + i : INT64_MAX;
+    const int64_t qrow = (t * a->H_q + h) * (int64_t)a->D;
+
+    for (int64_t beta = 0; beta < a->MB; ++beta) {
+        double best = 0.0;
+        int any = 0;
+        for (int64_t j = beta * a->P; j < beta * a->P + a->P; ++j) {
+            if (j >= L || j > qpos)
+                continue;                                    /* MASK */
+            int64_t sidx = 0;
+            int64_t koff = key_offset(a, b, j, hk, &sidx);
+            if (koff < 0) {
+                bad = 1;
+                continue;
+            }
+            double s = 0.0;                                  /* DOT */
+            for (int d = 0; d < a->D; ++d)
+                s += load_elem(a->query, a->q_dtype, qrow + d) *
+                     load_elem(a->key, a->k_dtype, koff + d);
+            if (a->k_dtype == 2)
+                s *= (double)a->scale[sidx];                 /* DEQUANT (column scale) */
+            if (!any || s > best)                            /* MAX */
+                best = s;
+            any = 1;
+        }
+        dst[beta] = any ? (float)best : a->fill_value;
+    }
+
+    /* local mask: forced scores for blocks the downstream top-k must keep */
+    if (L > 0 && (a->init_blocks > 0 || a->local_blocks > 0)) {
+        for (int64_t beta = 0; beta < a->init_blocks && beta < a->MB; ++beta)
+            dst[beta] = 1e30f;
+        const int64_t sl = a->start_loc[b];
+        int64_t lo = sl + 1 - a->local_blocks;
+        if (lo < 0)
+            lo = 0;
+        for (int64_t beta = lo; beta <= sl && beta < a->MB; ++beta)
+            dst[beta] = 1e29f;
+    }
+    return bad;
+}
+
+/*
+ * Compute the listed output rows.  rows[r] = h * T + t; out holds
+ * nrows x RoundUp(MB,16) floats.  nthreads <= 0 uses the OpenMP default.
+ * Returns the number of rows that met an unaddressable key row.
+ */
+int msa_oracle_rows(const msa_oracle_args *a, const int64_t *rows, int64_t nrows,
+                    float *out, int nthreads)
+{
+    const int64_t MBp = ((int64_t)a->MB + 15) / 16 * 16;
+    int nbad = 0;
+#ifdef _OPENMP
+    if (nthreads > 0)
+        omp_set_num_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 1) reduction(+ : nbad)
+#endif
+    for (int64_t r = 0; r < nrows; ++r) {
+        int h = (int)(rows[r] / a->T);
+        int64_t t = rows[r] % a->T;
+        nbad += oracle_row(a, h, t, out + r * MBp);
+    }
+    return nbad;
+}
+
+/* Full output [H_q, T, RoundUp(MB,16)]. */
+int msa_oracle_full(const msa_oracle_args *a, float *out, int nthreads)
+{
+    const int64_t MBp = ((int64_t)a->MB + 15) / 16 * 16;
+    const int64_t n = (int64_t)a->H_q * a->T;
+    int nbad = 0;
+#ifdef _OPENMP
+    if (nthreads > 0)
+        omp_set_num_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 1) reduction(+ : nbad)
+#endif
+    for (int64_t r = 0; r < n; ++r)
+        nbad += oracle_row(a, (int)(r / a->T), r % a->T, out + r * MBp);
+    return nbad;
+}
+
+/* Threads an OpenMP region would use with the given request (for reports). */
+int msa_oracle_threads(int nthreads)
+{
+#ifdef _OPENMP
+    int n = 0;
+    if (nthreads > 0)
+        omp_set_num_threads(nthreads);
+#pragma omp parallel
+    {
+#pragma omp single
+        n = omp_get_num_threads();
+    }
+    return n;
+#else
+    (void)nthreads;
+    return 1;
+#endif
+}
