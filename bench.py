@@ -1,0 +1,445 @@
+"""Benchmark of the MSA index-branch block score on GB300.
+
+One step = one full call of the op (plan kernel + persistent tensor-core score
+kernel) over one resident batch of synthetic inputs.  Default workload: the
+batched decode case (B=64 single-token requests, H_q=16, H_kv=1, D=P=128,
+kv_len uniform in [1024, 65536], BBND bf16 paged cache, 545 MB of keys).
+
+Prints ONE JSON line (rank 0).  ``value`` is microseconds per call for the
+whole job (lower is better); the line also carries TFLOP/s, K-cache GB/s, the
+roofline of the dominant kernel, the CPU oracle timed on the host cores, an
+end-to-end figure through the C ABI with host buffers, and the SM clocks seen
+during the timed region.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 1..5]
+    python bench.py --impl reference ...   # the CPU oracle as the reference arm
+
+Multi-GPU: the op does not shard across GPUs in a way that needs an
+exchange; N>1 runs N independent replicas (one process per GPU under
+torchrun), times them between barriers and takes the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import synth  # noqa: E402
+
+METRIC = "MsaIndexScore µs/call, TFLOP/s and K-cache GB/s vs GB300 roofline (1 GPU)"
+DEFAULT_WORKLOAD = 2
+DTYPE_NAME = {torch.float16: "f16", torch.bfloat16: "bf16", torch.int8: "i8"}
+
+
+# ----------------------------------------------------------------------------
+# algorithmic work of a case (what the op must do, not what the tiles do)
+# ----------------------------------------------------------------------------
+def algorithmic_work(case):
+    """FLOPs = 2*D*sum over (h,t) of visible keys; bytes = visible K once per kv head
+    (+ int8 scale) + Q + the fp32 output + the table entries read."""
+    D, P = case.D, case.P
+    es_k = 1 if case.key.dtype == torch.int8 else 2
+    vis_rows = 0
+    k_tokens = 0
+    tab = 0
+    for Lq, L in zip(case.q_lens, case.kv_lens):
+        if Lq == 0:
+            continue
+        if case.sparse_mode == 3:
+            # row i sees min(L, L - Lq + i + 1) keys (none if negative)
+            for i in range(Lq):
+                vis_rows += max(0, min(L, L - Lq + i + 1))
+        else:
+            vis_rows += Lq * L
+        k_tokens += L
+        tab += -(-L // P)
+    flops = 2.0 * D * case.H_q * vis_rows
+    k_bytes = k_tokens * case.H_kv * D * es_k
+    if case.key.dtype == torch.int8:
+        k_bytes += k_tokens * case.H_kv * 4
+    q_bytes = case.T * case.H_q * D * 2
+    out_bytes = case.H_q * case.T * case.MBp * 4
+    total = k_bytes + q_bytes + out_bytes + 4 * tab
+    return {"flops": flops, "k_bytes": k_bytes, "q_bytes": q_bytes, "out_bytes": out_bytes,
+            "bytes": total}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        return {"hbm_gbs": float(pk["hbm_gbs"]), "bf16_tflops": float(pk["bf16_tflops"]),
+                "bf16_tflops_sustained": float(pk.get("bf16_tflops_sustained",
+                                                      pk["bf16_tflops"])),
+                "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                "source": "fallback"}
+
+
+# ----------------------------------------------------------------------------
+# clocks during the timed region
+# ----------------------------------------------------------------------------
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.rows = []
+        self.proc = None
+        self.t_start = self.t_stop = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self._th = threading.Thread(target=self._reader, daemon=True)
+        self._th.start()
+
+    def _reader(self):
+        for line in self.proc.stdout:
+            self.rows.append((time.time(), line.strip()))
+
+    def mark(self, which):
+        if which == "start":
+            self.t_start = time.time()
+        else:
+            self.t_stop = time.time()
+
+    def stop(self):
+        if self.proc is None:
+            return
+        time.sleep(0.12)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self._th.join(timeout=2)
+
+    def summary(self):
+        if not self.rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"]}
+        inside = [r for t, r in self.rows
+                  if self.t_start is not None and self.t_start - 0.05 <= t <= self.t_stop + 0.05]
+        use = inside if inside else [r for _, r in self.rows]
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in use:
+            f = [x.strip() for x in r.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons),
+                "samples": len(use), "samples_in_timed_region": len(inside)}
+
+
+# ----------------------------------------------------------------------------
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def max_over_ranks(x: float, ws: int, device) -> float:
+    if ws == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(ws: int):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def cpu_oracle_baseline(case, target_s: float = 12.0):
+    """Time the CPU oracle (as it stands) on a bounded row sample; scale to one call."""
+    import oracle
+    rows_total = case.H_q * case.T
+    threads = oracle.oracle_threads()
+    # probe a small sample, then size the sample for ~target_s of CPU work
+    probe = list(range(0, rows_total, max(1, rows_total // 64)))
+    t0 = time.perf_counter()
+    oracle.oracle_rows(case, probe)
+    dt = max(time.perf_counter() - t0, 1e-4)
+    per_row = dt / len(probe)
+    n = int(min(rows_total, max(len(probe), target_s / per_row)))
+    step = max(1, rows_total // n)
+    rows = list(range(0, rows_total, step))
+    t0 = time.perf_counter()
+    oracle.oracle_rows(case, rows)
+    dt = time.perf_counter() - t0
+    us_per_call = dt / len(rows) * rows_total * 1e6
+    frac = len(rows) / rows_total
+    sample = ("full workload" if len(rows) == rows_total else
+              f"{len(rows)} of {rows_total} (h,t) output rows, every {step}th, scaled by row count")
+    return {"value": us_per_call, "unit": "us/call", "cores": threads, "kind": "oracle",
+            "sample": sample, "sample_fraction": frac, "seconds": dt}
+
+
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    case = synth.config(args.workload)
+    work = algorithmic_work(case)
+    import oracle
+    rows_total = case.H_q * case.T
+    # each step: a bounded, fixed row sample (about a second of CPU work)
+    probe = list(range(0, rows_total, max(1, rows_total // 64)))
+    t0 = time.perf_counter()
+    oracle.oracle_rows(case, probe)
+    per_row = max(time.perf_counter() - t0, 1e-4) / len(probe)
+    n = int(min(rows_total, max(len(probe), 1.0 / per_row)))
+    step = max(1, rows_total // n)
+    rows = list(range(0, rows_total, step))
+    for _ in range(args.warmup):
+        oracle.oracle_rows(case, rows)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle.oracle_rows(case, rows)
+        times.append(time.perf_counter() - t0)
+    per_call_s = statistics.mean(times) / len(rows) * rows_total
+    us = per_call_s * 1e6
+    threads = oracle.oracle_threads()
+    sample = (f"{len(rows)} of {rows_total} (h,t) output rows per step, every {step}th, "
+              "scaled by row count")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": us, "unit": "us/call",
+        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": statistics.mean(times) * 1e3, "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": config_block(case, args.workload),
+        "tflops": work["flops"] / per_call_s / 1e12,
+        "k_cache_gbs": work["k_bytes"] / per_call_s / 1e9,
+        "cpu_baseline": {"value": us, "unit": "us/call", "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": us, "unit": "us/call", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def config_block(case, workload):
+    kb = algorithmic_work(case)["k_bytes"]
+    return {"workload": f"cfg{workload}:{case.name}", "B": case.B, "T": case.T,
+            "H_q": case.H_q, "H_kv": case.H_kv, "D": case.D, "P": case.P, "MB": case.MB,
+            "layout": case.layout, "k_dtype": DTYPE_NAME[case.key.dtype],
+            "sparse_mode": case.sparse_mode, "init_blocks": case.init_blocks,
+            "local_blocks": case.local_blocks,
+            "l2": (f"inputs larger than L2: K cache {kb / 1e6:.0f} MB > 129 MB"
+                   if kb > 129e6 else "inputs fit in L2 (no flush; latency-bound case)")}
+
+
+def run_ours(args):
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    import block_score_gb300 as bs
+    bs.load_library()
+
+    case = synth.config(args.workload)
+    work = algorithmic_work(case)
+    peaks = load_peaks()
+    prep = bs.from_case(case, device)
+    stream = torch.cuda.current_stream(device)
+
+    # correctness gate before timing (the parity tests are the full check)
+    prep()
+    if prep.device_error(stream):
+        raise RuntimeError("device error during the first call")
+
+    for _ in range(args.warmup):
+        prep(stream)
+    torch.cuda.synchronize(device)
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    # per-launch timing of the dominant kernel: events around the run half
+    ev_k = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for _ in range(args.steps)]
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(ws)
+    torch.cuda.synchronize(device)
+    sampler.mark("start")
+    ev0.record(stream)
+    for i in range(args.steps):
+        prep.plan(stream)
+        ev_k[i][0].record(stream)
+        prep.run(stream)
+        ev_k[i][1].record(stream)
+    ev1.record(stream)
+    torch.cuda.synchronize(device)
+    sampler.mark("stop")
+    barrier(ws)
+    sampler.stop()
+    total_ms = ev0.elapsed_time(ev1)
+    kern_ms = statistics.mean(a.elapsed_time(b) for a, b in ev_k)
+    step_ms = max_over_ranks(total_ms / args.steps, ws, device)
+    kern_ms = max_over_ranks(kern_ms, ws, device)
+    if prep.device_error(stream):
+        raise RuntimeError("device error during the timed region")
+
+    # end to end through the C ABI with host buffers: H2D of the inputs, the
+    # call, D2H of the scores, every step
+    e2e = e2e_run(case, device, stream, args)
+
+    us_per_call = step_ms * 1e3 / ws
+    call_s = step_ms / 1e3
+    kern_s = kern_ms / 1e3
+    tflops = work["flops"] / call_s / 1e12
+    kgbs = work["k_bytes"] / call_s / 1e9
+    hbm_gbs_kernel = work["bytes"] / kern_s / 1e9
+    tflops_kernel = work["flops"] / kern_s / 1e12
+    dominant_bound = "hbm" if work["bytes"] / (peaks["hbm_gbs"] * 1e9) >= \
+        work["flops"] / (peaks["bf16_tflops"] * 1e12) else "tensor"
+    if dominant_bound == "hbm":
+        roof = {"bound": "hbm", "achieved": hbm_gbs_kernel, "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": hbm_gbs_kernel / peaks["hbm_gbs"],
+                "traffic": args.traffic, "peak_source": peaks["source"] + " hbm_gbs"}
+    else:
+        pk = peaks["bf16_tflops"]
+        roof = {"bound": "tensor", "achieved": tflops_kernel, "peak": pk, "unit": "TFLOP/s",
+                "frac": tflops_kernel / pk, "traffic": args.traffic,
+                "peak_source": peaks["source"] + " bf16_tflops (burst)"}
+    roof["kernel"] = "score_kernel"
+    roof["kernel_us"] = kern_ms * 1e3
+    roof["algorithmic_bytes"] = work["bytes"]
+    roof["algorithmic_flops"] = work["flops"]
+
+    line = {
+        "metric": METRIC, "value": us_per_call, "unit": "us/call", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
+        "dtype": DTYPE_NAME[case.query.dtype] if case.key.dtype != torch.int8 else "f16xi8",
+        "data": "synthetic (seeded; shapes and length mix of the workload recipe)",
+        "config": config_block(case, args.workload),
+        "tflops": tflops, "k_cache_gbs": kgbs,
+        "frac_hbm": (work["bytes"] / call_s / 1e9) / peaks["hbm_gbs"],
+        "frac_tensor": tflops / peaks["bf16_tflops"],
+        "roofline": roof,
+        "e2e": e2e,
+        "gpu_launches": 2 * args.steps,
+        "clocks": sampler.summary(),
+    }
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_oracle_baseline(case)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def e2e_run(case, device, stream, args):
+    """Same metric through the public call with pinned host inputs."""
+    import block_score_gb300 as bs
+    host = {}
+    for name in ("query", "block_table", "cu_seqlens_q", "kv_len", "cu_seqlens_k",
+                 "start_loc", "scale"):
+        t = getattr(case, name)
+        host[name] = None if t is None else t.contiguous().pin_memory()
+    key = case.key
+    base = key
+    while base._base is not None:
+        base = base._base
+    host_key_base = base.contiguous().pin_memory()
+    dev = {k: (None if v is None else torch.empty_like(v, device=device)) for k, v in host.items()}
+    key_base_dev = torch.empty_like(host_key_base, device=device)
+    key_dev = torch.as_strided(key_base_dev, key.shape, key.stride(), key.storage_offset())
+    klen = dev["cu_seqlens_k"] if case.layout == "TND" else dev["kv_len"]
+    prep = bs.Prepared(dev["query"], key_dev, dev["start_loc"], block_table=dev["block_table"],
+                       scale=dev["scale"], actual_seq_qlen=dev["cu_seqlens_q"],
+                       actual_seq_klen=klen, layout_key=case.layout,
+                       sparse_mode=case.sparse_mode, init_blocks=case.init_blocks,
+                       local_blocks=case.local_blocks,
+                       max_blocks=case.MB if case.layout == "TND" else None)
+    out_host = torch.empty(prep.shape, dtype=torch.float32).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in host.values() if v is not None)
+    h2d += host_key_base.numel() * host_key_base.element_size()
+    d2h = out_host.numel() * 4
+
+    def step():
+        for k, v in host.items():
+            if v is not None:
+                dev[k].copy_(v, non_blocking=True)
+        key_base_dev.copy_(host_key_base, non_blocking=True)
+        prep(stream)
+        out_host.copy_(prep.out, non_blocking=True)
+
+    steps = max(1, min(args.steps, 20))
+    for _ in range(min(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize(device)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize(device)
+    ms = e0.elapsed_time(e1) / steps
+    return {"value": ms * 1e3, "unit": "us/call", "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(d2h), "steps": steps}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", type=int, default=DEFAULT_WORKLOAD, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--traffic", type=float, default=None,
+                    help="DRAM bytes per launch of the score kernel from an ncu capture")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

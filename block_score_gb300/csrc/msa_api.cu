@@ -1,0 +1,308 @@
+// C ABI of the block-score library: argument validation (the op's rules from
+// the torch API guide "CANN ops-transformer ... msa_index_score", sec. 3, 4,
+// 8.1 and 10), output shape (sec. 5 / 8.5), workspace sizing, TMA tensor maps
+// and the two launches (plan, score).  No device memory is allocated here.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/msa_index_score.h"
+#include "msa_common.cuh"
+
+namespace {
+
+thread_local char g_msg[512] = "";
+
+msa_status_t fail(msa_status_t st, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_msg, sizeof g_msg, fmt, ap);
+  va_end(ap);
+  return st;
+}
+
+msa_status_t cuda_fail(cudaError_t e, const char* what) {
+  return fail(MSA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int64_t round16(int64_t x) { return (x + 15) / 16 * 16; }
+
+int elem_size(msa_dtype_t t) { return t == MSA_I8 ? 1 : 2; }
+
+// Host-side checks; everything that can be judged without reading device memory.
+msa_status_t validate(const msa_index_score_args* a) {
+  if (!a) return fail(MSA_ERR_INVALID_ARG, "args is NULL");
+  if (a->layout != MSA_LAYOUT_BBND && a->layout != MSA_LAYOUT_BNBD && a->layout != MSA_LAYOUT_TND)
+    return fail(MSA_ERR_INVALID_ARG, "layout must be BBND, BNBD or TND");
+  if (a->sparse_mode != 0 && a->sparse_mode != 3)
+    return fail(MSA_ERR_INVALID_ARG, "sparse_mode must be 0 or 3");
+  if (a->q_dtype != MSA_F16 && a->q_dtype != MSA_BF16)
+    return fail(MSA_ERR_INVALID_ARG, "query dtype must be fp16 or bf16");
+  if (a->k_dtype == MSA_I8) {
+    if (a->q_dtype != MSA_F16) return fail(MSA_ERR_INVALID_ARG, "int8 key requires an fp16 query");
+    if (!a->scale) return fail(MSA_ERR_INVALID_ARG, "int8 key requires scale");
+  } else if (a->k_dtype == MSA_F16 || a->k_dtype == MSA_BF16) {
+    if (a->k_dtype != a->q_dtype) return fail(MSA_ERR_INVALID_ARG, "key dtype must match query");
+    if (a->scale) return fail(MSA_ERR_INVALID_ARG, "scale is only allowed with int8 keys");
+  } else {
+    return fail(MSA_ERR_INVALID_ARG, "key dtype must be fp16, bf16 or int8");
+  }
+  if (a->T < 0 || a->B < 0) return fail(MSA_ERR_INVALID_ARG, "T and B must be >= 0");
+  if (a->B == 0 && a->T > 0) return fail(MSA_ERR_INVALID_ARG, "T > 0 needs at least one request");
+  if (a->H_q <= 0 || a->H_kv <= 0) return fail(MSA_ERR_INVALID_ARG, "head counts must be > 0");
+  if (a->H_q % a->H_kv != 0) return fail(MSA_ERR_INVALID_ARG, "H_q must be a multiple of H_kv");
+  if (a->D != msa::kD) return fail(MSA_ERR_UNSUPPORTED, "only D = 128 is built (got %d)", a->D);
+  if (a->P != msa::kP) return fail(MSA_ERR_UNSUPPORTED, "only block_size P = 128 is built (got %d)", a->P);
+  if (a->H_q / a->H_kv > 128)
+    return fail(MSA_ERR_UNSUPPORTED, "GQA group size H_q/H_kv > 128 is not built");
+  if (a->MB < 1) return fail(MSA_ERR_INVALID_ARG, "MB must be >= 1");
+  const int64_t mbp = round16(a->MB);
+  const int64_t cap = a->layout == MSA_LAYOUT_TND ? mbp : a->MB;
+  if (a->init_blocks < 0 || a->local_blocks < 0 || a->init_blocks > cap || a->local_blocks > cap)
+    return fail(MSA_ERR_INVALID_ARG, "init_blocks/local_blocks must be in [0, %lld]", (long long)cap);
+  if (a->T > 0x7fffffffLL - 1) return fail(MSA_ERR_UNSUPPORTED, "T too large");
+  if (a->NP < 1 || a->NP > 0x7fffffffLL - 1)
+    return fail(MSA_ERR_INVALID_ARG, "NP (pages or TND rows) must be in [1, 2^31-2]");
+  const int es = elem_size(a->k_dtype);
+  if (a->layout == MSA_LAYOUT_TND) {
+    if (a->block_table) return fail(MSA_ERR_INVALID_ARG, "TND takes no block_table");
+    if (!a->cu_seqlens_k || a->kv_len)
+      return fail(MSA_ERR_INVALID_ARG, "TND takes cu_seqlens_k [B+1] and no kv_len");
+    if (a->page_stride != (int64_t)a->H_kv * a->D)
+      return fail(MSA_ERR_INVALID_ARG, "TND key must be contiguous");
+  } else {
+    if (a->B > 0 && !a->block_table) return fail(MSA_ERR_INVALID_ARG, "paged layout needs block_table");
+    if (a->B > 0 && !a->kv_len) return fail(MSA_ERR_INVALID_ARG, "paged layout needs kv_len [B]");
+    if (a->cu_seqlens_k) return fail(MSA_ERR_INVALID_ARG, "cu_seqlens_k is for TND only");
+    if (a->page_stride < (int64_t)a->P * a->H_kv * a->D)
+      return fail(MSA_ERR_INVALID_ARG, "page_stride smaller than a compact page");
+    if ((a->page_stride * es) % 16 != 0)
+      return fail(MSA_ERR_UNSUPPORTED, "page stride must be a multiple of 16 bytes");
+  }
+  if (a->T > 0 && a->B > 0) {
+    if (!a->query || !a->key_cache || !a->cu_seqlens_q || !a->start_loc)
+      return fail(MSA_ERR_INVALID_ARG, "query, key_cache, cu_seqlens_q and start_loc are required");
+    if (!aligned(a->query, 16) || !aligned(a->key_cache, 16))
+      return fail(MSA_ERR_INVALID_ARG, "query and key_cache must be 16-byte aligned");
+    if (a->scale && !aligned(a->scale, 4)) return fail(MSA_ERR_INVALID_ARG, "scale must be 4-byte aligned");
+  }
+  return MSA_OK;
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+int sm_count(int dev) {
+  static int cache[64] = {};
+  if (dev >= 0 && dev < 64 && cache[dev] > 0) return cache[dev];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 1;
+  if (dev >= 0 && dev < 64) cache[dev] = n;
+  return n;
+}
+
+msa_status_t fill_params(const msa_index_score_args* a, float* out, void* ws, msa::Params& p) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  const int g = a->H_q / a->H_kv;
+  p.T = a->T;
+  p.NP = a->NP;
+  p.H_q = a->H_q;
+  p.H_kv = a->H_kv;
+  p.g = g;
+  p.np = msa::kTileRows / g;
+  p.B = a->B;
+  p.MB = a->MB;
+  p.MBp = (int32_t)round16(a->MB);
+  p.layout = (int32_t)a->layout;
+  p.sparse_mode = a->sparse_mode;
+  p.init_blocks = a->init_blocks;
+  p.local_blocks = a->local_blocks;
+  p.num_sms = sm_count(dev);
+  p.block_table = a->block_table;
+  p.cu_q = a->cu_seqlens_q;
+  p.kv_len = a->kv_len;
+  p.cu_k = a->cu_seqlens_k;
+  p.start_loc = a->start_loc;
+  p.scale = a->scale;
+  p.out = out;
+  p.ws = static_cast<uint8_t*>(ws);
+  p.wait_limit_ns = 4000000000ull;   // 4 s: far above any legitimate wait
+  return MSA_OK;
+}
+
+msa_status_t check_ws(const msa_index_score_args* a, void* ws, size_t bytes) {
+  if (!ws) return fail(MSA_ERR_WORKSPACE, "workspace is NULL");
+  if (!aligned(ws, 256)) return fail(MSA_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+  const size_t need = msa::workspace_bytes_for(a->B);
+  if (bytes < need)
+    return fail(MSA_ERR_WORKSPACE, "workspace needs %zu bytes, got %zu", need, bytes);
+  return MSA_OK;
+}
+
+msa_status_t make_maps(const msa_index_score_args* a, const msa::Params& p, CUtensorMap* tq,
+                       CUtensorMap* tk) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return fail(MSA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  const CUtensorMapDataType qdt =
+      a->q_dtype == MSA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  {
+    // query [T, H_q, D]: dims (D, H_q, T); a box is (64, g, np) = one GQA group x np positions
+    cuuint64_t dims[3] = {(cuuint64_t)a->D, (cuuint64_t)a->H_q, (cuuint64_t)a->T};
+    cuuint64_t strides[2] = {(cuuint64_t)a->D * 2, (cuuint64_t)a->H_q * a->D * 2};
+    cuuint32_t box[3] = {64, (cuuint32_t)p.g, (cuuint32_t)p.np};
+    cuuint32_t es[3] = {1, 1, 1};
+    CUresult r = enc(tq, qdt, 3, const_cast<void*>(a->query), dims, strides, box, es,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(MSA_ERR_CUDA, "query tensor map: CUresult %d", (int)r);
+  }
+  {
+    const bool i8 = a->k_dtype == MSA_I8;
+    const cuuint64_t esz = i8 ? 1 : 2;
+    const CUtensorMapDataType kdt = i8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : qdt;
+    cuuint64_t dims[4];
+    cuuint64_t strides[3];
+    cuuint32_t box[4];
+    const cuuint32_t bx = i8 ? 128 : 64;
+    if (a->layout == MSA_LAYOUT_BNBD) {         // [NP, H_kv, P, D]
+      dims[0] = a->D; dims[1] = a->P; dims[2] = a->H_kv; dims[3] = a->NP;
+      strides[0] = a->D * esz; strides[1] = (cuuint64_t)a->P * a->D * esz;
+      strides[2] = (cuuint64_t)a->page_stride * esz;
+      box[0] = bx; box[1] = 128; box[2] = 1; box[3] = 1;
+    } else if (a->layout == MSA_LAYOUT_BBND) {  // [NP, P, H_kv, D]
+      dims[0] = a->D; dims[1] = a->H_kv; dims[2] = a->P; dims[3] = a->NP;
+      strides[0] = a->D * esz; strides[1] = (cuuint64_t)a->H_kv * a->D * esz;
+      strides[2] = (cuuint64_t)a->page_stride * esz;
+      box[0] = bx; box[1] = 1; box[2] = 128; box[3] = 1;
+    } else {                                    // TND [T2, H_kv, D]
+      dims[0] = a->D; dims[1] = a->H_kv; dims[2] = a->NP; dims[3] = 1;
+      strides[0] = a->D * esz; strides[1] = (cuuint64_t)a->H_kv * a->D * esz;
+      strides[2] = (cuuint64_t)a->NP * a->H_kv * a->D * esz;
+      box[0] = bx; box[1] = 1; box[2] = 128; box[3] = 1;
+    }
+    cuuint32_t es[4] = {1, 1, 1, 1};
+    CUresult r = enc(tk, kdt, 4, const_cast<void*>(a->key_cache), dims, strides, box, es,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     i8 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(MSA_ERR_CUDA, "key tensor map: CUresult %d", (int)r);
+  }
+  return MSA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t msa_abi_version(void) { return MSA_ABI_VERSION; }
+
+msa_status_t msa_index_score_out_shape(const msa_index_score_args* args, int64_t shape[3]) {
+  msa_status_t st = validate(args);
+  if (st != MSA_OK) return st;
+  if (!shape) return fail(MSA_ERR_INVALID_ARG, "shape is NULL");
+  shape[0] = args->H_q;
+  shape[1] = args->T;
+  shape[2] = round16(args->MB);
+  return MSA_OK;
+}
+
+msa_status_t msa_index_score_workspace_size(const msa_index_score_args* args, size_t* bytes) {
+  msa_status_t st = validate(args);
+  if (st != MSA_OK) return st;
+  if (!bytes) return fail(MSA_ERR_INVALID_ARG, "bytes is NULL");
+  *bytes = msa::workspace_bytes_for(args->B);
+  return MSA_OK;
+}
+
+msa_status_t msa_index_score_plan(const msa_index_score_args* args, void* workspace,
+                                  size_t workspace_bytes, msa_stream_t stream) {
+  g_msg[0] = 0;
+  msa_status_t st = validate(args);
+  if (st != MSA_OK) return st;
+  if (args->T == 0 || args->B == 0) return MSA_OK;
+  if ((st = check_ws(args, workspace, workspace_bytes)) != MSA_OK) return st;
+  msa::Params p;
+  if ((st = fill_params(args, nullptr, workspace, p)) != MSA_OK) return st;
+  cudaError_t e = msa::launch_plan(p, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "plan kernel launch");
+  return MSA_OK;
+}
+
+msa_status_t msa_index_score_run(const msa_index_score_args* args, float* out, void* workspace,
+                                 size_t workspace_bytes, msa_stream_t stream) {
+  g_msg[0] = 0;
+  msa_status_t st = validate(args);
+  if (st != MSA_OK) return st;
+  if (args->T == 0 || args->B == 0) return MSA_OK;
+  if ((st = check_ws(args, workspace, workspace_bytes)) != MSA_OK) return st;
+  if (!out || !aligned(out, 16)) return fail(MSA_ERR_INVALID_ARG, "out must be a 16-byte aligned pointer");
+  msa::Params p;
+  if ((st = fill_params(args, out, workspace, p)) != MSA_OK) return st;
+  CUtensorMap tq, tk;
+  if ((st = make_maps(args, p, &tq, &tk)) != MSA_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = args->k_dtype == MSA_I8
+                      ? msa::launch_score_i8(&tq, &tk, p, s)
+                      : msa::launch_score_16(&tq, &tk, p, args->q_dtype == MSA_BF16, s);
+  if (e != cudaSuccess) return cuda_fail(e, "score kernel launch");
+  return MSA_OK;
+}
+
+msa_status_t msa_index_score(const msa_index_score_args* args, float* out, void* workspace,
+                             size_t workspace_bytes, msa_stream_t stream) {
+  msa_status_t st = msa_index_score_plan(args, workspace, workspace_bytes, stream);
+  if (st != MSA_OK) return st;
+  return msa_index_score_run(args, out, workspace, workspace_bytes, stream);
+}
+
+msa_status_t msa_get_device_error(const void* workspace, int32_t* bits, msa_stream_t stream) {
+  if (!workspace || !bits) return fail(MSA_ERR_INVALID_ARG, "workspace and bits are required");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  int32_t v = 0;
+  const auto* hdr = static_cast<const msa::PlanHeader*>(workspace);
+  cudaError_t e = cudaMemcpyAsync(&v, &hdr->err, sizeof v, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "reading the device error word");
+  *bits = v;
+  return MSA_OK;
+}
+
+const char* msa_status_string(msa_status_t st) {
+  switch (st) {
+    case MSA_OK: return "ok";
+    case MSA_ERR_INVALID_ARG: return "invalid argument";
+    case MSA_ERR_UNSUPPORTED: return "unsupported configuration";
+    case MSA_ERR_CUDA: return "CUDA error";
+    case MSA_ERR_DEVICE_DATA: return "bad device data";
+    case MSA_ERR_WORKSPACE: return "bad workspace";
+  }
+  return "unknown status";
+}
+
+const char* msa_last_error_message(void) { return g_msg; }
+
+}  // extern "C"

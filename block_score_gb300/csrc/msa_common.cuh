@@ -1,0 +1,94 @@
+// Internal definitions shared by the host launcher and the kernels of the
+// block-score library: workspace (plan) layout, kernel parameters, unit
+// descriptors.  Nothing here is part of the public ABI.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace msa {
+
+constexpr int kD = 128;          // head dim handled by this build
+constexpr int kP = 128;          // tokens per page (block_size)
+constexpr int kTileRows = 128;   // MMA rows per work unit: floor(128/g) positions x g heads
+
+constexpr int kErrCuQ = 0x01;
+constexpr int kErrKvLen = 0x02;
+constexpr int kErrCuK = 0x04;
+constexpr int kErrBlockTable = 0x08;
+constexpr int kErrTimeout = 0x10;
+
+// Workspace layout: [PlanHeader | ReqInfo x B | int32 unit_prefix x (B+1)].
+struct PlanHeader {
+  int32_t counter;    // next unit to hand out (atomic)
+  int32_t n_units;    // total work units
+  int32_t n_req;      // entries of ReqInfo in schedule order
+  int32_t chunk;      // blocks per KV chunk (multiple of 8)
+  int32_t err;        // device error bits
+  int32_t pad[11];
+};
+static_assert(sizeof(PlanHeader) == 64, "header is 64 bytes");
+
+// One request in schedule order.  Its units are H_kv x ntiles x nchunks,
+// numbered kv-head-major, then query tiles from the last (most blocks) to the
+// first, then KV chunks.
+struct ReqInfo {
+  int32_t b;         // original request index
+  int32_t t0;        // first global query token (cu_seqlens_q[b])
+  int32_t Lq;        // query tokens
+  int32_t L;         // visible KV length
+  int32_t ntiles;    // ceil(Lq / positions per tile)
+  int32_t nchunks;   // KV chunks per tile
+  int32_t kbase;     // TND: first key row of the request; else 0
+  int32_t sl;        // start_loc[b]
+};
+static_assert(sizeof(ReqInfo) == 32, "ReqInfo is 32 bytes");
+
+__host__ __device__ inline size_t workspace_bytes_for(int64_t B) {
+  size_t n = sizeof(PlanHeader) + sizeof(ReqInfo) * (size_t)B + sizeof(int32_t) * (size_t)(B + 1);
+  return (n + 255) / 256 * 256;
+}
+
+struct Params {
+  int64_t T;
+  int64_t NP;              // pages (paged) or T2 (TND)
+  int32_t H_q, H_kv, g, np;
+  int32_t B, MB, MBp;
+  int32_t layout;          // 0 BBND, 1 BNBD, 2 TND
+  int32_t sparse_mode, init_blocks, local_blocks;
+  int32_t num_sms;
+  const int32_t* block_table;
+  const int32_t* cu_q;
+  const int32_t* kv_len;
+  const int32_t* cu_k;
+  const int32_t* start_loc;
+  const float* scale;
+  float* out;
+  uint8_t* ws;
+  uint64_t wait_limit_ns;  // bound of every on-chip wait
+};
+
+// One work unit as handed from the scheduler thread to the other roles.
+struct UnitDesc {
+  int32_t live;      // 1 = unit, 0 = no more work
+  int32_t b, hk;     // request, kv head
+  int32_t t0;        // global token of the tile's first position
+  int32_t npos;      // valid positions in the tile
+  int32_t i0;        // position of the tile's first token inside its request
+  int32_t Lq, L;     // request query / KV lengths
+  int32_t c0, c1;    // output columns [c0, c1) this unit writes (multiples of 8)
+  int32_t b1;        // blocks [c0, b1) are computed; [b1, c1) are fill / forced
+  int32_t kbase;     // TND key row base
+  int32_t sl;        // start_loc of the request
+  int32_t pad[3];
+};
+static_assert(sizeof(UnitDesc) == 64, "UnitDesc is 64 bytes");
+
+// Host-side launchers (defined in the .cu files).
+cudaError_t launch_plan(const Params& p, cudaStream_t s);
+cudaError_t launch_score_16(const void* tmap_q, const void* tmap_k, const Params& p, bool bf16,
+                            cudaStream_t s);
+cudaError_t launch_score_i8(const void* tmap_q, const void* tmap_k, const Params& p,
+                            cudaStream_t s);
+
+}  // namespace msa

@@ -1,0 +1,210 @@
+// Plan kernel: one CTA turns the per-request arrays (cu_seqlens_q, kv_len or
+// cu_seqlens_k, start_loc) into the work plan the score kernel consumes.
+//
+// A work unit is (request, kv head, query tile, KV chunk).  A query tile packs
+// floor(128/g) consecutive query positions x the g heads of one GQA group into
+// the 128 MMA rows (the "query concatenation" of the MSA kernel notes, sec.
+// 5.9).  Blocks are independent maxima, so splitting the KV range of a tile
+// into chunks needs no combine step; chunks keep every SM busy on short-query
+// (decode) batches, in the spirit of the reference tiling's KV split for
+// "short M, long S" decode (torch API guide, sec. 8.3).
+//
+// The plan also validates the device arrays (guide sec. 4 rules) and records
+// violations in the error word instead of faulting.
+#include "msa_common.cuh"
+
+namespace msa {
+
+namespace {
+
+constexpr int kPlanThreads = 1024;
+
+__device__ __forceinline__ int cdiv(int a, int b) { return (a + b - 1) / b; }
+
+// Inclusive block scan of one value per thread (kPlanThreads threads).
+__device__ int block_incl_scan(int v, int* s_warp) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int n = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += n;
+  }
+  if (lane == 31) s_warp[warp] = v;
+  __syncthreads();
+  if (warp == 0) {
+    int w = s_warp[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int n = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += n;
+    }
+    s_warp[lane] = w;
+  }
+  __syncthreads();
+  if (warp > 0) v += s_warp[warp - 1];
+  __syncthreads();
+  return v;
+}
+
+struct ReqScratch {
+  int Lq, L, t0, kbase, ntiles, nbc_max;
+};
+
+__device__ ReqScratch read_request(const Params& p, int b, int& err) {
+  ReqScratch r;
+  const int64_t q0 = p.cu_q[b], q1 = p.cu_q[b + 1];
+  if ((b == 0 && q0 != 0) || q1 < q0 || q0 < 0 || q1 > p.T || (b == p.B - 1 && q1 != p.T))
+    err |= kErrCuQ;
+  int64_t lo = q0 < 0 ? 0 : (q0 > p.T ? p.T : q0);
+  int64_t hi = q1 < lo ? lo : (q1 > p.T ? p.T : q1);
+  r.t0 = (int)lo;
+  r.Lq = (int)(hi - lo);
+  int64_t L;
+  if (p.layout == 2) {
+    const int64_t k0 = p.cu_k[b], k1 = p.cu_k[b + 1];
+    if ((b == 0 && k0 != 0) || k1 < k0 || k0 < 0 || k1 > p.NP) err |= kErrCuK;
+    int64_t a = k0 < 0 ? 0 : (k0 > p.NP ? p.NP : k0);
+    int64_t e = k1 < a ? a : (k1 > p.NP ? p.NP : k1);
+    r.kbase = (int)a;
+    L = e - a;
+  } else {
+    L = p.kv_len[b];
+    r.kbase = 0;
+    if (L < 0) {
+      err |= kErrKvLen;
+      L = 0;
+    }
+  }
+  const int64_t nb = (L + kP - 1) / kP;
+  if (nb > p.MB) err |= kErrKvLen;
+  r.L = (int)(L > 0x7fffffff ? 0x7fffffff : L);
+  r.ntiles = cdiv(r.Lq, p.np);
+  // the last query row sees the most blocks: q_pos = L - 1 in both modes
+  r.nbc_max = L > 0 ? (int)(nb < p.MB ? nb : p.MB) : 0;
+  return r;
+}
+
+__global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const Params p) {
+  // Let the score kernel start its prologue (barrier init, TMEM allocation);
+  // it waits for this grid's completion before it reads the plan.
+  asm volatile("griddepcontrol.launch_dependents;");
+
+  __shared__ int s_warp[32];
+  __shared__ unsigned long long s_work;
+  __shared__ int s_err;
+  __shared__ int s_key[kPlanThreads];
+  __shared__ int s_idx[kPlanThreads];
+  __shared__ int s_tot;
+
+  PlanHeader* hdr = reinterpret_cast<PlanHeader*>(p.ws);
+  ReqInfo* req = reinterpret_cast<ReqInfo*>(p.ws + sizeof(PlanHeader));
+  int32_t* prefix = reinterpret_cast<int32_t*>(p.ws + sizeof(PlanHeader) + sizeof(ReqInfo) * p.B);
+  const int tid = threadIdx.x;
+
+  if (tid == 0) {
+    s_work = 0ull;
+    s_err = 0;
+  }
+  __syncthreads();
+
+  // pass 1: validation and total work (blocks x kv heads x tiles, upper bound)
+  int err = 0;
+  unsigned long long work = 0;
+  for (int b = tid; b < p.B; b += kPlanThreads) {
+    ReqScratch r = read_request(p, b, err);
+    work += (unsigned long long)p.H_kv * r.ntiles * r.nbc_max;
+  }
+  if (err) atomicOr(&s_err, err);
+  if (work) atomicAdd(&s_work, work);
+  __syncthreads();
+
+  // chunk size: about 8 units per SM on average, never below 8 blocks
+  unsigned long long target = (unsigned long long)p.num_sms * 8ull;
+  unsigned long long c = (s_work + target - 1) / target;
+  if (c < 8) c = 8;
+  c = (c + 7) / 8 * 8;
+  if (c > (unsigned long long)p.MBp) c = (unsigned long long)p.MBp;
+  const int chunk = (int)c;
+
+  const bool sorted = p.B <= kPlanThreads;
+  if (sorted) {
+    // longest-first order: key = cost of the request's largest unit
+    int key = -1;
+    if (tid < p.B) {
+      int e2 = 0;
+      ReqScratch r = read_request(p, tid, e2);
+      if (r.Lq > 0) key = r.nbc_max < chunk ? r.nbc_max : chunk;
+    }
+    s_key[tid] = key;
+    s_idx[tid] = tid;
+    __syncthreads();
+    // bitonic sort, descending key, ascending index on ties
+    for (int k = 2; k <= kPlanThreads; k <<= 1) {
+      for (int j = k >> 1; j > 0; j >>= 1) {
+        const int partner = tid ^ j;
+        if (partner > tid) {
+          const int ka = s_key[tid], kb = s_key[partner];
+          const int ia = s_idx[tid], ib = s_idx[partner];
+          // "a before b" in the final order
+          const bool a_first = (ka > kb) || (ka == kb && ia < ib);
+          const bool up = ((tid & k) == 0);
+          if (up ? !a_first : a_first) {
+            s_key[tid] = kb;
+            s_key[partner] = ka;
+            s_idx[tid] = ib;
+            s_idx[partner] = ia;
+          }
+        }
+        __syncthreads();
+      }
+    }
+  }
+
+  // pass 2: request records in schedule order and the unit prefix sum
+  int carry = 0;
+  for (int base = 0; base < p.B; base += kPlanThreads) {
+    const int slot = base + tid;
+    int units = 0;
+    if (slot < p.B) {
+      const int b = sorted ? s_idx[slot] : slot;
+      int e2 = 0;
+      ReqScratch r = read_request(p, b, e2);
+      int nchunks = r.nbc_max > 0 ? cdiv(r.nbc_max, chunk) : 1;
+      units = r.Lq > 0 ? p.H_kv * r.ntiles * nchunks : 0;
+      ReqInfo ri;
+      ri.b = b;
+      ri.t0 = r.t0;
+      ri.Lq = r.Lq;
+      ri.L = r.L;
+      ri.ntiles = r.ntiles;
+      ri.nchunks = nchunks;
+      ri.kbase = r.kbase;
+      ri.sl = p.start_loc[b];
+      req[slot] = ri;
+    }
+    const int incl = block_incl_scan(units, s_warp);
+    if (slot < p.B) prefix[slot + 1] = carry + incl;
+    // last thread's inclusive value is the chunk total
+    if (tid == kPlanThreads - 1) s_tot = incl;
+    __syncthreads();
+    carry += s_tot;
+    __syncthreads();
+  }
+  if (tid == 0) {
+    prefix[0] = 0;
+    hdr->counter = 0;
+    hdr->n_units = carry;
+    hdr->n_req = p.B;
+    hdr->chunk = chunk;
+    hdr->err = s_err;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_plan(const Params& p, cudaStream_t s) {
+  plan_kernel<<<1, kPlanThreads, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace msa

@@ -1,0 +1,38 @@
+// Score kernel instantiations for fp16 / bf16 keys (same type as the query).
+#include "msa_score.cuh"
+
+namespace msa {
+
+template <bool BF16>
+static cudaError_t launch16(const void* tq, const void* tk, const Params& p, cudaStream_t s) {
+  using L = SmemLayout<false>;
+  auto kern = score_kernel<false, BF16>;
+  static bool configured[64] = {};   // per device; setting it twice is harmless
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 64 || !configured[dev]) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::bytes);
+    if (e != cudaSuccess) return e;
+    if (dev < 64) configured[dev] = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)p.num_sms);
+  cfg.blockDim = dim3(ScoreCfg<false>::kThreads);
+  cfg.dynamicSmemBytes = L::bytes;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, *static_cast<const CUtensorMap*>(tq),
+                            *static_cast<const CUtensorMap*>(tk), p);
+}
+
+cudaError_t launch_score_16(const void* tq, const void* tk, const Params& p, bool bf16,
+                            cudaStream_t s) {
+  return bf16 ? launch16<true>(tq, tk, p, s) : launch16<false>(tq, tk, p, s);
+}
+
+}  // namespace msa

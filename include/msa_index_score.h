@@ -1,0 +1,165 @@
+/*
+ * msa_index_score -- MSA (MiniMax Sparse Attention) index-branch block score
+ * on NVIDIA GB300 (sm_103a).  C ABI.
+ *
+ * Operation (feature request "MsaIndexScore",
+ * gitcode.com/cann/ops-transformer/issues/4117, section "calculation"):
+ *
+ *   for token t of request b, head h, logical KV block beta:
+ *     score[h, t, beta] = max over visible j in [beta*P, beta*P + P) of
+ *                         < query[t, h, :], k~[j, h / g, :] >,   g = H_q / H_kv
+ *
+ *   k~ is read from the paged cache through block_table (BBND / BNBD) or from
+ *   the packed keys (TND).  int8 keys are dequantised by a per-(page, head,
+ *   token) fp32 scale applied to the dot product before the mask
+ *   (order DOT -> DEQUANT -> MASK -> MAX).  A key j is visible to token t
+ *   when j < kv_len[b] and, for sparse_mode 3 (rightDownCausal),
+ *   j <= kv_len[b] - Lq[b] + (t - cu_seqlens_q[b]).  sparse_mode 0 has no
+ *   causal bound.  A block with no visible key gets -inf.
+ *
+ *   Local mask (torch API guide "CANN ops-transformer ... msa_index_score",
+ *   sec. 2), applied after the max to every row of a request with
+ *   kv_len > 0: blocks [0, init_blocks) get 1e30f; blocks
+ *   [max(0, start_loc+1-local_blocks), start_loc] get 1e29f (overriding the
+ *   init value).  Both clipped to [0, MB).
+ *
+ *   Output (same guide, sec. 5): fp32 [H_q, T, RoundUp(MB, 16)], row-major.
+ *   Columns [MB, RoundUp(MB,16)) hold -inf.  Every element is written, so the
+ *   caller need not initialise it.
+ *
+ * All pointers in msa_index_score_args are DEVICE pointers owned by the
+ * caller, except where marked.  Calls are asynchronous on `stream`; the
+ * library never synchronises the host inside a compute call and never
+ * allocates device memory.  Scratch state lives in a caller-provided
+ * workspace (size from msa_index_score_workspace_size, two-phase like the
+ * reference op's aclnn interface).  Two calls that share a workspace must be
+ * ordered (same stream, or joined by events).
+ *
+ * Scope of this build: D == 128 and P == 128; g = H_q / H_kv <= 128.
+ */
+#ifndef MSA_INDEX_SCORE_H_
+#define MSA_INDEX_SCORE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MSA_ABI_VERSION 1
+
+/* Same object as cudaStream_t / CUstream (NULL = legacy default stream). */
+typedef struct CUstream_st *msa_stream_t;
+
+typedef enum {
+    MSA_OK = 0,
+    MSA_ERR_INVALID_ARG = 1,   /* argument violates the op's rules (layout, dtype, shapes) */
+    MSA_ERR_UNSUPPORTED = 2,   /* legal for the op, outside this build (D != 128, P != 128, g > 128) */
+    MSA_ERR_CUDA = 3,          /* a CUDA runtime/driver call failed; see msa_last_error_message() */
+    MSA_ERR_DEVICE_DATA = 4,   /* device-side data check failed; see msa_get_device_error() */
+    MSA_ERR_WORKSPACE = 5      /* workspace NULL, too small or misaligned */
+} msa_status_t;
+
+typedef enum { MSA_LAYOUT_BBND = 0, MSA_LAYOUT_BNBD = 1, MSA_LAYOUT_TND = 2 } msa_layout_t;
+typedef enum { MSA_F16 = 0, MSA_BF16 = 1, MSA_I8 = 2 } msa_dtype_t;
+
+/* Bits of the device error word (msa_get_device_error). */
+#define MSA_DEVERR_CU_Q        0x01  /* cu_seqlens_q[0] != 0, decreasing, or cu_seqlens_q[B] != T */
+#define MSA_DEVERR_KV_LEN      0x02  /* kv_len < 0, or ceil(kv_len/P) > MB */
+#define MSA_DEVERR_CU_K        0x04  /* TND: cu_seqlens_k[0] != 0, decreasing, or beyond T2 */
+#define MSA_DEVERR_BLOCK_TABLE 0x08  /* a block_table entry that is read lies outside [0, NP) */
+#define MSA_DEVERR_TIMEOUT     0x10  /* an on-chip pipeline wait ran past its limit (kernel returned early) */
+
+typedef struct {
+    /* query: [T, H_q, D] contiguous, fp16 or bf16 ("TND" query of the guide, sec. 4). */
+    const void *query;
+    msa_dtype_t q_dtype;
+    int64_t T;                  /* total query tokens = cu_seqlens_q[B] */
+    int32_t H_q;
+    int32_t D;                  /* head dim; 128 */
+
+    /* key cache (guide sec. 4, 6, 8.1):
+     *   BBND [NP, P, H_kv, D], BNBD [NP, H_kv, P, D]: dim0 may be strided
+     *        (page_stride elements, >= the compact page size, multiple of 16 bytes);
+     *        the inner three dims are compact.
+     *   TND  [T2, H_kv, D] contiguous; page_stride must equal H_kv*D.
+     * dtype: same as query, or int8 with fp16 query (then scale is required). */
+    const void *key_cache;
+    msa_dtype_t k_dtype;
+    msa_layout_t layout;
+    int64_t NP;                 /* number of pages (paged) or T2 key rows (TND) */
+    int32_t P;                  /* block_size = tokens per page; 128 */
+    int32_t H_kv;
+    int64_t page_stride;        /* elements between consecutive dim0 entries of key_cache */
+
+    /* block_table [B, MB] int32, logical block -> physical page (paged only; NULL for TND).
+     * Entries at or beyond ceil(kv_len/P) are never read.  For TND, MB is the
+     * caller's max over requests of ceil(kv_len/P), at least 1 (guide sec. 8.5). */
+    const int32_t *block_table;
+    int32_t B;
+    int32_t MB;
+
+    const int32_t *cu_seqlens_q;   /* [B+1] prefix sums of query lengths, cu[0] == 0 */
+    const int32_t *kv_len;         /* [B] visible KV length (paged); NULL for TND */
+    const int32_t *cu_seqlens_k;   /* [B+1] prefix sums of key lengths (TND); NULL for paged */
+    const int32_t *start_loc;      /* [B] logical block index of the current query (local mask only) */
+    const float *scale;            /* int8 only: paged [NP, H_kv, P], TND [T2, H_kv]; else NULL */
+
+    int32_t sparse_mode;           /* 0 = no causal mask, 3 = rightDownCausal (default 3) */
+    int32_t init_blocks;           /* default 0, <= MB */
+    int32_t local_blocks;          /* default 1, <= MB */
+} msa_index_score_args;
+
+/* Library ABI version (MSA_ABI_VERSION of the build). */
+int32_t msa_abi_version(void);
+
+/* Output shape {H_q, T, RoundUp(MB, 16)} (guide sec. 5, 8.5).  Host-only, validates args. */
+msa_status_t msa_index_score_out_shape(const msa_index_score_args *args, int64_t shape[3]);
+
+/* Bytes of device workspace one call needs (>= 256, grows with B).  Host-only. */
+msa_status_t msa_index_score_workspace_size(const msa_index_score_args *args, size_t *bytes);
+
+/*
+ * Compute the block scores into `out` (device, fp32 [H_q, T, RoundUp(MB,16)],
+ * 16-byte aligned).  `workspace` is device memory of at least
+ * msa_index_score_workspace_size() bytes, 256-byte aligned, owned by the
+ * caller; it need not be initialised.  Equivalent to msa_index_score_plan
+ * followed by msa_index_score_run on the same stream.
+ *
+ * Errors: argument problems return before anything is enqueued.  Bad values
+ * inside the device arrays (cu_seqlens, kv_len, block_table) are detected on
+ * the device, recorded in the workspace's error word and do not fault; read
+ * them with msa_get_device_error.  T == 0 or B == 0 enqueues nothing.
+ */
+msa_status_t msa_index_score(const msa_index_score_args *args, float *out, void *workspace,
+                             size_t workspace_bytes, msa_stream_t stream);
+
+/* First half of msa_index_score: one small kernel that validates the
+ * per-request arrays and writes the work plan (request order, unit counts,
+ * cleared work counter and error word) into `workspace`. */
+msa_status_t msa_index_score_plan(const msa_index_score_args *args, void *workspace,
+                                  size_t workspace_bytes, msa_stream_t stream);
+
+/* Second half: the persistent tensor-core kernel that consumes the plan in
+ * `workspace` and writes every element of `out`.  `args` must be the ones
+ * given to the plan call. */
+msa_status_t msa_index_score_run(const msa_index_score_args *args, float *out, void *workspace,
+                                 size_t workspace_bytes, msa_stream_t stream);
+
+/* Synchronise `stream` and read the device error word left in `workspace`
+ * by the last call (MSA_DEVERR_* bits; 0 = clean).  Returns MSA_OK, or
+ * MSA_ERR_CUDA if the copy fails. */
+msa_status_t msa_get_device_error(const void *workspace, int32_t *bits, msa_stream_t stream);
+
+/* Static description of a status code. */
+const char *msa_status_string(msa_status_t status);
+
+/* Detail of the last failing call on this host thread ("" if none). */
+const char *msa_last_error_message(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MSA_INDEX_SCORE_H_ */

@@ -1,0 +1,145 @@
+"""C-ABI library checks that need no GPU: it builds, loads, exports every
+declared entry point, and its host-side argument rules behave as documented."""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "msa_index_score.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from block_score_gb300 import _build
+    _build.build()
+    import block_score_gb300 as bs
+    return bs.load_library()
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*[A-Za-z_][\w \*]*?\b(msa_\w+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_entry_points():
+    names = _declared_functions()
+    for want in ("msa_index_score", "msa_index_score_plan", "msa_index_score_run",
+                 "msa_index_score_out_shape", "msa_index_score_workspace_size",
+                 "msa_get_device_error", "msa_status_string", "msa_last_error_message",
+                 "msa_abi_version"):
+        assert want in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_library_is_sm103a_only():
+    from block_score_gb300 import _build
+    assert "arch=compute_103a,code=sm_103a" in _build.ARCH
+
+
+def test_abi_version(lib):
+    assert lib.msa_abi_version() == 1
+
+
+def _args(**over):
+    import block_score_gb300 as bs
+    a = bs._Args()
+    base = dict(query=16, q_dtype=1, T=32, H_q=8, D=128, key_cache=16, k_dtype=1, layout=0, NP=8,
+                P=128, H_kv=1, page_stride=128 * 128, block_table=16, B=1, MB=2,
+                cu_seqlens_q=16, kv_len=16, cu_seqlens_k=None, start_loc=16, scale=None,
+                sparse_mode=3, init_blocks=0, local_blocks=1)
+    base.update(over)
+    for k, v in base.items():
+        setattr(a, k, v)
+    return a
+
+
+def _shape(lib, a):
+    shape = (ctypes.c_int64 * 3)()
+    st = lib.msa_index_score_out_shape(ctypes.byref(a), shape)
+    return st, tuple(shape)
+
+
+def test_out_shape_rounds_mb_to_16(lib):
+    st, shape = _shape(lib, _args(MB=2))
+    assert st == 0 and shape == (8, 32, 16)
+    st, shape = _shape(lib, _args(MB=1100))
+    assert st == 0 and shape == (8, 32, 1104)
+    st, shape = _shape(lib, _args(MB=257))
+    assert st == 0 and shape == (8, 32, 272)
+
+
+def test_workspace_size_grows_with_batch(lib):
+    n1, n2 = ctypes.c_size_t(), ctypes.c_size_t()
+    assert lib.msa_index_score_workspace_size(ctypes.byref(_args(B=1)), ctypes.byref(n1)) == 0
+    assert lib.msa_index_score_workspace_size(ctypes.byref(_args(B=5000)), ctypes.byref(n2)) == 0
+    assert n1.value >= 256 and n2.value > n1.value and n2.value % 256 == 0
+
+
+@pytest.mark.parametrize("over,status", [
+    (dict(layout=7), 1),                        # layout outside BBND/BNBD/TND
+    (dict(sparse_mode=1), 1),                   # modes 0 and 3 only
+    (dict(H_q=9, H_kv=2), 1),                   # H_q % H_kv
+    (dict(D=64), 2),                            # scope of this build
+    (dict(P=64, page_stride=64 * 128), 2),
+    (dict(k_dtype=2, q_dtype=1, scale=16), 1),  # int8 keys need an fp16 query
+    (dict(k_dtype=2, q_dtype=0, scale=None), 1),  # int8 keys need a scale
+    (dict(scale=16), 1),                        # scale only with int8 keys
+    (dict(k_dtype=0), 1),                       # key dtype must match query
+    (dict(init_blocks=3), 1),                   # init_blocks <= MB
+    (dict(local_blocks=-1), 1),
+    (dict(layout=2, block_table=16, kv_len=None, cu_seqlens_k=16, page_stride=128), 1),
+    (dict(layout=2, block_table=None, kv_len=16, cu_seqlens_k=None, page_stride=128), 1),
+    (dict(page_stride=100), 1),                 # smaller than a compact page
+    (dict(H_q=256, H_kv=1), 2),                 # GQA group above 128 rows
+    (dict(query=17), 1),                        # TMA needs 16-byte aligned bases
+    (dict(B=0, T=4), 1),
+])
+def test_host_validation(lib, over, status):
+    st, _ = _shape(lib, _args(**over))
+    assert st == status
+    assert lib.msa_last_error_message()
+
+
+def test_tnd_init_blocks_may_reach_padded_width(lib):
+    # guide sec. 10: TND bounds init/local by the 16-aligned score width
+    st, _ = _shape(lib, _args(layout=2, block_table=None, kv_len=None, cu_seqlens_k=16,
+                              page_stride=128, MB=3, init_blocks=16))
+    assert st == 0
+
+
+def test_status_strings(lib):
+    for s in range(6):
+        assert lib.msa_status_string(s)
+
+
+def test_python_binding_rejects_bad_layout_key():
+    import block_score_gb300 as bs
+    q = torch.zeros(4, 2, 128, dtype=torch.float16)
+    k = torch.zeros(2, 128, 1, 128, dtype=torch.float16)
+    with pytest.raises(ValueError):
+        bs.msa_index_score_out_shape(q, k, torch.zeros(1, dtype=torch.int32),
+                                     layout_key="bshd",
+                                     actual_seq_qlen=torch.tensor([0, 4], dtype=torch.int32),
+                                     actual_seq_klen=torch.tensor([10], dtype=torch.int32),
+                                     block_table=torch.zeros(1, 1, dtype=torch.int32))
+
+
+def test_python_binding_unsqueezes_3d_bbnd_key():
+    import block_score_gb300 as bs
+    q = torch.zeros(4, 2, 128, dtype=torch.float16)
+    k = torch.zeros(2, 128, 128, dtype=torch.float16)   # [NP, P, D] -> N2 = 1
+    shape = bs.msa_index_score_out_shape(
+        q, k, torch.zeros(1, dtype=torch.int32), layout_key="bbnd",
+        actual_seq_qlen=torch.tensor([0, 4], dtype=torch.int32),
+        actual_seq_klen=torch.tensor([10], dtype=torch.int32),
+        block_table=torch.zeros(1, 3, dtype=torch.int32))
+    assert shape == (2, 4, 16)

@@ -1,0 +1,275 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle.
+
+Tolerance (fp inputs): |gpu - oracle| <= 1e-3 + 1e-4 * |oracle| on finite
+scores.  Fill (-inf), forced (1e30 / 1e29) and padding positions must match
+bit for bit, and so must every score of the integer-valued cases, where all
+products and sums are exact in fp32.
+
+Case categories follow the reference op's test matrix (torch API guide,
+sec. 9.2): fp16 / bf16 / int8 x BBND / BNBD / TND, mixed batches with
+q_len = 0 / kv_len = 0, a strided paged cache whose gap pages hold poison,
+wide block tables (257, 275), short decode (q4-kv4, q4-kv275), speculative
+multi-token decode, long KV over many blocks and tiny-KV tails.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+
+pytestmark = pytest.mark.gpu
+
+ATOL, RTOL = 1e-3, 1e-4
+
+
+@pytest.fixture(scope="module")
+def dev():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import block_score_gb300 as bs
+    bs.load_library()
+    return torch.device("cuda:0")
+
+
+def run_gpu(case, dev):
+    import block_score_gb300 as bs
+    prep = bs.from_case(case, dev)
+    out = prep()
+    err = prep.device_error()
+    return out.cpu(), err, prep
+
+
+def assert_parity(out, ref, exact=False, what=""):
+    assert tuple(out.shape) == tuple(ref.shape), what
+    inf_r = torch.isinf(ref)
+    inf_o = torch.isinf(out)
+    bad = (inf_r != inf_o).nonzero()
+    assert bad.numel() == 0, f"{what}: fill pattern differs at {bad[:8].tolist()}"
+    assert torch.equal(out[inf_r], ref[inf_r]), f"{what}: sign of fill differs"
+    forced = ref.abs() >= 1e28
+    assert torch.equal(out[forced], ref[forced]), f"{what}: forced scores differ"
+    fin = ~inf_r & ~forced
+    if exact:
+        neq = (out[fin] != ref[fin])
+        assert not bool(neq.any()), f"{what}: {int(neq.sum())} inexact scores"
+        return
+    o, r = out[fin].double(), ref[fin].double()
+    diff = (o - r).abs()
+    tol = ATOL + RTOL * r.abs()
+    if diff.numel():
+        worst = int(torch.argmax(diff - tol))
+        assert bool((diff <= tol).all()), (
+            f"{what}: max excess {float((diff - tol).max()):.3e} "
+            f"(gpu {float(o[worst])}, oracle {float(r[worst])})")
+
+
+def test_tiny_paged_prefill_workload(dev):
+    case = synth.config(1)
+    out, err, _ = run_gpu(case, dev)
+    assert err == 0
+    assert_parity(out, oracle.oracle_full(case), what="cfg1")
+
+
+def test_integer_inputs_bit_exact(dev):
+    # several tiles per request (g=4 -> 32 positions per tile), ragged tails,
+    # diagonal blocks, GQA heads, permuted pages
+    case = synth.make_case([70, 1, 0, 33, 129], [700, 130, 50, 33, 129], H_q=8, H_kv=2,
+                           layout="BBND", q_dtype=torch.float16, q_kind="int_small",
+                           k_kind="int_small", MB=7, init_blocks=0, local_blocks=0, seed=101)
+    out, err, _ = run_gpu(case, dev)
+    assert err == 0
+    assert_parity(out, oracle.oracle_full(case), exact=True, what="int exact")
+
+
+def test_integer_inputs_bit_exact_bf16_mode0(dev):
+    case = synth.make_case([17, 40], [300, 1000], H_q=16, H_kv=1, layout="BNBD",
+                           q_dtype=torch.bfloat16, q_kind="int_small", k_kind="int_small",
+                           MB=9, sparse_mode=0, init_blocks=1, local_blocks=2, seed=102)
+    out, err, _ = run_gpu(case, dev)
+    assert err == 0
+    assert_parity(out, oracle.oracle_full(case), exact=True, what="int exact mode0")
+
+
+MATRIX = []
+for layout in ("BBND", "BNBD", "TND"):
+    for kdt in ("fp16", "bf16", "int8"):
+        MATRIX.append((layout, kdt))
+
+
+@pytest.mark.parametrize("layout,kdt", MATRIX)
+def test_dtype_layout_matrix_mixed_batch(dev, layout, kdt):
+    qdt = torch.bfloat16 if kdt == "bf16" else torch.float16
+    kdtype = {"fp16": torch.float16, "bf16": torch.bfloat16, "int8": torch.int8}[kdt]
+    # mixed batch: prefill, decode, q_len=0, kv_len=0, tail, long kv
+    q = [37, 1, 0, 4, 200, 1]
+    kv = [290, 1, 77, 0, 600, 4100]
+    case = synth.make_case(q, kv, H_q=16, H_kv=2, layout=layout, q_dtype=qdt, k_dtype=kdtype,
+                           k_kind="int8_full" if kdt == "int8" else "randn",
+                           MB=None if layout == "TND" else 40, init_blocks=1, local_blocks=2,
+                           seed=200 + len(layout) + len(kdt))
+    out, err, _ = run_gpu(case, dev)
+    assert err == 0
+    assert_parity(out, oracle.oracle_full(case), what=f"{layout}/{kdt}")
+
+
+@pytest.mark.parametrize("mode", [0, 3])
+def test_sparse_modes(dev, mode):
+    case = synth.make_case([64, 9], [333, 129], H_q=8, H_kv=8, layout="BBND",
+                           q_dtype=torch.float16, MB=5, sparse_mode=mode, seed=300 + mode)
+    out, err, _ = run_gpu(case, dev)
+    assert err == 0
+    assert_parity(out, oracle.oracle_full(case), what=f"mode{mode}")
+
+
+def test_strided_cache_poisoned_gaps(dev):
+    case = synth.make_case([20, 3], [500, 260], H_q=8, H_kv=1, layout="BBND",
+                           q_dtype=torch.float16, q_kind="abs_randn", MB=6, page_gap=2,
+                           poison=1.0e4, seed=310)
+    assert case.key.stride(0) == 2 * case.key[0].numel()
+    out, err, _ = run_gpu(case, dev)
+    assert err == 0
+    ref = oracle.oracle_full(case)
+    assert_parity(out, ref, what="gap poison")
+    assert float(out[torch.isfinite(out) & (out.abs() < 1e28)].max()) < 1.0e4
+
+
+@pytest.mark.parametrize("width", [257, 275])
+def test_wide_block_table(dev, width):
+    case = synth.make_case([4, 2], [4, 275], H_q=8, H_kv=1, layout="BBND",
+                           q_dtype=torch.float16, MB=width, seed=320 + width)
+    out, err, _ = run_gpu(case, dev)
+    assert err == 0
+    assert out.shape[2] == (width + 15) // 16 * 16
+    assert_parity(out, oracle.oracle_full(case), what=f"wide {width}")
+
+
+def test_short_decode_and_speculative(dev):
+    # q4-kv4, q4-kv275, q_len 3 speculative, single-token decode with g=16
+    case = synth.make_case([4, 4, 3, 1, 1], [4, 275, 1000, 7000, 128], H_q=16, H_kv=1,
+                           layout="BNBD", q_dtype=torch.bfloat16, MB=60, seed=330)
+    out, err, _ = run_gpu(case, dev)
+    assert err == 0
+    assert_parity(out, oracle.oracle_full(case), what="short decode")
+
+
+def test_all_requests_empty(dev):
+    case = synth.make_case([3, 5], [0, 0], H_q=4, H_kv=1, layout="BBND",
+                           q_dtype=torch.float16, MB=3, init_blocks=1, seed=340)
+    out, err, _ = run_gpu(case, dev)
+    assert err == 0
+    assert torch.isneginf(out).all()
+
+
+def test_group_size_not_a_power_of_two(dev):
+    # g = 3: 42 positions x 3 heads = 126 of the 128 MMA rows are used
+    case = synth.make_case([100, 50], [400, 90], H_q=6, H_kv=2, layout="BBND",
+                           q_dtype=torch.float16, MB=4, seed=350)
+    out, err, _ = run_gpu(case, dev)
+    assert err == 0
+    assert_parity(out, oracle.oracle_full(case), what="g=3")
+
+
+def test_plan_run_split_and_repeat_are_identical(dev):
+    import block_score_gb300 as bs
+    case = synth.make_case([50, 1], [900, 2000], H_q=16, H_kv=2, layout="BBND",
+                           q_dtype=torch.bfloat16, MB=16, seed=360)
+    prep = bs.from_case(case, dev)
+    a = prep().clone()
+    prep.out.fill_(7.0)
+    prep.plan()
+    b = prep.run().clone()
+    c = prep().clone()
+    assert torch.equal(a, b) and torch.equal(a, c)
+
+
+def test_bad_block_table_entry_is_reported_not_faulted(dev):
+    case = synth.make_case([5], [300], H_q=4, H_kv=1, layout="BBND", q_dtype=torch.float16,
+                           MB=4, seed=370)
+    case.block_table[0, 1] = 10_000          # beyond NP, inside the needed range
+    _, err, _ = run_gpu(case, dev)
+    assert err & 0x08
+    case.block_table[0, 1] = -3
+    _, err, _ = run_gpu(case, dev)
+    assert err & 0x08
+
+
+def test_bad_lengths_are_reported(dev):
+    case = synth.make_case([5], [300], H_q=4, H_kv=1, layout="BBND", q_dtype=torch.float16,
+                           MB=4, seed=380)
+    case.kv_len[0] = 600                      # needs 5 blocks, table has 4
+    _, err, _ = run_gpu(case, dev)
+    assert err & 0x02
+    case.kv_len[0] = 300
+    case.cu_seqlens_q[1] = 4                  # cu_q[B] != T
+    _, err, _ = run_gpu(case, dev)
+    assert err & 0x01
+
+
+# ---------------------------------------------------------------------------
+# the benchmark workloads at full size
+# ---------------------------------------------------------------------------
+
+def _sample_rows(case, n, seed):
+    """Rows (h*T + t) spread over heads and tokens, plus each request's first/last token."""
+    rng = np.random.default_rng(seed)
+    T, H = case.T, case.H_q
+    rows = set(int(x) for x in rng.integers(0, H * T, size=n))
+    cu = case.cu_seqlens_q.tolist()
+    for b in range(len(cu) - 1):
+        if cu[b + 1] > cu[b]:
+            for t in (cu[b], cu[b + 1] - 1):
+                h = int(rng.integers(0, H))
+                rows.add(h * T + t)
+    return sorted(rows)
+
+
+def _structural_checks(out, case):
+    """Properties of the whole output that hold at any size."""
+    MB, MBp, P = case.MB, case.MBp, case.P
+    assert torch.isneginf(out[:, :, MB:]).all()
+    cu = case.cu_seqlens_q.tolist()
+    for b in range(len(cu) - 1):
+        t0, t1 = cu[b], cu[b + 1]
+        if t1 == t0:
+            continue
+        L = case.kv_lens[b]
+        blk = out[:, t0:t1, :MB]
+        if L == 0:
+            assert torch.isneginf(blk).all()
+            continue
+        sl = int(case.start_loc[b])
+        lo = max(0, sl + 1 - case.local_blocks)
+        forced = torch.zeros(MB, dtype=torch.bool)
+        forced[:min(case.init_blocks, MB)] = True
+        if sl >= lo:
+            forced[lo:min(sl, MB - 1) + 1] = True
+        if case.init_blocks:
+            init_cols = [c for c in range(min(case.init_blocks, MB)) if not (lo <= c <= sl)]
+            if init_cols:
+                assert (blk[:, :, init_cols] == np.float32(1e30)).all()
+        if sl >= lo and lo < MB:
+            assert (blk[:, :, lo:min(sl, MB - 1) + 1] == np.float32(1e29)).all()
+        nb = -(-L // P)
+        if nb < MB:
+            tail = blk[:, :, nb:][:, :, ~forced[nb:]]
+            assert torch.isneginf(tail).all()
+
+
+@pytest.mark.parametrize("n", [2, 3, 4, 5])
+def test_benchmark_workload_sampled(dev, n):
+    case = synth.config(n)
+    out, err, _ = run_gpu(case, dev)
+    assert err == 0
+    _structural_checks(out, case)
+    rows = _sample_rows(case, 512 if n != 5 else 256, seed=n)
+    ref = oracle.oracle_rows(case, rows)
+    got = out.reshape(-1, out.shape[2])[torch.tensor(rows)]
+    assert_parity(got, ref, what=f"cfg{n} sampled")
+
+
+def test_batched_decode_workload_full(dev):
+    case = synth.config(2)
+    out, err, _ = run_gpu(case, dev)
+    assert err == 0
+    assert_parity(out, oracle.oracle_full(case), what="cfg2 full")
