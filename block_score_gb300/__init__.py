@@ -27,7 +27,7 @@ import torch
 __all__ = [
     "msa_index_score", "msa_index_score_plan", "msa_index_score_run",
     "msa_index_score_workspace_size", "msa_index_score_out_shape", "msa_get_device_error",
-    "MsaError", "library_path", "load_library", "DEVERR",
+    "MsaError", "library_path", "load_library", "DEVERR", "msa_index_score_noalloc",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -90,12 +90,13 @@ def load_library():
     lib.msa_index_score_plan.argtypes = [P, vp, sz, vp]
     lib.msa_index_score_run.argtypes = [P, vp, vp, sz, vp]
     lib.msa_get_device_error.argtypes = [vp, ctypes.POINTER(ctypes.c_int32), vp]
+    lib.msa_index_score_noalloc.argtypes = [P, vp, vp]
     lib.msa_status_string.restype = ctypes.c_char_p
     lib.msa_status_string.argtypes = [ctypes.c_int]
     lib.msa_last_error_message.restype = ctypes.c_char_p
     for name in ("msa_index_score_out_shape", "msa_index_score_workspace_size",
                  "msa_index_score", "msa_index_score_plan", "msa_index_score_run",
-                 "msa_get_device_error"):
+                 "msa_get_device_error", "msa_index_score_noalloc"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -270,6 +271,21 @@ def msa_index_score(query: torch.Tensor, key: torch.Tensor, start_loc: torch.Ten
     _check(load_library().msa_index_score(ctypes.byref(c.args), out.data_ptr(),
                                           workspace.data_ptr(), ws_bytes,
                                           _stream_handle(stream)))
+    return out
+
+
+def msa_index_score_noalloc(prepared: "Prepared", out: Optional[torch.Tensor] = None,
+                            stream=None) -> torch.Tensor:
+    """Same scores as ``msa_index_score`` without a caller workspace.
+
+    For callers that cannot allocate device memory on their hot path: the
+    library keeps the plan scratch in a fixed array of its own (at most 1024
+    requests).  Calls that overlap on the GPU share that array and race, so
+    keep them on one stream.  ``out`` defaults to ``prepared.out``.
+    """
+    out = prepared.out if out is None else out
+    _check(load_library().msa_index_score_noalloc(ctypes.byref(prepared.call.args),
+                                                  out.data_ptr(), _stream_handle(stream)))
     return out
 
 

@@ -16,7 +16,8 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 OBJ = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libmsa_index_score.so")
-SOURCES = ["msa_api.cu", "msa_plan.cu", "msa_score_16.cu", "msa_score_i8.cu"]
+SOURCES = ["msa_api.cu", "msa_plan.cu", "msa_score_16.cu", "msa_score_i8.cu",
+           "msa_noalloc.cu"]
 HEADERS = ["msa_common.cuh", "msa_ptx.cuh", "msa_score.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -216,6 +216,10 @@ msa_status_t make_maps(const msa_index_score_args* a, const msa::Params& p, CUte
 
 }  // namespace
 
+namespace msa {
+void set_last_error_message(const char* msg) { snprintf(g_msg, sizeof g_msg, "%s", msg); }
+}  // namespace msa
+
 extern "C" {
 
 int32_t msa_abi_version(void) { return MSA_ABI_VERSION; }

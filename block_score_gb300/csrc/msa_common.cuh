@@ -44,9 +44,9 @@ struct ReqInfo {
 };
 static_assert(sizeof(ReqInfo) == 32, "ReqInfo is 32 bytes");
 
-__host__ __device__ inline size_t workspace_bytes_for(int64_t B) {
-  size_t n = sizeof(PlanHeader) + sizeof(ReqInfo) * (size_t)B + sizeof(int32_t) * (size_t)(B + 1);
-  return (n + 255) / 256 * 256;
+__host__ __device__ constexpr size_t workspace_bytes_for(int64_t B) {
+  return (sizeof(PlanHeader) + sizeof(ReqInfo) * (size_t)B + sizeof(int32_t) * (size_t)(B + 1) +
+          255) / 256 * 256;
 }
 
 struct Params {
@@ -83,6 +83,9 @@ struct UnitDesc {
   int32_t pad[3];
 };
 static_assert(sizeof(UnitDesc) == 64, "UnitDesc is 64 bytes");
+
+// Record the message returned by msa_last_error_message() on this host thread.
+void set_last_error_message(const char* msg);
 
 // Host-side launchers (defined in the .cu files).
 cudaError_t launch_plan(const Params& p, cudaStream_t s);

@@ -147,6 +147,34 @@ msa_status_t msa_index_score_plan(const msa_index_score_args *args, void *worksp
 msa_status_t msa_index_score_run(const msa_index_score_args *args, float *out, void *workspace,
                                  size_t workspace_bytes, msa_stream_t stream);
 
+/*
+ * Allocation-free variant of msa_index_score, for callers that cannot
+ * allocate device memory (a serving loop that forbids allocator calls after
+ * start-up, or a host program without a device allocator of its own).  The
+ * pages define no such call: this entry point has no counterpart there.
+ *
+ * Same arguments and results as msa_index_score, without the workspace: the
+ * plan scratch is a fixed array inside the library (MSA_NOALLOC_WORKSPACE_BYTES
+ * bytes on every GPU that loads the library, held until the process exits).
+ * It handles at most MSA_NOALLOC_MAX_BATCH requests; a larger B returns
+ * MSA_ERR_WORKSPACE and enqueues nothing.  No device memory is allocated or
+ * freed.
+ *
+ * - The first call on a device looks up the array's device address
+ *   (cudaGetSymbolAddress) with that device current and caches it; make that
+ *   first call before any stream capture on that device.
+ * - Every call uses the same array and leaves its contents behind; each call
+ *   clears the parts that must start at zero (work counter, error word) itself.
+ * - Calls whose kernels overlap on the GPU (different streams, or several
+ *   host threads) race on the array: order them, e.g. on one stream.
+ * - The device error word of these calls lives in the library's array and is
+ *   not readable through msa_get_device_error.
+ */
+#define MSA_NOALLOC_MAX_BATCH 1024
+#define MSA_NOALLOC_WORKSPACE_BYTES 37120
+msa_status_t msa_index_score_noalloc(const msa_index_score_args *args, float *out,
+                                     msa_stream_t stream);
+
 /* Synchronise `stream` and read the device error word left in `workspace`
  * by the last call (MSA_DEVERR_* bits; 0 = clean).  Returns MSA_OK, or
  * MSA_ERR_CUDA if the copy fails. */
