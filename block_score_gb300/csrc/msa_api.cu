@@ -10,7 +10,7 @@
 #include <cstring>
 #include <mutex>
 
-#include "../../include/msa_index_score.h"
+#include "msa_index_score.h"
 #include "msa_common.cuh"
 
 namespace {

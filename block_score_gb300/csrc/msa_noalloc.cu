@@ -18,7 +18,7 @@
 #include <cstdio>
 #include <mutex>
 
-#include "../../include/msa_index_score.h"
+#include "msa_index_score.h"
 #include "msa_common.cuh"
 
 namespace {

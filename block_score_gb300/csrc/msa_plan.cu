@@ -93,7 +93,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const Params p) {
   __shared__ unsigned long long s_work;
   __shared__ int s_err;
   __shared__ int s_key[kPlanThreads];
-  __shared__ int s_idx[kPlanThreads];
+  __shared__ int s_units[kPlanThreads];
   __shared__ int s_tot;
 
   PlanHeader* hdr = reinterpret_cast<PlanHeader*>(p.ws);
@@ -107,93 +107,104 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const Params p) {
   }
   __syncthreads();
 
-  // pass 1: validation and total work (blocks x kv heads x tiles, upper bound)
+  // pass 1: read every request once, validate, and sum the work
+  // (blocks x kv heads x tiles, an upper bound that only sets the chunk size)
+  const bool small = p.B <= kPlanThreads;
   int err = 0;
   unsigned long long work = 0;
+  ReqScratch mine{};
+  int my_sl = 0;
   for (int b = tid; b < p.B; b += kPlanThreads) {
     ReqScratch r = read_request(p, b, err);
     work += (unsigned long long)p.H_kv * r.ntiles * r.nbc_max;
+    if (small) {
+      mine = r;
+      my_sl = p.start_loc[b];
+    }
   }
   if (err) atomicOr(&s_err, err);
   if (work) atomicAdd(&s_work, work);
   __syncthreads();
 
   // chunk size: about 8 units per SM on average, never below 8 blocks
-  unsigned long long target = (unsigned long long)p.num_sms * 8ull;
+  const unsigned long long target = (unsigned long long)p.num_sms * 8ull;
   unsigned long long c = (s_work + target - 1) / target;
   if (c < 8) c = 8;
   c = (c + 7) / 8 * 8;
   if (c > (unsigned long long)p.MBp) c = (unsigned long long)p.MBp;
   const int chunk = (int)c;
 
-  const bool sorted = p.B <= kPlanThreads;
-  if (sorted) {
-    // longest-first order: key = cost of the request's largest unit
-    int key = -1;
+  if (small) {
+    // longest-first order by the cost of each request's largest unit; the
+    // rank of a request is the number of requests that go before it
+    int key = -1, units = 0, nchunks = 1;
     if (tid < p.B) {
-      int e2 = 0;
-      ReqScratch r = read_request(p, tid, e2);
-      if (r.Lq > 0) key = r.nbc_max < chunk ? r.nbc_max : chunk;
+      nchunks = mine.nbc_max > 0 ? cdiv(mine.nbc_max, chunk) : 1;
+      units = mine.Lq > 0 ? p.H_kv * mine.ntiles * nchunks : 0;
+      if (mine.Lq > 0) key = mine.nbc_max < chunk ? mine.nbc_max : chunk;
+      s_key[tid] = key;
     }
-    s_key[tid] = key;
-    s_idx[tid] = tid;
     __syncthreads();
-    // bitonic sort, descending key, ascending index on ties
-    for (int k = 2; k <= kPlanThreads; k <<= 1) {
-      for (int j = k >> 1; j > 0; j >>= 1) {
-        const int partner = tid ^ j;
-        if (partner > tid) {
-          const int ka = s_key[tid], kb = s_key[partner];
-          const int ia = s_idx[tid], ib = s_idx[partner];
-          // "a before b" in the final order
-          const bool a_first = (ka > kb) || (ka == kb && ia < ib);
-          const bool up = ((tid & k) == 0);
-          if (up ? !a_first : a_first) {
-            s_key[tid] = kb;
-            s_key[partner] = ka;
-            s_idx[tid] = ib;
-            s_idx[partner] = ia;
-          }
-        }
-        __syncthreads();
+    if (tid < p.B) {
+      int rank = 0;
+      for (int j = 0; j < p.B; ++j) {
+        const int kj = s_key[j];
+        rank += (kj > key) || (kj == key && j < tid);
       }
-    }
-  }
-
-  // pass 2: request records in schedule order and the unit prefix sum
-  int carry = 0;
-  for (int base = 0; base < p.B; base += kPlanThreads) {
-    const int slot = base + tid;
-    int units = 0;
-    if (slot < p.B) {
-      const int b = sorted ? s_idx[slot] : slot;
-      int e2 = 0;
-      ReqScratch r = read_request(p, b, e2);
-      int nchunks = r.nbc_max > 0 ? cdiv(r.nbc_max, chunk) : 1;
-      units = r.Lq > 0 ? p.H_kv * r.ntiles * nchunks : 0;
       ReqInfo ri;
-      ri.b = b;
-      ri.t0 = r.t0;
-      ri.Lq = r.Lq;
-      ri.L = r.L;
-      ri.ntiles = r.ntiles;
+      ri.b = tid;
+      ri.t0 = mine.t0;
+      ri.Lq = mine.Lq;
+      ri.L = mine.L;
+      ri.ntiles = mine.ntiles;
       ri.nchunks = nchunks;
-      ri.kbase = r.kbase;
-      ri.sl = p.start_loc[b];
-      req[slot] = ri;
+      ri.kbase = mine.kbase;
+      ri.sl = my_sl;
+      req[rank] = ri;
+      s_units[rank] = units;
     }
-    const int incl = block_incl_scan(units, s_warp);
-    if (slot < p.B) prefix[slot + 1] = carry + incl;
-    // last thread's inclusive value is the chunk total
+    __syncthreads();
+    const int v = tid < p.B ? s_units[tid] : 0;
+    const int incl = block_incl_scan(v, s_warp);
+    if (tid < p.B) prefix[tid + 1] = incl;
     if (tid == kPlanThreads - 1) s_tot = incl;
     __syncthreads();
-    carry += s_tot;
+  } else {
+    // large batches: natural order, prefix sum over slices of kPlanThreads
+    int carry = 0;
+    for (int base = 0; base < p.B; base += kPlanThreads) {
+      const int b = base + tid;
+      int units = 0;
+      if (b < p.B) {
+        int e2 = 0;
+        ReqScratch r = read_request(p, b, e2);
+        const int nchunks = r.nbc_max > 0 ? cdiv(r.nbc_max, chunk) : 1;
+        units = r.Lq > 0 ? p.H_kv * r.ntiles * nchunks : 0;
+        ReqInfo ri;
+        ri.b = b;
+        ri.t0 = r.t0;
+        ri.Lq = r.Lq;
+        ri.L = r.L;
+        ri.ntiles = r.ntiles;
+        ri.nchunks = nchunks;
+        ri.kbase = r.kbase;
+        ri.sl = p.start_loc[b];
+        req[b] = ri;
+      }
+      const int incl = block_incl_scan(units, s_warp);
+      if (b < p.B) prefix[b + 1] = carry + incl;
+      if (tid == kPlanThreads - 1) s_tot = incl;
+      __syncthreads();
+      carry += s_tot;
+      __syncthreads();
+    }
+    if (tid == 0) s_tot = carry;
     __syncthreads();
   }
   if (tid == 0) {
     prefix[0] = 0;
     hdr->counter = 0;
-    hdr->n_units = carry;
+    hdr->n_units = s_tot;
     hdr->n_req = p.B;
     hdr->chunk = chunk;
     hdr->err = s_err;

@@ -9,12 +9,14 @@
 // head) pairs of one GQA group, so one K page read serves g heads.
 //
 // Roles (one CTA per SM, persistent over units fetched with an atomic counter):
-//   warp 0      scheduler + TMA producer (Q tiles, K pages through block_table)
-//   warp 1      TMEM owner + single-thread tcgen05.mma issuer
-//   warps 2..5  epilogue: TMEM -> registers, (scale), mask, 128-wide max,
-//               local-mask constants, 32-byte vector stores of the fp32 scores
-//   warps 6..9  (int8 keys only) int8 -> fp16 conversion of K pages into the
-//               swizzled operand layout, and the per-token scale for the epilogue
+//   warp 0       scheduler: claims the next unit from the global counter a few
+//                blocks before the producer needs it and decodes it from the plan
+//   warp 1       TMEM owner + single-thread tcgen05.mma issuer
+//   warp 2       TMA producer (Q tiles, K pages through block_table)
+//   warps 3..6   epilogue: TMEM -> registers, (scale), mask, 128-wide max,
+//                local-mask constants, 32-byte vector stores of the fp32 scores
+//   warps 7..10  (int8 keys only) int8 -> fp16 conversion of K pages into the
+//                swizzled operand layout, and the per-token scale for the epilogue
 //
 // Shared memory: Q double buffer (2 x 32 KiB), K ring of 32 KiB stages, for
 // int8 also a ring of raw 16 KiB pages.  TMEM: 4 accumulators of 128 columns.
@@ -35,15 +37,19 @@ template <>
 struct ScoreCfg<false> {
   static constexpr int kStages = 5;      // 16-bit K pages in flight
   static constexpr int kRawStages = 0;
-  static constexpr int kThreads = 192;
+  static constexpr int kThreads = 224;
 };
 
 template <>
 struct ScoreCfg<true> {
   static constexpr int kStages = 2;      // converted fp16 pages
   static constexpr int kRawStages = 5;   // int8 pages in flight
-  static constexpr int kThreads = 320;
+  static constexpr int kThreads = 352;
 };
+
+constexpr int kEpiWarp0 = 3;             // first epilogue warp
+constexpr int kCvtWarp0 = 7;             // first int8 converter warp
+constexpr int kLead = 4;                 // blocks before the end of a unit at which the next is claimed
 
 constexpr int kQBufs = 2;
 constexpr int kAcc = 4;
@@ -64,7 +70,7 @@ struct SmemLayout {
   static constexpr uint32_t bar_off = ring_off + kSched * sizeof(UnitDesc);
   static constexpr uint32_t n_bars = 2 * kSched + 2 * kQBufs + 2 * ScoreCfg<KI8>::kStages +
                                      2 * ScoreCfg<KI8>::kRawStages + 2 * kAcc +
-                                     (KI8 ? 2 * kAcc : 0) + 1;
+                                     (KI8 ? 2 * kAcc : 0) + 2;
   static constexpr uint32_t misc_off = bar_off + n_bars * 8;           // tmem base, abort, raw pages
   static constexpr uint32_t end = misc_off + 16 + 4 * (ScoreCfg<KI8>::kRawStages + 1);
   static constexpr uint32_t bytes = end + 1024;                        // + alignment slack
@@ -180,6 +186,7 @@ __global__ void __launch_bounds__(ScoreCfg<KI8>::kThreads, 1)
   const uint32_t b_sc_full = b_acc_empty + 8 * kAcc;
   const uint32_t b_sc_empty = b_sc_full + (KI8 ? 8 * kAcc : 0);
   const uint32_t b_drain = b_sc_empty + (KI8 ? 8 * kAcc : 0);
+  const uint32_t b_sched_req = b_drain + 8;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::misc_off);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::misc_off + 4);
   volatile int* raw_page = reinterpret_cast<volatile int*>(smem + L::misc_off + 16);
@@ -187,7 +194,8 @@ __global__ void __launch_bounds__(ScoreCfg<KI8>::kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  constexpr int kConsumers = KI8 ? 9 : 5;   // MMA + 4 epilogue warps (+ 4 converter warps)
+  // readers of each unit descriptor: producer, MMA, 4 epilogue warps (+ 4 converter warps)
+  constexpr int kConsumers = KI8 ? 10 : 6;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kSched; ++i) {
@@ -215,6 +223,7 @@ __global__ void __launch_bounds__(ScoreCfg<KI8>::kThreads, 1)
       }
     }
     mbar_init(b_drain, 1);
+    mbar_init(b_sched_req, 1);
     *abort_flag = 0;
     fence_mbar_init();
     prefetch_tmap(&tm_q);
@@ -239,15 +248,19 @@ __global__ void __launch_bounds__(ScoreCfg<KI8>::kThreads, 1)
   WaitCtl ctl{abort_flag, &hdr->err, p.wait_limit_ns};
 
   if (warp == 0) {
-    // ------------------------------------------------ scheduler + producer --
+    // -------------------------------------------------------- scheduler --
+    // Claims one unit ahead: the first at once, each later one when the
+    // producer is kLead blocks from the end of its current unit, so a CTA
+    // never sits on work another CTA could be doing.
     if (lane == 0) {
       const int n_units = *reinterpret_cast<volatile int*>(&hdr->n_units);
       const int chunk = *reinterpret_cast<volatile int*>(&hdr->chunk);
-      const uint64_t pol_k = l2_policy_evict_last();
-      const uint32_t q_bytes = 2u * 128u * (uint32_t)(p.g * p.np);
-      uint32_t ss = 0, sph = 0, qb = 0, qph = 0, ks = 0, kph = 0;
-      uint32_t n_q = 0, n_k = 0;   // loads issued (for the teardown drain)
-      for (;;) {
+      uint32_t ss = 0, sph = 0, rph = 0;
+      for (bool first = true;; first = false) {
+        if (!first) {
+          if (!mbar_wait(b_sched_req, rph, ctl)) break;
+          rph ^= 1;
+        }
         UnitDesc d;
         make_unit(p, hdr, req, prefix, n_units, chunk, atomicAdd(&hdr->counter, 1), d);
         if (!mbar_wait(b_sched_empty + 8 * ss, sph ^ 1, ctl)) break;
@@ -255,7 +268,28 @@ __global__ void __launch_bounds__(ScoreCfg<KI8>::kThreads, 1)
         mbar_arrive(b_sched_full + 8 * ss);
         if (++ss == kSched) { ss = 0; sph ^= 1; }
         if (!d.live) break;
-        if (d.b1 <= d.c0) continue;
+      }
+    }
+    __syncwarp();
+  } else if (warp == 2) {
+    // ------------------------------------------------------- producer --
+    if (lane == 0) {
+      const uint64_t pol_k = l2_policy_evict_last();
+      const uint32_t q_bytes = 2u * 128u * (uint32_t)(p.g * p.np);
+      const bool paged = p.layout != 2;
+      uint32_t ss = 0, sph = 0, qb = 0, qph = 0, ks = 0, kph = 0;
+      uint32_t n_q = 0, n_k = 0;   // loads issued (for the teardown drain)
+      for (;;) {
+        if (!mbar_wait(b_sched_full + 8 * ss, sph, ctl)) break;
+        const UnitDesc d = ring[ss];
+        mbar_arrive(b_sched_empty + 8 * ss);
+        if (++ss == kSched) { ss = 0; sph ^= 1; }
+        if (!d.live) break;
+        if (d.b1 <= d.c0) {
+          mbar_arrive(b_sched_req);
+          continue;
+        }
+        const int req_at = max(d.c0, d.b1 - kLead);
         if (!mbar_wait(b_q_empty + 8 * qb, qph ^ 1, ctl)) break;
         const uint32_t qdst = sbase + L::q_off + qb * kTileBytes;
         mbar_arrive_expect_tx(b_q_full + 8 * qb, q_bytes);
@@ -263,23 +297,36 @@ __global__ void __launch_bounds__(ScoreCfg<KI8>::kThreads, 1)
         tma_load_3d(qdst + kHalfBytes, &tm_q, b_q_full + 8 * qb, 64, d.hk * p.g, d.t0);
         ++n_q;
         if (++qb == kQBufs) { qb = 0; qph ^= 1; }
+        // page indices run four blocks ahead of their use
+        const int32_t* trow = p.block_table + (int64_t)d.b * p.MB;
+        int pg0 = 0, pg1 = 0, pg2 = 0, pg3 = 0;
+        if (paged) {
+          pg0 = __ldg(trow + d.c0);
+          if (d.c0 + 1 < d.b1) pg1 = __ldg(trow + d.c0 + 1);
+          if (d.c0 + 2 < d.b1) pg2 = __ldg(trow + d.c0 + 2);
+          if (d.c0 + 3 < d.b1) pg3 = __ldg(trow + d.c0 + 3);
+        }
         bool ok = true;
         for (int beta = d.c0; beta < d.b1; ++beta) {
-          int page, tok;
-          if (p.layout == 2) {
-            page = 0;
-            tok = d.kbase + beta * kP;
-          } else {
-            page = __ldg(p.block_table + (int64_t)d.b * p.MB + beta);
+          if (beta == req_at) mbar_arrive(b_sched_req);
+          int page = 0, tok;
+          if (paged) {
+            page = pg0;
+            pg0 = pg1;
+            pg1 = pg2;
+            pg2 = pg3;
+            pg3 = beta + 4 < d.b1 ? __ldg(trow + beta + 4) : 0;
             tok = 0;
             if (page < 0 || (int64_t)page >= p.NP) {
               atomicOr(&hdr->err, kErrBlockTable);
               page = (int)(p.NP < 0x7fffffffLL ? p.NP : 0x7fffffffLL);   // out of bounds: zero fill
             }
+          } else {
+            tok = d.kbase + beta * kP;
           }
           if constexpr (KI8) {
             if (!mbar_wait(b_raw_empty + 8 * ks, kph ^ 1, ctl)) { ok = false; break; }
-            raw_page[ks] = p.layout == 2 ? tok : page;
+            raw_page[ks] = paged ? page : tok;
             mbar_arrive_expect_tx(b_raw_full + 8 * ks, kRawBytes);
             tma_k(sbase + L::raw_off + ks * kRawBytes, &tm_k, b_raw_full + 8 * ks, 0, tok, d.hk,
                   page, p.layout, pol_k);
@@ -299,19 +346,18 @@ __global__ void __launch_bounds__(ScoreCfg<KI8>::kThreads, 1)
       }
       // Teardown: never leave the CTA with a TMA write in flight.  Only the
       // last (ring size) loads of each ring can still be pending.
-      WaitCtl drain{abort_flag, &hdr->err, p.wait_limit_ns};
       const uint32_t nk_ring = KI8 ? (uint32_t)R : (uint32_t)S;
       const uint32_t kfull = KI8 ? b_raw_full : b_k_full;
       for (uint32_t j = n_k > nk_ring ? n_k - nk_ring : 0; j < n_k; ++j) {
         const uint32_t st = j % nk_ring, ph = (j / nk_ring) & 1u;
-        uint64_t t0 = global_timer_ns();
-        while (!mbar_try_wait(kfull + 8 * st, ph) && global_timer_ns() - t0 < drain.limit_ns) {
+        const uint64_t t0 = global_timer_ns();
+        while (!mbar_try_wait(kfull + 8 * st, ph) && global_timer_ns() - t0 < p.wait_limit_ns) {
         }
       }
       for (uint32_t j = n_q > (uint32_t)kQBufs ? n_q - kQBufs : 0; j < n_q; ++j) {
         const uint32_t st = j % kQBufs, ph = (j / kQBufs) & 1u;
-        uint64_t t0 = global_timer_ns();
-        while (!mbar_try_wait(b_q_full + 8 * st, ph) && global_timer_ns() - t0 < drain.limit_ns) {
+        const uint64_t t0 = global_timer_ns();
+        while (!mbar_try_wait(b_q_full + 8 * st, ph) && global_timer_ns() - t0 < p.wait_limit_ns) {
         }
       }
     }
@@ -360,7 +406,7 @@ __global__ void __launch_bounds__(ScoreCfg<KI8>::kThreads, 1)
       }
     }
     __syncwarp();
-  } else if (warp < 6) {
+  } else if (warp < kEpiWarp0 + 4) {
     // --------------------------------------------------------- epilogue --
     const int quarter = warp & 3;                  // TMEM lane quarter this warp may read
     const int r = quarter * 32 + lane;             // MMA row = TMEM lane
@@ -384,51 +430,55 @@ __global__ void __launch_bounds__(ScoreCfg<KI8>::kThreads, 1)
       const int h = d.hk * p.g + hl;
       float* orow = p.out + ((int64_t)h * p.T + (d.t0 + pos)) * (int64_t)p.MBp;
       const int lo = max(0, d.sl + 1 - p.local_blocks);
+      // value of a column that has no computed score: the local-mask constant
+      // if forced, else the fill value (padding columns >= MB always fill)
+      const bool live_kv = d.L > 0;
+      auto fill_value = [&](int beta) -> float {
+        float f = ninf;
+        if (live_kv && beta < p.init_blocks) f = 1e30f;
+        if (live_kv && beta >= lo && beta <= d.sl) f = 1e29f;
+        return beta < p.MB ? f : ninf;
+      };
       float v[8];
       bool ok = true;
-      for (int beta = d.c0; beta < d.c1; ++beta) {
+      int beta = d.c0;
+      for (; beta < d.b1; ++beta) {
         float m = ninf;
-        if (beta < d.b1) {
-          if (!warp_wait(b_acc_full + 8 * ab, aph, ctl)) { ok = false; break; }
-          tc_fence_after();
-          float x[128];
+        if (!warp_wait(b_acc_full + 8 * ab, aph, ctl)) { ok = false; break; }
+        tc_fence_after();
+        float x[128];
+        if (warp_valid) {
+          const uint32_t ta = t_lane + ab * 128u;
+          tmem_ld32(ta + 0, *reinterpret_cast<float(*)[32]>(&x[0]));
+          tmem_ld32(ta + 32, *reinterpret_cast<float(*)[32]>(&x[32]));
+          tmem_ld32(ta + 64, *reinterpret_cast<float(*)[32]>(&x[64]));
+          tmem_ld32(ta + 96, *reinterpret_cast<float(*)[32]>(&x[96]));
+          tmem_wait_ld();
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(b_acc_empty + 8 * ab);
+        if constexpr (KI8) {
+          // DEQUANT: column multiply by the per-token scale, before the mask
+          if (!warp_wait(b_sc_full + 8 * ab, aph, ctl)) { ok = false; break; }
           if (warp_valid) {
-            const uint32_t ta = t_lane + ab * 128u;
-            tmem_ld32(ta + 0, *reinterpret_cast<float(*)[32]>(&x[0]));
-            tmem_ld32(ta + 32, *reinterpret_cast<float(*)[32]>(&x[32]));
-            tmem_ld32(ta + 64, *reinterpret_cast<float(*)[32]>(&x[64]));
-            tmem_ld32(ta + 96, *reinterpret_cast<float(*)[32]>(&x[96]));
-            tmem_wait_ld();
-          }
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(b_acc_empty + 8 * ab);
-          if constexpr (KI8) {
-            // DEQUANT: column multiply by the per-token scale, before the mask
-            if (!warp_wait(b_sc_full + 8 * ab, aph, ctl)) { ok = false; break; }
-            if (warp_valid) {
-              const float4* sc = reinterpret_cast<const float4*>(scale_s + ab * 128);
+            const float4* sc = reinterpret_cast<const float4*>(scale_s + ab * 128);
 #pragma unroll
-              for (int c = 0; c < 32; ++c) {
-                const float4 s4 = sc[c];
-                x[4 * c + 0] *= s4.x;
-                x[4 * c + 1] *= s4.y;
-                x[4 * c + 2] *= s4.z;
-                x[4 * c + 3] *= s4.w;
-              }
+            for (int c = 0; c < 32; ++c) {
+              const float4 s4 = sc[c];
+              x[4 * c + 0] *= s4.x;
+              x[4 * c + 1] *= s4.y;
+              x[4 * c + 2] *= s4.z;
+              x[4 * c + 3] *= s4.w;
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(b_sc_empty + 8 * ab);
           }
-          if (valid) m = masked_row_max(x, lim - beta * kP);
-          if (++ab == kAcc) { ab = 0; aph ^= 1; }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(b_sc_empty + 8 * ab);
         }
-        // local mask after the max (forced scores); padding columns stay -inf
-        if (d.L > 0) {
-          if (beta < p.init_blocks) m = 1e30f;
-          if (beta >= lo && beta <= d.sl) m = 1e29f;
-        }
-        if (beta >= p.MB) m = ninf;
+        if (valid) m = masked_row_max(x, lim - beta * kP);
+        if (++ab == kAcc) { ab = 0; aph ^= 1; }
+        // local mask after the max: forced blocks take their constant
+        if (live_kv && (beta < p.init_blocks || (beta >= lo && beta <= d.sl))) m = fill_value(beta);
         const int e = beta & 7;
 #pragma unroll
         for (int k = 0; k < 8; ++k)
@@ -440,10 +490,34 @@ __global__ void __launch_bounds__(ScoreCfg<KI8>::kThreads, 1)
         }
       }
       if (!ok) break;
+      // columns past the computed blocks: finish the open group of 8, then
+      // write whole groups of closed-form values
+      if (valid) {
+        if (beta & 7) {
+          for (; beta & 7; ++beta) {
+            const float f = fill_value(beta);
+            const int e = beta & 7;
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+              if (k == e) v[k] = f;
+          }
+          float4* dst = reinterpret_cast<float4*>(orow + (beta - 8));
+          __stcs(dst, make_float4(v[0], v[1], v[2], v[3]));
+          __stcs(dst + 1, make_float4(v[4], v[5], v[6], v[7]));
+        }
+        for (; beta < d.c1; beta += 8) {
+          float4* dst = reinterpret_cast<float4*>(orow + beta);
+          __stcs(dst, make_float4(fill_value(beta), fill_value(beta + 1), fill_value(beta + 2),
+                                  fill_value(beta + 3)));
+          __stcs(dst + 1, make_float4(fill_value(beta + 4), fill_value(beta + 5),
+                                      fill_value(beta + 6), fill_value(beta + 7)));
+        }
+      }
+      if (!ok) break;
     }
   } else if (KI8) {
     // ------------------------------------------- int8 -> fp16 converters --
-    const int ct = threadIdx.x - 192;           // 0..127
+    const int ct = threadIdx.x - kCvtWarp0 * 32;   // 0..127
     uint32_t ss = 0, sph = 0, rs = 0, rph = 0, ks = 0, kph = 0, ab = 0, aph = 0;
     for (;;) {
       if (!warp_wait(b_sched_full + 8 * ss, sph, ctl)) break;
