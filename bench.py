@@ -295,25 +295,32 @@ def run_ours(args):
     sampler = ClockSampler(local)
     sampler.start()
     time.sleep(0.3)
-    # per-launch timing of the dominant kernel: events around the run half
-    ev_k = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-            for _ in range(args.steps)]
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # timed region: K back-to-back calls of the op (plan + score kernel), events
+    # only at its ends so the score kernel's launch overlaps the plan kernel
     barrier(ws)
     torch.cuda.synchronize(device)
     sampler.mark("start")
     ev0.record(stream)
+    for _ in range(args.steps):
+        prep(stream)
+    ev1.record(stream)
+    torch.cuda.synchronize(device)
+    sampler.mark("stop")
+    barrier(ws)
+    total_ms = ev0.elapsed_time(ev1)
+    # dominant kernel: a second pass of K calls with events around each
+    # score-kernel launch, on the launching stream
+    ev_k = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for _ in range(args.steps)]
+    torch.cuda.synchronize(device)
     for i in range(args.steps):
         prep.plan(stream)
         ev_k[i][0].record(stream)
         prep.run(stream)
         ev_k[i][1].record(stream)
-    ev1.record(stream)
     torch.cuda.synchronize(device)
-    sampler.mark("stop")
-    barrier(ws)
     sampler.stop()
-    total_ms = ev0.elapsed_time(ev1)
     kern_ms = statistics.mean(a.elapsed_time(b) for a, b in ev_k)
     step_ms = max_over_ranks(total_ms / args.steps, ws, device)
     kern_ms = max_over_ranks(kern_ms, ws, device)
@@ -343,6 +350,8 @@ def run_ours(args):
                 "frac": tflops_kernel / pk, "traffic": args.traffic,
                 "peak_source": peaks["source"] + " bf16_tflops (burst)"}
     roof["kernel"] = "score_kernel"
+    roof["kernel_timing"] = ("second pass of K calls with CUDA events around each "
+                             "score-kernel launch")
     roof["kernel_us"] = kern_ms * 1e3
     roof["algorithmic_bytes"] = work["bytes"]
     roof["algorithmic_flops"] = work["flops"]

@@ -126,8 +126,9 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const Params p) {
   if (work) atomicAdd(&s_work, work);
   __syncthreads();
 
-  // chunk size: about 8 units per SM on average, never below 8 blocks
-  const unsigned long long target = (unsigned long long)p.num_sms * 8ull;
+  // chunk size: about 16 units per SM on average, never below 8 blocks (the
+  // tail of a call is then a fraction of one short unit)
+  const unsigned long long target = (unsigned long long)p.num_sms * 16ull;
   unsigned long long c = (s_work + target - 1) / target;
   if (c < 8) c = 8;
   c = (c + 7) / 8 * 8;
