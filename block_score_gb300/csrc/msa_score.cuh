@@ -107,6 +107,21 @@ __device__ __forceinline__ float masked_row_max(const float (&x)[128], int climi
   return fmax3(a0, a1, fmaxf(a2, a3));
 }
 
+// Four signed int8 values (one 32-bit word, little-endian) to four fp16
+// values, exactly: x + 128 is placed in the low mantissa byte of 1024.0
+// (bit pattern 0x64xx, whose unit in the last place is 1), and 1152 = 1024 + 128
+// is subtracted; every step is exact for |x| <= 128.
+__device__ __forceinline__ void int8x4_to_half4(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  const uint32_t u = w ^ 0x80808080u;                      // bytes x + 128 in [0, 255]
+  const uint32_t a = __byte_perm(u, 0x64646464u, 0x4140);  // (1024 + u0, 1024 + u1)
+  const uint32_t b = __byte_perm(u, 0x64646464u, 0x4342);  // (1024 + u2, 1024 + u3)
+  const __half2 bias = __half2half2(__ushort_as_half((unsigned short)0x6480));   // 1152.0
+  const __half2 ra = __hsub2(*reinterpret_cast<const __half2*>(&a), bias);
+  const __half2 rb = __hsub2(*reinterpret_cast<const __half2*>(&b), bias);
+  lo = *reinterpret_cast<const uint32_t*>(&ra);
+  hi = *reinterpret_cast<const uint32_t*>(&rb);
+}
+
 // K page tile load.  The tensor map's dimensions are ordered by increasing
 // stride: BNBD (D, P, H_kv, NP); BBND (D, H_kv, P, NP); TND (D, H_kv, T2, 1).
 __device__ __forceinline__ void tma_k(uint32_t dst, const CUtensorMap* m, uint32_t bar, int x,
@@ -449,10 +464,7 @@ __global__ void __launch_bounds__(ScoreCfg<KI8>::kThreads, 1)
         float x[128];
         if (warp_valid) {
           const uint32_t ta = t_lane + ab * 128u;
-          tmem_ld32(ta + 0, *reinterpret_cast<float(*)[32]>(&x[0]));
-          tmem_ld32(ta + 32, *reinterpret_cast<float(*)[32]>(&x[32]));
-          tmem_ld32(ta + 64, *reinterpret_cast<float(*)[32]>(&x[64]));
-          tmem_ld32(ta + 96, *reinterpret_cast<float(*)[32]>(&x[96]));
+          tmem_ld128(ta, x);
           tmem_wait_ld();
         }
         tc_fence_before();
@@ -537,17 +549,10 @@ __global__ void __launch_bounds__(ScoreCfg<KI8>::kThreads, 1)
           const int id = ct + 128 * it;           // 16-byte chunk of the int8 page
           const int row = id >> 3, c16 = id & 7;
           const int4 raw = *reinterpret_cast<const int4*>(src + row * 128 + c16 * 16);
-          const int32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+          const uint32_t w[4] = {(uint32_t)raw.x, (uint32_t)raw.y, (uint32_t)raw.z, (uint32_t)raw.w};
           uint32_t hv[8];
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const int8_t b0 = (int8_t)(w[q] & 0xff), b1 = (int8_t)((w[q] >> 8) & 0xff);
-            const int8_t b2 = (int8_t)((w[q] >> 16) & 0xff), b3 = (int8_t)((w[q] >> 24) & 0xff);
-            const __half2 h01 = __halves2half2(__int2half_rn(b0), __int2half_rn(b1));
-            const __half2 h23 = __halves2half2(__int2half_rn(b2), __int2half_rn(b3));
-            hv[2 * q] = *reinterpret_cast<const uint32_t*>(&h01);
-            hv[2 * q + 1] = *reinterpret_cast<const uint32_t*>(&h23);
-          }
+          for (int q = 0; q < 4; ++q) int8x4_to_half4(w[q], hv[2 * q], hv[2 * q + 1]);
           // 16 fp16 values = two 16-byte chunks of the 128-byte swizzled row
           const int half = c16 >> 2;
           const int j0 = (c16 & 3) * 2;

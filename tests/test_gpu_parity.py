@@ -91,6 +91,19 @@ def test_integer_inputs_bit_exact_bf16_mode0(dev):
     assert_parity(out, oracle.oracle_full(case), exact=True, what="int exact mode0")
 
 
+def test_int8_with_unit_scale_is_bit_exact(dev):
+    # integer queries and int8 keys with scale 1: every product and sum is exact
+    # in fp32, so the int8 path (convert, MMA, column scale, max) must match the
+    # oracle bit for bit, including decode and prefill rows
+    case = synth.make_case([1, 40, 1, 130], [5000, 700, 128, 1000], H_q=16, H_kv=2,
+                           layout="BBND", q_dtype=torch.float16, k_dtype=torch.int8,
+                           q_kind="int_small", k_kind="int8_full", scale_const=1.0, MB=40,
+                           seed=105)
+    out, err, _ = run_gpu(case, dev)
+    assert err == 0
+    assert_parity(out, oracle.oracle_full(case), exact=True, what="int8 unit scale")
+
+
 MATRIX = []
 for layout in ("BBND", "BNBD", "TND"):
     for kdt in ("fp16", "bf16", "int8"):
