@@ -75,6 +75,34 @@ def algorithmic_work(case):
             "bytes": total}
 
 
+def kernel_source_hash() -> str:
+    """Hash of the CUDA sources: an ncu traffic figure is only valid for the code it measured."""
+    import hashlib
+    h = hashlib.sha256()
+    d = os.path.join(ROOT, "block_score_gb300", "csrc")
+    for name in sorted(os.listdir(d)):
+        if name.endswith((".cu", ".cuh")):
+            with open(os.path.join(d, name), "rb") as f:
+                h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload_key: str):
+    """DRAM bytes per score-kernel launch from the committed ncu summary, if it
+    was taken on the current sources (else None)."""
+    path = os.path.join(ROOT, "profiles", "score_kernel_dram_traffic.txt")
+    try:
+        with open(path) as f:
+            for line in f:
+                parts = line.split()
+                if len(parts) >= 3 and not line.startswith("#") and parts[0] == workload_key:
+                    if parts[2] == kernel_source_hash():
+                        return float(parts[1])
+    except OSError:
+        pass
+    return None
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -210,11 +238,22 @@ def cpu_oracle_baseline(case, target_s: float = 12.0):
             "sample": sample, "sample_fraction": frac, "seconds": dt}
 
 
+def make_workload(args):
+    case = synth.config(args.workload)
+    if args.decode_subset:
+        case = synth.decode_subset(case)
+    return case
+
+
+def workload_key(args) -> str:
+    return f"cfg{args.workload}" + ("_decode" if args.decode_subset else "")
+
+
 def run_reference(args):
     ws, rank, _ = dist_env()
     if rank != 0:
         return 0
-    case = synth.config(args.workload)
+    case = make_workload(args)
     work = algorithmic_work(case)
     import oracle
     rows_total = case.H_q * case.T
@@ -243,7 +282,7 @@ def run_reference(args):
         "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": statistics.mean(times) * 1e3, "higher_is_better": False,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": config_block(case, args.workload),
+        "data": "synthetic", "config": config_block(case, workload_key(args)),
         "tflops": work["flops"] / per_call_s / 1e12,
         "k_cache_gbs": work["k_bytes"] / per_call_s / 1e9,
         "cpu_baseline": {"value": us, "unit": "us/call", "cores": threads, "kind": "oracle",
@@ -257,7 +296,7 @@ def run_reference(args):
 
 def config_block(case, workload):
     kb = algorithmic_work(case)["k_bytes"]
-    return {"workload": f"cfg{workload}:{case.name}", "B": case.B, "T": case.T,
+    return {"workload": f"{workload}:{case.name}", "B": case.B, "T": case.T,
             "H_q": case.H_q, "H_kv": case.H_kv, "D": case.D, "P": case.P, "MB": case.MB,
             "layout": case.layout, "k_dtype": DTYPE_NAME[case.key.dtype],
             "sparse_mode": case.sparse_mode, "init_blocks": case.init_blocks,
@@ -277,9 +316,11 @@ def run_ours(args):
     import block_score_gb300 as bs
     bs.load_library()
 
-    case = synth.config(args.workload)
+    case = make_workload(args)
     work = algorithmic_work(case)
     peaks = load_peaks()
+    if args.traffic is None:
+        args.traffic = recorded_traffic(workload_key(args))
     prep = bs.from_case(case, device)
     stream = torch.cuda.current_stream(device)
 
@@ -362,7 +403,7 @@ def run_ours(args):
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
         "dtype": DTYPE_NAME[case.query.dtype] if case.key.dtype != torch.int8 else "f16xi8",
         "data": "synthetic (seeded; shapes and length mix of the workload recipe)",
-        "config": config_block(case, args.workload),
+        "config": config_block(case, workload_key(args)),
         "tflops": tflops, "k_cache_gbs": kgbs,
         "frac_hbm": (work["bytes"] / call_s / 1e9) / peaks["hbm_gbs"],
         "frac_tensor": tflops / peaks["bf16_tflops"],
@@ -439,6 +480,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", type=int, default=DEFAULT_WORKLOAD, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--decode-subset", action="store_true",
+                    help="time only the single-token requests of the workload (cfg4)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--traffic", type=float, default=None,
                     help="DRAM bytes per launch of the score kernel from an ncu capture")
