@@ -1,7 +1,8 @@
 // C ABI of the block-score library: argument validation (the op's rules from
 // the torch API guide "CANN ops-transformer ... msa_index_score", sec. 3, 4,
 // 8.1 and 10), output shape (sec. 5 / 8.5), workspace sizing, TMA tensor maps
-// and the two launches (plan, score).  No device memory is allocated here.
+// and the launches (plan, tile-class score kernel, short-query score kernel).
+// No device memory is allocated here.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -91,6 +92,8 @@ msa_status_t validate(const msa_index_score_args* a) {
     if (!aligned(a->query, 16) || !aligned(a->key_cache, 16))
       return fail(MSA_ERR_INVALID_ARG, "query and key_cache must be 16-byte aligned");
     if (a->scale && !aligned(a->scale, 4)) return fail(MSA_ERR_INVALID_ARG, "scale must be 4-byte aligned");
+    if (a->scale && a->layout != MSA_LAYOUT_TND && !aligned(a->scale, 16))
+      return fail(MSA_ERR_UNSUPPORTED, "paged int8 scale must be 16-byte aligned");
   }
   return MSA_OK;
 }
@@ -134,10 +137,12 @@ msa_status_t fill_params(const msa_index_score_args* a, float* out, void* ws, ms
   p.H_kv = a->H_kv;
   p.g = g;
   p.np = msa::kTileRows / g;
+  p.np_short = g <= msa::kShortRows ? msa::kShortRows / g : 1;
   p.B = a->B;
   p.MB = a->MB;
   p.MBp = (int32_t)round16(a->MB);
   p.layout = (int32_t)a->layout;
+  p.k_int8 = a->k_dtype == MSA_I8 ? 1 : 0;
   p.sparse_mode = a->sparse_mode;
   p.init_blocks = a->init_blocks;
   p.local_blocks = a->local_blocks;
@@ -164,23 +169,26 @@ msa_status_t check_ws(const msa_index_score_args* a, void* ws, size_t bytes) {
 }
 
 msa_status_t make_maps(const msa_index_score_args* a, const msa::Params& p, CUtensorMap* tq,
-                       CUtensorMap* tk) {
+                       CUtensorMap* tk, CUtensorMap* tq_short, CUtensorMap* tk_short) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return fail(MSA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
   const CUtensorMapDataType qdt =
       a->q_dtype == MSA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-  {
-    // query [T, H_q, D]: dims (D, H_q, T); a box is (64, g, np) = one GQA group x np positions
+  // query [T, H_q, D]: dims (D, H_q, T); a box is (64, g, positions): one GQA
+  // group x a run of positions, 128-byte swizzled
+  auto qmap = [&](CUtensorMap* m, int positions, const char* what) -> msa_status_t {
     cuuint64_t dims[3] = {(cuuint64_t)a->D, (cuuint64_t)a->H_q, (cuuint64_t)a->T};
     cuuint64_t strides[2] = {(cuuint64_t)a->D * 2, (cuuint64_t)a->H_q * a->D * 2};
-    cuuint32_t box[3] = {64, (cuuint32_t)p.g, (cuuint32_t)p.np};
+    cuuint32_t box[3] = {64, (cuuint32_t)p.g, (cuuint32_t)positions};
     cuuint32_t es[3] = {1, 1, 1};
-    CUresult r = enc(tq, qdt, 3, const_cast<void*>(a->query), dims, strides, box, es,
+    CUresult r = enc(m, qdt, 3, const_cast<void*>(a->query), dims, strides, box, es,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS) return fail(MSA_ERR_CUDA, "query tensor map: CUresult %d", (int)r);
-  }
-  {
+    if (r != CUDA_SUCCESS) return fail(MSA_ERR_CUDA, "%s tensor map: CUresult %d", what, (int)r);
+    return MSA_OK;
+  };
+  // one 128-token key page of one kv head; dims ordered by increasing stride
+  auto kmap = [&](CUtensorMap* m, bool swizzle_int8, const char* what) -> msa_status_t {
     const bool i8 = a->k_dtype == MSA_I8;
     const cuuint64_t esz = i8 ? 1 : 2;
     const CUtensorMapDataType kdt = i8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : qdt;
@@ -205,11 +213,20 @@ msa_status_t make_maps(const msa_index_score_args* a, const msa::Params& p, CUte
       box[0] = bx; box[1] = 1; box[2] = 128; box[3] = 1;
     }
     cuuint32_t es[4] = {1, 1, 1, 1};
-    CUresult r = enc(tk, kdt, 4, const_cast<void*>(a->key_cache), dims, strides, box, es,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE,
-                     i8 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
-                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS) return fail(MSA_ERR_CUDA, "key tensor map: CUresult %d", (int)r);
+    const CUtensorMapSwizzle sw =
+        (!i8 || swizzle_int8) ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE;
+    CUresult r = enc(m, kdt, 4, const_cast<void*>(a->key_cache), dims, strides, box, es,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(MSA_ERR_CUDA, "%s tensor map: CUresult %d", what, (int)r);
+    return MSA_OK;
+  };
+  msa_status_t st;
+  if ((st = qmap(tq, p.np, "query")) != MSA_OK) return st;
+  if ((st = kmap(tk, false, "key")) != MSA_OK) return st;
+  if (tq_short) {
+    if ((st = qmap(tq_short, p.np_short, "short query")) != MSA_OK) return st;
+    if ((st = kmap(tk_short, true, "short key")) != MSA_OK) return st;
   }
   return MSA_OK;
 }
@@ -266,12 +283,16 @@ msa_status_t msa_index_score_run(const msa_index_score_args* args, float* out, v
   if (!out || !aligned(out, 16)) return fail(MSA_ERR_INVALID_ARG, "out must be a 16-byte aligned pointer");
   msa::Params p;
   if ((st = fill_params(args, out, workspace, p)) != MSA_OK) return st;
-  CUtensorMap tq, tk;
-  if ((st = make_maps(args, p, &tq, &tk)) != MSA_OK) return st;
+  // short-query requests exist only for int8 keys and when a query row group
+  // fits 32 MMA columns
+  const bool short_ok = args->k_dtype == MSA_I8 && p.g <= msa::kShortRows;
+  CUtensorMap tq, tk, tqs, tks;
+  if ((st = make_maps(args, p, &tq, &tk, short_ok ? &tqs : nullptr, &tks)) != MSA_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e = args->k_dtype == MSA_I8
-                      ? msa::launch_score_i8(&tq, &tk, p, s)
-                      : msa::launch_score_16(&tq, &tk, p, args->q_dtype == MSA_BF16, s);
+  const bool i8 = args->k_dtype == MSA_I8;
+  const bool bf16 = args->q_dtype == MSA_BF16;
+  cudaError_t e = i8 ? msa::launch_score_i8(&tq, &tk, p, s) : msa::launch_score_16(&tq, &tk, p, bf16, s);
+  if (e == cudaSuccess && short_ok) e = msa::launch_short_i8(&tqs, &tks, p, s);
   if (e != cudaSuccess) return cuda_fail(e, "score kernel launch");
   return MSA_OK;
 }

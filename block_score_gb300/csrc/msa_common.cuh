@@ -18,20 +18,30 @@ constexpr int kErrCuK = 0x04;
 constexpr int kErrBlockTable = 0x08;
 constexpr int kErrTimeout = 0x10;
 
-// Workspace layout: [PlanHeader | ReqInfo x B | int32 unit_prefix x (B+1)].
+// Requests are split into two classes, each consumed by its own kernel:
+//   class 0 ("tile" class): query tiles of floor(128/g) positions x g heads,
+//           QK^T with the query tile as the MMA's M side;
+//   class 1 ("short" class, int8 keys): Lq * g <= kShortRows, all query
+//           rows of the request as the MMA's N side against 128-token key
+//           pages (M side).
+constexpr int kShortRows = 32;
+
+// Workspace layout:
+//   [PlanHeader | ReqInfo x B | int32 prefix0 x (B+1) | int32 prefix1 x (B+1)]
+// Class-0 request records come first (schedule order), then class 1.
 struct PlanHeader {
-  int32_t counter;    // next unit to hand out (atomic)
-  int32_t n_units;    // total work units
-  int32_t n_req;      // entries of ReqInfo in schedule order
-  int32_t chunk;      // blocks per KV chunk (multiple of 8)
-  int32_t err;        // device error bits
-  int32_t pad[11];
+  int32_t counter[2];   // next unit of each class (atomic)
+  int32_t n_units[2];   // units of each class
+  int32_t n_req[2];     // request records of each class
+  int32_t chunk[2];     // blocks per KV chunk of each class (multiple of 8)
+  int32_t err;          // device error bits
+  int32_t pad[7];
 };
 static_assert(sizeof(PlanHeader) == 64, "header is 64 bytes");
 
 // One request in schedule order.  Its units are H_kv x ntiles x nchunks,
 // numbered kv-head-major, then query tiles from the last (most blocks) to the
-// first, then KV chunks.
+// first, then KV chunks.  Short-class requests have ntiles == 1.
 struct ReqInfo {
   int32_t b;         // original request index
   int32_t t0;        // first global query token (cu_seqlens_q[b])
@@ -45,16 +55,23 @@ struct ReqInfo {
 static_assert(sizeof(ReqInfo) == 32, "ReqInfo is 32 bytes");
 
 __host__ __device__ constexpr size_t workspace_bytes_for(int64_t B) {
-  return (sizeof(PlanHeader) + sizeof(ReqInfo) * (size_t)B + sizeof(int32_t) * (size_t)(B + 1) +
-          255) / 256 * 256;
+  return (sizeof(PlanHeader) + sizeof(ReqInfo) * (size_t)B +
+          2 * sizeof(int32_t) * (size_t)(B + 1) + 255) / 256 * 256;
+}
+
+__host__ __device__ inline const int32_t* plan_prefix(const uint8_t* ws, int B, int cls) {
+  return reinterpret_cast<const int32_t*>(ws + sizeof(PlanHeader) + sizeof(ReqInfo) * B) +
+         (cls ? (B + 1) : 0);
 }
 
 struct Params {
   int64_t T;
   int64_t NP;              // pages (paged) or T2 (TND)
-  int32_t H_q, H_kv, g, np;
+  int32_t H_q, H_kv, g, np;   // np: positions per class-0 tile = floor(128 / g)
+  int32_t np_short;            // positions the class-1 query box covers = floor(32 / g)
   int32_t B, MB, MBp;
   int32_t layout;          // 0 BBND, 1 BNBD, 2 TND
+  int32_t k_int8;          // keys are int8 (short-query class enabled)
   int32_t sparse_mode, init_blocks, local_blocks;
   int32_t num_sms;
   const int32_t* block_table;
@@ -92,6 +109,8 @@ cudaError_t launch_plan(const Params& p, cudaStream_t s);
 cudaError_t launch_score_16(const void* tmap_q, const void* tmap_k, const Params& p, bool bf16,
                             cudaStream_t s);
 cudaError_t launch_score_i8(const void* tmap_q, const void* tmap_k, const Params& p,
+                            cudaStream_t s);
+cudaError_t launch_short_i8(const void* tmap_q, const void* tmap_k, const Params& p,
                             cudaStream_t s);
 
 }  // namespace msa

@@ -47,7 +47,7 @@ __device__ int block_incl_scan(int v, int* s_warp) {
 }
 
 struct ReqScratch {
-  int Lq, L, t0, kbase, ntiles, nbc_max;
+  int Lq, L, t0, kbase, ntiles, nbc_max, cls;
 };
 
 __device__ ReqScratch read_request(const Params& p, int b, int& err) {
@@ -78,79 +78,100 @@ __device__ ReqScratch read_request(const Params& p, int b, int& err) {
   const int64_t nb = (L + kP - 1) / kP;
   if (nb > p.MB) err |= kErrKvLen;
   r.L = (int)(L > 0x7fffffff ? 0x7fffffff : L);
-  r.ntiles = cdiv(r.Lq, p.np);
+  // short class (int8 keys): every query row of the request fits the N side
+  // of one MMA; 16-bit keys stream through the tile kernel at HBM speed
+  r.cls = (p.k_int8 && r.Lq > 0 && (int64_t)r.Lq * p.g <= kShortRows) ? 1 : 0;
+  r.ntiles = r.cls ? 1 : cdiv(r.Lq, p.np);
   // the last query row sees the most blocks: q_pos = L - 1 in both modes
   r.nbc_max = L > 0 ? (int)(nb < p.MB ? nb : p.MB) : 0;
   return r;
 }
 
+__device__ int chunk_for(unsigned long long work, int num_sms, int MBp) {
+  // about 16 units per SM on average, never below 8 blocks (the tail of a
+  // call is then a fraction of one short unit)
+  const unsigned long long target = (unsigned long long)num_sms * 16ull;
+  unsigned long long c = (work + target - 1) / target;
+  if (c < 8) c = 8;
+  c = (c + 7) / 8 * 8;
+  if (c > (unsigned long long)MBp) c = (unsigned long long)MBp;
+  return (int)c;
+}
+
 __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const Params p) {
-  // Let the score kernel start its prologue (barrier init, TMEM allocation);
-  // it waits for this grid's completion before it reads the plan.
+  // Let the score kernels start their prologue (barrier init, TMEM
+  // allocation); they wait for this grid's completion before reading the plan.
   asm volatile("griddepcontrol.launch_dependents;");
 
   __shared__ int s_warp[32];
-  __shared__ unsigned long long s_work;
+  __shared__ unsigned long long s_work[2];
   __shared__ int s_err;
   __shared__ int s_key[kPlanThreads];
+  __shared__ int s_cls[kPlanThreads];
   __shared__ int s_units[kPlanThreads];
-  __shared__ int s_tot;
+  __shared__ int s_tot[2];
+  __shared__ int s_nreq[2];
 
   PlanHeader* hdr = reinterpret_cast<PlanHeader*>(p.ws);
   ReqInfo* req = reinterpret_cast<ReqInfo*>(p.ws + sizeof(PlanHeader));
-  int32_t* prefix = reinterpret_cast<int32_t*>(p.ws + sizeof(PlanHeader) + sizeof(ReqInfo) * p.B);
+  int32_t* prefix0 = const_cast<int32_t*>(plan_prefix(p.ws, p.B, 0));
+  int32_t* prefix1 = const_cast<int32_t*>(plan_prefix(p.ws, p.B, 1));
   const int tid = threadIdx.x;
 
   if (tid == 0) {
-    s_work = 0ull;
+    s_work[0] = s_work[1] = 0ull;
     s_err = 0;
+    s_nreq[0] = s_nreq[1] = 0;
   }
   __syncthreads();
 
-  // pass 1: read every request once, validate, and sum the work
-  // (blocks x kv heads x tiles, an upper bound that only sets the chunk size)
+  // pass 1: read every request once, validate, sum the work of each class
+  // (blocks x kv heads x tiles, an upper bound that only sets the chunk sizes)
   const bool small = p.B <= kPlanThreads;
   int err = 0;
-  unsigned long long work = 0;
+  unsigned long long work[2] = {0ull, 0ull};
+  int nreq[2] = {0, 0};
   ReqScratch mine{};
   int my_sl = 0;
   for (int b = tid; b < p.B; b += kPlanThreads) {
     ReqScratch r = read_request(p, b, err);
-    work += (unsigned long long)p.H_kv * r.ntiles * r.nbc_max;
+    work[r.cls] += (unsigned long long)p.H_kv * r.ntiles * r.nbc_max;
+    nreq[r.cls] += 1;
     if (small) {
       mine = r;
       my_sl = p.start_loc[b];
     }
   }
   if (err) atomicOr(&s_err, err);
-  if (work) atomicAdd(&s_work, work);
+  if (work[0]) atomicAdd(&s_work[0], work[0]);
+  if (work[1]) atomicAdd(&s_work[1], work[1]);
+  if (nreq[0]) atomicAdd(&s_nreq[0], nreq[0]);
+  if (nreq[1]) atomicAdd(&s_nreq[1], nreq[1]);
   __syncthreads();
-
-  // chunk size: about 16 units per SM on average, never below 8 blocks (the
-  // tail of a call is then a fraction of one short unit)
-  const unsigned long long target = (unsigned long long)p.num_sms * 16ull;
-  unsigned long long c = (s_work + target - 1) / target;
-  if (c < 8) c = 8;
-  c = (c + 7) / 8 * 8;
-  if (c > (unsigned long long)p.MBp) c = (unsigned long long)p.MBp;
-  const int chunk = (int)c;
+  const int chunk0 = chunk_for(s_work[0], p.num_sms, p.MBp);
+  const int chunk1 = chunk_for(s_work[1], p.num_sms, p.MBp);
+  const int n0 = s_nreq[0];
 
   if (small) {
-    // longest-first order by the cost of each request's largest unit; the
-    // rank of a request is the number of requests that go before it
-    int key = -1, units = 0, nchunks = 1;
+    // schedule order: class 0 first, then class 1; inside a class longest
+    // first by the cost of the request's largest unit; the rank of a
+    // request is the number of requests that go before it
+    int key = -1, cls = 0, units = 0, nchunks = 1;
     if (tid < p.B) {
+      cls = mine.cls;
+      const int chunk = cls ? chunk1 : chunk0;
       nchunks = mine.nbc_max > 0 ? cdiv(mine.nbc_max, chunk) : 1;
       units = mine.Lq > 0 ? p.H_kv * mine.ntiles * nchunks : 0;
       if (mine.Lq > 0) key = mine.nbc_max < chunk ? mine.nbc_max : chunk;
       s_key[tid] = key;
+      s_cls[tid] = cls;
     }
     __syncthreads();
+    int rank = 0;
     if (tid < p.B) {
-      int rank = 0;
       for (int j = 0; j < p.B; ++j) {
-        const int kj = s_key[j];
-        rank += (kj > key) || (kj == key && j < tid);
+        const int kj = s_key[j], cj = s_cls[j];
+        rank += (cj < cls) || (cj == cls && ((kj > key) || (kj == key && j < tid)));
       }
       ReqInfo ri;
       ri.b = tid;
@@ -165,49 +186,77 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const Params p) {
       s_units[rank] = units;
     }
     __syncthreads();
-    const int v = tid < p.B ? s_units[tid] : 0;
-    const int incl = block_incl_scan(v, s_warp);
-    if (tid < p.B) prefix[tid + 1] = incl;
-    if (tid == kPlanThreads - 1) s_tot = incl;
+    // per-class inclusive scans over the ranked slots
+    const int v0 = tid < n0 ? s_units[tid] : 0;
+    const int incl0 = block_incl_scan(v0, s_warp);
+    if (tid < n0) prefix0[tid + 1] = incl0;
+    if (tid == kPlanThreads - 1) s_tot[0] = incl0;
+    const int n1 = p.B - n0;
+    const int v1 = tid < n1 ? s_units[n0 + tid] : 0;
+    const int incl1 = block_incl_scan(v1, s_warp);
+    if (tid < n1) prefix1[tid + 1] = incl1;
+    if (tid == kPlanThreads - 1) s_tot[1] = incl1;
     __syncthreads();
   } else {
-    // large batches: natural order, prefix sum over slices of kPlanThreads
-    int carry = 0;
+    // large batches: natural order inside each class; compaction by a scan of
+    // the class flags, then per-class unit prefix sums
+    int carry_slot[2] = {0, 0}, carry_units[2] = {0, 0};
     for (int base = 0; base < p.B; base += kPlanThreads) {
       const int b = base + tid;
-      int units = 0;
-      if (b < p.B) {
+      ReqScratch r{};
+      int units = 0, nchunks = 1;
+      const bool live = b < p.B;
+      if (live) {
         int e2 = 0;
-        ReqScratch r = read_request(p, b, e2);
-        const int nchunks = r.nbc_max > 0 ? cdiv(r.nbc_max, chunk) : 1;
+        r = read_request(p, b, e2);
+        const int chunk = r.cls ? chunk1 : chunk0;
+        nchunks = r.nbc_max > 0 ? cdiv(r.nbc_max, chunk) : 1;
         units = r.Lq > 0 ? p.H_kv * r.ntiles * nchunks : 0;
-        ReqInfo ri;
-        ri.b = b;
-        ri.t0 = r.t0;
-        ri.Lq = r.Lq;
-        ri.L = r.L;
-        ri.ntiles = r.ntiles;
-        ri.nchunks = nchunks;
-        ri.kbase = r.kbase;
-        ri.sl = p.start_loc[b];
-        req[b] = ri;
       }
-      const int incl = block_incl_scan(units, s_warp);
-      if (b < p.B) prefix[b + 1] = carry + incl;
-      if (tid == kPlanThreads - 1) s_tot = incl;
-      __syncthreads();
-      carry += s_tot;
-      __syncthreads();
+      for (int c = 0; c < 2; ++c) {
+        const int mine_c = live && r.cls == c;
+        const int slot_incl = block_incl_scan(mine_c, s_warp);
+        const int units_incl = block_incl_scan(mine_c ? units : 0, s_warp);
+        if (mine_c) {
+          const int slot = carry_slot[c] + slot_incl - 1;
+          ReqInfo ri;
+          ri.b = b;
+          ri.t0 = r.t0;
+          ri.Lq = r.Lq;
+          ri.L = r.L;
+          ri.ntiles = r.ntiles;
+          ri.nchunks = nchunks;
+          ri.kbase = r.kbase;
+          ri.sl = p.start_loc[b];
+          req[(c ? n0 : 0) + slot] = ri;
+          (c ? prefix1 : prefix0)[slot + 1] = carry_units[c] + units_incl;
+        }
+        if (tid == kPlanThreads - 1) {
+          s_tot[0] = slot_incl;
+          s_tot[1] = units_incl;
+        }
+        __syncthreads();
+        carry_slot[c] += s_tot[0];
+        carry_units[c] += s_tot[1];
+        __syncthreads();
+      }
     }
-    if (tid == 0) s_tot = carry;
+    if (tid == 0) {
+      s_tot[0] = carry_units[0];
+      s_tot[1] = carry_units[1];
+    }
     __syncthreads();
   }
   if (tid == 0) {
-    prefix[0] = 0;
-    hdr->counter = 0;
-    hdr->n_units = s_tot;
-    hdr->n_req = p.B;
-    hdr->chunk = chunk;
+    prefix0[0] = 0;
+    prefix1[0] = 0;
+    hdr->counter[0] = hdr->counter[1] = 0;
+    hdr->n_units[0] = s_tot[0];
+    hdr->n_units[1] = s_tot[1];
+    hdr->n_req[0] = n0;
+    hdr->n_req[1] = p.B - n0;
+    hdr->chunk[0] = chunk0;
+    hdr->chunk[1] = chunk1;
     hdr->err = s_err;
   }
 }

@@ -27,6 +27,7 @@
 
 #include "msa_common.cuh"
 #include "msa_ptx.cuh"
+#include "msa_units.cuh"
 
 namespace msa {
 
@@ -47,24 +48,17 @@ struct ScoreCfg<true> {
   static constexpr int kThreads = 352;
 };
 
-constexpr int kEpiWarp0 = 3;             // first epilogue warp
-constexpr int kCvtWarp0 = 7;             // first int8 converter warp
-constexpr int kLead = 4;                 // blocks before the end of a unit at which the next is claimed
 
 constexpr int kQBufs = 2;
 constexpr int kAcc = 4;
-constexpr int kSched = 4;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kTileBytes = 128 * 128 * 2;   // one 16-bit 128x128 operand tile
-constexpr uint32_t kHalfBytes = kTileBytes / 2;  // 64-element (128-byte) K half
-constexpr uint32_t kRawBytes = 128 * 128;        // one int8 page tile
 
 template <bool KI8>
 struct SmemLayout {
   static constexpr uint32_t q_off = 0;
   static constexpr uint32_t k_off = q_off + kQBufs * kTileBytes;
   static constexpr uint32_t raw_off = k_off + ScoreCfg<KI8>::kStages * kTileBytes;
-  static constexpr uint32_t scale_off = raw_off + ScoreCfg<KI8>::kRawStages * kRawBytes;
+  static constexpr uint32_t scale_off = raw_off + ScoreCfg<KI8>::kRawStages * kRawStride;
   static constexpr uint32_t scale_bytes = KI8 ? kAcc * 128 * 4 : 0;
   static constexpr uint32_t ring_off = scale_off + scale_bytes;        // UnitDesc x kSched
   static constexpr uint32_t bar_off = ring_off + kSched * sizeof(UnitDesc);
@@ -76,11 +70,6 @@ struct SmemLayout {
   static constexpr uint32_t bytes = end + 1024;                        // + alignment slack
 };
 
-__device__ __forceinline__ uint64_t desc_at(uint32_t tile_base, int k) {
-  // k-th 16-element slice of a 128-deep K-major tile: halves of 64 elements
-  // are separate 16 KiB swizzled tiles; inside a half, slices are 32 bytes apart.
-  return smem_desc_sw128(tile_base + (uint32_t)(k >> 2) * kHalfBytes + (uint32_t)(k & 3) * 32u);
-}
 
 // Max of the first (climit + 1) of 128 values (all if climit >= 127).
 __device__ __forceinline__ float masked_row_max(const float (&x)[128], int climit) {
@@ -105,71 +94,6 @@ __device__ __forceinline__ float masked_row_max(const float (&x)[128], int climi
     }
   }
   return fmax3(a0, a1, fmaxf(a2, a3));
-}
-
-// Four signed int8 values (one 32-bit word, little-endian) to four fp16
-// values, exactly: x + 128 is placed in the low mantissa byte of 1024.0
-// (bit pattern 0x64xx, whose unit in the last place is 1), and 1152 = 1024 + 128
-// is subtracted; every step is exact for |x| <= 128.
-__device__ __forceinline__ void int8x4_to_half4(uint32_t w, uint32_t& lo, uint32_t& hi) {
-  const uint32_t u = w ^ 0x80808080u;                      // bytes x + 128 in [0, 255]
-  const uint32_t a = __byte_perm(u, 0x64646464u, 0x4140);  // (1024 + u0, 1024 + u1)
-  const uint32_t b = __byte_perm(u, 0x64646464u, 0x4342);  // (1024 + u2, 1024 + u3)
-  const __half2 bias = __half2half2(__ushort_as_half((unsigned short)0x6480));   // 1152.0
-  const __half2 ra = __hsub2(*reinterpret_cast<const __half2*>(&a), bias);
-  const __half2 rb = __hsub2(*reinterpret_cast<const __half2*>(&b), bias);
-  lo = *reinterpret_cast<const uint32_t*>(&ra);
-  hi = *reinterpret_cast<const uint32_t*>(&rb);
-}
-
-// K page tile load.  The tensor map's dimensions are ordered by increasing
-// stride: BNBD (D, P, H_kv, NP); BBND (D, H_kv, P, NP); TND (D, H_kv, T2, 1).
-__device__ __forceinline__ void tma_k(uint32_t dst, const CUtensorMap* m, uint32_t bar, int x,
-                                      int tok, int hk, int page, int layout, uint64_t pol) {
-  if (layout == 1)
-    tma_load_4d(dst, m, bar, x, tok, hk, page, pol);
-  else
-    tma_load_4d(dst, m, bar, x, hk, tok, page, pol);
-}
-
-// Build the descriptor of unit u from the plan (scheduler thread only).
-__device__ __forceinline__ void make_unit(const Params& p, const PlanHeader* hdr,
-                                          const ReqInfo* req, const int32_t* prefix, int n_units,
-                                          int chunk, int u, UnitDesc& d) {
-  d.live = 0;
-  if (u >= n_units) return;
-  // request r: last r with prefix[r] <= u
-  int lo = 0, hi = hdr->n_req - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (__ldg(prefix + mid) <= u) lo = mid; else hi = mid - 1;
-  }
-  const ReqInfo ri = req[lo];
-  const int ul = u - __ldg(prefix + lo);
-  const int per_hk = ri.ntiles * ri.nchunks;
-  const int hk = ul / per_hk;
-  const int rem = ul - hk * per_hk;
-  const int tile_rank = rem / ri.nchunks;
-  const int ch = rem - tile_rank * ri.nchunks;
-  const int tile = ri.ntiles - 1 - tile_rank;
-  const int i0 = tile * p.np;
-  const int npos = min(p.np, ri.Lq - i0);
-  const int i_last = i0 + npos - 1;
-  const int lim_last = p.sparse_mode == 3 ? ri.L - ri.Lq + i_last : ri.L - 1;
-  const int nbc = (ri.L > 0 && lim_last >= 0) ? min(p.MB, lim_last / kP + 1) : 0;
-  d.live = 1;
-  d.b = ri.b;
-  d.hk = hk;
-  d.t0 = ri.t0 + i0;
-  d.npos = npos;
-  d.i0 = i0;
-  d.Lq = ri.Lq;
-  d.L = ri.L;
-  d.c0 = ch * chunk;
-  d.c1 = (ch == ri.nchunks - 1) ? p.MBp : d.c0 + chunk;
-  d.b1 = max(d.c0, min(d.c1, nbc));
-  d.kbase = ri.kbase;
-  d.sl = ri.sl;
 }
 
 template <bool KI8, bool BF16>
@@ -212,6 +136,7 @@ __global__ void __launch_bounds__(ScoreCfg<KI8>::kThreads, 1)
   // readers of each unit descriptor: producer, MMA, 4 epilogue warps (+ 4 converter warps)
   constexpr int kConsumers = KI8 ? 10 : 6;
 
+  asm volatile("griddepcontrol.launch_dependents;");
   if (threadIdx.x == 0) {
     for (int i = 0; i < kSched; ++i) {
       mbar_init(b_sched_full + 8 * i, 1);
@@ -258,18 +183,21 @@ __global__ void __launch_bounds__(ScoreCfg<KI8>::kThreads, 1)
 
   PlanHeader* hdr = reinterpret_cast<PlanHeader*>(p.ws);
   const ReqInfo* req = reinterpret_cast<const ReqInfo*>(p.ws + sizeof(PlanHeader));
-  const int32_t* prefix =
-      reinterpret_cast<const int32_t*>(p.ws + sizeof(PlanHeader) + sizeof(ReqInfo) * p.B);
+  const int32_t* prefix = plan_prefix(p.ws, p.B, 0);
   WaitCtl ctl{abort_flag, &hdr->err, p.wait_limit_ns};
+  const int n_units0 = *reinterpret_cast<volatile int*>(&hdr->n_units[0]);
 
-  if (warp == 0) {
+  if (n_units0 == 0) {
+    // no tile-class requests in this call
+  } else if (warp == 0) {
     // -------------------------------------------------------- scheduler --
     // Claims one unit ahead: the first at once, each later one when the
     // producer is kLead blocks from the end of its current unit, so a CTA
     // never sits on work another CTA could be doing.
     if (lane == 0) {
-      const int n_units = *reinterpret_cast<volatile int*>(&hdr->n_units);
-      const int chunk = *reinterpret_cast<volatile int*>(&hdr->chunk);
+      const int n_units = *reinterpret_cast<volatile int*>(&hdr->n_units[0]);
+      const int chunk = *reinterpret_cast<volatile int*>(&hdr->chunk[0]);
+      const int n_req = *reinterpret_cast<volatile int*>(&hdr->n_req[0]);
       uint32_t ss = 0, sph = 0, rph = 0;
       for (bool first = true;; first = false) {
         if (!first) {
@@ -277,7 +205,7 @@ __global__ void __launch_bounds__(ScoreCfg<KI8>::kThreads, 1)
           rph ^= 1;
         }
         UnitDesc d;
-        make_unit(p, hdr, req, prefix, n_units, chunk, atomicAdd(&hdr->counter, 1), d);
+        make_unit(p, req, prefix, n_req, n_units, chunk, p.np, atomicAdd(&hdr->counter[0], 1), d);
         if (!mbar_wait(b_sched_empty + 8 * ss, sph ^ 1, ctl)) break;
         ring[ss] = d;
         mbar_arrive(b_sched_full + 8 * ss);
@@ -342,9 +270,14 @@ __global__ void __launch_bounds__(ScoreCfg<KI8>::kThreads, 1)
           if constexpr (KI8) {
             if (!mbar_wait(b_raw_empty + 8 * ks, kph ^ 1, ctl)) { ok = false; break; }
             raw_page[ks] = paged ? page : tok;
-            mbar_arrive_expect_tx(b_raw_full + 8 * ks, kRawBytes);
-            tma_k(sbase + L::raw_off + ks * kRawBytes, &tm_k, b_raw_full + 8 * ks, 0, tok, d.hk,
-                  page, p.layout, pol_k);
+            const uint32_t rdst = sbase + L::raw_off + ks * kRawStride;
+            // the page's 128 scales ride along with the int8 tile (one bulk copy)
+            const bool with_scale = paged && (int64_t)page < p.NP;
+            mbar_arrive_expect_tx(b_raw_full + 8 * ks, kRawBytes + (with_scale ? kRawScaleBytes : 0u));
+            tma_k(rdst, &tm_k, b_raw_full + 8 * ks, 0, tok, d.hk, page, p.layout, pol_k);
+            if (with_scale)
+              bulk_load(rdst + kRawBytes, p.scale + ((int64_t)page * p.H_kv + d.hk) * kP,
+                        kRawScaleBytes, b_raw_full + 8 * ks);
             ++n_k;
             if (++ks == R) { ks = 0; kph ^= 1; }
           } else {
@@ -542,14 +475,33 @@ __global__ void __launch_bounds__(ScoreCfg<KI8>::kThreads, 1)
       for (int beta = d.c0; beta < d.b1; ++beta) {
         if (!warp_wait(b_raw_full + 8 * rs, rph, ctl)) { ok = false; break; }
         if (!warp_wait(b_k_empty + 8 * ks, kph ^ 1, ctl)) { ok = false; break; }
-        const uint8_t* src = smem + L::raw_off + rs * kRawBytes;
+        const uint8_t* src = smem + L::raw_off + rs * kRawStride;
+        // this thread's token scale: from the stage (paged) or, for packed keys,
+        // a global load issued now so that it overlaps the conversion
+        const int page = raw_page[rs];
+        float sv = 0.f;
+        if (p.layout == 2) {
+          const int64_t row = (int64_t)page + ct;      // page holds the first key row here
+          if (row < (int64_t)d.kbase + d.L && row < p.NP) sv = __ldg(p.scale + row * p.H_kv + d.hk);
+        } else if (page >= 0 && (int64_t)page < p.NP) {
+          sv = reinterpret_cast<const float*>(src + kRawBytes)[ct];
+        }
         uint8_t* dst = smem + L::k_off + ks * kTileBytes;
+        // all eight 16-byte chunks of this thread are loaded before any store,
+        // so the loads overlap (the compiler cannot reorder them past stores
+        // into the same shared memory)
+        int4 raw[8];
 #pragma unroll
         for (int it = 0; it < 8; ++it) {
           const int id = ct + 128 * it;           // 16-byte chunk of the int8 page
+          raw[it] = *reinterpret_cast<const int4*>(src + (id >> 3) * 128 + (id & 7) * 16);
+        }
+#pragma unroll
+        for (int it = 0; it < 8; ++it) {
+          const int id = ct + 128 * it;
           const int row = id >> 3, c16 = id & 7;
-          const int4 raw = *reinterpret_cast<const int4*>(src + row * 128 + c16 * 16);
-          const uint32_t w[4] = {(uint32_t)raw.x, (uint32_t)raw.y, (uint32_t)raw.z, (uint32_t)raw.w};
+          const uint32_t w[4] = {(uint32_t)raw[it].x, (uint32_t)raw[it].y, (uint32_t)raw[it].z,
+                                 (uint32_t)raw[it].w};
           uint32_t hv[8];
 #pragma unroll
           for (int q = 0; q < 4; ++q) int8x4_to_half4(w[q], hv[2 * q], hv[2 * q + 1]);
@@ -562,7 +514,6 @@ __global__ void __launch_bounds__(ScoreCfg<KI8>::kThreads, 1)
           *reinterpret_cast<uint4*>(rowp + (((j0 + 1) ^ (row & 7)) << 4)) =
               make_uint4(hv[4], hv[5], hv[6], hv[7]);
         }
-        const int page = raw_page[rs];
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
@@ -573,13 +524,6 @@ __global__ void __launch_bounds__(ScoreCfg<KI8>::kThreads, 1)
         if (++ks == S) { ks = 0; kph ^= 1; }
         // per-token scale of this block for the epilogue (slot follows the accumulator ring)
         if (!warp_wait(b_sc_empty + 8 * ab, aph ^ 1, ctl)) { ok = false; break; }
-        float sv = 0.f;
-        if (p.layout == 2) {
-          const int64_t row = (int64_t)page + ct;      // page holds the first key row here
-          if (row < (int64_t)d.kbase + d.L && row < p.NP) sv = __ldg(p.scale + row * p.H_kv + d.hk);
-        } else if (page >= 0 && (int64_t)page < p.NP) {
-          sv = __ldg(p.scale + ((int64_t)page * p.H_kv + d.hk) * kP + ct);
-        }
         scale_s[ab * 128 + ct] = sv;
         __syncwarp();
         if (lane == 0) mbar_arrive(b_sc_full + 8 * ab);

@@ -1,0 +1,97 @@
+// Device helpers shared by the two score kernels: int8 -> fp16 conversion,
+// K page TMA loads, and decoding a work unit from the plan.
+#pragma once
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_fp16.h>
+
+#include "msa_common.cuh"
+#include "msa_ptx.cuh"
+
+namespace msa {
+
+// warp roles and pipeline constants shared by both score kernels
+constexpr int kEpiWarp0 = 3;             // first epilogue warp
+constexpr int kCvtWarp0 = 7;             // first int8 converter warp
+constexpr int kLead = 4;                 // blocks before the end of a unit at which the next is claimed
+constexpr int kSched = 4;
+constexpr uint32_t kTileBytes = 128 * 128 * 2;   // one 16-bit 128x128 operand tile
+constexpr uint32_t kHalfBytes = kTileBytes / 2;  // 64-element (128-byte) K half
+constexpr uint32_t kRawBytes = 128 * 128;        // one int8 page tile
+constexpr uint32_t kRawScaleBytes = 128 * 4;     // the page's per-token scales (paged layouts)
+constexpr uint32_t kRawStride = kRawBytes + 1024;  // int8 tile + scales, 1 KiB aligned
+
+__device__ __forceinline__ uint64_t desc_at(uint32_t tile_base, int k) {
+  // k-th 16-element slice of a 128-deep K-major tile: halves of 64 elements
+  // are separate 16 KiB swizzled tiles; inside a half, slices are 32 bytes apart.
+  return smem_desc_sw128(tile_base + (uint32_t)(k >> 2) * kHalfBytes + (uint32_t)(k & 3) * 32u);
+}
+
+// Four signed int8 values (one 32-bit word, little-endian) to four fp16
+// values, exactly: x + 128 is placed in the low mantissa byte of 1024.0
+// (bit pattern 0x64xx, whose unit in the last place is 1), and 1152 = 1024 + 128
+// is subtracted; every step is exact for |x| <= 128.
+__device__ __forceinline__ void int8x4_to_half4(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  const uint32_t u = w ^ 0x80808080u;                      // bytes x + 128 in [0, 255]
+  const uint32_t a = __byte_perm(u, 0x64646464u, 0x4140);  // (1024 + u0, 1024 + u1)
+  const uint32_t b = __byte_perm(u, 0x64646464u, 0x4342);  // (1024 + u2, 1024 + u3)
+  const __half2 bias = __half2half2(__ushort_as_half((unsigned short)0x6480));   // 1152.0
+  const __half2 ra = __hsub2(*reinterpret_cast<const __half2*>(&a), bias);
+  const __half2 rb = __hsub2(*reinterpret_cast<const __half2*>(&b), bias);
+  lo = *reinterpret_cast<const uint32_t*>(&ra);
+  hi = *reinterpret_cast<const uint32_t*>(&rb);
+}
+
+// K page tile load.  The tensor map's dimensions are ordered by increasing
+// stride: BNBD (D, P, H_kv, NP); BBND (D, H_kv, P, NP); TND (D, H_kv, T2, 1).
+__device__ __forceinline__ void tma_k(uint32_t dst, const CUtensorMap* m, uint32_t bar, int x,
+                                      int tok, int hk, int page, int layout, uint64_t pol) {
+  if (layout == 1)
+    tma_load_4d(dst, m, bar, x, tok, hk, page, pol);
+  else
+    tma_load_4d(dst, m, bar, x, hk, tok, page, pol);
+}
+
+// Build the descriptor of unit u of one request class from the plan
+// (scheduler thread only).  `req` / `prefix` point at that class's records and
+// unit prefix sums; `np` is the number of query positions per tile.
+__device__ __forceinline__ void make_unit(const Params& p, const ReqInfo* req,
+                                          const int32_t* prefix, int n_req, int n_units,
+                                          int chunk, int np, int u, UnitDesc& d) {
+  d.live = 0;
+  if (u >= n_units) return;
+  // request r: last r with prefix[r] <= u
+  int lo = 0, hi = n_req - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (__ldg(prefix + mid) <= u) lo = mid; else hi = mid - 1;
+  }
+  const ReqInfo ri = req[lo];
+  const int ul = u - __ldg(prefix + lo);
+  const int per_hk = ri.ntiles * ri.nchunks;
+  const int hk = ul / per_hk;
+  const int rem = ul - hk * per_hk;
+  const int tile_rank = rem / ri.nchunks;
+  const int ch = rem - tile_rank * ri.nchunks;
+  const int tile = ri.ntiles - 1 - tile_rank;
+  const int i0 = tile * np;
+  const int npos = min(np, ri.Lq - i0);
+  const int i_last = i0 + npos - 1;
+  const int lim_last = p.sparse_mode == 3 ? ri.L - ri.Lq + i_last : ri.L - 1;
+  const int nbc = (ri.L > 0 && lim_last >= 0) ? min(p.MB, lim_last / kP + 1) : 0;
+  d.live = 1;
+  d.b = ri.b;
+  d.hk = hk;
+  d.t0 = ri.t0 + i0;
+  d.npos = npos;
+  d.i0 = i0;
+  d.Lq = ri.Lq;
+  d.L = ri.L;
+  d.c0 = ch * chunk;
+  d.c1 = (ch == ri.nchunks - 1) ? p.MBp : d.c0 + chunk;
+  d.b1 = max(d.c0, min(d.c1, nbc));
+  d.kbase = ri.kbase;
+  d.sl = ri.sl;
+}
+
+}  // namespace msa

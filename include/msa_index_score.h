@@ -171,7 +171,7 @@ msa_status_t msa_index_score_run(const msa_index_score_args *args, float *out, v
  *   not readable through msa_get_device_error.
  */
 #define MSA_NOALLOC_MAX_BATCH 1024
-#define MSA_NOALLOC_WORKSPACE_BYTES 37120
+#define MSA_NOALLOC_WORKSPACE_BYTES 41216
 msa_status_t msa_index_score_noalloc(const msa_index_score_args *args, float *out,
                                      msa_stream_t stream);
 
