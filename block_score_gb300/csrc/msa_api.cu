@@ -168,6 +168,57 @@ msa_status_t check_ws(const msa_index_score_args* a, void* ws, size_t bytes) {
   return MSA_OK;
 }
 
+// Encoded tensor maps of recent calls, per host thread: re-encoding costs
+// microseconds of host time per launch, and repeated calls on the same
+// buffers (a decode loop) reuse the same maps.
+struct MapKey {
+  const void* base;
+  int32_t dtype, rank, swizzle;
+  cuuint64_t dims[5], strides[4];
+  cuuint32_t box[5];
+};
+
+CUresult encode_cached(EncodeTiledFn enc, CUtensorMap* m, CUtensorMapDataType dt, cuuint32_t rank,
+                       void* base, const cuuint64_t* dims, const cuuint64_t* strides,
+                       const cuuint32_t* box, const cuuint32_t* es, CUtensorMapSwizzle sw) {
+  constexpr int kEntries = 16;
+  struct Entry {
+    MapKey key;
+    CUtensorMap map;
+    uint64_t stamp;
+  };
+  thread_local Entry cache[kEntries];
+  thread_local uint64_t clock = 0;
+  MapKey k;
+  std::memset(&k, 0, sizeof k);
+  k.base = base;
+  k.dtype = (int32_t)dt;
+  k.rank = (int32_t)rank;
+  k.swizzle = (int32_t)sw;
+  for (cuuint32_t i = 0; i < rank; ++i) {
+    k.dims[i] = dims[i];
+    k.box[i] = box[i];
+    if (i + 1 < rank) k.strides[i] = strides[i];
+  }
+  int victim = 0;
+  for (int i = 0; i < kEntries; ++i) {
+    if (cache[i].stamp && std::memcmp(&cache[i].key, &k, sizeof k) == 0) {
+      cache[i].stamp = ++clock;
+      *m = cache[i].map;
+      return CUDA_SUCCESS;
+    }
+    if (cache[i].stamp < cache[victim].stamp) victim = i;
+  }
+  CUresult r = enc(m, dt, rank, base, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r == CUDA_SUCCESS) {
+    cache[victim].key = k;
+    cache[victim].map = *m;
+    cache[victim].stamp = ++clock;
+  }
+  return r;
+}
+
 msa_status_t make_maps(const msa_index_score_args* a, const msa::Params& p, CUtensorMap* tq,
                        CUtensorMap* tk, CUtensorMap* tq_short, CUtensorMap* tk_short) {
   EncodeTiledFn enc = encode_fn();
@@ -181,9 +232,8 @@ msa_status_t make_maps(const msa_index_score_args* a, const msa::Params& p, CUte
     cuuint64_t strides[2] = {(cuuint64_t)a->D * 2, (cuuint64_t)a->H_q * a->D * 2};
     cuuint32_t box[3] = {64, (cuuint32_t)p.g, (cuuint32_t)positions};
     cuuint32_t es[3] = {1, 1, 1};
-    CUresult r = enc(m, qdt, 3, const_cast<void*>(a->query), dims, strides, box, es,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    CUresult r = encode_cached(enc, m, qdt, 3, const_cast<void*>(a->query), dims, strides, box, es,
+                               CU_TENSOR_MAP_SWIZZLE_128B);
     if (r != CUDA_SUCCESS) return fail(MSA_ERR_CUDA, "%s tensor map: CUresult %d", what, (int)r);
     return MSA_OK;
   };
@@ -215,9 +265,8 @@ msa_status_t make_maps(const msa_index_score_args* a, const msa::Params& p, CUte
     cuuint32_t es[4] = {1, 1, 1, 1};
     const CUtensorMapSwizzle sw =
         (!i8 || swizzle_int8) ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE;
-    CUresult r = enc(m, kdt, 4, const_cast<void*>(a->key_cache), dims, strides, box, es,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    CUresult r = encode_cached(enc, m, kdt, 4, const_cast<void*>(a->key_cache), dims, strides,
+                               box, es, sw);
     if (r != CUDA_SUCCESS) return fail(MSA_ERR_CUDA, "%s tensor map: CUresult %d", what, (int)r);
     return MSA_OK;
   };
@@ -259,36 +308,24 @@ msa_status_t msa_index_score_workspace_size(const msa_index_score_args* args, si
   return MSA_OK;
 }
 
-msa_status_t msa_index_score_plan(const msa_index_score_args* args, void* workspace,
-                                  size_t workspace_bytes, msa_stream_t stream) {
-  g_msg[0] = 0;
-  msa_status_t st = validate(args);
-  if (st != MSA_OK) return st;
-  if (args->T == 0 || args->B == 0) return MSA_OK;
-  if ((st = check_ws(args, workspace, workspace_bytes)) != MSA_OK) return st;
-  msa::Params p;
-  if ((st = fill_params(args, nullptr, workspace, p)) != MSA_OK) return st;
-  cudaError_t e = msa::launch_plan(p, reinterpret_cast<cudaStream_t>(stream));
+}  // extern "C"
+
+namespace {
+
+msa_status_t launch_plan_checked(const msa::Params& p, cudaStream_t s) {
+  cudaError_t e = msa::launch_plan(p, s);
   if (e != cudaSuccess) return cuda_fail(e, "plan kernel launch");
   return MSA_OK;
 }
 
-msa_status_t msa_index_score_run(const msa_index_score_args* args, float* out, void* workspace,
-                                 size_t workspace_bytes, msa_stream_t stream) {
-  g_msg[0] = 0;
-  msa_status_t st = validate(args);
-  if (st != MSA_OK) return st;
-  if (args->T == 0 || args->B == 0) return MSA_OK;
-  if ((st = check_ws(args, workspace, workspace_bytes)) != MSA_OK) return st;
-  if (!out || !aligned(out, 16)) return fail(MSA_ERR_INVALID_ARG, "out must be a 16-byte aligned pointer");
-  msa::Params p;
-  if ((st = fill_params(args, out, workspace, p)) != MSA_OK) return st;
+msa_status_t launch_score_checked(const msa_index_score_args* args, const msa::Params& p,
+                                  cudaStream_t s) {
   // short-query requests exist only for int8 keys and when a query row group
   // fits 32 MMA columns
   const bool short_ok = args->k_dtype == MSA_I8 && p.g <= msa::kShortRows;
   CUtensorMap tq, tk, tqs, tks;
-  if ((st = make_maps(args, p, &tq, &tk, short_ok ? &tqs : nullptr, &tks)) != MSA_OK) return st;
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  msa_status_t st = make_maps(args, p, &tq, &tk, short_ok ? &tqs : nullptr, &tks);
+  if (st != MSA_OK) return st;
   const bool i8 = args->k_dtype == MSA_I8;
   const bool bf16 = args->q_dtype == MSA_BF16;
   cudaError_t e = i8 ? msa::launch_score_i8(&tq, &tk, p, s) : msa::launch_score_16(&tq, &tk, p, bf16, s);
@@ -297,11 +334,52 @@ msa_status_t msa_index_score_run(const msa_index_score_args* args, float* out, v
   return MSA_OK;
 }
 
+// Shared front half of the entry points: validation, empty-call shortcut,
+// workspace and output checks, kernel parameters.
+msa_status_t prepare(const msa_index_score_args* args, float* out, bool need_out, void* ws,
+                     size_t ws_bytes, msa::Params& p, bool& empty) {
+  g_msg[0] = 0;
+  msa_status_t st = validate(args);
+  if (st != MSA_OK) return st;
+  empty = args->T == 0 || args->B == 0;
+  if (empty) return MSA_OK;
+  if ((st = check_ws(args, ws, ws_bytes)) != MSA_OK) return st;
+  if (need_out && (!out || !aligned(out, 16)))
+    return fail(MSA_ERR_INVALID_ARG, "out must be a 16-byte aligned pointer");
+  return fill_params(args, out, ws, p);
+}
+
+}  // namespace
+
+extern "C" {
+
+msa_status_t msa_index_score_plan(const msa_index_score_args* args, void* workspace,
+                                  size_t workspace_bytes, msa_stream_t stream) {
+  msa::Params p;
+  bool empty = false;
+  msa_status_t st = prepare(args, nullptr, false, workspace, workspace_bytes, p, empty);
+  if (st != MSA_OK || empty) return st;
+  return launch_plan_checked(p, reinterpret_cast<cudaStream_t>(stream));
+}
+
+msa_status_t msa_index_score_run(const msa_index_score_args* args, float* out, void* workspace,
+                                 size_t workspace_bytes, msa_stream_t stream) {
+  msa::Params p;
+  bool empty = false;
+  msa_status_t st = prepare(args, out, true, workspace, workspace_bytes, p, empty);
+  if (st != MSA_OK || empty) return st;
+  return launch_score_checked(args, p, reinterpret_cast<cudaStream_t>(stream));
+}
+
 msa_status_t msa_index_score(const msa_index_score_args* args, float* out, void* workspace,
                              size_t workspace_bytes, msa_stream_t stream) {
-  msa_status_t st = msa_index_score_plan(args, workspace, workspace_bytes, stream);
-  if (st != MSA_OK) return st;
-  return msa_index_score_run(args, out, workspace, workspace_bytes, stream);
+  msa::Params p;
+  bool empty = false;
+  msa_status_t st = prepare(args, out, true, workspace, workspace_bytes, p, empty);
+  if (st != MSA_OK || empty) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if ((st = launch_plan_checked(p, s)) != MSA_OK) return st;
+  return launch_score_checked(args, p, s);
 }
 
 msa_status_t msa_get_device_error(const void* workspace, int32_t* bits, msa_stream_t stream) {

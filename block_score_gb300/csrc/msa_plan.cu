@@ -21,9 +21,11 @@ constexpr int kPlanThreads = 1024;
 
 __device__ __forceinline__ int cdiv(int a, int b) { return (a + b - 1) / b; }
 
-// Inclusive block scan of one value per thread (kPlanThreads threads).
+// Inclusive block scan of one value per thread (blockDim.x threads, a
+// multiple of 32 and at most 1024).
 __device__ int block_incl_scan(int v, int* s_warp) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nwarps = blockDim.x >> 5;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
     int n = __shfl_up_sync(0xffffffffu, v, o);
@@ -32,7 +34,7 @@ __device__ int block_incl_scan(int v, int* s_warp) {
   if (lane == 31) s_warp[warp] = v;
   __syncthreads();
   if (warp == 0) {
-    int w = s_warp[lane];
+    int w = lane < nwarps ? s_warp[lane] : 0;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       int n = __shfl_up_sync(0xffffffffu, w, o);
@@ -106,8 +108,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const Params p) {
   __shared__ int s_warp[32];
   __shared__ unsigned long long s_work[2];
   __shared__ int s_err;
-  __shared__ int s_key[kPlanThreads];
-  __shared__ int s_cls[kPlanThreads];
+  __shared__ __align__(16) int s_key[kPlanThreads];
   __shared__ int s_units[kPlanThreads];
   __shared__ int s_tot[2];
   __shared__ int s_nreq[2];
@@ -127,26 +128,38 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const Params p) {
 
   // pass 1: read every request once, validate, sum the work of each class
   // (blocks x kv heads x tiles, an upper bound that only sets the chunk sizes)
-  const bool small = p.B <= kPlanThreads;
+  const bool small = p.B <= (int)blockDim.x;
   int err = 0;
   unsigned long long work[2] = {0ull, 0ull};
   int nreq[2] = {0, 0};
   ReqScratch mine{};
   int my_sl = 0;
-  for (int b = tid; b < p.B; b += kPlanThreads) {
+  for (int b = tid; b < p.B; b += blockDim.x) {
+    const int sl = __ldg(p.start_loc + b);       // issued together with the length loads
     ReqScratch r = read_request(p, b, err);
     work[r.cls] += (unsigned long long)p.H_kv * r.ntiles * r.nbc_max;
     nreq[r.cls] += 1;
     if (small) {
       mine = r;
-      my_sl = p.start_loc[b];
+      my_sl = sl;
     }
   }
-  if (err) atomicOr(&s_err, err);
-  if (work[0]) atomicAdd(&s_work[0], work[0]);
-  if (work[1]) atomicAdd(&s_work[1], work[1]);
-  if (nreq[0]) atomicAdd(&s_nreq[0], nreq[0]);
-  if (nreq[1]) atomicAdd(&s_nreq[1], nreq[1]);
+  // warp-level reductions first: one shared atomic per warp, not per request
+  err = __reduce_or_sync(0xffffffffu, (unsigned)err);
+  nreq[0] = __reduce_add_sync(0xffffffffu, (unsigned)nreq[0]);
+  nreq[1] = __reduce_add_sync(0xffffffffu, (unsigned)nreq[1]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    work[0] += __shfl_xor_sync(0xffffffffu, work[0], o);
+    work[1] += __shfl_xor_sync(0xffffffffu, work[1], o);
+  }
+  if ((tid & 31) == 0) {
+    if (err) atomicOr(&s_err, err);
+    if (work[0]) atomicAdd(&s_work[0], work[0]);
+    if (work[1]) atomicAdd(&s_work[1], work[1]);
+    if (nreq[0]) atomicAdd(&s_nreq[0], nreq[0]);
+    if (nreq[1]) atomicAdd(&s_nreq[1], nreq[1]);
+  }
   __syncthreads();
   const int chunk0 = chunk_for(s_work[0], p.num_sms, p.MBp);
   const int chunk1 = chunk_for(s_work[1], p.num_sms, p.MBp);
@@ -156,22 +169,33 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const Params p) {
     // schedule order: class 0 first, then class 1; inside a class longest
     // first by the cost of the request's largest unit; the rank of a
     // request is the number of requests that go before it
-    int key = -1, cls = 0, units = 0, nchunks = 1;
+    int cls = 0, units = 0, nchunks = 1;
+    // one sort key per request: class 0 before class 1, then larger unit cost
+    // first (requests without query rows last in their class), then index
+    int key = 0x7fffffff;
     if (tid < p.B) {
       cls = mine.cls;
       const int chunk = cls ? chunk1 : chunk0;
       nchunks = mine.nbc_max > 0 ? cdiv(mine.nbc_max, chunk) : 1;
       units = mine.Lq > 0 ? p.H_kv * mine.ntiles * nchunks : 0;
-      if (mine.Lq > 0) key = mine.nbc_max < chunk ? mine.nbc_max : chunk;
-      s_key[tid] = key;
-      s_cls[tid] = cls;
+      const int cost = mine.Lq > 0 ? (mine.nbc_max < chunk ? mine.nbc_max : chunk) + 1 : 0;
+      key = (cls << 30) | (0x3fffffff - cost);
     }
+    s_key[tid] = key;
     __syncthreads();
-    int rank = 0;
     if (tid < p.B) {
-      for (int j = 0; j < p.B; ++j) {
-        const int kj = s_key[j], cj = s_cls[j];
-        rank += (cj < cls) || (cj == cls && ((kj > key) || (kj == key && j < tid)));
+      // rank = requests that sort before this one; keys are read four at a time
+      int rank = 0;
+      const int4* k4 = reinterpret_cast<const int4*>(s_key);
+      const int nq = (p.B + 3) >> 2;
+#pragma unroll 4
+      for (int q = 0; q < nq; ++q) {
+        const int4 v = k4[q];
+        const int j = q * 4;
+        rank += (v.x < key) || (v.x == key && j + 0 < tid);
+        rank += (j + 1 < p.B) && ((v.y < key) || (v.y == key && j + 1 < tid));
+        rank += (j + 2 < p.B) && ((v.z < key) || (v.z == key && j + 2 < tid));
+        rank += (j + 3 < p.B) && ((v.w < key) || (v.w == key && j + 3 < tid));
       }
       ReqInfo ri;
       ri.b = tid;
@@ -190,18 +214,18 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const Params p) {
     const int v0 = tid < n0 ? s_units[tid] : 0;
     const int incl0 = block_incl_scan(v0, s_warp);
     if (tid < n0) prefix0[tid + 1] = incl0;
-    if (tid == kPlanThreads - 1) s_tot[0] = incl0;
+    if (tid == (int)blockDim.x - 1) s_tot[0] = incl0;
     const int n1 = p.B - n0;
     const int v1 = tid < n1 ? s_units[n0 + tid] : 0;
     const int incl1 = block_incl_scan(v1, s_warp);
     if (tid < n1) prefix1[tid + 1] = incl1;
-    if (tid == kPlanThreads - 1) s_tot[1] = incl1;
+    if (tid == (int)blockDim.x - 1) s_tot[1] = incl1;
     __syncthreads();
   } else {
     // large batches: natural order inside each class; compaction by a scan of
     // the class flags, then per-class unit prefix sums
     int carry_slot[2] = {0, 0}, carry_units[2] = {0, 0};
-    for (int base = 0; base < p.B; base += kPlanThreads) {
+    for (int base = 0; base < p.B; base += (int)blockDim.x) {
       const int b = base + tid;
       ReqScratch r{};
       int units = 0, nchunks = 1;
@@ -231,7 +255,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const Params p) {
           req[(c ? n0 : 0) + slot] = ri;
           (c ? prefix1 : prefix0)[slot + 1] = carry_units[c] + units_incl;
         }
-        if (tid == kPlanThreads - 1) {
+        if (tid == (int)blockDim.x - 1) {
           s_tot[0] = slot_incl;
           s_tot[1] = units_incl;
         }
@@ -264,7 +288,9 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const Params p) {
 }  // namespace
 
 cudaError_t launch_plan(const Params& p, cudaStream_t s) {
-  plan_kernel<<<1, kPlanThreads, 0, s>>>(p);
+  // small batches need few threads: fewer warps make every barrier cheaper
+  const int threads = p.B <= 128 ? 128 : kPlanThreads;
+  plan_kernel<<<1, threads, 0, s>>>(p);
   return cudaGetLastError();
 }
 

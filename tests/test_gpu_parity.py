@@ -174,6 +174,24 @@ def test_all_requests_empty(dev):
     assert torch.isneginf(out).all()
 
 
+@pytest.mark.parametrize("kdt", ["bf16", "int8"])
+def test_batch_above_one_thousand_requests(dev, kdt):
+    # more requests than the plan kernel has threads: the plan takes its
+    # slice-by-slice path (and, for int8 keys, splits both request classes)
+    rng = np.random.default_rng(77)
+    B = 1100
+    q = [int(x) for x in rng.integers(0, 4, size=B)]
+    kv = [int(x) for x in rng.integers(0, 300, size=B)]
+    kdtype = torch.int8 if kdt == "int8" else torch.bfloat16
+    case = synth.make_case(q, kv, H_q=8, H_kv=2, layout="BBND",
+                           q_dtype=torch.float16 if kdt == "int8" else torch.bfloat16,
+                           k_dtype=kdtype, k_kind="int8_full" if kdt == "int8" else "randn",
+                           MB=3, init_blocks=1, local_blocks=1, seed=378)
+    out, err, _ = run_gpu(case, dev)
+    assert err == 0
+    assert_parity(out, oracle.oracle_full(case), what=f"B=1100 {kdt}")
+
+
 def test_group_size_not_a_power_of_two(dev):
     # g = 3: 42 positions x 3 heads = 126 of the 128 MMA rows are used
     case = synth.make_case([100, 50], [400, 90], H_q=6, H_kv=2, layout="BBND",
