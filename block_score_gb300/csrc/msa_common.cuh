@@ -86,7 +86,7 @@ struct Params {
 };
 
 // One work unit as handed from the scheduler thread to the other roles.
-struct UnitDesc {
+struct alignas(16) UnitDesc {
   int32_t live;      // 1 = unit, 0 = no more work
   int32_t b, hk;     // request, kv head
   int32_t t0;        // global token of the tile's first position

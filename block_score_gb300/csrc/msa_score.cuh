@@ -51,7 +51,6 @@ struct ScoreCfg<true> {
 
 constexpr int kQBufs = 2;
 constexpr int kAcc = 4;
-constexpr uint32_t kTmemCols = 512;
 
 template <bool KI8>
 struct SmemLayout {
@@ -70,31 +69,6 @@ struct SmemLayout {
   static constexpr uint32_t bytes = end + 1024;                        // + alignment slack
 };
 
-
-// Max of the first (climit + 1) of 128 values (all if climit >= 127).
-__device__ __forceinline__ float masked_row_max(const float (&x)[128], int climit) {
-  const float ninf = __int_as_float(0xff800000);
-  if (climit < 0) return ninf;
-  float a0 = ninf, a1 = ninf, a2 = ninf, a3 = ninf;
-  if (climit >= 127) {
-#pragma unroll
-    for (int c = 0; c < 128; c += 8) {
-      a0 = fmax3(a0, x[c + 0], x[c + 1]);
-      a1 = fmax3(a1, x[c + 2], x[c + 3]);
-      a2 = fmax3(a2, x[c + 4], x[c + 5]);
-      a3 = fmax3(a3, x[c + 6], x[c + 7]);
-    }
-  } else {
-#pragma unroll
-    for (int c = 0; c < 128; c += 8) {
-      a0 = fmax3(a0, c + 0 <= climit ? x[c + 0] : ninf, c + 1 <= climit ? x[c + 1] : ninf);
-      a1 = fmax3(a1, c + 2 <= climit ? x[c + 2] : ninf, c + 3 <= climit ? x[c + 3] : ninf);
-      a2 = fmax3(a2, c + 4 <= climit ? x[c + 4] : ninf, c + 5 <= climit ? x[c + 5] : ninf);
-      a3 = fmax3(a3, c + 6 <= climit ? x[c + 6] : ninf, c + 7 <= climit ? x[c + 7] : ninf);
-    }
-  }
-  return fmax3(a0, a1, fmaxf(a2, a3));
-}
 
 template <bool KI8, bool BF16>
 __global__ void __launch_bounds__(ScoreCfg<KI8>::kThreads, 1)

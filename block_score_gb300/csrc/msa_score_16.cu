@@ -1,25 +1,24 @@
-// Score kernel instantiations for fp16 / bf16 keys (same type as the query).
-#include "msa_score.cuh"
+// Score kernel for fp16 / bf16 keys (same type as the query).
+#include "msa_tile16.cuh"
 
 namespace msa {
 
 template <bool BF16>
 static cudaError_t launch16(const void* tq, const void* tk, const Params& p, cudaStream_t s) {
-  using L = SmemLayout<false>;
-  auto kern = score_kernel<false, BF16>;
+  auto kern = tile16_kernel<BF16>;
   static bool configured[64] = {};   // per device; setting it twice is harmless
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev >= 64 || !configured[dev]) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::bytes);
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Tile16::bytes);
     if (e != cudaSuccess) return e;
     if (dev < 64) configured[dev] = true;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)p.num_sms);
-  cfg.blockDim = dim3(ScoreCfg<false>::kThreads);
-  cfg.dynamicSmemBytes = L::bytes;
+  cfg.blockDim = dim3(Tile16::kThreads);
+  cfg.dynamicSmemBytes = Tile16::bytes;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

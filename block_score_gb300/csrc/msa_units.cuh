@@ -1,5 +1,5 @@
-// Device helpers shared by the two score kernels: int8 -> fp16 conversion,
-// K page TMA loads, and decoding a work unit from the plan.
+// Device helpers shared by the score kernels: int8 -> fp16 conversion, K page
+// TMA loads, decoding a work unit from the plan, and the masked row max.
 #pragma once
 #include <cstdint>
 #include <cuda.h>
@@ -10,11 +10,12 @@
 
 namespace msa {
 
-// warp roles and pipeline constants shared by both score kernels
+// warp roles and pipeline constants shared by the score kernels
 constexpr int kEpiWarp0 = 3;             // first epilogue warp
 constexpr int kCvtWarp0 = 7;             // first int8 converter warp
 constexpr int kLead = 4;                 // blocks before the end of a unit at which the next is claimed
 constexpr int kSched = 4;
+constexpr uint32_t kTmemCols = 512;         // TMEM columns a score kernel allocates
 constexpr uint32_t kTileBytes = 128 * 128 * 2;   // one 16-bit 128x128 operand tile
 constexpr uint32_t kHalfBytes = kTileBytes / 2;  // 64-element (128-byte) K half
 constexpr uint32_t kRawBytes = 128 * 128;        // one int8 page tile
@@ -92,6 +93,31 @@ __device__ __forceinline__ void make_unit(const Params& p, const ReqInfo* req,
   d.b1 = max(d.c0, min(d.c1, nbc));
   d.kbase = ri.kbase;
   d.sl = ri.sl;
+}
+
+// Max of the first (climit + 1) of 128 values (all if climit >= 127).
+__device__ __forceinline__ float masked_row_max(const float (&x)[128], int climit) {
+  const float ninf = __int_as_float(0xff800000);
+  if (climit < 0) return ninf;
+  float a0 = ninf, a1 = ninf, a2 = ninf, a3 = ninf;
+  if (climit >= 127) {
+#pragma unroll
+    for (int c = 0; c < 128; c += 8) {
+      a0 = fmax3(a0, x[c + 0], x[c + 1]);
+      a1 = fmax3(a1, x[c + 2], x[c + 3]);
+      a2 = fmax3(a2, x[c + 4], x[c + 5]);
+      a3 = fmax3(a3, x[c + 6], x[c + 7]);
+    }
+  } else {
+#pragma unroll
+    for (int c = 0; c < 128; c += 8) {
+      a0 = fmax3(a0, c + 0 <= climit ? x[c + 0] : ninf, c + 1 <= climit ? x[c + 1] : ninf);
+      a1 = fmax3(a1, c + 2 <= climit ? x[c + 2] : ninf, c + 3 <= climit ? x[c + 3] : ninf);
+      a2 = fmax3(a2, c + 4 <= climit ? x[c + 4] : ninf, c + 5 <= climit ? x[c + 5] : ninf);
+      a3 = fmax3(a3, c + 6 <= climit ? x[c + 6] : ninf, c + 7 <= climit ? x[c + 7] : ninf);
+    }
+  }
+  return fmax3(a0, a1, fmaxf(a2, a3));
 }
 
 }  // namespace msa
