@@ -20,12 +20,16 @@
 //   warp 1       TMEM owner + single-thread tcgen05.mma issuer
 //   warp 2       TMA producer (Q tiles, K pages through block_table)
 //   warps 3..10  epilogue, two groups of four warps (one per TMEM lane
-//                quarter); group g drains accumulator g: TMEM -> registers,
-//                mask, 128-wide max per block, local-mask constants, stores
+//                quarter); of every pair, group 0 takes the first block and
+//                group 1 the second: TMEM -> registers, release of the
+//                accumulator, then mask, 128-wide max, local-mask constants,
+//                store
 //
-// Shared memory: Q double buffer (2 x 32 KiB) and a ring of two K pair stages
-// (64 KiB: both pages' first 64-element halves, then both second halves, so one
-// descriptor spans 256 rows).  TMEM: two 256-column accumulators.
+// Shared memory: Q double buffer (2 x 32 KiB) and a ring of five 32 KiB K
+// slots.  A pair of blocks takes two consecutive slots: the first holds both
+// pages' first 64-element halves (256 rows, so one descriptor spans both
+// pages), the second both pages' second halves.  Each slot is released as soon
+// as the four MMAs reading it are done.  TMEM: two 256-column accumulators.
 #pragma once
 #include <cstdint>
 #include <cuda.h>
@@ -39,32 +43,28 @@ namespace msa {
 struct Tile16 {
   static constexpr int kThreads = 352;
   static constexpr int kQBufs = 2;
-  static constexpr int kPairStages = 2;
+  static constexpr int kSlots = 5;                             // K slots of one K half of two pages
   static constexpr int kAcc = 2;                               // accumulators of 256 columns
   static constexpr int kGroups = 2;                            // epilogue groups
-  static constexpr uint32_t kPairBytes = 2 * kTileBytes;       // two pages
-  static constexpr uint32_t kPairHalf = 2 * kHalfBytes;        // 256 rows x 128 bytes
+  static constexpr uint32_t kSlotBytes = 2 * kHalfBytes;       // 256 rows x 128 bytes
   static constexpr uint32_t q_off = 0;
   static constexpr uint32_t k_off = q_off + kQBufs * kTileBytes;
-  static constexpr uint32_t ring_off = k_off + kPairStages * kPairBytes;
+  static constexpr uint32_t ring_off = k_off + kSlots * kSlotBytes;
   static constexpr uint32_t bar_off = ring_off + kSched * sizeof(UnitDesc);
-  static constexpr uint32_t n_bars = 2 * kSched + 2 * kQBufs + 2 * kPairStages + 2 * kAcc + 2;
+  static constexpr uint32_t n_bars = 2 * kSched + 2 * kQBufs + 2 * kSlots + 2 * kAcc + 2;
   static constexpr uint32_t misc_off = bar_off + n_bars * 8;   // tmem base, abort flag
   static constexpr uint32_t end = misc_off + 16;
   static constexpr uint32_t bytes = end + 1024;                // + alignment slack
 };
 
-// k-th 16-element slice of the 256-row B operand of a pair stage
-__device__ __forceinline__ uint64_t pair_desc_at(uint32_t stage, int k) {
-  return smem_desc_sw128(stage + (uint32_t)(k >> 2) * Tile16::kPairHalf + (uint32_t)(k & 3) * 32u);
-}
+static_assert(Tile16::bytes <= 232448, "shared memory per CTA");
 
 template <bool BF16>
 __global__ void __launch_bounds__(Tile16::kThreads, 1)
     tile16_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const Params p) {
   using C = Tile16;
-  constexpr int PS = C::kPairStages;
+  constexpr int PS = C::kSlots;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -106,7 +106,7 @@ __global__ void __launch_bounds__(Tile16::kThreads, 1)
     }
     for (int i = 0; i < C::kAcc; ++i) {
       mbar_init(b_acc_full + 8 * i, 1);
-      mbar_init(b_acc_empty + 8 * i, 4);
+      mbar_init(b_acc_empty + 8 * i, 4 * C::kGroups);
     }
     mbar_init(b_drain, 1);
     mbar_init(b_sched_req, 1);
@@ -202,28 +202,30 @@ __global__ void __launch_bounds__(Tile16::kThreads, 1)
             nx0 = beta + 2 < d.b1 ? __ldg(trow + beta + 2) : 0;
             nx1 = beta + 3 < d.b1 ? __ldg(trow + beta + 3) : 0;
           }
-          if (!mbar_wait(b_k_empty + 8 * ks, kph ^ 1, ctl)) { ok = false; break; }
-          const uint32_t kdst = sbase + C::k_off + ks * C::kPairBytes;
-          mbar_arrive_expect_tx(b_k_full + 8 * ks, (uint32_t)nblk * kTileBytes);
+          int page[2] = {0, 0}, tok[2] = {0, 0};
           for (int j = 0; j < nblk; ++j) {
-            int page = 0, tok;
             if (paged) {
-              page = pg[j];
-              tok = 0;
-              if (page < 0 || (int64_t)page >= p.NP) {
+              page[j] = pg[j];
+              if (page[j] < 0 || (int64_t)page[j] >= p.NP) {
                 atomicOr(&hdr->err, kErrBlockTable);
-                page = page_oob;   // out of bounds: the copy fills zeros
+                page[j] = page_oob;   // out of bounds: the copy fills zeros
               }
             } else {
-              tok = d.kbase + (beta + j) * kP;
+              tok[j] = d.kbase + (beta + j) * kP;
             }
-            // page j's 128 rows: first halves at [j * 16K), second halves 32 KiB on
-            const uint32_t dst = kdst + (uint32_t)j * kHalfBytes;
-            tma_k(dst, &tm_k, b_k_full + 8 * ks, 0, tok, d.hk, page, p.layout, pol_k);
-            tma_k(dst + C::kPairHalf, &tm_k, b_k_full + 8 * ks, 64, tok, d.hk, page, p.layout, pol_k);
           }
-          ++n_k;
-          if (++ks == PS) { ks = 0; kph ^= 1; }
+          // K half x of both pages into one slot: page j's 128 rows at j * 16 KiB
+          for (int x = 0; x < 2 && ok; ++x) {
+            if (!mbar_wait(b_k_empty + 8 * ks, kph ^ 1, ctl)) { ok = false; break; }
+            const uint32_t kdst = sbase + C::k_off + ks * C::kSlotBytes;
+            mbar_arrive_expect_tx(b_k_full + 8 * ks, (uint32_t)nblk * kHalfBytes);
+            for (int j = 0; j < nblk; ++j)
+              tma_k(kdst + (uint32_t)j * kHalfBytes, &tm_k, b_k_full + 8 * ks, 64 * x, tok[j], d.hk,
+                    page[j], p.layout, pol_k);
+            ++n_k;
+            if (++ks == PS) { ks = 0; kph ^= 1; }
+          }
+          if (!ok) break;
         }
         if (!ok) break;
       }
@@ -260,20 +262,24 @@ __global__ void __launch_bounds__(Tile16::kThreads, 1)
         if (!mbar_wait(b_q_full + 8 * qb, qph, ctl)) break;
         const uint32_t qsrc = sbase + C::q_off + qb * kTileBytes;
         bool ok = true;
-        for (int beta = d.c0; beta < d.b1; beta += 2) {
-          if (!mbar_wait(b_k_full + 8 * ks, kph, ctl)) { ok = false; break; }
+        for (int beta = d.c0; beta < d.b1 && ok; beta += 2) {
           if (!mbar_wait(b_acc_empty + 8 * ab, aph ^ 1, ctl)) { ok = false; break; }
-          tc_fence_after();
-          const uint32_t ksrc = sbase + C::k_off + ks * C::kPairBytes;
           const uint32_t dt = tmem_base + ab * 256u;
           const uint32_t idesc = beta + 1 < d.b1 ? idesc2 : idesc1;
+          for (int x = 0; x < 2; ++x) {
+            if (!mbar_wait(b_k_full + 8 * ks, kph, ctl)) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t ksrc = sbase + C::k_off + ks * C::kSlotBytes;
 #pragma unroll
-          for (int k = 0; k < 8; ++k)
-            tc_mma_f16(dt, desc_at(qsrc, k), pair_desc_at(ksrc, k), idesc, k > 0 ? 1u : 0u);
-          tc_commit(b_k_empty + 8 * ks);
+            for (int kk = 0; kk < 4; ++kk)
+              tc_mma_f16(dt, desc_at(qsrc, 4 * x + kk), smem_desc_sw128(ksrc + 32u * kk), idesc,
+                         (x | kk) ? 1u : 0u);
+            tc_commit(b_k_empty + 8 * ks);   // the slot is free once these four MMAs are done
+            if (++ks == PS) { ks = 0; kph ^= 1; }
+          }
+          if (!ok) break;
           tc_commit(b_acc_full + 8 * ab);
           issued = true;
-          if (++ks == PS) { ks = 0; kph ^= 1; }
           if (++ab == C::kAcc) { ab = 0; aph ^= 1; }
         }
         if (!ok) break;
@@ -291,10 +297,10 @@ __global__ void __launch_bounds__(Tile16::kThreads, 1)
     __syncwarp();
   } else if (warp < kEpiWarp0 + 4 * C::kGroups) {
     // --------------------------------------------------------- epilogue --
-    const int grp = (warp - kEpiWarp0) >> 2;       // the accumulator this group drains
+    const int grp = (warp - kEpiWarp0) >> 2;       // block of each pair this group drains
     const int quarter = warp & 3;                  // TMEM lane quarter this warp may read
     const int r = quarter * 32 + lane;             // MMA row = TMEM lane
-    const uint32_t t_lane = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)grp * 256u;
+    const uint32_t t_lane = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)grp * 128u;
     const float ninf = __int_as_float(0xff800000);
     const int rows = p.g * p.np;
     const int pos = r / p.g;
@@ -331,30 +337,25 @@ __global__ void __launch_bounds__(Tile16::kThreads, 1)
       for (; beta < d.b1; beta += 2) {
         const uint32_t a = ab, a_ph = aph;
         if (++ab == C::kAcc) { ab = 0; aph ^= 1; }
-        if ((int)a != grp) continue;   // the other group's pair
-        const bool two = beta + 1 < d.b1;
+        const int col = beta + grp;        // this group's block of the pair
+        const bool has = col < d.b1;       // else a lone last block's partner (a fill column)
+        const bool ld = warp_valid && has;
         if (!warp_wait(b_acc_full + 8 * a, a_ph, ctl)) { ok = false; break; }
         tc_fence_after();
-        float m0 = ninf, m1 = ninf;
-        if (warp_valid) {
-          float x[128];
-          tmem_ld128(t_lane, x);
+        float x[128];
+        if (ld) {
+          tmem_ld128(t_lane + a * 256u, x);
           tmem_wait_ld();
-          if (valid) m0 = masked_row_max(x, lim - beta * kP);
-          if (two) {
-            tmem_ld128(t_lane + 128u, x);
-            tmem_wait_ld();
-            if (valid) m1 = masked_row_max(x, lim - (beta + 1) * kP);
-          }
         }
+        // the accumulator is free once both groups hold their block in registers
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(b_acc_empty + 8 * a);
-        // local mask after the max: forced blocks take their constant; a
-        // lone last block's partner column is a fill column
-        if (forced(beta)) m0 = fill_value(beta);
-        if (!two || forced(beta + 1)) m1 = fill_value(beta + 1);
-        if (valid) __stcs(reinterpret_cast<float2*>(orow + beta), make_float2(m0, m1));
+        float m = ninf;
+        if (ld && valid) m = masked_row_max(x, lim - col * kP);
+        // local mask after the max: forced blocks take their constant
+        if (!has || forced(col)) m = fill_value(col);
+        if (valid) __stcs(orow + col, m);
       }
       if (!ok) break;
       // columns past the computed pairs (group 0): pairs up to a multiple of
