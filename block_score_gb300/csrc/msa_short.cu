@@ -3,23 +3,21 @@
 
 namespace msa {
 
-template <bool KI8, bool BF16>
-static cudaError_t launch_short(const void* tq, const void* tk, const Params& p, cudaStream_t s) {
-  using L = ShortSmem<KI8>;
-  auto kern = short_kernel<KI8, BF16>;
+cudaError_t launch_short_i8(const void* tq, const void* tk, const Params& p, cudaStream_t s) {
+  auto kern = short_kernel<false>;
   static bool configured[64] = {};   // per device; setting it twice is harmless
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev >= 64 || !configured[dev]) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::bytes);
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Short8::bytes);
     if (e != cudaSuccess) return e;
     if (dev < 64) configured[dev] = true;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)p.num_sms);
-  cfg.blockDim = dim3(ShortCfg<KI8>::kThreads);
-  cfg.dynamicSmemBytes = L::bytes;
+  cfg.blockDim = dim3(Short8::kThreads);
+  cfg.dynamicSmemBytes = Short8::bytes;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -28,10 +26,6 @@ static cudaError_t launch_short(const void* tq, const void* tk, const Params& p,
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kern, *static_cast<const CUtensorMap*>(tq),
                             *static_cast<const CUtensorMap*>(tk), p);
-}
-
-cudaError_t launch_short_i8(const void* tq, const void* tk, const Params& p, cudaStream_t s) {
-  return launch_short<true, false>(tq, tk, p, s);
 }
 
 }  // namespace msa
