@@ -272,7 +272,7 @@ msa_status_t make_maps(const msa_index_score_args* a, const msa::Params& p, CUte
   };
   msa_status_t st;
   if ((st = qmap(tq, p.np, "query")) != MSA_OK) return st;
-  if ((st = kmap(tk, false, "key")) != MSA_OK) return st;
+  if ((st = kmap(tk, true, "key")) != MSA_OK) return st;
   if (tq_short) {
     if ((st = qmap(tq_short, p.np_short, "short query")) != MSA_OK) return st;
     if ((st = kmap(tk_short, true, "short key")) != MSA_OK) return st;

@@ -1,12 +1,12 @@
-// Score kernel instantiation for int8 keys with an fp16 query (pre-quantised
+// Tile kernel instantiation for int8 keys with an fp16 query (pre-quantised
 // K cache with per-token scale).
-#include "msa_score.cuh"
+#include "msa_tile.cuh"
 
 namespace msa {
 
 cudaError_t launch_score_i8(const void* tq, const void* tk, const Params& p, cudaStream_t s) {
-  using L = SmemLayout<true>;
-  auto kern = score_kernel<true, false>;
+  using L = TileLayout<true>;
+  auto kern = tile_kernel<true, false>;
   static bool configured[64] = {};   // per device; setting it twice is harmless
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -18,7 +18,7 @@ cudaError_t launch_score_i8(const void* tq, const void* tk, const Params& p, cud
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)p.num_sms);
-  cfg.blockDim = dim3(ScoreCfg<true>::kThreads);
+  cfg.blockDim = dim3(TileCfg<true>::kThreads);
   cfg.dynamicSmemBytes = L::bytes;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];

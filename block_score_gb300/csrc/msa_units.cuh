@@ -95,14 +95,16 @@ __device__ __forceinline__ void make_unit(const Params& p, const ReqInfo* req,
   d.sl = ri.sl;
 }
 
-// Max of the first (climit + 1) of 128 values (all if climit >= 127).
-__device__ __forceinline__ float masked_row_max(const float (&x)[128], int climit) {
+// Max of the first (climit + 1) of N values (all if climit >= N - 1).
+template <int N>
+__device__ __forceinline__ float masked_max(const float (&x)[N], int climit) {
+  static_assert(N % 8 == 0, "groups of 8");
   const float ninf = __int_as_float(0xff800000);
   if (climit < 0) return ninf;
   float a0 = ninf, a1 = ninf, a2 = ninf, a3 = ninf;
-  if (climit >= 127) {
+  if (climit >= N - 1) {
 #pragma unroll
-    for (int c = 0; c < 128; c += 8) {
+    for (int c = 0; c < N; c += 8) {
       a0 = fmax3(a0, x[c + 0], x[c + 1]);
       a1 = fmax3(a1, x[c + 2], x[c + 3]);
       a2 = fmax3(a2, x[c + 4], x[c + 5]);
@@ -110,7 +112,7 @@ __device__ __forceinline__ float masked_row_max(const float (&x)[128], int climi
     }
   } else {
 #pragma unroll
-    for (int c = 0; c < 128; c += 8) {
+    for (int c = 0; c < N; c += 8) {
       a0 = fmax3(a0, c + 0 <= climit ? x[c + 0] : ninf, c + 1 <= climit ? x[c + 1] : ninf);
       a1 = fmax3(a1, c + 2 <= climit ? x[c + 2] : ninf, c + 3 <= climit ? x[c + 3] : ninf);
       a2 = fmax3(a2, c + 4 <= climit ? x[c + 4] : ninf, c + 5 <= climit ? x[c + 5] : ninf);
