@@ -75,29 +75,54 @@ def algorithmic_work(case):
             "bytes": total}
 
 
-def kernel_source_hash() -> str:
-    """Hash of the CUDA sources: an ncu traffic figure is only valid for the code it measured."""
+# sources each score kernel is built from (an ncu figure is only valid for the
+# code it measured)
+KERNEL_SOURCES = {
+    "tile_kernel": ["msa_tile.cuh", "msa_units.cuh", "msa_ptx.cuh", "msa_common.cuh",
+                    "msa_score_16.cu", "msa_score_i8.cu"],
+    "short_kernel": ["msa_short.cuh", "msa_units.cuh", "msa_ptx.cuh", "msa_common.cuh",
+                     "msa_short.cu"],
+}
+
+
+def kernel_source_hash(kernel: str) -> str:
+    """Hash of the CUDA sources of one kernel."""
     import hashlib
     h = hashlib.sha256()
     d = os.path.join(ROOT, "block_score_gb300", "csrc")
-    for name in sorted(os.listdir(d)):
-        if name.endswith((".cu", ".cuh")):
-            with open(os.path.join(d, name), "rb") as f:
-                h.update(name.encode() + b"\0" + f.read())
+    for name in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(d, name), "rb") as f:
+            h.update(name.encode() + b"\0" + f.read())
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(workload_key: str):
-    """DRAM bytes per score-kernel launch from the committed ncu summary, if it
-    was taken on the current sources (else None)."""
-    path = os.path.join(ROOT, "profiles", "score_kernel_dram_traffic.txt")
+def dominant_kernel(case) -> str:
+    """The kernel that does the work of a workload: the short-query kernel when
+    every request is a short int8 request, else the tile kernel."""
+    g = case.H_q // case.H_kv
+    short = case.key.dtype == torch.int8 and all(
+        lq == 0 or lq * g <= 32 for lq in case.q_lens)
+    return "short_kernel" if short and any(lq > 0 for lq in case.q_lens) else "tile_kernel"
+
+
+def launches_per_call(case) -> int:
+    """Kernels one call launches: the plan, the tile kernel and, for int8 keys
+    with a query-row group of at most 32, the short-query kernel."""
+    g = case.H_q // case.H_kv
+    return 2 + (1 if case.key.dtype == torch.int8 and g <= 32 else 0)
+
+
+def recorded_traffic(workload_key: str, kernel: str):
+    """DRAM bytes per launch of the dominant kernel from the committed ncu
+    summary, if it was taken on the current sources of that kernel (else None)."""
+    path = os.path.join(ROOT, "profiles", "kernel_dram_traffic.txt")
     try:
         with open(path) as f:
             for line in f:
                 parts = line.split()
-                if len(parts) >= 3 and not line.startswith("#") and parts[0] == workload_key:
-                    if parts[2] == kernel_source_hash():
-                        return float(parts[1])
+                if (len(parts) >= 4 and not line.startswith("#") and parts[0] == workload_key
+                        and parts[1] == kernel and parts[3] == kernel_source_hash(kernel)):
+                    return float(parts[2])
     except OSError:
         pass
     return None
@@ -328,7 +353,7 @@ def run_ours(args):
     work = algorithmic_work(case)
     peaks = load_peaks()
     if args.traffic is None:
-        args.traffic = recorded_traffic(workload_key(args))
+        args.traffic = recorded_traffic(workload_key(args), dominant_kernel(case))
     prep = bs.from_case(case, device)
     stream = torch.cuda.current_stream(device)
 
@@ -397,9 +422,10 @@ def run_ours(args):
         roof = {"bound": "tensor", "achieved": tflops_kernel, "peak": pk, "unit": "TFLOP/s",
                 "frac": tflops_kernel / pk, "traffic": args.traffic,
                 "peak_source": peaks["source"] + " bf16_tflops (burst)"}
-    roof["kernel"] = "score_kernel"
-    roof["kernel_timing"] = ("second pass of K calls with CUDA events around each "
-                             "score-kernel launch")
+    roof["kernel"] = dominant_kernel(case)
+    roof["kernel_timing"] = ("second pass of K calls with CUDA events around the score "
+                             "launches of each call (tile kernel, plus the short-query "
+                             "kernel for int8 keys), after its plan")
     roof["kernel_us"] = kern_ms * 1e3
     roof["algorithmic_bytes"] = work["bytes"]
     roof["algorithmic_flops"] = work["flops"]
@@ -416,7 +442,7 @@ def run_ours(args):
         "frac_tensor": tflops / peaks["bf16_tflops"],
         "roofline": roof,
         "e2e": e2e,
-        "gpu_launches": 2 * args.steps,
+        "gpu_launches": launches_per_call(case) * args.steps,
         "clocks": sampler.summary(),
     }
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
