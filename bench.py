@@ -106,10 +106,14 @@ def dominant_kernel(case) -> str:
 
 
 def launches_per_call(case) -> int:
-    """Kernels one call launches: the plan, the tile kernel and, for int8 keys
-    with a query-row group of at most 32, the short-query kernel."""
+    """Kernels one call launches: the plan, the tile kernel unless the host
+    length bound puts every request on the short path, and, for int8 keys with
+    a query-row group of at most 32, the short-query kernel."""
     g = case.H_q // case.H_kv
-    return 2 + (1 if case.key.dtype == torch.int8 and g <= 32 else 0)
+    short_ok = case.key.dtype == torch.int8 and g <= 32
+    max_q = max(case.q_lens) if case.q_lens else 0
+    tile = not (short_ok and max_q > 0 and max_q * g <= 32)
+    return 1 + (1 if tile else 0) + (1 if short_ok else 0)
 
 
 def recorded_traffic(workload_key: str, kernel: str):
@@ -354,7 +358,8 @@ def run_ours(args):
     peaks = load_peaks()
     if args.traffic is None:
         args.traffic = recorded_traffic(workload_key(args), dominant_kernel(case))
-    prep = bs.from_case(case, device)
+    # the caller knows its requests' query lengths (as a serving loop does)
+    prep = bs.from_case(case, device, max_seqlen_q=max(case.q_lens) if case.q_lens else None)
     stream = torch.cuda.current_stream(device)
 
     # correctness gate before timing (the parity tests are the full check)
@@ -477,7 +482,8 @@ def e2e_run(case, device, stream, args):
                        actual_seq_klen=klen, layout_key=case.layout,
                        sparse_mode=case.sparse_mode, init_blocks=case.init_blocks,
                        local_blocks=case.local_blocks,
-                       max_blocks=case.MB if case.layout == "TND" else None)
+                       max_blocks=case.MB if case.layout == "TND" else None,
+                       max_seqlen_q=max(case.q_lens) if case.q_lens else None)
     out_host = torch.empty(prep.shape, dtype=torch.float32).pin_memory()
     h2d = sum(v.numel() * v.element_size() for v in host.values() if v is not None)
     h2d += host_key_base.numel() * host_key_base.element_size()

@@ -60,7 +60,7 @@ class _Args(ctypes.Structure):
         ("cu_seqlens_k", ctypes.c_void_p), ("start_loc", ctypes.c_void_p),
         ("scale", ctypes.c_void_p),
         ("sparse_mode", ctypes.c_int32), ("init_blocks", ctypes.c_int32),
-        ("local_blocks", ctypes.c_int32),
+        ("local_blocks", ctypes.c_int32), ("max_seqlen_q", ctypes.c_int32),
     ]
 
 
@@ -136,7 +136,7 @@ class _Call:
 
     def __init__(self, query, key, start_loc, block_table, scale, actual_seq_qlen,
                  actual_seq_klen, layout_key, sparse_mode, init_blocks, local_blocks,
-                 max_blocks):
+                 max_blocks, max_seqlen_q=None):
         layout = str(layout_key).upper()
         if layout not in _LAYOUT:
             raise ValueError(f"layout_key must be one of TND/BBND/BNBD, got {layout_key!r}")
@@ -217,6 +217,7 @@ class _Call:
         a.sparse_mode = int(sparse_mode)
         a.init_blocks = int(init_blocks)
         a.local_blocks = int(local_blocks)
+        a.max_seqlen_q = 0 if max_seqlen_q is None else int(max_seqlen_q)
         self.args = a
         self.device = query.device
 
@@ -233,9 +234,10 @@ class _Call:
 
 
 def _prepare(query, key, start_loc, block_table, scale, actual_seq_qlen, actual_seq_klen,
-             layout_key, sparse_mode, init_blocks, local_blocks, max_blocks) -> _Call:
+             layout_key, sparse_mode, init_blocks, local_blocks, max_blocks,
+             max_seqlen_q=None) -> _Call:
     return _Call(query, key, start_loc, block_table, scale, actual_seq_qlen, actual_seq_klen,
-                 layout_key, sparse_mode, init_blocks, local_blocks, max_blocks)
+                 layout_key, sparse_mode, init_blocks, local_blocks, max_blocks, max_seqlen_q)
 
 
 def msa_index_score(query: torch.Tensor, key: torch.Tensor, start_loc: torch.Tensor, *,
@@ -245,6 +247,7 @@ def msa_index_score(query: torch.Tensor, key: torch.Tensor, start_loc: torch.Ten
                     actual_seq_klen: Optional[torch.Tensor] = None,
                     layout_key: str = "BBND", sparse_mode: int = 3, init_blocks: int = 0,
                     local_blocks: int = 1, max_blocks: Optional[int] = None,
+                    max_seqlen_q: Optional[int] = None,
                     out: Optional[torch.Tensor] = None,
                     workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
     """Block scores ``[H_q, T, RoundUp(MB, 16)]`` fp32 on the query's device.
@@ -252,10 +255,12 @@ def msa_index_score(query: torch.Tensor, key: torch.Tensor, start_loc: torch.Ten
     ``actual_seq_qlen`` is the [B+1] prefix sum of query lengths;
     ``actual_seq_klen`` is [B] kv lengths for BBND/BNBD and the [B+1] prefix
     sum for TND.  ``max_blocks`` is MB for TND (computed from actual_seq_klen
-    when omitted, which reads it on the host).
+    when omitted, which reads it on the host).  ``max_seqlen_q`` is an optional
+    host-known bound on every request's query length (an addition of this
+    library: with int8 keys and short requests only, it saves a kernel launch).
     """
     c = _prepare(query, key, start_loc, block_table, scale, actual_seq_qlen, actual_seq_klen,
-                 layout_key, sparse_mode, init_blocks, local_blocks, max_blocks)
+                 layout_key, sparse_mode, init_blocks, local_blocks, max_blocks, max_seqlen_q)
     if not query.is_cuda:
         raise ValueError("msa_index_score runs on CUDA tensors only")
     shape = c.out_shape()
@@ -316,7 +321,8 @@ class Prepared:
                              kw.pop("scale", None), kw.pop("actual_seq_qlen", None),
                              kw.pop("actual_seq_klen", None), kw.pop("layout_key", "BBND"),
                              kw.pop("sparse_mode", 3), kw.pop("init_blocks", 0),
-                             kw.pop("local_blocks", 1), kw.pop("max_blocks", None))
+                             kw.pop("local_blocks", 1), kw.pop("max_blocks", None),
+                             kw.pop("max_seqlen_q", None))
         if kw:
             raise TypeError(f"unknown arguments {sorted(kw)}")
         self.shape = self.call.out_shape()
@@ -362,8 +368,11 @@ def msa_get_device_error(workspace: torch.Tensor, stream=None) -> int:
     return int(v.value)
 
 
-def from_case(case, device) -> Prepared:
-    """Move a synthetic case (``synth.MsaCase``) to ``device`` and marshal it."""
+def from_case(case, device, max_seqlen_q: Optional[int] = None) -> Prepared:
+    """Move a synthetic case (``synth.MsaCase``) to ``device`` and marshal it.
+
+    ``max_seqlen_q`` is passed through as the host-side length bound (None: not
+    given)."""
     def mv(t):
         return None if t is None else t.to(device)
     key = case.key
@@ -382,4 +391,5 @@ def from_case(case, device) -> Prepared:
                     actual_seq_qlen=mv(case.cu_seqlens_q), actual_seq_klen=mv(klen),
                     layout_key=case.layout, sparse_mode=case.sparse_mode,
                     init_blocks=case.init_blocks, local_blocks=case.local_blocks,
-                    max_blocks=case.MB if case.layout == "TND" else None)
+                    max_blocks=case.MB if case.layout == "TND" else None,
+                    max_seqlen_q=max_seqlen_q)

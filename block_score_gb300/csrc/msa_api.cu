@@ -67,6 +67,7 @@ msa_status_t validate(const msa_index_score_args* a) {
   const int64_t cap = a->layout == MSA_LAYOUT_TND ? mbp : a->MB;
   if (a->init_blocks < 0 || a->local_blocks < 0 || a->init_blocks > cap || a->local_blocks > cap)
     return fail(MSA_ERR_INVALID_ARG, "init_blocks/local_blocks must be in [0, %lld]", (long long)cap);
+  if (a->max_seqlen_q < 0) return fail(MSA_ERR_INVALID_ARG, "max_seqlen_q must be >= 0 (0: not given)");
   if (a->T > 0x7fffffffLL - 1) return fail(MSA_ERR_UNSUPPORTED, "T too large");
   if (a->NP < 1 || a->NP > 0x7fffffffLL - 1)
     return fail(MSA_ERR_INVALID_ARG, "NP (pages or TND rows) must be in [1, 2^31-2]");
@@ -146,6 +147,7 @@ msa_status_t fill_params(const msa_index_score_args* a, float* out, void* ws, ms
   p.sparse_mode = a->sparse_mode;
   p.init_blocks = a->init_blocks;
   p.local_blocks = a->local_blocks;
+  p.max_q = a->max_seqlen_q;
   p.num_sms = sm_count(dev);
   p.block_table = a->block_table;
   p.cu_q = a->cu_seqlens_q;
@@ -328,7 +330,13 @@ msa_status_t launch_score_checked(const msa_index_score_args* args, const msa::P
   if (st != MSA_OK) return st;
   const bool i8 = args->k_dtype == MSA_I8;
   const bool bf16 = args->q_dtype == MSA_BF16;
-  cudaError_t e = i8 ? msa::launch_score_i8(&tq, &tk, p, s) : msa::launch_score_16(&tq, &tk, p, bf16, s);
+  // a host bound that puts every request in the short class: no tile launch
+  // (the plan flags any request longer than the bound)
+  const bool short_only =
+      short_ok && args->max_seqlen_q > 0 && (int64_t)args->max_seqlen_q * p.g <= msa::kShortRows;
+  cudaError_t e = cudaSuccess;
+  if (!short_only)
+    e = i8 ? msa::launch_score_i8(&tq, &tk, p, s) : msa::launch_score_16(&tq, &tk, p, bf16, s);
   if (e == cudaSuccess && short_ok) e = msa::launch_short_i8(&tqs, &tks, p, s);
   if (e != cudaSuccess) return cuda_fail(e, "score kernel launch");
   return MSA_OK;

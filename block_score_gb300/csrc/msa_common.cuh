@@ -73,6 +73,7 @@ struct Params {
   int32_t layout;          // 0 BBND, 1 BNBD, 2 TND
   int32_t k_int8;          // keys are int8 (short-query class enabled)
   int32_t sparse_mode, init_blocks, local_blocks;
+  int32_t max_q;            // host bound on every request's query length (0: none)
   int32_t num_sms;
   const int32_t* block_table;
   const int32_t* cu_q;

@@ -61,6 +61,9 @@ __device__ ReqScratch read_request(const Params& p, int b, int& err) {
   int64_t hi = q1 < lo ? lo : (q1 > p.T ? p.T : q1);
   r.t0 = (int)lo;
   r.Lq = (int)(hi - lo);
+  // a host length bound that this request breaks: the launch may have left
+  // out the kernel that would have scored it
+  if (p.max_q > 0 && r.Lq > p.max_q) err |= kErrCuQ;
   int64_t L;
   if (p.layout == 2) {
     const int64_t k0 = p.cu_k[b], k1 = p.cu_k[b + 1];

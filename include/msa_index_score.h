@@ -47,7 +47,7 @@
 extern "C" {
 #endif
 
-#define MSA_ABI_VERSION 1
+#define MSA_ABI_VERSION 2
 
 /* Same object as cudaStream_t / CUstream (NULL = legacy default stream). */
 typedef struct CUstream_st *msa_stream_t;
@@ -65,7 +65,7 @@ typedef enum { MSA_LAYOUT_BBND = 0, MSA_LAYOUT_BNBD = 1, MSA_LAYOUT_TND = 2 } ms
 typedef enum { MSA_F16 = 0, MSA_BF16 = 1, MSA_I8 = 2 } msa_dtype_t;
 
 /* Bits of the device error word (msa_get_device_error). */
-#define MSA_DEVERR_CU_Q        0x01  /* cu_seqlens_q[0] != 0, decreasing, or cu_seqlens_q[B] != T */
+#define MSA_DEVERR_CU_Q        0x01  /* cu_seqlens_q[0] != 0, decreasing, cu_seqlens_q[B] != T, or a query length above a nonzero max_seqlen_q */
 #define MSA_DEVERR_KV_LEN      0x02  /* kv_len < 0, or ceil(kv_len/P) > MB */
 #define MSA_DEVERR_CU_K        0x04  /* TND: cu_seqlens_k[0] != 0, decreasing, or beyond T2 */
 #define MSA_DEVERR_BLOCK_TABLE 0x08  /* a block_table entry that is read lies outside [0, NP) */
@@ -109,6 +109,14 @@ typedef struct {
     int32_t sparse_mode;           /* 0 = no causal mask, 3 = rightDownCausal (default 3) */
     int32_t init_blocks;           /* default 0, <= MB */
     int32_t local_blocks;          /* default 1, <= MB */
+
+    /* Optional host-side upper bound on every request's query length (0 = not
+     * known).  This build's own addition, not an argument of the op in the
+     * pages: like the max_seqlen_q of varlen attention calls, it lets the host
+     * skip the query-tile kernel when every request is a short int8 request
+     * (max_seqlen_q * H_q / H_kv <= 32).  A request longer than a nonzero bound
+     * is reported as MSA_DEVERR_CU_Q; its scores are then not written. */
+    int32_t max_seqlen_q;
 } msa_index_score_args;
 
 /* Library ABI version (MSA_ABI_VERSION of the build). */

@@ -46,7 +46,7 @@ def test_library_is_sm103a_only():
 
 
 def test_abi_version(lib):
-    assert lib.msa_abi_version() == 1
+    assert lib.msa_abi_version() == 2
 
 
 def _args(**over):

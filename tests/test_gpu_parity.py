@@ -214,6 +214,40 @@ def test_plan_run_split_and_repeat_are_identical(dev):
     assert torch.equal(a, b) and torch.equal(a, c)
 
 
+def test_host_length_bound_skips_nothing_it_should_not(dev):
+    # int8 decode batch (every request short): with the host bound the tile
+    # kernel is not launched; the scores are the same bits as without it
+    import block_score_gb300 as bs
+    case = synth.make_case([1, 1, 2, 1], [700, 3000, 1500, 0], H_q=16, H_kv=2, layout="BBND",
+                           q_dtype=torch.float16, k_dtype=torch.int8, k_kind="int8_full",
+                           MB=30, init_blocks=1, local_blocks=2, seed=385)
+    a = bs.from_case(case, dev)
+    out_a = a().cpu()
+    assert a.device_error() == 0
+    b = bs.from_case(case, dev, max_seqlen_q=2)
+    out_b = b().cpu()
+    assert b.device_error() == 0
+    assert torch.equal(out_a, out_b)
+    assert_parity(out_b, oracle.oracle_full(case), what="host bound, int8 decode")
+    # 16-bit keys have no short path: the bound changes nothing
+    c16 = synth.make_case([1, 3], [900, 260], H_q=8, H_kv=1, layout="BNBD",
+                          q_dtype=torch.bfloat16, MB=8, seed=386)
+    o1 = bs.from_case(c16, dev)().cpu()
+    o2 = bs.from_case(c16, dev, max_seqlen_q=3)().cpu()
+    assert torch.equal(o1, o2)
+
+
+def test_host_length_bound_that_is_broken_is_reported(dev):
+    # a prefill request longer than the bound would have needed the tile kernel
+    import block_score_gb300 as bs
+    case = synth.make_case([1, 40], [700, 900], H_q=16, H_kv=2, layout="BBND",
+                           q_dtype=torch.float16, k_dtype=torch.int8, k_kind="int8_full",
+                           MB=8, seed=387)
+    prep = bs.from_case(case, dev, max_seqlen_q=1)
+    prep()
+    assert prep.device_error() & 0x01
+
+
 def test_bad_block_table_entry_is_reported_not_faulted(dev):
     case = synth.make_case([5], [300], H_q=4, H_kv=1, layout="BBND", q_dtype=torch.float16,
                            MB=4, seed=370)
