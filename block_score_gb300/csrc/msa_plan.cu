@@ -92,13 +92,16 @@ __device__ ReqScratch read_request(const Params& p, int b, int& err) {
   return r;
 }
 
-__device__ int chunk_for(unsigned long long work, int num_sms, int MBp) {
-  // about 16 units per SM on average, never below 8 blocks (the tail of a
-  // call is then a fraction of one short unit)
+__device__ int chunk_for(unsigned long long work, int num_sms, int MBp, int gran) {
+  // about 16 units per SM on average, never below `gran` blocks (the tail of
+  // a call is then a fraction of one short unit); a multiple of `gran` (the
+  // store width of the kernel's epilogue: 8 for the tile kernel, 4 for the
+  // short-query kernel)
   const unsigned long long target = (unsigned long long)num_sms * 16ull;
+  const unsigned long long g = (unsigned long long)gran;
   unsigned long long c = (work + target - 1) / target;
-  if (c < 8) c = 8;
-  c = (c + 7) / 8 * 8;
+  if (c < g) c = g;
+  c = (c + g - 1) / g * g;
   if (c > (unsigned long long)MBp) c = (unsigned long long)MBp;
   return (int)c;
 }
@@ -164,8 +167,8 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const Params p) {
     if (nreq[1]) atomicAdd(&s_nreq[1], nreq[1]);
   }
   __syncthreads();
-  const int chunk0 = chunk_for(s_work[0], p.num_sms, p.MBp);
-  const int chunk1 = chunk_for(s_work[1], p.num_sms, p.MBp);
+  const int chunk0 = chunk_for(s_work[0], p.num_sms, p.MBp, 8);
+  const int chunk1 = chunk_for(s_work[1], p.num_sms, p.MBp, 4);
   const int n0 = s_nreq[0];
 
   if (small) {

@@ -58,7 +58,7 @@ struct Short8 {
   static constexpr int kRed = 8;                         // partial-maximum ring (items)
   static constexpr uint32_t kQHalf = kN * 128;           // one 64-element half of the query rows
   static constexpr uint32_t kQBytes = 2 * kQHalf;
-  static constexpr int kQBufs = 2;
+  static constexpr int kQBufs = 4;                      // query rows of the next units (8 KiB each)
   static constexpr uint32_t q_off = 0;
   static constexpr uint32_t k_off = q_off + kQBufs * kQBytes;
   static constexpr uint32_t red_off = k_off + kStages * kStageBytes;
@@ -320,8 +320,9 @@ __global__ void __launch_bounds__(Short8::kThreads, 1)
         bool ok = true;
         for (int beta = d.c0; beta < d.b1; beta += 2, ++it) {
           const uint32_t as = it % C::kA, ds = it % C::kD;
-          if (!mbar_wait(b_a_full + 8 * as, (it / C::kA) & 1u, ctl) ||
-              !mbar_wait(b_d_free + 8 * ds, ((it / C::kD) & 1u) ^ 1u, ctl)) {
+          // the first converter group saw the accumulator pair free before it
+          // arrived, so one wait covers both operands' readiness
+          if (!mbar_wait(b_a_full + 8 * as, (it / C::kA) & 1u, ctl)) {
             ok = false;
             break;
           }
@@ -439,7 +440,7 @@ __global__ void __launch_bounds__(Short8::kThreads, 1)
     // ---------------------------------------------------------- combine --
     // Lane r owns output row r = (position r / g, head r % g): the max of the
     // four partial maxima of each computed block, the local-mask constants, the
-    // fill of the other columns, and 32-byte stores of 8 blocks at a time.
+    // fill of the other columns, and 16-byte stores of 4 blocks at a time.
     const float ninf = __int_as_float(0xff800000);
     uint32_t ss = 0, sph = 0, rr = 0, rph = 0;
     for (;;) {
@@ -465,7 +466,7 @@ __global__ void __launch_bounds__(Short8::kThreads, 1)
       auto forced = [&](int beta) -> bool {
         return live_kv && (beta < p.init_blocks || (beta >= lo && beta <= d.sl));
       };
-      float v[8];
+      float v[4];
       bool ok = true;
       int beta = d.c0;
       for (; beta < d.b1; beta += 2) {
@@ -479,37 +480,27 @@ __global__ void __launch_bounds__(Short8::kThreads, 1)
         // local mask after the max; a lone last block's partner is a fill column
         if (forced(beta)) m0 = fill_value(beta);
         if (beta + 1 >= d.b1 || forced(beta + 1)) m1 = fill_value(beta + 1);
-        const int e = beta & 7;   // even
-#pragma unroll
-        for (int k = 0; k < 8; k += 2)
-          if (k == e) { v[k] = m0; v[k + 1] = m1; }
-        if (e == 6 && row_valid) {
-          float4* dst = reinterpret_cast<float4*>(orow + (beta - 6));
-          __stcs(dst, make_float4(v[0], v[1], v[2], v[3]));
-          __stcs(dst + 1, make_float4(v[4], v[5], v[6], v[7]));
+        // 16-byte stores of 4 columns (units start on multiples of 4)
+        if ((beta & 3) == 0) {
+          v[0] = m0;
+          v[1] = m1;
+        } else {
+          v[2] = m0;
+          v[3] = m1;
+          if (row_valid) __stcs(reinterpret_cast<float4*>(orow + (beta - 2)), make_float4(v[0], v[1], v[2], v[3]));
         }
       }
       if (!ok) break;
       if (row_valid) {
-        if (beta & 7) {
-          for (; beta & 7; ++beta) {
-            const float f = fill_value(beta);
-            const int e = beta & 7;
-#pragma unroll
-            for (int k = 0; k < 8; ++k)
-              if (k == e) v[k] = f;
-          }
-          float4* dst = reinterpret_cast<float4*>(orow + (beta - 8));
-          __stcs(dst, make_float4(v[0], v[1], v[2], v[3]));
-          __stcs(dst + 1, make_float4(v[4], v[5], v[6], v[7]));
+        if (beta & 3) {   // an open group of 4 (beta is even): close it with fill columns
+          v[2] = fill_value(beta);
+          v[3] = fill_value(beta + 1);
+          __stcs(reinterpret_cast<float4*>(orow + (beta - 2)), make_float4(v[0], v[1], v[2], v[3]));
+          beta += 2;
         }
-        for (; beta < d.c1; beta += 8) {
-          float4* dst = reinterpret_cast<float4*>(orow + beta);
-          __stcs(dst, make_float4(fill_value(beta), fill_value(beta + 1), fill_value(beta + 2),
-                                  fill_value(beta + 3)));
-          __stcs(dst + 1, make_float4(fill_value(beta + 4), fill_value(beta + 5),
-                                      fill_value(beta + 6), fill_value(beta + 7)));
-        }
+        for (; beta < d.c1; beta += 4)
+          __stcs(reinterpret_cast<float4*>(orow + beta), make_float4(fill_value(beta), fill_value(beta + 1),
+                                                                     fill_value(beta + 2), fill_value(beta + 3)));
       }
     }
   } else if (warp >= C::kCvtW0) {
@@ -536,6 +527,10 @@ __global__ void __launch_bounds__(Short8::kThreads, 1)
           // group only completes the item's phases, after the A slot is free
           // (so it cannot run a whole stage ring ahead of the other group)
           if (!warp_wait(b_a_free + 8 * as, ((it / C::kA) & 1u) ^ 1u, ctl)) { ok = false; break; }
+          if (jp == 0 && !warp_wait(b_d_free + 8 * (it % C::kD), ((it / C::kD) & 1u) ^ 1u, ctl)) {
+            ok = false;
+            break;
+          }
           if (lane == 0) {
             mbar_arrive(b_st_empty + 8 * rs);
             mbar_arrive(b_a_full + 8 * as);
@@ -572,6 +567,12 @@ __global__ void __launch_bounds__(Short8::kThreads, 1)
         tmem_st64(t_lane + as * 128u + 64u * jp, hv);
         tmem_st1(t_lane + C::kScCol0 + (2u * it + jp) % C::kScCols, __float_as_uint(sv));
         tmem_wait_st();
+        // group 0 also waits until the epilogue has read the accumulator pair
+        // this item will use, so the MMA thread waits on one barrier per item
+        if (jp == 0 && !warp_wait(b_d_free + 8 * (it % C::kD), ((it / C::kD) & 1u) ^ 1u, ctl)) {
+          ok = false;
+          break;
+        }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(b_a_full + 8 * as);
