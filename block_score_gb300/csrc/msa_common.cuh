@@ -98,7 +98,8 @@ struct alignas(16) UnitDesc {
   int32_t b1;        // blocks [c0, b1) are computed; [b1, c1) are fill / forced
   int32_t kbase;     // TND key row base
   int32_t sl;        // start_loc of the request
-  int32_t pad[3];
+  int32_t pg0, pg1;  // paged layouts: block_table entries of blocks c0 and c0 + 1 (if computed)
+  int32_t pad;
 };
 static_assert(sizeof(UnitDesc) == 64, "UnitDesc is 64 bytes");
 

@@ -99,10 +99,14 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const W
   return mbar_wait_slow(bar, parity, ctl);
 }
 
-// Whole-warp wait: lane 0 polls, the outcome is broadcast, and __syncwarp
-// orders the other lanes' later shared-memory reads after lane 0's acquire.
-// Every lane of the warp gets the same answer, so loops exit together.
+// Whole-warp wait.  Fast path: every lane tests the phase itself (one
+// broadcast shared-memory read, an acquire in each lane) and the warp
+// proceeds when all saw it complete; this costs about half of a lane-0 poll
+// with a broadcast.  Otherwise lane 0 polls, the outcome is broadcast, and
+// __syncwarp orders the other lanes' later shared-memory reads after lane 0's
+// acquire.  Every lane gets the same answer, so loops exit together.
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const WaitCtl& ctl) {
+  if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
   int ok = 1;
   if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, ctl) ? 1 : 0;
   ok = __shfl_sync(0xffffffffu, ok, 0);

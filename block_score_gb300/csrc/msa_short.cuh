@@ -64,7 +64,13 @@ struct Short8 {
   static constexpr uint32_t red_off = k_off + kStages * kStageBytes;
   static constexpr uint32_t red_bytes = kRed * 4 * 2 * kN * 4;   // [item][quarter][page][row]
   static constexpr uint32_t ring_off = red_off + red_bytes;
-  static constexpr uint32_t bar_off = ring_off + kSched * sizeof(UnitDesc);
+  // the first kReqCache request records and the short class's unit prefix
+  // sums, copied once so that a claim costs one atomic and no dependent
+  // global loads
+  static constexpr int kReqCache = 128;
+  static constexpr uint32_t req_off = ring_off + kSched * sizeof(UnitDesc);
+  static constexpr uint32_t pfx_off = req_off + kReqCache * sizeof(ReqInfo);
+  static constexpr uint32_t bar_off = pfx_off + kReqCache * 4;
   static constexpr uint32_t n_bars =
       2 * kSched + 2 * kQBufs + 2 * kStages + 2 * kA + 2 * kD + 2 * kRed + 2;
   static constexpr uint32_t misc_off = bar_off + n_bars * 8;
@@ -176,19 +182,49 @@ __global__ void __launch_bounds__(Short8::kThreads, 1)
   asm volatile("griddepcontrol.wait;" ::: "memory");
 
   PlanHeader* hdr = reinterpret_cast<PlanHeader*>(p.ws);
-  const int n_units = *reinterpret_cast<volatile int*>(&hdr->n_units[1]);
+  // The header fields (constant during this grid) and, in warp 0, the first
+  // request records and the class's prefix sums are fetched together: their
+  // addresses depend only on B, so the first claim waits one round trip.
+  const int n_units = hdr->n_units[1];
+  const int n_req0 = hdr->n_req[0];
+  const int n_req = hdr->n_req[1];
+  const int chunk = hdr->chunk[1];
+  const int n_cache = p.B < C::kReqCache ? (int)p.B : C::kReqCache;
+  if (warp == 0) {
+    constexpr int kV = C::kReqCache * (int)(sizeof(ReqInfo) / 16) / 32;   // int4 per lane
+    constexpr int kP = C::kReqCache / 32;
+    const int4* grec = reinterpret_cast<const int4*>(p.ws + sizeof(PlanHeader));
+    const int32_t* gpfx = plan_prefix(p.ws, p.B, 1);
+    const int n4 = n_cache * (int)(sizeof(ReqInfo) / 16);
+    int4 v[kV];
+    int32_t pf[kP];
+#pragma unroll
+    for (int k = 0; k < kV; ++k)
+      if (lane + 32 * k < n4) v[k] = grec[lane + 32 * k];
+#pragma unroll
+    for (int k = 0; k < kP; ++k)
+      if (lane + 32 * k < n_cache) pf[k] = gpfx[lane + 32 * k];
+    int4* crec = reinterpret_cast<int4*>(smem + C::req_off);
+    int32_t* cpfx = reinterpret_cast<int32_t*>(smem + C::pfx_off);
+#pragma unroll
+    for (int k = 0; k < kV; ++k)
+      if (lane + 32 * k < n4) crec[lane + 32 * k] = v[k];
+#pragma unroll
+    for (int k = 0; k < kP; ++k)
+      if (lane + 32 * k < n_cache) cpfx[lane + 32 * k] = pf[k];
+    __syncwarp();
+  }
   WaitCtl ctl{abort_flag, &hdr->err, p.wait_limit_ns};
 
   if (n_units == 0) {
     // no short requests in this call
   } else if (warp == 0) {
     // -------------------------------------------------------- scheduler --
+    const bool cached = n_req0 + n_req <= n_cache;
+    const ReqInfo* req = (cached ? reinterpret_cast<const ReqInfo*>(smem + C::req_off)
+                                 : reinterpret_cast<const ReqInfo*>(p.ws + sizeof(PlanHeader))) + n_req0;
+    const int32_t* prefix = cached ? reinterpret_cast<const int32_t*>(smem + C::pfx_off) : plan_prefix(p.ws, p.B, 1);
     if (lane == 0) {
-      const int n_req0 = *reinterpret_cast<volatile int*>(&hdr->n_req[0]);
-      const int n_req = *reinterpret_cast<volatile int*>(&hdr->n_req[1]);
-      const int chunk = *reinterpret_cast<volatile int*>(&hdr->chunk[1]);
-      const ReqInfo* req = reinterpret_cast<const ReqInfo*>(p.ws + sizeof(PlanHeader)) + n_req0;
-      const int32_t* prefix = plan_prefix(p.ws, p.B, 1);
       uint32_t ss = 0, sph = 0, rph = 0;
       for (bool first = true;; first = false) {
         if (!first) {
@@ -196,8 +232,9 @@ __global__ void __launch_bounds__(Short8::kThreads, 1)
           rph ^= 1;
         }
         UnitDesc d;
+        // the first unit of CTA i is unit i; later claims count from the grid size
         make_unit(p, req, prefix, n_req, n_units, chunk, p.np_short,
-                  atomicAdd(&hdr->counter[1], 1), d);
+                  first ? (int)blockIdx.x : (int)gridDim.x + atomicAdd(&hdr->counter[1], 1), d);
         if (!mbar_wait(b_sched_empty + 8 * ss, sph ^ 1, ctl)) break;
         ring[ss] = d;
         mbar_arrive(b_sched_full + 8 * ss);
@@ -234,11 +271,7 @@ __global__ void __launch_bounds__(Short8::kThreads, 1)
         ++n_q;
         if (++qb == C::kQBufs) { qb = 0; qph ^= 1; }
         const int32_t* trow = p.block_table + (int64_t)d.b * p.MB;
-        int nx0 = 0, nx1 = 0;   // page indices of the next item, read one item ahead
-        if (paged) {
-          nx0 = __ldg(trow + d.c0);
-          if (d.c0 + 1 < d.b1) nx1 = __ldg(trow + d.c0 + 1);
-        }
+        int nx0 = d.pg0, nx1 = d.pg1;   // the first pair's pages come with the unit
         bool ok = true;
         for (int beta = d.c0; beta < d.b1; beta += 2) {
           if (req_at >= beta && req_at < beta + 2) mbar_arrive(b_sched_req);

@@ -188,7 +188,11 @@ __global__ void __launch_bounds__(TileCfg<KI8>::kThreads, 1)
   const ReqInfo* req = reinterpret_cast<const ReqInfo*>(p.ws + sizeof(PlanHeader));
   const int32_t* prefix = plan_prefix(p.ws, p.B, 0);
   WaitCtl ctl{abort_flag, &hdr->err, p.wait_limit_ns};
-  const int n_units0 = *reinterpret_cast<volatile int*>(&hdr->n_units[0]);
+  // the header fields are read together: one round trip before the first claim
+  // (plain loads: the header is constant during this grid)
+  const int n_units0 = hdr->n_units[0];
+  const int chunk0 = hdr->chunk[0];
+  const int n_req0 = hdr->n_req[0];
 
   if (n_units0 == 0) {
     // no tile-class requests in this call
@@ -197,9 +201,6 @@ __global__ void __launch_bounds__(TileCfg<KI8>::kThreads, 1)
     // Claims one unit ahead: the first at once, each later one when the
     // producer is kLead blocks from the end of its current unit.
     if (lane == 0) {
-      const int n_units = *reinterpret_cast<volatile int*>(&hdr->n_units[0]);
-      const int chunk = *reinterpret_cast<volatile int*>(&hdr->chunk[0]);
-      const int n_req = *reinterpret_cast<volatile int*>(&hdr->n_req[0]);
       uint32_t ss = 0, sph = 0, rph = 0;
       for (bool first = true;; first = false) {
         if (!first) {
@@ -207,7 +208,9 @@ __global__ void __launch_bounds__(TileCfg<KI8>::kThreads, 1)
           rph ^= 1;
         }
         UnitDesc d;
-        make_unit(p, req, prefix, n_req, n_units, chunk, p.np, atomicAdd(&hdr->counter[0], 1), d);
+        // the first unit of CTA i is unit i; later claims count from the grid size
+        make_unit(p, req, prefix, n_req0, n_units0, chunk0, p.np,
+                  first ? (int)blockIdx.x : (int)gridDim.x + atomicAdd(&hdr->counter[0], 1), d);
         if (!mbar_wait(b_sched_empty + 8 * ss, sph ^ 1, ctl)) break;
         ring[ss] = d;
         mbar_arrive(b_sched_full + 8 * ss);
@@ -245,11 +248,7 @@ __global__ void __launch_bounds__(TileCfg<KI8>::kThreads, 1)
         if (++qb == L::kQBufs) { qb = 0; qph ^= 1; }
         // page indices of the next pair are read one pair ahead
         const int32_t* trow = p.block_table + (int64_t)d.b * p.MB;
-        int nx0 = 0, nx1 = 0;
-        if (paged) {
-          nx0 = __ldg(trow + d.c0);
-          if (d.c0 + 1 < d.b1) nx1 = __ldg(trow + d.c0 + 1);
-        }
+        int nx0 = d.pg0, nx1 = d.pg1;   // the first pair's pages come with the unit
         bool ok = true;
         for (int beta = d.c0; beta < d.b1; beta += 2) {
           if (req_at >= beta && req_at < beta + 2) mbar_arrive(b_sched_req);

@@ -65,10 +65,10 @@ __device__ __forceinline__ void make_unit(const Params& p, const ReqInfo* req,
   int lo = 0, hi = n_req - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
-    if (__ldg(prefix + mid) <= u) lo = mid; else hi = mid - 1;
+    if (prefix[mid] <= u) lo = mid; else hi = mid - 1;
   }
   const ReqInfo ri = req[lo];
-  const int ul = u - __ldg(prefix + lo);
+  const int ul = u - prefix[lo];
   const int per_hk = ri.ntiles * ri.nchunks;
   const int hk = ul / per_hk;
   const int rem = ul - hk * per_hk;
@@ -93,6 +93,13 @@ __device__ __forceinline__ void make_unit(const Params& p, const ReqInfo* req,
   d.b1 = max(d.c0, min(d.c1, nbc));
   d.kbase = ri.kbase;
   d.sl = ri.sl;
+  // the first pair's pages, so the producer can start the unit's loads at once
+  d.pg0 = d.pg1 = 0;
+  if (p.layout != 2 && d.b1 > d.c0) {
+    const int32_t* trow = p.block_table + (int64_t)ri.b * p.MB;
+    d.pg0 = __ldg(trow + d.c0);
+    if (d.c0 + 1 < d.b1) d.pg1 = __ldg(trow + d.c0 + 1);
+  }
 }
 
 // Max of the first (climit + 1) of N values (all if climit >= N - 1).
