@@ -17,19 +17,25 @@
 // scale goes into a TMEM column that the epilogue reads with the accumulator.
 //
 // Pipeline granularity.  Per page there is little arithmetic, and an mbarrier
-// wait costs a warp ~150 cycles even when the phase is already complete (the
-// MMA thread loses more: its queued MMAs drain first).  So every stage works on
-// items of two consecutive pages of a unit: one TMA stage, one converted-A
-// slot, one accumulator pair, one partial-maximum slot and one set of waits
-// per item.  The two converter groups take the two pages of an item side by
-// side.
+// wait costs a warp ~100-150 cycles even when the phase is already complete.
+// So every stage works on items of two consecutive pages of a unit: one TMA
+// stage, one converted-A slot, one accumulator pair, one partial-maximum slot
+// and one set of waits per item.
+//
+// The MMA warp never waits on an mbarrier: any shared-memory access by the
+// warp that issues tcgen05.mma first lets its queued MMAs drain, which with
+// these small MMAs idles the tensor pipe for a few hundred cycles per wait.  A
+// helper warp waits instead and passes each item on through a named barrier
+// (bar.red.popc: the count of the helper's set predicates is the item's code),
+// which keeps the queue flowing.
 //
 // Roles (one CTA per SM, units fetched from the short class's counter):
 //   warp 0        scheduler         warp 1  TMEM owner + MMA issuer
 //   warp 2        TMA producer      warp 3  combine: the four partial maxima of
 //                                           each block, local mask, stores
 //   warps 4..7    epilogue (partial maxima per token quarter)
-//   warps 8..11   converters of an item's first page, 12..15 of its second
+//   warps 8..11   converters (one token quarter of both pages of an item)
+//   warp 12       MMA helper: waits for each item's operands
 #pragma once
 #include <cstdint>
 #include <cuda.h>
@@ -42,10 +48,14 @@
 namespace msa {
 
 struct Short8 {
-  static constexpr int kThreads = 512;
+  static constexpr int kThreads = 416;
   static constexpr int kCombineWarp = 3;
   static constexpr int kEpiW0 = 4;
   static constexpr int kCvtW0 = 8;
+  static constexpr int kHelperWarp = 12;
+  static constexpr uint32_t kMmaBar = 1;                 // named barrier: helper -> MMA warp
+  // item codes passed through that barrier (0 = no more items)
+  static constexpr uint32_t kCodeLive = 1, kCodeTwo = 2, kCodeNarrow = 4, kCodeLast = 8;
   static constexpr uint32_t kPageBytes = 16384 + 1024;   // int8 page + its 128 scales
   static constexpr int kStages = 5;                      // items (two pages) in flight
   static constexpr uint32_t kStageBytes = 2 * kPageBytes;
@@ -133,8 +143,8 @@ __global__ void __launch_bounds__(Short8::kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  // readers of each unit descriptor: producer, MMA, combine, 4 epilogue, 8 converter warps
-  constexpr int kConsumers = 15;
+  // readers of each unit descriptor: producer, MMA helper, combine, 4 epilogue, 4 converter warps
+  constexpr int kConsumers = 11;
 
   asm volatile("griddepcontrol.launch_dependents;");
   if (threadIdx.x == 0) {
@@ -148,10 +158,10 @@ __global__ void __launch_bounds__(Short8::kThreads, 1)
     }
     for (int i = 0; i < S; ++i) {
       mbar_init(b_st_full + 8 * i, 1);
-      mbar_init(b_st_empty + 8 * i, 8);
+      mbar_init(b_st_empty + 8 * i, 4);
     }
     for (int i = 0; i < C::kA; ++i) {
-      mbar_init(b_a_full + 8 * i, 8);
+      mbar_init(b_a_full + 8 * i, 4);
       mbar_init(b_a_free + 8 * i, 1);
     }
     for (int i = 0; i < C::kD; ++i) {
@@ -334,58 +344,82 @@ __global__ void __launch_bounds__(Short8::kThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------- MMA issuer --
     // Items are numbered in stream order (it); item it uses A slot it % kA and
-    // accumulator pair it % kD.
-    if (lane == 0) {
-      constexpr uint32_t idesc32 = idesc_f16(BF16, 128, 32);
-      constexpr uint32_t idesc16 = idesc_f16(BF16, 128, 16);
-      uint32_t ss = 0, sph = 0, qb = 0, qph = 0, it = 0;
-      bool issued = false;
-      for (;;) {
-        if (!mbar_wait(b_sched_full + 8 * ss, sph, ctl)) break;
-        const UnitDesc d = ring[ss];
-        mbar_arrive(b_sched_empty + 8 * ss);
-        if (++ss == kSched) { ss = 0; sph ^= 1; }
-        if (!d.live) break;
-        if (d.b1 <= d.c0) continue;
-        if (!mbar_wait(b_q_full + 8 * qb, qph, ctl)) break;
+    // accumulator pair it % kD.  The warp touches no shared memory: the helper
+    // warp does the waiting and hands over each item through a named barrier
+    // whose thread count carries the item's code (kCode* bits; 0 = stop), so
+    // the MMAs of one item are still running while the next is issued.
+    constexpr uint32_t idesc32 = idesc_f16(BF16, 128, 32);
+    constexpr uint32_t idesc16 = idesc_f16(BF16, 128, 16);
+    uint32_t qb = 0, it = 0;
+    bool issued = false;
+    for (;; ++it) {
+      __syncwarp();   // the barrier counts whole warps: reconverge first
+      const uint32_t code = named_bar_popc(C::kMmaBar, 64, false);
+      if (code == 0) break;
+      tc_fence_after();
+      if (lane == 0) {
+        const uint32_t as = it % C::kA, ds = it % C::kD;
         const uint32_t qsrc = sbase + C::q_off + qb * C::kQBytes;
-        const uint32_t idesc = d.Lq * p.g <= 16 ? idesc16 : idesc32;   // N = 16 or 32 query rows
-        bool ok = true;
-        for (int beta = d.c0; beta < d.b1; beta += 2, ++it) {
-          const uint32_t as = it % C::kA, ds = it % C::kD;
-          // the first converter group saw the accumulator pair free before it
-          // arrived, so one wait covers both operands' readiness
-          if (!mbar_wait(b_a_full + 8 * as, (it / C::kA) & 1u, ctl)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const int npg = beta + 1 < d.b1 ? 2 : 1;
-          for (int j = 0; j < npg; ++j) {
-            const uint32_t at = tmem_base + as * 128u + 64u * j;
-            const uint32_t dt = tmem_base + C::kDCol0 + ds * (2u * C::kN) + (uint32_t)C::kN * j;
+        const uint32_t idesc = (code & C::kCodeNarrow) ? idesc16 : idesc32;   // N = 16 or 32 query rows
+        const int npg = (code & C::kCodeTwo) ? 2 : 1;
+        for (int j = 0; j < npg; ++j) {
+          const uint32_t at = tmem_base + as * 128u + 64u * j;
+          const uint32_t dt = tmem_base + C::kDCol0 + ds * (2u * C::kN) + (uint32_t)C::kN * j;
 #pragma unroll
-            for (int k = 0; k < 8; ++k)
-              tc_mma_f16_ta(dt, at + 8u * k,
-                            smem_desc_sw128(qsrc + (uint32_t)(k >> 2) * C::kQHalf + (k & 3) * 32u),
-                            idesc, k > 0 ? 1u : 0u);
-          }
-          tc_commit(b_a_free + 8 * as);
-          tc_commit(b_d_full + 8 * ds);
-          issued = true;
+          for (int k = 0; k < 8; ++k)
+            tc_mma_f16_ta(dt, at + 8u * k,
+                          smem_desc_sw128(qsrc + (uint32_t)(k >> 2) * C::kQHalf + (k & 3) * 32u),
+                          idesc, k > 0 ? 1u : 0u);
         }
-        if (!ok) break;
-        tc_commit(b_q_empty + 8 * qb);
-        if (++qb == C::kQBufs) { qb = 0; qph ^= 1; }
+        tc_commit(b_a_free + 8 * as);
+        tc_commit(b_d_full + 8 * ds);
+        if (code & C::kCodeLast) tc_commit(b_q_empty + 8 * qb);
       }
-      if (issued) {
-        tc_commit(b_drain);
-        const uint64_t t0 = global_timer_ns();
-        while (!mbar_try_wait(b_drain, 0) && global_timer_ns() - t0 < p.wait_limit_ns) {
-        }
+      if (code & C::kCodeLast) qb = qb + 1 == (uint32_t)C::kQBufs ? 0u : qb + 1;
+      issued = true;
+    }
+    if (lane == 0 && issued) {
+      tc_commit(b_drain);
+      const uint64_t t0 = global_timer_ns();
+      while (!mbar_try_wait(b_drain, 0) && global_timer_ns() - t0 < p.wait_limit_ns) {
       }
     }
     __syncwarp();
+  } else if (warp == C::kHelperWarp) {
+    // ------------------------------------------------------ MMA helper --
+    // Waits for what each item's MMAs read (the unit's query rows, the
+    // converted page pair, which also implies a free accumulator pair) and
+    // passes the item to the MMA warp.  Every path out of the loop ends with
+    // exactly one stop code, so the MMA warp's barrier waits always pair up.
+    uint32_t ss = 0, sph = 0, qb = 0, qph = 0, it = 0;
+    for (;;) {
+      if (!warp_wait(b_sched_full + 8 * ss, sph, ctl)) break;
+      const UnitDesc d = ring[ss];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(b_sched_empty + 8 * ss);
+      if (++ss == kSched) { ss = 0; sph ^= 1; }
+      if (!d.live) break;
+      if (d.b1 <= d.c0) continue;
+      if (!warp_wait(b_q_full + 8 * qb, qph, ctl)) break;
+      const uint32_t narrow = d.Lq * p.g <= 16 ? C::kCodeNarrow : 0u;
+      bool ok = true;
+      for (int beta = d.c0; beta < d.b1; beta += 2, ++it) {
+        // the first converter warp saw the accumulator pair free before it
+        // arrived, so one wait covers both operands' readiness
+        if (!warp_wait(b_a_full + 8 * (it % C::kA), (it / C::kA) & 1u, ctl)) {
+          ok = false;
+          break;
+        }
+        const uint32_t code = C::kCodeLive | narrow | (beta + 1 < d.b1 ? C::kCodeTwo : 0u) |
+                              (beta + 2 >= d.b1 ? C::kCodeLast : 0u);
+        __syncwarp();
+        (void)named_bar_popc(C::kMmaBar, 64, (uint32_t)lane < code);
+      }
+      if (!ok) break;
+      if (++qb == C::kQBufs) { qb = 0; qph ^= 1; }
+    }
+    __syncwarp();
+    (void)named_bar_popc(C::kMmaBar, 64, false);
   } else if (warp >= C::kEpiW0 && warp < C::kEpiW0 + 4) {
     // --------------------------------------------------------- epilogue --
     // Every warp reduces its 32 tokens of each page of an item for all rows
@@ -536,10 +570,9 @@ __global__ void __launch_bounds__(Short8::kThreads, 1)
                                                                      fill_value(beta + 2), fill_value(beta + 3)));
       }
     }
-  } else if (warp >= C::kCvtW0) {
+  } else if (warp >= C::kCvtW0 && warp < C::kCvtW0 + 4) {
     // ----------------------------------------- int8 -> fp16 into TMEM --
-    // Group j converts page j of every item.
-    const int jp = (warp - C::kCvtW0) >> 2;
+    // Warp q converts token rows 32q..32q+31 of both pages of every item.
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;                  // token row of the page
     const uint32_t t_lane = tmem_base + ((uint32_t)(quarter * 32) << 16);
@@ -554,55 +587,47 @@ __global__ void __launch_bounds__(Short8::kThreads, 1)
       bool ok = true;
       for (int beta = d.c0; beta < d.b1; beta += 2, ++it) {
         const uint32_t rs = it % S, as = it % C::kA;
-        const bool mine = beta + jp < d.b1;               // this group's page exists
-        if (!mine) {
-          // a lone last page: the item's other group does the work; this
-          // group only completes the item's phases, after the A slot is free
-          // (so it cannot run a whole stage ring ahead of the other group)
-          if (!warp_wait(b_a_free + 8 * as, ((it / C::kA) & 1u) ^ 1u, ctl)) { ok = false; break; }
-          if (jp == 0 && !warp_wait(b_d_free + 8 * (it % C::kD), ((it / C::kD) & 1u) ^ 1u, ctl)) {
-            ok = false;
-            break;
-          }
-          if (lane == 0) {
-            mbar_arrive(b_st_empty + 8 * rs);
-            mbar_arrive(b_a_full + 8 * as);
-          }
-          continue;
-        }
+        const int npg = beta + 1 < d.b1 ? 2 : 1;
         if (!warp_wait(b_st_full + 8 * rs, (it / S) & 1u, ctl)) { ok = false; break; }
-        const uint8_t* src = smem + C::k_off + rs * C::kStageBytes + (uint32_t)jp * C::kPageBytes;
-        const int page = raw_page[2 * rs + jp];
-        float sv = 0.f;
-        if (p.layout == 2) {
-          const int64_t trow = (int64_t)page + row;       // page holds the first key row here
-          if (trow < (int64_t)d.kbase + d.L && trow < p.NP) sv = __ldg(p.scale + trow * p.H_kv + d.hk);
-        } else if (page >= 0 && (int64_t)page < p.NP) {
-          sv = reinterpret_cast<const float*>(src + kRawBytes)[row];
-        }
-        // row of the page: 8 chunks of 16 bytes, stored 128-byte swizzled
-        int4 raw[8];
+        for (int jp = 0; jp < npg; ++jp) {
+          const uint8_t* src = smem + C::k_off + rs * C::kStageBytes + (uint32_t)jp * C::kPageBytes;
+          const int page = raw_page[2 * rs + jp];
+          float sv = 0.f;
+          if (p.layout == 2) {
+            const int64_t trow = (int64_t)page + row;     // page holds the first key row here
+            if (trow < (int64_t)d.kbase + d.L && trow < p.NP) sv = __ldg(p.scale + trow * p.H_kv + d.hk);
+          } else if (page >= 0 && (int64_t)page < p.NP) {
+            sv = reinterpret_cast<const float*>(src + kRawBytes)[row];
+          }
+          // row of the page: 8 chunks of 16 bytes, stored 128-byte swizzled
+          int4 raw[8];
 #pragma unroll
-        for (int c = 0; c < 8; ++c)
-          raw[c] = *reinterpret_cast<const int4*>(src + row * 128 + ((c ^ (row & 7)) << 4));
-        __syncwarp();
-        if (lane == 0) mbar_arrive(b_st_empty + 8 * rs);
-        uint32_t hv[64];
+          for (int c = 0; c < 8; ++c)
+            raw[c] = *reinterpret_cast<const int4*>(src + row * 128 + ((c ^ (row & 7)) << 4));
+          if (jp == npg - 1) {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(b_st_empty + 8 * rs);
+          }
+          uint32_t hv[64];
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          int8x4_to_half4((uint32_t)raw[c].x, hv[8 * c + 0], hv[8 * c + 1]);
-          int8x4_to_half4((uint32_t)raw[c].y, hv[8 * c + 2], hv[8 * c + 3]);
-          int8x4_to_half4((uint32_t)raw[c].z, hv[8 * c + 4], hv[8 * c + 5]);
-          int8x4_to_half4((uint32_t)raw[c].w, hv[8 * c + 6], hv[8 * c + 7]);
+          for (int c = 0; c < 8; ++c) {
+            int8x4_to_half4((uint32_t)raw[c].x, hv[8 * c + 0], hv[8 * c + 1]);
+            int8x4_to_half4((uint32_t)raw[c].y, hv[8 * c + 2], hv[8 * c + 3]);
+            int8x4_to_half4((uint32_t)raw[c].z, hv[8 * c + 4], hv[8 * c + 5]);
+            int8x4_to_half4((uint32_t)raw[c].w, hv[8 * c + 6], hv[8 * c + 7]);
+          }
+          if (jp == 0) {
+            if (!warp_wait(b_a_free + 8 * as, ((it / C::kA) & 1u) ^ 1u, ctl)) { ok = false; break; }
+            tc_fence_after();
+          }
+          tmem_st64(t_lane + as * 128u + 64u * jp, hv);
+          tmem_st1(t_lane + C::kScCol0 + (2u * it + jp) % C::kScCols, __float_as_uint(sv));
         }
-        if (!warp_wait(b_a_free + 8 * as, ((it / C::kA) & 1u) ^ 1u, ctl)) { ok = false; break; }
-        tc_fence_after();
-        tmem_st64(t_lane + as * 128u + 64u * jp, hv);
-        tmem_st1(t_lane + C::kScCol0 + (2u * it + jp) % C::kScCols, __float_as_uint(sv));
+        if (!ok) break;
         tmem_wait_st();
-        // group 0 also waits until the epilogue has read the accumulator pair
-        // this item will use, so the MMA thread waits on one barrier per item
-        if (jp == 0 && !warp_wait(b_d_free + 8 * (it % C::kD), ((it / C::kD) & 1u) ^ 1u, ctl)) {
+        // one warp also waits until the epilogue has read the accumulator pair
+        // this item will use: the item is ready only after all four arrived
+        if (quarter == 0 && !warp_wait(b_d_free + 8 * (it % C::kD), ((it / C::kD) & 1u) ^ 1u, ctl)) {
           ok = false;
           break;
         }
