@@ -446,6 +446,12 @@ __global__ void __launch_bounds__(Short8::kThreads, 1)
         const int64_t m = (int64_t)(t - qbase) * p.g;
         return m > C::kN ? C::kN : (int)m;
       };
+      // both pages of the item below the kv length and at or before the
+      // first row's position: nothing to mask (warp-uniform)
+      auto all_visible = [&](int beta, bool two) -> bool {
+        const int t_end = (beta + 2) * kP;                // one past the item's last token
+        return two && t_end <= d.L && t_end - 1 <= qbase;
+      };
       bool ok = true;
       for (int beta = d.c0; beta < d.b1; beta += 2, ++it) {
         const uint32_t ds = it % C::kD;
@@ -468,11 +474,19 @@ __global__ void __launch_bounds__(Short8::kThreads, 1)
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(b_d_free + 8 * ds);
-          const int n0 = first_row(beta), n1 = two ? first_row(beta + 1) : C::kN;
+          if (all_visible(beta, two)) {
 #pragma unroll
-          for (int c = 0; c < 16; ++c) {
-            x[c] = c >= n0 ? x[c] * sc0 : ninf;                 // DEQUANT, MASK
-            x[16 + c] = c >= n1 ? x[16 + c] * sc1 : ninf;
+            for (int c = 0; c < 16; ++c) {
+              x[c] *= sc0;                                       // DEQUANT
+              x[16 + c] *= sc1;
+            }
+          } else {
+            const int n0 = first_row(beta), n1 = two ? first_row(beta + 1) : C::kN;
+#pragma unroll
+            for (int c = 0; c < 16; ++c) {
+              x[c] = c >= n0 ? x[c] * sc0 : ninf;               // DEQUANT, MASK
+              x[16 + c] = c >= n1 ? x[16 + c] * sc1 : ninf;
+            }
           }
           const float mine = warp_transpose_max32(x, lane);
           if (!warp_wait(b_red_empty + 8 * rr, rph ^ 1, ctl)) { ok = false; break; }
@@ -485,11 +499,19 @@ __global__ void __launch_bounds__(Short8::kThreads, 1)
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(b_d_free + 8 * ds);
-          const int n0 = first_row(beta), n1 = two ? first_row(beta + 1) : C::kN;
+          if (all_visible(beta, two)) {
 #pragma unroll
-          for (int c = 0; c < 32; ++c) {
-            x0[c] = c >= n0 ? x0[c] * sc0 : ninf;
-            x1[c] = c >= n1 ? x1[c] * sc1 : ninf;
+            for (int c = 0; c < 32; ++c) {
+              x0[c] *= sc0;
+              x1[c] *= sc1;
+            }
+          } else {
+            const int n0 = first_row(beta), n1 = two ? first_row(beta + 1) : C::kN;
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
+              x0[c] = c >= n0 ? x0[c] * sc0 : ninf;
+              x1[c] = c >= n1 ? x1[c] * sc1 : ninf;
+            }
           }
           const float m0 = warp_transpose_max32(x0, lane);
           const float m1 = warp_transpose_max32(x1, lane);
