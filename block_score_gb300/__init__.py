@@ -28,6 +28,7 @@ __all__ = [
     "msa_index_score", "msa_index_score_plan", "msa_index_score_run",
     "msa_index_score_workspace_size", "msa_index_score_out_shape", "msa_get_device_error",
     "MsaError", "library_path", "load_library", "DEVERR", "msa_index_score_noalloc",
+    "msa_block_topk",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -91,12 +92,14 @@ def load_library():
     lib.msa_index_score_run.argtypes = [P, vp, vp, sz, vp]
     lib.msa_get_device_error.argtypes = [vp, ctypes.POINTER(ctypes.c_int32), vp]
     lib.msa_index_score_noalloc.argtypes = [P, vp, vp]
+    lib.msa_block_topk.argtypes = [vp, ctypes.c_int32, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32,
+                                   ctypes.c_int32, vp, vp]
     lib.msa_status_string.restype = ctypes.c_char_p
     lib.msa_status_string.argtypes = [ctypes.c_int]
     lib.msa_last_error_message.restype = ctypes.c_char_p
     for name in ("msa_index_score_out_shape", "msa_index_score_workspace_size",
                  "msa_index_score", "msa_index_score_plan", "msa_index_score_run",
-                 "msa_get_device_error", "msa_index_score_noalloc"):
+                 "msa_get_device_error", "msa_index_score_noalloc", "msa_block_topk"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -291,6 +294,28 @@ def msa_index_score_noalloc(prepared: "Prepared", out: Optional[torch.Tensor] = 
     out = prepared.out if out is None else out
     _check(load_library().msa_index_score_noalloc(ctypes.byref(prepared.call.args),
                                                   out.data_ptr(), _stream_handle(stream)))
+    return out
+
+
+def msa_block_topk(score: torch.Tensor, k: int = 16, MB: Optional[int] = None,
+                   out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Top-k blocks of every score row: int32 ``[T, H, k]``, block indices ascending, -1 tail.
+
+    ``score`` is a contiguous fp32 CUDA tensor ``[H, T, MBp]`` (msa_index_score's
+    output); ``MB`` is the number of valid columns (default: all ``MBp``).
+    """
+    if not score.is_cuda or score.dtype != torch.float32 or score.dim() != 3:
+        raise ValueError("score must be a float32 CUDA tensor [H, T, MBp]")
+    score = score.contiguous()
+    H, T, MBp = score.shape
+    MB = MBp if MB is None else int(MB)
+    shape = (T, H, int(k))
+    if out is None:
+        out = torch.empty(shape, dtype=torch.int32, device=score.device)
+    elif tuple(out.shape) != shape or out.dtype != torch.int32 or not out.is_contiguous():
+        raise ValueError(f"out must be a contiguous int32 tensor of shape {shape}")
+    _check(load_library().msa_block_topk(score.data_ptr(), H, T, MBp, MB, int(k), out.data_ptr(),
+                                         _stream_handle(stream)))
     return out
 
 

@@ -390,6 +390,21 @@ msa_status_t msa_index_score(const msa_index_score_args* args, float* out, void*
   return launch_score_checked(args, p, s);
 }
 
+msa_status_t msa_block_topk(const float* score, int32_t H, int64_t T, int32_t MBp, int32_t MB,
+                            int32_t k, int32_t* out, msa_stream_t stream) {
+  if (H < 0 || T < 0 || MBp < 0 || MB < 0) return fail(MSA_ERR_INVALID_ARG, "sizes must be >= 0");
+  if (MB > MBp) return fail(MSA_ERR_INVALID_ARG, "MB must be <= MBp");
+  if (k < 1 || k > 32) return fail(MSA_ERR_INVALID_ARG, "k must be in [1, 32]");
+  if ((int64_t)H * T == 0) return MSA_OK;
+  if (!out || (!score && MB > 0)) return fail(MSA_ERR_INVALID_ARG, "score and out are required");
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  e = msa::launch_topk(score, H, T, MBp, MB, k, out, sm_count(dev), reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "top-k kernel launch");
+  return MSA_OK;
+}
+
 msa_status_t msa_get_device_error(const void* workspace, int32_t* bits, msa_stream_t stream) {
   if (!workspace || !bits) return fail(MSA_ERR_INVALID_ARG, "workspace and bits are required");
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);

@@ -108,6 +108,8 @@ void set_last_error_message(const char* msg);
 
 // Host-side launchers (defined in the .cu files).
 cudaError_t launch_plan(const Params& p, cudaStream_t s);
+cudaError_t launch_topk(const float* score, int H, long long T, int MBp, int MB, int k, int32_t* out,
+                        int num_sms, cudaStream_t s);
 cudaError_t launch_score_16(const void* tmap_q, const void* tmap_k, const Params& p, bool bf16,
                             cudaStream_t s);
 cudaError_t launch_score_i8(const void* tmap_q, const void* tmap_k, const Params& p,

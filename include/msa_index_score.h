@@ -47,7 +47,7 @@
 extern "C" {
 #endif
 
-#define MSA_ABI_VERSION 2
+#define MSA_ABI_VERSION 3
 
 /* Same object as cudaStream_t / CUstream (NULL = legacy default stream). */
 typedef struct CUstream_st *msa_stream_t;
@@ -182,6 +182,36 @@ msa_status_t msa_index_score_run(const msa_index_score_args *args, float *out, v
 #define MSA_NOALLOC_WORKSPACE_BYTES 41216
 msa_status_t msa_index_score_noalloc(const msa_index_score_args *args, float *out,
                                      msa_stream_t stream);
+
+/*
+ * Block top-k selection, the consumer of the block scores (MiniMax Sparse
+ * Attention notes, section 4.7: Equation (7) I_i = TopK_b(M_i, k) over a
+ * query's block scores, and the selector contract quoted there and in
+ * section 5.3).
+ *
+ *   score  device, fp32 [H, T, MBp] row-major: msa_index_score's output (or
+ *          any score tensor of that layout); read only.
+ *   MB     valid columns of a row (0 <= MB <= MBp); columns [MB, MBp) are
+ *          never selected.
+ *   k      blocks per row, 1 <= k <= 32 (the pages' selector fixes 16).
+ *   out    device, int32 [T, H, k] row-major, written completely: for row
+ *          (h, t), out[t, h, :] lists the k blocks with the highest score in
+ *          ascending block-index order (not score order), followed by -1
+ *          when fewer than k blocks are valid.
+ *
+ * A block is valid when its score is above -inf (-inf marks a block with no
+ * visible key; a NaN score is never selected).  Equal scores rank the smaller
+ * block index first.  The local mask's forced blocks (1e30 / 1e29) therefore
+ * always make the selection when k covers them.  When H_q > H_kv the
+ * selection is per index head; a caller that wants one selection per GQA group
+ * (section 4.3, Equation (3)) passes one representative head per group.
+ *
+ * Asynchronous on `stream`; no workspace, no allocation.  Returns
+ * MSA_ERR_INVALID_ARG for null pointers with work to do, negative sizes,
+ * MB > MBp or k outside [1, 32]; MSA_ERR_CUDA if the launch fails.
+ */
+msa_status_t msa_block_topk(const float *score, int32_t H, int64_t T, int32_t MBp, int32_t MB,
+                            int32_t k, int32_t *out, msa_stream_t stream);
 
 /* Synchronise `stream` and read the device error word left in `workspace`
  * by the last call (MSA_DEVERR_* bits; 0 = clean).  Returns MSA_OK, or

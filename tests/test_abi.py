@@ -31,7 +31,7 @@ def test_header_declares_the_entry_points():
     for want in ("msa_index_score", "msa_index_score_plan", "msa_index_score_run",
                  "msa_index_score_out_shape", "msa_index_score_workspace_size",
                  "msa_get_device_error", "msa_status_string", "msa_last_error_message",
-                 "msa_abi_version"):
+                 "msa_abi_version", "msa_block_topk"):
         assert want in names
 
 
@@ -46,7 +46,7 @@ def test_library_is_sm103a_only():
 
 
 def test_abi_version(lib):
-    assert lib.msa_abi_version() == 2
+    assert lib.msa_abi_version() == 3
 
 
 def _args(**over):
@@ -143,3 +143,15 @@ def test_python_binding_unsqueezes_3d_bbnd_key():
         actual_seq_klen=torch.tensor([10], dtype=torch.int32),
         block_table=torch.zeros(1, 3, dtype=torch.int32))
     assert shape == (2, 4, 16)
+
+
+@pytest.mark.parametrize("H,T,MBp,MB,k,status", [
+    (2, 3, 16, 6, 0, 1),      # k below 1
+    (2, 3, 16, 6, 33, 1),     # k above 32
+    (2, 3, 16, 17, 4, 1),     # MB > MBp
+    (-1, 3, 16, 6, 4, 1),     # negative size
+    (0, 3, 16, 6, 4, 0),      # no rows: nothing to do, no launch
+    (2, 0, 16, 6, 4, 0),
+])
+def test_block_topk_host_validation(lib, H, T, MBp, MB, k, status):
+    assert lib.msa_block_topk(None, H, T, MBp, MB, k, None, None) == status

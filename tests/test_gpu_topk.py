@@ -1,0 +1,133 @@
+"""GPU parity for the block top-k selection (msa_block_topk) against the oracle.
+
+The selection is integer output: the CUDA path must equal oracle.topk bit for
+bit on the same fp32 scores (hand fixture, random rows full of ties, -inf and
+NaN, oracle score tensors with forced blocks, a large multi-wave tensor on
+sampled rows).  Fed with the GPU's own scores, the selection is checked by
+properties against the oracle's scores, since scores within the score
+tolerance of each other may swap at the k-th place.
+
+Definition: MiniMax Sparse Attention notes, section 4.7 (Equation (7) and
+the selector contract) and section 5.3.
+"""
+import json
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from oracle import topk as otk
+
+pytestmark = pytest.mark.gpu
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "topk_hand_example.json")
+
+
+@pytest.fixture(scope="module")
+def dev():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import block_score_gb300 as bs
+    bs.load_library()
+    return torch.device("cuda:0")
+
+
+def gpu_topk(score_cpu, MB, k, dev):
+    import block_score_gb300 as bs
+    out = bs.msa_block_topk(score_cpu.to(dev), k=k, MB=MB)
+    torch.cuda.synchronize()
+    return out.cpu().numpy()
+
+
+def test_hand_example(dev):
+    spec = json.load(open(GOLDEN))
+    H, T, MB, MBp, k = spec["H"], spec["T"], spec["MB"], spec["MBp"], spec["k"]
+    score = torch.full((H, T, MBp), float("-inf"))
+    conv = {"-inf": float("-inf"), "nan": float("nan")}
+    for key, vals in spec["rows"].items():
+        score[int(key[1]), int(key[3]), :MB] = torch.tensor([conv.get(v, v) if isinstance(v, str) else v
+                                                             for v in vals])
+    for key, cols in spec["padding_overrides"].items():
+        for c, v in cols.items():
+            score[int(key[1]), int(key[3]), int(c)] = v
+    out = gpu_topk(score, MB, k, dev)
+    for key, exp in spec["expect"].items():
+        assert out[int(key[3]), int(key[1])].tolist() == exp, key
+
+
+@pytest.mark.parametrize("MB,k", [(0, 4), (1, 1), (5, 16), (31, 16), (32, 16), (33, 7), (100, 32),
+                                  (512, 16), (1104, 16), (2000, 32), (4100, 8)])
+@pytest.mark.parametrize("kind", ["ties", "normal", "forced"])
+def test_random_rows_bit_exact(dev, MB, k, kind):
+    g = torch.Generator().manual_seed(MB * 7 + k + len(kind))
+    H, T = 3, 37
+    MBp = max(16, (MB + 15) // 16 * 16)
+    score = torch.full((H, T, MBp), float("-inf"))
+    if MB:
+        if kind == "ties":
+            body = torch.randint(-3, 4, (H, T, MB), generator=g).float()
+        elif kind == "normal":
+            body = torch.randn(H, T, MB, generator=g)
+        else:
+            body = torch.randn(H, T, MB, generator=g)
+            forced = torch.rand(H, T, MB, generator=g) < 0.05
+            body[forced] = 1e29
+            body[:, :, 0] = 1e30
+        body[torch.rand(H, T, MB, generator=g) < 0.2] = float("-inf")
+        body[torch.rand(H, T, MB, generator=g) < 0.01] = float("nan")
+        score[:, :, :MB] = body
+    if MBp > MB:
+        score[:, :, MB:] = 5e30                      # padding columns are never selected
+    out = gpu_topk(score, MB, k, dev)
+    assert np.array_equal(out, otk.block_topk(score, MB, k))
+
+
+def test_oracle_scores_with_local_mask(dev):
+    case = synth.make_case([5, 1, 3], [2000, 900, 0], H_q=4, H_kv=2, layout="BNBD",
+                           q_dtype=torch.bfloat16, MB=20, init_blocks=2, local_blocks=4, seed=11)
+    score = oracle.oracle_full(case)
+    for k in (1, 6, 16, 32):
+        assert np.array_equal(gpu_topk(score, case.MB, k, dev), otk.block_topk(score, case.MB, k))
+
+
+def test_large_tensor_sampled_rows(dev):
+    # [16, 4096, 1104]: ~290 MB, many waves of the persistent grid
+    g = torch.Generator().manual_seed(5)
+    H, T, MB, MBp, k = 16, 4096, 1100, 1104, 16
+    score = torch.randn(H, T, MBp, generator=g)
+    score[:, :, :4] = 1e30
+    score[:, :, MB - 8:MB] = 1e29
+    score[:, :, MB:] = float("-inf")
+    out = gpu_topk(score, MB, k, dev)
+    rows = torch.randint(0, H * T, (1500,), generator=g).tolist() + [0, H * T - 1]
+    ref = otk.block_topk(score, MB, k, rows=rows)
+    for r in rows:
+        h, t = divmod(r, T)
+        assert out[t, h].tolist() == ref[t, h].tolist(), r
+
+
+def test_gpu_scores_then_topk_by_property(dev):
+    import block_score_gb300 as bs
+    case = synth.config(3)
+    ref = oracle.oracle_rows(case, list(range(0, case.H_q * case.T, 997)))
+    prep = bs.from_case(case, dev)
+    scores = prep()
+    sel = bs.msa_block_topk(scores, k=16, MB=case.MB).cpu().numpy()
+    torch.cuda.synchronize()
+    rows = list(range(0, case.H_q * case.T, 997))
+    for i, r in enumerate(rows):
+        h, t = divmod(r, case.T)
+        s = ref[i, :case.MB].numpy().astype(np.float64)
+        valid = np.nonzero(s > -np.inf)[0]
+        chosen = sel[t, h][sel[t, h] >= 0]
+        assert chosen.size == min(16, valid.size)
+        assert set(chosen.tolist()) <= set(valid.tolist())
+        if chosen.size < valid.size:
+            kth = np.sort(s[valid])[::-1][15]
+            tol = 1e-3 + 1e-4 * abs(kth)
+            rest = np.setdiff1d(valid, chosen)
+            assert s[chosen].min() >= kth - tol
+            assert s[rest].max() <= kth + tol
