@@ -35,6 +35,8 @@ if ROOT not in sys.path:
 
 import torch  # noqa: E402
 
+L2_BYTES = 126 * 1024 * 1024   # GB300 L2 (spec: ~129 MB); inputs below it are cache-resident
+
 import synth  # noqa: E402
 
 METRIC = "MsaIndexScore µs/call, TFLOP/s and K-cache GB/s vs GB300 roofline (1 GPU)"
@@ -409,6 +411,9 @@ def run_ours(args):
     # end to end through the C ABI with host buffers: H2D of the inputs, the
     # call, D2H of the scores, every step
     e2e = e2e_run(case, device, stream, args)
+    # the block top-k selection over this call's scores (the scores' consumer;
+    # not part of the metric above)
+    topk = topk_run(prep.out, case.MB, 16, device, stream, peaks, min(args.steps, 200))
 
     call_s = step_ms / 1e3
     kern_s = kern_ms / 1e3
@@ -447,6 +452,7 @@ def run_ours(args):
         "frac_tensor": tflops / peaks["bf16_tflops"],
         "roofline": roof,
         "e2e": e2e,
+        "topk": topk,
         "gpu_launches": launches_per_call(case) * args.steps,
         "clocks": sampler.summary(),
     }
@@ -458,6 +464,29 @@ def run_ours(args):
         import torch.distributed as dist
         dist.destroy_process_group()
     return 0
+
+
+def topk_run(score, MB: int, k: int, device, stream, peaks, steps: int):
+    """Time msa_block_topk over a score tensor: events around each launch."""
+    import block_score_gb300 as bs
+    H, T, MBp = score.shape
+    out = bs.msa_block_topk(score, k=k, MB=MB, stream=stream)
+    for _ in range(3):
+        bs.msa_block_topk(score, k=k, MB=MB, out=out, stream=stream)
+    torch.cuda.synchronize(device)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    for a, b in evs:
+        a.record(stream)
+        bs.msa_block_topk(score, k=k, MB=MB, out=out, stream=stream)
+        b.record(stream)
+    torch.cuda.synchronize(device)
+    us = statistics.mean(a.elapsed_time(b) for a, b in evs) * 1e3
+    nbytes = H * T * MBp * 4 + T * H * k * 4      # scores read once, indices written
+    gbs = nbytes / us / 1e3
+    return {"k": k, "rows": H * T, "us_per_call": us, "bytes": nbytes, "achieved_gbs": gbs,
+            "peak_gbs": peaks["hbm_gbs"], "frac": gbs / peaks["hbm_gbs"],
+            "inputs_in_l2": nbytes < L2_BYTES, "kernel": "topk_kernel"}
 
 
 def e2e_run(case, device, stream, args):
