@@ -37,7 +37,8 @@ _LIB = os.path.join(_HERE, "libmsa_oracle.so")
 _lock = threading.Lock()
 _lib = None
 
-_DT = {torch.float16: 0, torch.bfloat16: 1, torch.int8: 2}
+_DT = {torch.float16: 0, torch.bfloat16: 1, torch.int8: 2,
+       torch.float8_e4m3fn: 3, torch.float8_e5m2: 4}
 _LAYOUT = {"BBND": 0, "BNBD": 1, "TND": 2}
 
 
@@ -82,6 +83,8 @@ def _load():
         lib.msa_oracle_full.restype = ctypes.c_int
         lib.msa_oracle_threads.argtypes = [ctypes.c_int]
         lib.msa_oracle_threads.restype = ctypes.c_int
+        lib.msa_oracle_decode.argtypes = [ctypes.c_int32, ctypes.c_uint32]
+        lib.msa_oracle_decode.restype = ctypes.c_double
         _lib = lib
     return _lib
 
@@ -176,6 +179,11 @@ def oracle_rows(case, rows: Sequence[int], nthreads: int = 0,
         if nbad:
             raise ValueError(f"oracle: {nbad} rows read an out-of-range table entry")
     return out
+
+
+def decode(dtype: torch.dtype, bits: int) -> float:
+    """The oracle's decoding of one element bit pattern of ``dtype``."""
+    return float(_load().msa_oracle_decode(_DT[dtype], bits))
 
 
 def oracle_threads(nthreads: int = 0) -> int:

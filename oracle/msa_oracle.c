@@ -33,7 +33,11 @@
  *   - arithmetic: products and sums in fp64 (all inputs are exact in fp64),
  *     int8 scale multiplied in fp64, one rounding to fp32 at the end.
  *
- * Element types: 0 = fp16, 1 = bf16, 2 = int8 (keys only).
+ * Element types: 0 = fp16, 1 = bf16, 2 = int8 (keys only), 3 = fp8 e4m3fn,
+ * 4 = fp8 e5m2 (query and key of the same FP8 type, no scale: torch API guide,
+ * sec. 4 and 7.2).  The FP8 decodings follow the OCP 8-bit floating point
+ * formats (E4M3: bias 7, no infinities, S.1111.111 is NaN; E5M2: bias 15,
+ * IEEE-style infinities and NaNs).
  * Layouts: 0 = BBND [NP,P,H_kv,D], 1 = BNBD [NP,H_kv,P,D], 2 = TND [T2,H_kv,D].
  */
 #include <math.h>
@@ -46,11 +50,11 @@
 
 typedef struct {
     const void *query;          /* [T, H_q, D] contiguous */
-    int32_t q_dtype;            /* 0 fp16, 1 bf16 */
+    int32_t q_dtype;            /* 0 fp16, 1 bf16, 3 e4m3fn, 4 e5m2 */
     int64_t T;
     int32_t H_q, D;
     const void *key;            /* layout below; dim0 stride = page_stride elements */
-    int32_t k_dtype;            /* 0 fp16, 1 bf16, 2 int8 */
+    int32_t k_dtype;            /* 0 fp16, 1 bf16, 2 int8, 3 e4m3fn, 4 e5m2 */
     int32_t layout;             /* 0 BBND, 1 BNBD, 2 TND */
     int64_t NP;                 /* pages (paged) or T2 rows (TND) */
     int32_t P, H_kv;
@@ -89,10 +93,42 @@ static double bf16_to_double(uint16_t h)
     return (double)f;
 }
 
+/* FP8 E4M3 (the "fn" variant: finite only) -> double: 1/4/3 bits, bias 7. */
+static double e4m3_to_double(uint8_t b)
+{
+    int s = (b >> 7) & 1, e = (b >> 3) & 0xf, m = b & 7;
+    double v;
+    if (e == 15 && m == 7)
+        v = NAN;
+    else if (e == 0)
+        v = ldexp((double)m, -9);                /* subnormal: (m/8) * 2^-6 */
+    else
+        v = ldexp((double)(m + 8), e - 10);      /* (1 + m/8) * 2^(e-7) */
+    return s ? -v : v;
+}
+
+/* FP8 E5M2 -> double: 1/5/2 bits, bias 15, exponent 31 = inf / NaN. */
+static double e5m2_to_double(uint8_t b)
+{
+    int s = (b >> 7) & 1, e = (b >> 2) & 0x1f, m = b & 3;
+    double v;
+    if (e == 31)
+        v = m ? NAN : INFINITY;
+    else if (e == 0)
+        v = ldexp((double)m, -16);               /* subnormal: (m/4) * 2^-14 */
+    else
+        v = ldexp((double)(m + 4), e - 17);      /* (1 + m/4) * 2^(e-15) */
+    return s ? -v : v;
+}
+
 static double load_elem(const void *base, int32_t dtype, int64_t idx)
 {
     if (dtype == 2)
         return (double)((const int8_t *)base)[idx];
+    if (dtype == 3)
+        return e4m3_to_double(((const uint8_t *)base)[idx]);
+    if (dtype == 4)
+        return e5m2_to_double(((const uint8_t *)base)[idx]);
     uint16_t bits = ((const uint16_t *)base)[idx];
     return dtype == 1 ? bf16_to_double(bits) : half_to_double(bits);
 }
@@ -243,4 +279,13 @@ int msa_oracle_threads(int nthreads)
     (void)nthreads;
     return 1;
 #endif
+}
+
+/* Decode one element of the given type (for tests of the decoders). */
+double msa_oracle_decode(int32_t dtype, uint32_t bits)
+{
+    if (dtype == 2) return (double)(int8_t)(uint8_t)bits;
+    if (dtype == 3) return e4m3_to_double((uint8_t)bits);
+    if (dtype == 4) return e5m2_to_double((uint8_t)bits);
+    return dtype == 1 ? bf16_to_double((uint16_t)bits) : half_to_double((uint16_t)bits);
 }

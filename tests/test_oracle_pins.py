@@ -408,3 +408,41 @@ def test_row_sampling_matches_full():
     part = oracle.oracle_rows(case, rows).numpy()
     for i, r in enumerate(rows):
         assert np.array_equal(part[i], full[r // case.T, r % case.T])
+
+
+# ---------------------------------------------------------------- FP8 inputs
+# FP8 query and key of one type, no scale (torch API guide, sec. 4 and 7.2).
+
+@pytest.mark.parametrize("dt", [torch.float8_e4m3fn, torch.float8_e5m2])
+def test_fp8_decoding_matches_torch_for_every_bit_pattern(dt):
+    bits = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    ref = bits.view(dt).to(torch.float64).numpy()
+    got = np.array([oracle.decode(dt, int(b)) for b in range(256)])
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+
+
+@pytest.mark.parametrize("layout", ["BBND", "BNBD", "TND"])
+@pytest.mark.parametrize("dt", [torch.float8_e4m3fn, torch.float8_e5m2])
+@pytest.mark.parametrize("mode", [0, 3])
+def test_fp8_oracle_matches_dense_amax(layout, dt, mode):
+    case = make_case([5, 0, 3, 9, 1], [21, 6, 0, 9, 33], H_q=6, H_kv=3, P=8, D=16,
+                     layout=layout, q_dtype=dt, k_dtype=dt, sparse_mode=mode,
+                     init_blocks=1, local_blocks=2, MB=6 if layout != "TND" else None,
+                     seed=41 + mode)
+    _compare_with_bruteforce(case)
+
+
+def test_fp8_one_hot_reads_the_key_value():
+    # q = e_0 (1.0 is exact in both formats): each score is the largest visible
+    # k[j, 0] of the block, decoded by torch from the same bytes
+    dt = torch.float8_e4m3fn
+    case = make_case([1], [300], H_q=2, H_kv=1, P=128, D=128, layout="BBND",
+                     q_dtype=dt, k_dtype=dt, q_kind="onehot_d0", sparse_mode=0,
+                     init_blocks=0, local_blocks=0, MB=3, seed=3)
+    out = oracle.oracle_full(case).numpy()
+    keys = bruteforce._gather_keys(case, 0, 300, 3)      # [300, H_kv, D] fp64 via torch
+    for beta in range(3):
+        lo, hi = beta * 128, min(300, beta * 128 + 128)
+        assert out[0, 0, beta] == np.float32(keys[lo:hi, 0, 0].max())
