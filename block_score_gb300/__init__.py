@@ -38,7 +38,8 @@ MSA_OK = 0
 _STATUS_EXC = {1: ValueError, 2: NotImplementedError}
 DEVERR = {0x01: "cu_seqlens_q", 0x02: "kv_len", 0x04: "cu_seqlens_k",
           0x08: "block_table", 0x10: "timeout"}
-_DT = {torch.float16: 0, torch.bfloat16: 1, torch.int8: 2}
+_DT = {torch.float16: 0, torch.bfloat16: 1, torch.int8: 2,
+       torch.float8_e4m3fn: 3, torch.float8_e5m2: 4}
 _LAYOUT = {"BBND": 0, "BNBD": 1, "TND": 2}
 
 

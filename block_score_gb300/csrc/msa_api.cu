@@ -34,7 +34,9 @@ bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 
 int64_t round16(int64_t x) { return (x + 15) / 16 * 16; }
 
-int elem_size(msa_dtype_t t) { return t == MSA_I8 ? 1 : 2; }
+bool is_f8(msa_dtype_t t) { return t == MSA_E4M3 || t == MSA_E5M2; }
+
+int elem_size(msa_dtype_t t) { return (t == MSA_I8 || is_f8(t)) ? 1 : 2; }
 
 // Host-side checks; everything that can be judged without reading device memory.
 msa_status_t validate(const msa_index_score_args* a) {
@@ -43,9 +45,13 @@ msa_status_t validate(const msa_index_score_args* a) {
     return fail(MSA_ERR_INVALID_ARG, "layout must be BBND, BNBD or TND");
   if (a->sparse_mode != 0 && a->sparse_mode != 3)
     return fail(MSA_ERR_INVALID_ARG, "sparse_mode must be 0 or 3");
-  if (a->q_dtype != MSA_F16 && a->q_dtype != MSA_BF16)
-    return fail(MSA_ERR_INVALID_ARG, "query dtype must be fp16 or bf16");
-  if (a->k_dtype == MSA_I8) {
+  if (a->q_dtype != MSA_F16 && a->q_dtype != MSA_BF16 && !is_f8(a->q_dtype))
+    return fail(MSA_ERR_INVALID_ARG, "query dtype must be fp16, bf16, fp8 e4m3 or fp8 e5m2");
+  if (is_f8(a->q_dtype) || is_f8(a->k_dtype)) {
+    if (a->k_dtype != a->q_dtype)
+      return fail(MSA_ERR_INVALID_ARG, "fp8 query and key must be of the same fp8 type");
+    if (a->scale) return fail(MSA_ERR_INVALID_ARG, "fp8 inputs take no scale");
+  } else if (a->k_dtype == MSA_I8) {
     if (a->q_dtype != MSA_F16) return fail(MSA_ERR_INVALID_ARG, "int8 key requires an fp16 query");
     if (!a->scale) return fail(MSA_ERR_INVALID_ARG, "int8 key requires scale");
   } else if (a->k_dtype == MSA_F16 || a->k_dtype == MSA_BF16) {
@@ -225,14 +231,17 @@ msa_status_t make_maps(const msa_index_score_args* a, const msa::Params& p, CUte
                        CUtensorMap* tk, CUtensorMap* tq_short, CUtensorMap* tk_short) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return fail(MSA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
-  const CUtensorMapDataType qdt =
-      a->q_dtype == MSA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-  // query [T, H_q, D]: dims (D, H_q, T); a box is (64, g, positions): one GQA
-  // group x a run of positions, 128-byte swizzled
+  const bool f8 = is_f8(a->q_dtype);
+  const CUtensorMapDataType qdt = f8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                  : a->q_dtype == MSA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                           : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  const cuuint64_t qsz = f8 ? 1 : 2;
+  // query [T, H_q, D]: dims (D, H_q, T); a box is (128 bytes of D, g, positions):
+  // one GQA group x a run of positions, 128-byte swizzled
   auto qmap = [&](CUtensorMap* m, int positions, const char* what) -> msa_status_t {
     cuuint64_t dims[3] = {(cuuint64_t)a->D, (cuuint64_t)a->H_q, (cuuint64_t)a->T};
-    cuuint64_t strides[2] = {(cuuint64_t)a->D * 2, (cuuint64_t)a->H_q * a->D * 2};
-    cuuint32_t box[3] = {64, (cuuint32_t)p.g, (cuuint32_t)positions};
+    cuuint64_t strides[2] = {(cuuint64_t)a->D * qsz, (cuuint64_t)a->H_q * a->D * qsz};
+    cuuint32_t box[3] = {(cuuint32_t)(128 / qsz), (cuuint32_t)p.g, (cuuint32_t)positions};
     cuuint32_t es[3] = {1, 1, 1};
     CUresult r = encode_cached(enc, m, qdt, 3, const_cast<void*>(a->query), dims, strides, box, es,
                                CU_TENSOR_MAP_SWIZZLE_128B);
@@ -242,12 +251,13 @@ msa_status_t make_maps(const msa_index_score_args* a, const msa::Params& p, CUte
   // one 128-token key page of one kv head; dims ordered by increasing stride
   auto kmap = [&](CUtensorMap* m, bool swizzle_int8, const char* what) -> msa_status_t {
     const bool i8 = a->k_dtype == MSA_I8;
-    const cuuint64_t esz = i8 ? 1 : 2;
-    const CUtensorMapDataType kdt = i8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : qdt;
+    const bool byte = i8 || f8;                  // one-byte elements: a 128-element row is 128 bytes
+    const cuuint64_t esz = byte ? 1 : 2;
+    const CUtensorMapDataType kdt = byte ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : qdt;
     cuuint64_t dims[4];
     cuuint64_t strides[3];
     cuuint32_t box[4];
-    const cuuint32_t bx = i8 ? 128 : 64;
+    const cuuint32_t bx = byte ? 128 : 64;
     if (a->layout == MSA_LAYOUT_BNBD) {         // [NP, H_kv, P, D]
       dims[0] = a->D; dims[1] = a->P; dims[2] = a->H_kv; dims[3] = a->NP;
       strides[0] = a->D * esz; strides[1] = (cuuint64_t)a->P * a->D * esz;
@@ -335,8 +345,14 @@ msa_status_t launch_score_checked(const msa_index_score_args* args, const msa::P
   const bool short_only =
       short_ok && args->max_seqlen_q > 0 && (int64_t)args->max_seqlen_q * p.g <= msa::kShortRows;
   cudaError_t e = cudaSuccess;
-  if (!short_only)
-    e = i8 ? msa::launch_score_i8(&tq, &tk, p, s) : msa::launch_score_16(&tq, &tk, p, bf16, s);
+  if (!short_only) {
+    if (i8)
+      e = msa::launch_score_i8(&tq, &tk, p, s);
+    else if (is_f8(args->q_dtype))
+      e = msa::launch_score_f8(&tq, &tk, p, args->q_dtype == MSA_E5M2, s);
+    else
+      e = msa::launch_score_16(&tq, &tk, p, bf16, s);
+  }
   if (e == cudaSuccess && short_ok) e = msa::launch_short_i8(&tqs, &tks, p, s);
   if (e != cudaSuccess) return cuda_fail(e, "score kernel launch");
   return MSA_OK;

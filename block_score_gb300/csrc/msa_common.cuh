@@ -112,6 +112,8 @@ cudaError_t launch_topk(const float* score, int H, long long T, int MBp, int MB,
                         int num_sms, cudaStream_t s);
 cudaError_t launch_score_16(const void* tmap_q, const void* tmap_k, const Params& p, bool bf16,
                             cudaStream_t s);
+cudaError_t launch_score_f8(const void* tmap_q, const void* tmap_k, const Params& p, bool e5m2,
+                            cudaStream_t s);
 cudaError_t launch_score_i8(const void* tmap_q, const void* tmap_k, const Params& p,
                             cudaStream_t s);
 cudaError_t launch_short_i8(const void* tmap_q, const void* tmap_k, const Params& p,

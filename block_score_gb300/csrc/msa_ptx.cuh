@@ -219,6 +219,18 @@ __device__ __forceinline__ void tc_mma_f16(uint32_t d_tmem, uint64_t a_desc, uin
       : "memory");
 }
 
+// D[tmem] (+)= A[smem] * B[smem]^T with 8-bit floating-point operands
+// (kind::f8f6f4: K = 32 elements, i.e. 32 bytes, per instruction).
+__device__ __forceinline__ void tc_mma_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // D[tmem] (+)= A[tmem] * B[smem]^T: A (M x 16 fp16/bf16 per instruction) is
 // read from tensor memory, one row per lane, two elements per 32-bit column.
 __device__ __forceinline__ void tc_mma_f16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
@@ -327,6 +339,16 @@ __host__ __device__ constexpr uint32_t idesc_f16(bool bf16, int M, int N) {
   return (1u << 4)                                    // D format: f32
          | ((bf16 ? 1u : 0u) << 7)                    // A format
          | ((bf16 ? 1u : 0u) << 10)                   // B format
+         | (static_cast<uint32_t>(N >> 3) << 17)      // N / 8
+         | (static_cast<uint32_t>(M >> 4) << 24);     // M / 16
+}
+
+// Instruction descriptor of kind::f8f6f4 with both operands E4M3 (code 0) or
+// both E5M2 (code 1), fp32 accumulation; same field layout as kind::f16.
+__host__ __device__ constexpr uint32_t idesc_f8(bool e5m2, int M, int N) {
+  return (1u << 4)                                    // D format: f32
+         | ((e5m2 ? 1u : 0u) << 7)                    // A format
+         | ((e5m2 ? 1u : 0u) << 10)                   // B format
          | (static_cast<uint32_t>(N >> 3) << 17)      // N / 8
          | (static_cast<uint32_t>(M >> 4) << 24);     // M / 16
 }

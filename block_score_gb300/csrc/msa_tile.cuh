@@ -99,10 +99,17 @@ struct TileLayout {
 static_assert(TileLayout<false>::bytes <= 232448, "shared memory per CTA");
 static_assert(TileLayout<true>::bytes <= 232448, "shared memory per CTA");
 
-template <bool KI8, bool BF16>
+// F8: 0 = 16-bit operands (fp16 / bf16, or int8 keys converted to fp16);
+// 1 = FP8 E4M3 query and keys; 2 = FP8 E5M2.  An FP8 row of 128 elements is
+// one 128-byte swizzle row, so a query tile is one box and a pair of pages
+// fills one K slot; four kind::f8f6f4 MMAs (K = 32) cover the head dimension.
+template <bool KI8, bool BF16, int F8 = 0>
 __global__ void __launch_bounds__(TileCfg<KI8>::kThreads, 1)
     tile_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const Params p) {
+  static_assert(F8 == 0 || !KI8, "FP8 operands come with FP8 keys");
+  constexpr bool kF8 = F8 != 0;
+  constexpr int kHalves = kF8 ? 1 : 2;             // K slots (and Q boxes) per pair of blocks
   using Cfg = TileCfg<KI8>;
   using L = TileLayout<KI8>;
   constexpr int PS = Cfg::kSlots;
@@ -223,7 +230,7 @@ __global__ void __launch_bounds__(TileCfg<KI8>::kThreads, 1)
     // ------------------------------------------------------- producer --
     if (lane == 0) {
       const uint64_t pol_k = l2_policy_evict_last();
-      const uint32_t q_bytes = 2u * 128u * (uint32_t)(p.g * p.np);
+      const uint32_t q_bytes = (uint32_t)kHalves * 128u * (uint32_t)(p.g * p.np);
       const bool paged = p.layout != 2;
       const int32_t page_oob = (int32_t)(p.NP < 0x7fffffffLL ? p.NP : 0x7fffffffLL);
       uint32_t ss = 0, sph = 0, qb = 0, qph = 0, ks = 0, kph = 0;
@@ -243,7 +250,7 @@ __global__ void __launch_bounds__(TileCfg<KI8>::kThreads, 1)
         const uint32_t qdst = sbase + L::q_off + qb * kTileBytes;
         mbar_arrive_expect_tx(b_q_full + 8 * qb, q_bytes);
         tma_load_3d(qdst, &tm_q, b_q_full + 8 * qb, 0, d.hk * p.g, d.t0);
-        tma_load_3d(qdst + kHalfBytes, &tm_q, b_q_full + 8 * qb, 64, d.hk * p.g, d.t0);
+        if constexpr (!kF8) tma_load_3d(qdst + kHalfBytes, &tm_q, b_q_full + 8 * qb, 64, d.hk * p.g, d.t0);
         ++n_q;
         if (++qb == L::kQBufs) { qb = 0; qph ^= 1; }
         // page indices of the next pair are read one pair ahead
@@ -287,7 +294,7 @@ __global__ void __launch_bounds__(TileCfg<KI8>::kThreads, 1)
             }
           } else {
             // K half x of both pages into one slot: page j's 128 rows at j * 16 KiB
-            for (int x = 0; x < 2 && ok; ++x) {
+            for (int x = 0; x < kHalves && ok; ++x) {
               if (!mbar_wait(b_k_empty + 8 * ks, kph ^ 1, ctl)) { ok = false; break; }
               const uint32_t kdst = sbase + L::k_off + ks * L::kSlotBytes;
               mbar_arrive_expect_tx(b_k_full + 8 * ks, (uint32_t)nblk * kHalfBytes);
@@ -323,8 +330,8 @@ __global__ void __launch_bounds__(TileCfg<KI8>::kThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------- MMA issuer --
     if (lane == 0) {
-      constexpr uint32_t idesc2 = idesc_f16(BF16, 128, 256);   // two blocks
-      constexpr uint32_t idesc1 = idesc_f16(BF16, 128, 128);   // odd last block of a unit
+      constexpr uint32_t idesc2 = kF8 ? idesc_f8(F8 == 2, 128, 256) : idesc_f16(BF16, 128, 256);
+      constexpr uint32_t idesc1 = kF8 ? idesc_f8(F8 == 2, 128, 128) : idesc_f16(BF16, 128, 128);
       uint32_t ss = 0, sph = 0, qb = 0, qph = 0, ks = 0, kph = 0, ab = 0, aph = 0;
       bool issued = false;
       for (;;) {
@@ -341,14 +348,18 @@ __global__ void __launch_bounds__(TileCfg<KI8>::kThreads, 1)
           if (!mbar_wait(b_acc_empty + 8 * ab, aph ^ 1, ctl)) { ok = false; break; }
           const uint32_t dt = tmem_base + ab * 256u;
           const uint32_t idesc = beta + 1 < d.b1 ? idesc2 : idesc1;
-          for (int x = 0; x < 2; ++x) {
+          for (int x = 0; x < kHalves; ++x) {
             if (!mbar_wait(b_k_full + 8 * ks, kph, ctl)) { ok = false; break; }
             tc_fence_after();
             const uint32_t ksrc = sbase + L::k_off + ks * L::kSlotBytes;
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              tc_mma_f16(dt, desc_at(qsrc, 4 * x + kk), smem_desc_sw128(ksrc + 32u * kk), idesc,
-                         (x | kk) ? 1u : 0u);
+            for (int kk = 0; kk < 4; ++kk) {
+              if constexpr (kF8)
+                tc_mma_f8(dt, desc_at(qsrc, kk), smem_desc_sw128(ksrc + 32u * kk), idesc, kk ? 1u : 0u);
+              else
+                tc_mma_f16(dt, desc_at(qsrc, 4 * x + kk), smem_desc_sw128(ksrc + 32u * kk), idesc,
+                           (x | kk) ? 1u : 0u);
+            }
             tc_commit(b_k_empty + 8 * ks);   // the slot is free once these four MMAs are done
             if (++ks == PS) { ks = 0; kph ^= 1; }
           }
@@ -603,6 +614,35 @@ __global__ void __launch_bounds__(TileCfg<KI8>::kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem_base, kTmemCols);
   }
+}
+
+// Launch one instantiation: persistent grid of one CTA per SM, programmatic
+// dependent launch after the plan kernel.
+template <bool KI8, bool BF16, int F8>
+inline cudaError_t launch_tile(const void* tq, const void* tk, const Params& p, cudaStream_t s) {
+  using L = TileLayout<KI8>;
+  auto kern = tile_kernel<KI8, BF16, F8>;
+  static bool configured[64] = {};   // per device; setting it twice is harmless
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 64 || !configured[dev]) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::bytes);
+    if (e != cudaSuccess) return e;
+    if (dev < 64) configured[dev] = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)p.num_sms);
+  cfg.blockDim = dim3(TileCfg<KI8>::kThreads);
+  cfg.dynamicSmemBytes = L::bytes;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, *static_cast<const CUtensorMap*>(tq),
+                            *static_cast<const CUtensorMap*>(tk), p);
 }
 
 }  // namespace msa

@@ -62,7 +62,12 @@ typedef enum {
 } msa_status_t;
 
 typedef enum { MSA_LAYOUT_BBND = 0, MSA_LAYOUT_BNBD = 1, MSA_LAYOUT_TND = 2 } msa_layout_t;
-typedef enum { MSA_F16 = 0, MSA_BF16 = 1, MSA_I8 = 2 } msa_dtype_t;
+/* Element types.  Query: fp16, bf16, FP8 E4M3 (e4m3fn: finite only) or FP8
+ * E5M2.  Key: the query's type, or int8 with an fp16 query and a scale.  FP8
+ * query and key must be of the same FP8 type and take no scale (torch API
+ * guide "CANN ops-transformer ... msa_index_score", sec. 4 and 7.2; on this
+ * GPU they run on tcgen05 kind::f8f6f4 with fp32 accumulation). */
+typedef enum { MSA_F16 = 0, MSA_BF16 = 1, MSA_I8 = 2, MSA_E4M3 = 3, MSA_E5M2 = 4 } msa_dtype_t;
 
 /* Bits of the device error word (msa_get_device_error). */
 #define MSA_DEVERR_CU_Q        0x01  /* cu_seqlens_q[0] != 0, decreasing, cu_seqlens_q[B] != T, or a query length above a nonzero max_seqlen_q */

@@ -338,3 +338,61 @@ def test_batched_decode_workload_full(dev):
     out, err, _ = run_gpu(case, dev)
     assert err == 0
     assert_parity(out, oracle.oracle_full(case), what="cfg2 full")
+
+
+# ------------------------------------------------------------------ FP8 inputs
+# FP8 query and key of one type, no scale (torch API guide, sec. 4 and 7.2),
+# on tcgen05 kind::f8f6f4: the products are exact in fp32, so the scores stay
+# within the fp16 path's tolerance of the fp64 oracle.
+
+@pytest.mark.parametrize("layout", ["BBND", "BNBD", "TND"])
+@pytest.mark.parametrize("dt", [torch.float8_e4m3fn, torch.float8_e5m2])
+def test_fp8_layout_matrix_mixed_batch(dev, layout, dt):
+    q = [37, 1, 0, 4, 200, 1]
+    kv = [290, 1, 77, 0, 600, 4100]
+    case = synth.make_case(q, kv, H_q=16, H_kv=2, layout=layout, q_dtype=dt, k_dtype=dt,
+                           MB=None if layout == "TND" else 40, init_blocks=1, local_blocks=2,
+                           seed=300 + len(layout) + (dt == torch.float8_e5m2))
+    out, err, _ = run_gpu(case, dev)
+    assert err == 0
+    assert_parity(out, oracle.oracle_full(case), what=f"{layout}/{dt}")
+
+
+@pytest.mark.parametrize("g", [1, 8, 3])
+def test_fp8_gqa_groups_and_modes(dev, g):
+    dt = torch.float8_e4m3fn
+    for mode in (0, 3):
+        case = synth.make_case([130, 9, 1], [1000, 140, 333], H_q=2 * g, H_kv=2, layout="BBND",
+                               q_dtype=dt, k_dtype=dt, sparse_mode=mode, MB=12, init_blocks=0,
+                               local_blocks=1, seed=310 + g + mode)
+        out, err, _ = run_gpu(case, dev)
+        assert err == 0
+        assert_parity(out, oracle.oracle_full(case), what=f"fp8 g={g} mode={mode}")
+
+
+def test_fp8_integer_inputs_bit_exact(dev):
+    # integers in [-8, 8] are exact in E4M3; products and 128-term sums are exact in fp32
+    dt = torch.float8_e4m3fn
+    case = synth.make_case([70, 1], [500, 260], H_q=8, H_kv=1, layout="BNBD", q_dtype=dt, k_dtype=dt,
+                           q_kind="int_small", k_kind="int_small", MB=6, seed=320)
+    out, err, _ = run_gpu(case, dev)
+    assert err == 0
+    assert_parity(out, oracle.oracle_full(case), exact=True, what="fp8 integers")
+
+
+def test_fp8_validation():
+    import block_score_gb300 as bs
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    d = torch.device("cuda:0")
+    q = torch.zeros(4, 2, 128, device=d).to(torch.float8_e4m3fn)
+    k = torch.zeros(2, 128, 1, 128, device=d).to(torch.float8_e5m2)
+    args = dict(block_table=torch.zeros(1, 2, dtype=torch.int32, device=d),
+                actual_seq_qlen=torch.tensor([0, 4], dtype=torch.int32, device=d),
+                actual_seq_klen=torch.tensor([100], dtype=torch.int32, device=d))
+    with pytest.raises(ValueError):   # mixed fp8 types
+        bs.msa_index_score(q, k, torch.zeros(1, dtype=torch.int32, device=d), **args)
+    with pytest.raises(ValueError):   # a scale with fp8
+        bs.msa_index_score(q, k.to(torch.float32).to(torch.float8_e4m3fn),
+                           torch.zeros(1, dtype=torch.int32, device=d),
+                           scale=torch.ones(2, 1, 128, device=d), **args)
