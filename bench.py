@@ -21,6 +21,7 @@ torchrun), times them between barriers and takes the max over ranks.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 import os
 import statistics
@@ -41,7 +42,9 @@ import synth  # noqa: E402
 
 METRIC = "MsaIndexScore µs/call, TFLOP/s and K-cache GB/s vs GB300 roofline (1 GPU)"
 DEFAULT_WORKLOAD = 2
-DTYPE_NAME = {torch.float16: "f16", torch.bfloat16: "bf16", torch.int8: "i8"}
+DTYPE_NAME = {torch.float16: "f16", torch.bfloat16: "bf16", torch.int8: "i8",
+              torch.float8_e4m3fn: "e4m3", torch.float8_e5m2: "e5m2"}
+FP8 = {"e4m3": torch.float8_e4m3fn, "e5m2": torch.float8_e5m2}
 
 
 # ----------------------------------------------------------------------------
@@ -51,7 +54,7 @@ def algorithmic_work(case):
     """FLOPs = 2*D*sum over (h,t) of visible keys; bytes = visible K once per kv head
     (+ int8 scale) + Q + the fp32 output + the table entries read."""
     D, P = case.D, case.P
-    es_k = 1 if case.key.dtype == torch.int8 else 2
+    es_k = case.key.element_size()
     vis_rows = 0
     k_tokens = 0
     tab = 0
@@ -70,7 +73,7 @@ def algorithmic_work(case):
     k_bytes = k_tokens * case.H_kv * D * es_k
     if case.key.dtype == torch.int8:
         k_bytes += k_tokens * case.H_kv * 4
-    q_bytes = case.T * case.H_q * D * 2
+    q_bytes = case.T * case.H_q * D * case.query.element_size()
     out_bytes = case.H_q * case.T * case.MBp * 4
     total = k_bytes + q_bytes + out_bytes + 4 * tab
     return {"flops": flops, "k_bytes": k_bytes, "q_bytes": q_bytes, "out_bytes": out_bytes,
@@ -81,7 +84,7 @@ def algorithmic_work(case):
 # code it measured)
 KERNEL_SOURCES = {
     "tile_kernel": ["msa_tile.cuh", "msa_units.cuh", "msa_ptx.cuh", "msa_common.cuh",
-                    "msa_score_16.cu", "msa_score_i8.cu"],
+                    "msa_score_16.cu", "msa_score_i8.cu", "msa_score_f8.cu"],
     "short_kernel": ["msa_short.cuh", "msa_units.cuh", "msa_ptx.cuh", "msa_common.cuh",
                      "msa_short.cu"],
 }
@@ -281,11 +284,20 @@ def make_workload(args):
     case = synth.config(args.workload)
     if args.decode_subset:
         case = synth.decode_subset(case)
+    if args.fp8:
+        # the same workload with FP8 query and keys of one type (no scale):
+        # the 16-bit draws rounded to FP8
+        if case.key.dtype == torch.int8:
+            raise SystemExit("--fp8 applies to the fp16 / bf16 workloads")
+        dt = FP8[args.fp8]
+        case = dataclasses.replace(case, query=case.query.float().to(dt), key=case.key.float().to(dt),
+                                   name=f"{case.name}_{args.fp8}")
     return case
 
 
 def workload_key(args) -> str:
-    return f"cfg{args.workload}" + ("_decode" if args.decode_subset else "")
+    return (f"cfg{args.workload}" + ("_decode" if args.decode_subset else "")
+            + (f"_{args.fp8}" if args.fp8 else ""))
 
 
 def run_reference(args):
@@ -427,6 +439,12 @@ def run_ours(args):
         roof = {"bound": "hbm", "achieved": hbm_gbs_kernel, "peak": peaks["hbm_gbs"],
                 "unit": "GB/s", "frac": hbm_gbs_kernel / peaks["hbm_gbs"],
                 "traffic": args.traffic, "peak_source": peaks["source"] + " hbm_gbs"}
+    elif case.query.element_size() == 1:
+        # FP8 operands: the measured bf16 peak times the nominal dense ratio 4.5 / 2.25
+        pk = peaks["bf16_tflops"] * 2.0
+        roof = {"bound": "tensor", "achieved": tflops_kernel, "peak": pk, "unit": "TFLOP/s",
+                "frac": tflops_kernel / pk, "traffic": args.traffic,
+                "peak_source": peaks["source"] + " bf16_tflops (burst) x 2 (nominal fp8 / bf16)"}
     else:
         pk = peaks["bf16_tflops"]
         roof = {"bound": "tensor", "achieved": tflops_kernel, "peak": pk, "unit": "TFLOP/s",
@@ -449,7 +467,7 @@ def run_ours(args):
         "config": config_block(case, workload_key(args)),
         "tflops": tflops, "k_cache_gbs": kgbs,
         "frac_hbm": (work["bytes"] / call_s / 1e9) / peaks["hbm_gbs"],
-        "frac_tensor": tflops / peaks["bf16_tflops"],
+        "frac_tensor": tflops / (peaks["bf16_tflops"] * (2.0 if case.query.element_size() == 1 else 1.0)),
         "roofline": roof,
         "e2e": e2e,
         "topk": topk,
@@ -550,6 +568,8 @@ def main(argv=None):
     ap.add_argument("--workload", type=int, default=DEFAULT_WORKLOAD, choices=[1, 2, 3, 4, 5])
     ap.add_argument("--decode-subset", action="store_true",
                     help="time only the single-token requests of the workload (cfg4)")
+    ap.add_argument("--fp8", choices=sorted(FP8), default=None,
+                    help="run the (fp16 / bf16) workload with FP8 query and keys")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--traffic", type=float, default=None,
                     help="DRAM bytes per launch of the score kernel from an ncu capture")
