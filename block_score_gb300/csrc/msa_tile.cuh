@@ -54,8 +54,8 @@ template <bool KI8>
 struct TileCfg;
 
 template <>
-struct TileCfg<false> {           // fp16 / bf16 keys: TMA straight into the K slots
-  static constexpr int kThreads = 352;
+struct TileCfg<false> {           // fp16 / bf16 / fp8 keys: TMA straight into the K slots
+  static constexpr int kThreads = 384;         // the last warp feeds the MMA warp
   static constexpr int kSlots = 5;
   static constexpr int kRaw = 0;
   static constexpr int kScPairs = 0;
@@ -98,6 +98,12 @@ struct TileLayout {
 
 static_assert(TileLayout<false>::bytes <= 232448, "shared memory per CTA");
 static_assert(TileLayout<true>::bytes <= 232448, "shared memory per CTA");
+
+// MMA handoff of the 16-bit / FP8 kernel: helper warp -> MMA warp through
+// named barrier kMmaBar; item codes (0 = stop)
+constexpr int kHelperWarp = kEpiWarp0 + 8;       // after the two epilogue groups
+constexpr uint32_t kMmaBar = 1;
+constexpr uint32_t kCodeLive = 1, kCodeFirst = 2, kCodeLast = 4, kCodeLone = 8, kCodeUnitEnd = 16;
 
 // F8: 0 = 16-bit operands (fp16 / bf16, or int8 keys converted to fp16);
 // 1 = FP8 E4M3 query and keys; 2 = FP8 E5M2.  An FP8 row of 128 elements is
@@ -327,6 +333,91 @@ __global__ void __launch_bounds__(TileCfg<KI8>::kThreads, 1)
       }
     }
     __syncwarp();
+  } else if (warp == 1 && !KI8) {
+    // ------------------------------------------------------- MMA issuer --
+    // (16-bit and FP8 keys) The warp waits on nothing but a named barrier
+    // shared with the helper warp, which waits on the mbarriers and passes each
+    // K slot on as the popcount of its lanes' predicates (kCode* bits; 0 =
+    // stop): an mbarrier wait by this warp would first let its queued MMAs
+    // drain, idling the tensor pipe for a few hundred cycles per wait.
+    constexpr uint32_t idesc2 = kF8 ? idesc_f8(F8 == 2, 128, 256) : idesc_f16(BF16, 128, 256);
+    constexpr uint32_t idesc1 = kF8 ? idesc_f8(F8 == 2, 128, 128) : idesc_f16(BF16, 128, 128);
+    uint32_t qb = 0, ks = 0, ab = 0, x = 0;
+    bool issued = false;
+    for (;;) {
+      __syncwarp();   // the barrier counts whole warps: reconverge first
+      const uint32_t code = named_bar_popc(kMmaBar, 64, false);
+      if (code == 0) break;
+      tc_fence_after();
+      if (code & kCodeFirst) x = 0;
+      if (lane == 0) {
+        const uint32_t qsrc = sbase + L::q_off + qb * kTileBytes;
+        const uint32_t dt = tmem_base + ab * 256u;
+        const uint32_t idesc = (code & kCodeLone) ? idesc1 : idesc2;
+        const uint32_t ksrc = sbase + L::k_off + ks * L::kSlotBytes;
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          if constexpr (kF8)
+            tc_mma_f8(dt, desc_at(qsrc, kk), smem_desc_sw128(ksrc + 32u * kk), idesc, kk ? 1u : 0u);
+          else
+            tc_mma_f16(dt, desc_at(qsrc, 4 * (int)x + kk), smem_desc_sw128(ksrc + 32u * kk), idesc,
+                       (x | (uint32_t)kk) ? 1u : 0u);
+        }
+        tc_commit(b_k_empty + 8 * ks);   // the slot is free once these four MMAs are done
+        if (code & kCodeLast) tc_commit(b_acc_full + 8 * ab);
+        if (code & kCodeUnitEnd) tc_commit(b_q_empty + 8 * qb);
+      }
+      ++x;
+      if (++ks == (uint32_t)PS) ks = 0;
+      if ((code & kCodeLast) && ++ab == (uint32_t)L::kAcc) ab = 0;
+      if ((code & kCodeUnitEnd) && ++qb == (uint32_t)L::kQBufs) qb = 0;
+      issued = true;
+    }
+    if (lane == 0 && issued) {
+      // every MMA of this CTA has landed before TMEM is released
+      tc_commit(b_drain);
+      const uint64_t t0 = global_timer_ns();
+      while (!mbar_try_wait(b_drain, 0) && global_timer_ns() - t0 < p.wait_limit_ns) {
+      }
+    }
+    __syncwarp();
+  } else if (warp == kHelperWarp && !KI8) {
+    // ------------------------------------------------------ MMA helper --
+    // Waits for what each K slot's MMAs need (the unit's query tile, a free
+    // accumulator at a pair's first slot, the slot's pages) and passes the
+    // slot on.  Every path out of the loop ends with exactly one stop code,
+    // so the MMA warp's barrier waits always pair up.
+    uint32_t ss = 0, sph = 0, qb = 0, qph = 0, ks = 0, kph = 0, ab = 0, aph = 0;
+    for (;;) {
+      if (!warp_wait(b_sched_full + 8 * ss, sph, ctl)) break;
+      const UnitDesc d = ring[ss];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(b_sched_empty + 8 * ss);
+      if (++ss == kSched) { ss = 0; sph ^= 1; }
+      if (!d.live) break;
+      if (d.b1 <= d.c0) continue;
+      if (!warp_wait(b_q_full + 8 * qb, qph, ctl)) break;
+      bool ok = true;
+      for (int beta = d.c0; beta < d.b1 && ok; beta += 2) {
+        if (!warp_wait(b_acc_empty + 8 * ab, aph ^ 1, ctl)) { ok = false; break; }
+        for (int xx = 0; xx < kHalves; ++xx) {
+          if (!warp_wait(b_k_full + 8 * ks, kph, ctl)) { ok = false; break; }
+          const uint32_t code = kCodeLive | (xx == 0 ? kCodeFirst : 0u) |
+                                (xx == kHalves - 1 ? kCodeLast : 0u) |
+                                (beta + 1 < d.b1 ? 0u : kCodeLone) |
+                                (xx == kHalves - 1 && beta + 2 >= d.b1 ? kCodeUnitEnd : 0u);
+          __syncwarp();
+          (void)named_bar_popc(kMmaBar, 64, (uint32_t)lane < code);
+          if (++ks == PS) { ks = 0; kph ^= 1; }
+        }
+        if (!ok) break;
+        if (++ab == L::kAcc) { ab = 0; aph ^= 1; }
+      }
+      if (!ok) break;
+      if (++qb == L::kQBufs) { qb = 0; qph ^= 1; }
+    }
+    __syncwarp();
+    (void)named_bar_popc(kMmaBar, 64, false);
   } else if (warp == 1) {
     // ------------------------------------------------------- MMA issuer --
     if (lane == 0) {
