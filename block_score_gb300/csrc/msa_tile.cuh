@@ -259,17 +259,24 @@ __global__ void __launch_bounds__(TileCfg<KI8>::kThreads, 1)
         if constexpr (!kF8) tma_load_3d(qdst + kHalfBytes, &tm_q, b_q_full + 8 * qb, 64, d.hk * p.g, d.t0);
         ++n_q;
         if (++qb == L::kQBufs) { qb = 0; qph ^= 1; }
-        // page indices of the next pair are read one pair ahead
         const int32_t* trow = p.block_table + (int64_t)d.b * p.MB;
-        int nx0 = d.pg0, nx1 = d.pg1;   // the first pair's pages come with the unit
+        // page indices two pairs ahead (an FP8 pair's MMAs take about one L2
+        // round trip); the first pair's pages come with the unit
+        int nx0 = d.pg0, nx1 = d.pg1, nn0 = 0, nn1 = 0;
+        if (paged) {
+          nn0 = d.c0 + 2 < d.b1 ? __ldg(trow + d.c0 + 2) : 0;
+          nn1 = d.c0 + 3 < d.b1 ? __ldg(trow + d.c0 + 3) : 0;
+        }
         bool ok = true;
         for (int beta = d.c0; beta < d.b1; beta += 2) {
           if (req_at >= beta && req_at < beta + 2) mbar_arrive(b_sched_req);
           const int nblk = beta + 1 < d.b1 ? 2 : 1;
           int pg[2] = {nx0, nx1};
+          nx0 = nn0;
+          nx1 = nn1;
           if (paged) {
-            nx0 = beta + 2 < d.b1 ? __ldg(trow + beta + 2) : 0;
-            nx1 = beta + 3 < d.b1 ? __ldg(trow + beta + 3) : 0;
+            nn0 = beta + 4 < d.b1 ? __ldg(trow + beta + 4) : 0;
+            nn1 = beta + 5 < d.b1 ? __ldg(trow + beta + 5) : 0;
           }
           int page[2] = {0, 0}, tok[2] = {0, 0};
           for (int j = 0; j < nblk; ++j) {
