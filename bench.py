@@ -281,7 +281,7 @@ def cpu_oracle_baseline(case, target_s: float = 12.0):
 
 
 def make_workload(args):
-    case = synth.config(args.workload)
+    case = synth.config(args.workload, layout=args.layout)
     if args.decode_subset:
         case = synth.decode_subset(case)
     if args.fp8:
@@ -297,6 +297,7 @@ def make_workload(args):
 
 def workload_key(args) -> str:
     return (f"cfg{args.workload}" + ("_decode" if args.decode_subset else "")
+            + (f"_{args.layout.lower()}" if args.layout else "")
             + (f"_{args.fp8}" if args.fp8 else ""))
 
 
@@ -568,6 +569,8 @@ def main(argv=None):
     ap.add_argument("--workload", type=int, default=DEFAULT_WORKLOAD, choices=[1, 2, 3, 4, 5])
     ap.add_argument("--decode-subset", action="store_true",
                     help="time only the single-token requests of the workload (cfg4)")
+    ap.add_argument("--layout", choices=["BBND", "BNBD", "TND"], default=None,
+                    help="draw the workload's keys in another layout (same lengths)")
     ap.add_argument("--fp8", choices=sorted(FP8), default=None,
                     help="run the (fp16 / bf16) workload with FP8 query and keys")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -254,20 +254,37 @@ def _randint(gen, lo, hi):
     return int(torch.randint(lo, hi + 1, (1,), generator=gen).item())
 
 
-def config(n: int, seed: Optional[int] = None) -> MsaCase:
-    """Workload ``n`` (1..5) with its default seed ``1234 + n``."""
+def config(n: int, seed: Optional[int] = None, layout: Optional[str] = None) -> MsaCase:
+    """Workload ``n`` (1..5) with its default seed ``1234 + n``.
+
+    ``layout`` (optional) stores the same lengths in another key layout
+    (BBND, BNBD or packed TND; for TND, MB becomes the longest request's block
+    count); the drawn values then differ, the shapes and lengths do not.
+    """
     seed = 1234 + n if seed is None else seed
     g = torch.Generator().manual_seed(seed)
     name = CONFIG_NAMES[n]
+    build = make_case
+    if layout is not None:
+        lay = layout.upper()
+
+        def build(q, kv, **kw):   # the same builder with the layout replaced
+            kw["layout"] = lay
+            if lay == "TND":
+                kw["MB"] = None
+                kw.pop("NP", None)
+                kw.pop("permute_pages", None)
+            kw["name"] = kw.get("name", name) + "_" + lay.lower()
+            return make_case(q, kv, **kw)
     if n == 1:
         # B=1, T=32, H_q=8, H_kv=1, kv_len=256, NP=8 pages, table = arange(2)
-        return make_case([32], [256], H_q=8, H_kv=1, layout="BBND",
+        return build([32], [256], H_q=8, H_kv=1, layout="BBND",
                          q_dtype=torch.float16, MB=2, NP=8, permute_pages=False,
                          sparse_mode=3, init_blocks=0, local_blocks=1,
                          start_loc=[1], seed=seed, name=name)
     if n == 2:
         kv = [_randint(g, 1024, 65536) for _ in range(64)]
-        return make_case([1] * 64, kv, H_q=16, H_kv=1, layout="BBND",
+        return build([1] * 64, kv, H_q=16, H_kv=1, layout="BBND",
                          q_dtype=torch.bfloat16, q_kind="randn01", k_kind="randn01",
                          MB=512, sparse_mode=3, init_blocks=0, local_blocks=1,
                          seed=seed + 1, name=name)
@@ -280,7 +297,7 @@ def config(n: int, seed: Optional[int] = None) -> MsaCase:
         reqs.append((256, 0))
         order = torch.randperm(len(reqs), generator=g).tolist()
         reqs = [reqs[i] for i in order]
-        return make_case([r[0] for r in reqs], [r[1] for r in reqs], H_q=32, H_kv=4,
+        return build([r[0] for r in reqs], [r[1] for r in reqs], H_q=32, H_kv=4,
                          layout="BNBD", q_dtype=torch.bfloat16, MB=128,
                          sparse_mode=3, init_blocks=1, local_blocks=4,
                          seed=seed + 1, name=name)
@@ -289,12 +306,12 @@ def config(n: int, seed: Optional[int] = None) -> MsaCase:
         reqs += [(512, _randint(g, 8192, 32768)) for _ in range(8)]
         order = torch.randperm(len(reqs), generator=g).tolist()
         reqs = [reqs[i] for i in order]
-        return make_case([r[0] for r in reqs], [r[1] for r in reqs], H_q=16, H_kv=2,
+        return build([r[0] for r in reqs], [r[1] for r in reqs], H_q=16, H_kv=2,
                          layout="BBND", q_dtype=torch.float16, k_dtype=torch.int8,
                          k_kind="int8_full", MB=256, sparse_mode=3,
                          init_blocks=0, local_blocks=1, seed=seed + 1, name=name)
     if n == 5:
-        return make_case([16384], [131072], H_q=64, H_kv=8, layout="BBND",
+        return build([16384], [131072], H_q=64, H_kv=8, layout="BBND",
                          q_dtype=torch.bfloat16, MB=1100, NP=1024, sparse_mode=3,
                          init_blocks=4, local_blocks=8, start_loc=[1023],
                          seed=seed + 1, name=name)
