@@ -25,6 +25,7 @@ the CPU, so a case is reproducible byte for byte on any host.
 from __future__ import annotations
 
 import dataclasses
+import itertools
 import math
 from typing import List, Optional, Sequence
 
@@ -331,10 +332,19 @@ def decode_subset(case: MsaCase) -> MsaCase:
     cu_q = torch.arange(len(keep) + 1, dtype=torch.int32)
     table = case.block_table[keep].contiguous() if case.block_table is not None else None
     kv = case.kv_len[keep].contiguous() if case.kv_len is not None else None
-    return MsaCase(name=case.name + "_decode_subset", query=q, key=case.key,
+    key, scale, cu_k = case.key, case.scale, None
+    if case.layout.upper() == "TND":
+        # packed keys: the kept requests' rows, re-packed with their prefix sums
+        ck = case.cu_seqlens_k.tolist()
+        spans = [(ck[b], ck[b + 1]) for b in keep]
+        key = torch.cat([case.key[a:e] for a, e in spans]).contiguous()
+        if case.scale is not None:
+            scale = torch.cat([case.scale[a:e] for a, e in spans]).contiguous()
+        cu_k = torch.tensor([0] + list(itertools.accumulate(e - a for a, e in spans)), dtype=torch.int32)
+    return MsaCase(name=case.name + "_decode_subset", query=q, key=key,
                    block_table=table, cu_seqlens_q=cu_q, kv_len=kv,
-                   cu_seqlens_k=None, start_loc=case.start_loc[keep].contiguous(),
-                   scale=case.scale, layout=case.layout, sparse_mode=case.sparse_mode,
+                   cu_seqlens_k=cu_k, start_loc=case.start_loc[keep].contiguous(),
+                   scale=scale, layout=case.layout, sparse_mode=case.sparse_mode,
                    init_blocks=case.init_blocks, local_blocks=case.local_blocks,
                    MB=case.MB, P=case.P, q_lens=[1] * len(keep),
                    kv_lens=[case.kv_lens[b] for b in keep])
