@@ -66,7 +66,7 @@ struct TileCfg<false> {           // fp16 / bf16 / fp8 keys: TMA straight into t
 
 template <>
 struct TileCfg<true> {            // int8 keys: raw pages, converters, scales
-  static constexpr int kThreads = 608;
+  static constexpr int kThreads = 640;         // the last warp feeds the MMA warp
   static constexpr int kCvtGroups = 2;         // page j of every pair by group j
   static constexpr int kSlots = 3;
   static constexpr int kRaw = 5;               // int8 pages in flight (L2 latency)
@@ -101,7 +101,8 @@ static_assert(TileLayout<true>::bytes <= 232448, "shared memory per CTA");
 
 // MMA handoff of the 16-bit / FP8 kernel: helper warp -> MMA warp through
 // named barrier kMmaBar; item codes (0 = stop)
-constexpr int kHelperWarp = kEpiWarp0 + 8;       // after the two epilogue groups
+// the helper is the last warp: after the two epilogue groups (16-bit / FP8
+// keys) or after the converters (int8 keys)
 constexpr uint32_t kMmaBar = 1;
 constexpr uint32_t kCodeLive = 1, kCodeFirst = 2, kCodeLast = 4, kCodeLone = 8, kCodeUnitEnd = 16;
 
@@ -340,9 +341,9 @@ __global__ void __launch_bounds__(TileCfg<KI8>::kThreads, 1)
       }
     }
     __syncwarp();
-  } else if (warp == 1 && !KI8) {
+  } else if (warp == 1) {
     // ------------------------------------------------------- MMA issuer --
-    // (16-bit and FP8 keys) The warp waits on nothing but a named barrier
+    // The warp waits on nothing but a named barrier
     // shared with the helper warp, which waits on the mbarriers and passes each
     // K slot on as the popcount of its lanes' predicates (kCode* bits; 0 =
     // stop): an mbarrier wait by this warp would first let its queued MMAs
@@ -388,7 +389,7 @@ __global__ void __launch_bounds__(TileCfg<KI8>::kThreads, 1)
       }
     }
     __syncwarp();
-  } else if (warp == kHelperWarp && !KI8) {
+  } else if (warp == Cfg::kThreads / 32 - 1) {
     // ------------------------------------------------------ MMA helper --
     // Waits for what each K slot's MMAs need (the unit's query tile, a free
     // accumulator at a pair's first slot, the slot's pages) and passes the
@@ -425,60 +426,6 @@ __global__ void __launch_bounds__(TileCfg<KI8>::kThreads, 1)
     }
     __syncwarp();
     (void)named_bar_popc(kMmaBar, 64, false);
-  } else if (warp == 1) {
-    // ------------------------------------------------------- MMA issuer --
-    if (lane == 0) {
-      constexpr uint32_t idesc2 = kF8 ? idesc_f8(F8 == 2, 128, 256) : idesc_f16(BF16, 128, 256);
-      constexpr uint32_t idesc1 = kF8 ? idesc_f8(F8 == 2, 128, 128) : idesc_f16(BF16, 128, 128);
-      uint32_t ss = 0, sph = 0, qb = 0, qph = 0, ks = 0, kph = 0, ab = 0, aph = 0;
-      bool issued = false;
-      for (;;) {
-        if (!mbar_wait(b_sched_full + 8 * ss, sph, ctl)) break;
-        const UnitDesc d = ring[ss];
-        mbar_arrive(b_sched_empty + 8 * ss);
-        if (++ss == kSched) { ss = 0; sph ^= 1; }
-        if (!d.live) break;
-        if (d.b1 <= d.c0) continue;
-        if (!mbar_wait(b_q_full + 8 * qb, qph, ctl)) break;
-        const uint32_t qsrc = sbase + L::q_off + qb * kTileBytes;
-        bool ok = true;
-        for (int beta = d.c0; beta < d.b1 && ok; beta += 2) {
-          if (!mbar_wait(b_acc_empty + 8 * ab, aph ^ 1, ctl)) { ok = false; break; }
-          const uint32_t dt = tmem_base + ab * 256u;
-          const uint32_t idesc = beta + 1 < d.b1 ? idesc2 : idesc1;
-          for (int x = 0; x < kHalves; ++x) {
-            if (!mbar_wait(b_k_full + 8 * ks, kph, ctl)) { ok = false; break; }
-            tc_fence_after();
-            const uint32_t ksrc = sbase + L::k_off + ks * L::kSlotBytes;
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-              if constexpr (kF8)
-                tc_mma_f8(dt, desc_at(qsrc, kk), smem_desc_sw128(ksrc + 32u * kk), idesc, kk ? 1u : 0u);
-              else
-                tc_mma_f16(dt, desc_at(qsrc, 4 * x + kk), smem_desc_sw128(ksrc + 32u * kk), idesc,
-                           (x | kk) ? 1u : 0u);
-            }
-            tc_commit(b_k_empty + 8 * ks);   // the slot is free once these four MMAs are done
-            if (++ks == PS) { ks = 0; kph ^= 1; }
-          }
-          if (!ok) break;
-          tc_commit(b_acc_full + 8 * ab);
-          issued = true;
-          if (++ab == L::kAcc) { ab = 0; aph ^= 1; }
-        }
-        if (!ok) break;
-        tc_commit(b_q_empty + 8 * qb);
-        if (++qb == L::kQBufs) { qb = 0; qph ^= 1; }
-      }
-      if (issued) {
-        // every MMA of this CTA has landed before TMEM is released
-        tc_commit(b_drain);
-        uint64_t t0 = global_timer_ns();
-        while (!mbar_try_wait(b_drain, 0) && global_timer_ns() - t0 < p.wait_limit_ns) {
-        }
-      }
-    }
-    __syncwarp();
   } else if (warp < kEpiWarp0 + 4 * L::kGroups) {
     // --------------------------------------------------------- epilogue --
     const int grp = (warp - kEpiWarp0) >> 2;       // block of each pair this group drains
