@@ -99,6 +99,13 @@ struct TileLayout {
 static_assert(TileLayout<false>::bytes <= 232448, "shared memory per CTA");
 static_assert(TileLayout<true>::bytes <= 232448, "shared memory per CTA");
 
+// A claim costs an atomic and a chain of dependent L2 round trips (the search
+// over the unit prefix sums, the request record, the first table entries):
+// about 5,000 cycles while HBM is saturated, as long as a few FP8 block pairs
+// of a decode unit.  The next unit is therefore claimed this many blocks
+// before the end of the current one (at its start for short units).
+constexpr int kTileLead = 16;
+
 // MMA handoff of the 16-bit / FP8 kernel: helper warp -> MMA warp through
 // named barrier kMmaBar; item codes (0 = stop)
 // the helper is the last warp: after the two epilogue groups (16-bit / FP8
@@ -213,24 +220,30 @@ __global__ void __launch_bounds__(TileCfg<KI8>::kThreads, 1)
   } else if (warp == 0) {
     // -------------------------------------------------------- scheduler --
     // Claims one unit ahead: the first at once, each later one when the
-    // producer is kLead blocks from the end of its current unit.
-    if (lane == 0) {
-      uint32_t ss = 0, sph = 0, rph = 0;
-      for (bool first = true;; first = false) {
-        if (!first) {
-          if (!mbar_wait(b_sched_req, rph, ctl)) break;
-          rph ^= 1;
-        }
-        UnitDesc d;
-        // the first unit of CTA i is unit i; later claims count from the grid size
-        make_unit(p, req, prefix, n_req0, n_units0, chunk0, p.np,
-                  first ? (int)blockIdx.x : (int)gridDim.x + atomicAdd(&hdr->counter[0], 1), d);
-        if (!mbar_wait(b_sched_empty + 8 * ss, sph ^ 1, ctl)) break;
+    // producer is kTileLead blocks from the end of its current unit.  The
+    // whole warp looks the unit up (make_unit_warp); lane 0 claims and
+    // publishes it.
+    uint32_t ss = 0, sph = 0, rph = 0;
+    for (bool first = true;; first = false) {
+      if (!first) {
+        if (!warp_wait(b_sched_req, rph, ctl)) break;
+        rph ^= 1;
+      }
+      // the first unit of CTA i is unit i; later claims count from the grid size
+      int u = (int)blockIdx.x;
+      if (!first) {
+        if (lane == 0) u = (int)gridDim.x + atomicAdd(&hdr->counter[0], 1);
+        u = __shfl_sync(0xffffffffu, u, 0);
+      }
+      UnitDesc d;
+      make_unit_warp(p, req, prefix, n_req0, n_units0, chunk0, p.np, u, d);
+      if (!warp_wait(b_sched_empty + 8 * ss, sph ^ 1, ctl)) break;
+      if (lane == 0) {
         ring[ss] = d;
         mbar_arrive(b_sched_full + 8 * ss);
-        if (++ss == kSched) { ss = 0; sph ^= 1; }
-        if (!d.live) break;
       }
+      if (++ss == kSched) { ss = 0; sph ^= 1; }
+      if (u >= n_units0) break;
     }
     __syncwarp();
   } else if (warp == 2) {
@@ -252,7 +265,7 @@ __global__ void __launch_bounds__(TileCfg<KI8>::kThreads, 1)
           mbar_arrive(b_sched_req);
           continue;
         }
-        const int req_at = max(d.c0, d.b1 - kLead);
+        const int req_at = max(d.c0, d.b1 - kTileLead);
         if (!mbar_wait(b_q_empty + 8 * qb, qph ^ 1, ctl)) break;
         const uint32_t qdst = sbase + L::q_off + qb * kTileBytes;
         mbar_arrive_expect_tx(b_q_full + 8 * qb, q_bytes);

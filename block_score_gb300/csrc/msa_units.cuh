@@ -56,19 +56,9 @@ __device__ __forceinline__ void tma_k(uint32_t dst, const CUtensorMap* m, uint32
 // Build the descriptor of unit u of one request class from the plan
 // (scheduler thread only).  `req` / `prefix` point at that class's records and
 // unit prefix sums; `np` is the number of query positions per tile.
-__device__ __forceinline__ void make_unit(const Params& p, const ReqInfo* req,
-                                          const int32_t* prefix, int n_req, int n_units,
-                                          int chunk, int np, int u, UnitDesc& d) {
-  d.live = 0;
-  if (u >= n_units) return;
-  // request r: last r with prefix[r] <= u
-  int lo = 0, hi = n_req - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (prefix[mid] <= u) lo = mid; else hi = mid - 1;
-  }
-  const ReqInfo ri = req[lo];
-  const int ul = u - prefix[lo];
+// Unit `ul` of request record `ri` (its units counted from 0).
+__device__ __forceinline__ void unit_of_request(const Params& p, const ReqInfo& ri, int ul,
+                                                int chunk, int np, UnitDesc& d) {
   const int per_hk = ri.ntiles * ri.nchunks;
   const int hk = ul / per_hk;
   const int rem = ul - hk * per_hk;
@@ -100,6 +90,46 @@ __device__ __forceinline__ void make_unit(const Params& p, const ReqInfo* req,
     d.pg0 = __ldg(trow + d.c0);
     if (d.c0 + 1 < d.b1) d.pg1 = __ldg(trow + d.c0 + 1);
   }
+}
+
+__device__ __forceinline__ void make_unit(const Params& p, const ReqInfo* req,
+                                          const int32_t* prefix, int n_req, int n_units,
+                                          int chunk, int np, int u, UnitDesc& d) {
+  d.live = 0;
+  if (u >= n_units) return;
+  // request r: last r with prefix[r] <= u
+  int lo = 0, hi = n_req - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (prefix[mid] <= u) lo = mid; else hi = mid - 1;
+  }
+  unit_of_request(p, req[lo], u - prefix[lo], chunk, np, d);
+}
+
+// The same lookup by a whole warp over records in global memory: each round
+// reads 32 prefix sums at once and narrows the range 32-fold, so the chain
+// of dependent loads is ceil(log32(n_req)) + 2 long instead of
+// log2(n_req) + 2.  Every lane passes the same u; the descriptor is valid in
+// lane 0 only.
+__device__ __forceinline__ void make_unit_warp(const Params& p, const ReqInfo* req,
+                                               const int32_t* prefix, int n_req, int n_units,
+                                               int chunk, int np, int u, UnitDesc& d) {
+  const int lane = (int)(threadIdx.x & 31);
+  d.live = 0;
+  if (u >= n_units) return;
+  // invariant: prefix[base] == at <= u (prefix[0] == 0); the answer is in [base, base + span)
+  int base = 0, span = n_req, at = 0;
+  while (span > 1) {
+    const int step = (span + 31) >> 5;
+    const int off = lane * step;
+    const int v = off < span ? __ldg(prefix + base + off) : 0x7fffffff;
+    const uint32_t m = __ballot_sync(0xffffffffu, v <= u);
+    const int l = 31 - __clz((int)m);
+    at = __shfl_sync(0xffffffffu, v, l);
+    base += l * step;
+    span = min(step, span - l * step);
+  }
+  if (lane == 0) unit_of_request(p, req[base], u - at, chunk, np, d);
 }
 
 // Max of the first (climit + 1) of N values (all if climit >= N - 1).
