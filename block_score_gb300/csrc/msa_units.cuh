@@ -135,18 +135,26 @@ __device__ __forceinline__ void make_unit_warp(const Params& p, const ReqInfo* r
 // Max of the first (climit + 1) of N values (all if climit >= N - 1).
 template <int N>
 __device__ __forceinline__ float masked_max(const float (&x)[N], int climit) {
-  static_assert(N % 8 == 0, "groups of 8");
+  static_assert(N % 16 == 0, "groups of 16");
   const float ninf = __int_as_float(0xff800000);
   if (climit < 0) return ninf;
   float a0 = ninf, a1 = ninf, a2 = ninf, a3 = ninf;
   if (climit >= N - 1) {
+    // eight independent chains (depth N / 16), folded at the end
+    float b0 = ninf, b1 = ninf, b2 = ninf, b3 = ninf;
 #pragma unroll
-    for (int c = 0; c < N; c += 8) {
+    for (int c = 0; c < N; c += 16) {
       a0 = fmax3(a0, x[c + 0], x[c + 1]);
       a1 = fmax3(a1, x[c + 2], x[c + 3]);
       a2 = fmax3(a2, x[c + 4], x[c + 5]);
       a3 = fmax3(a3, x[c + 6], x[c + 7]);
+      b0 = fmax3(b0, x[c + 8], x[c + 9]);
+      b1 = fmax3(b1, x[c + 10], x[c + 11]);
+      b2 = fmax3(b2, x[c + 12], x[c + 13]);
+      b3 = fmax3(b3, x[c + 14], x[c + 15]);
     }
+    a0 = fmax3(a0, b0, b1);
+    a1 = fmax3(a1, b2, b3);
   } else {
 #pragma unroll
     for (int c = 0; c < N; c += 8) {
