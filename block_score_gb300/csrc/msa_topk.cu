@@ -43,17 +43,34 @@ __device__ __forceinline__ uint32_t order_key(float x) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// Bitonic sort of one value per lane across the warp.
-template <bool kDescending, typename V>
-__device__ __forceinline__ V warp_sort(V s, int lane) {
+// Per-lane directions of the 15 compare-exchange stages of a 32-wide bitonic
+// sort (stage j of the (size, stride) sequence 2/1, 4/2, 4/1, ...): bit j is
+// set when this lane keeps the larger value in a descending sort.  Depends
+// only on the lane, so it is computed once per thread.
+__device__ __forceinline__ uint32_t bitonic_dirs(int lane) {
+  uint32_t d = 0;
+  int j = 0;
 #pragma unroll
   for (int size = 2; size <= 32; size <<= 1) {
 #pragma unroll
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1, ++j)
+      if (((lane & size) == 0) == ((lane & stride) == 0)) d |= 1u << j;
+  }
+  return d;
+}
+
+// Bitonic sort of one value per lane across the warp; `dirs` from
+// bitonic_dirs(lane).  Each stage is one shuffle, a min, a max and a select.
+template <bool kDescending, typename V>
+__device__ __forceinline__ V warp_sort(V s, uint32_t dirs) {
+  int j = 0;
+#pragma unroll
+  for (int size = 2; size <= 32; size <<= 1) {
+#pragma unroll
+    for (int stride = size >> 1; stride > 0; stride >>= 1, ++j) {
       const V other = __shfl_xor_sync(0xffffffffu, s, stride);
-      const bool same = ((lane & size) == 0) == ((lane & stride) == 0);
-      const V hi = s > other ? s : other, lo = s > other ? other : s;
-      s = (same == kDescending) ? hi : lo;
+      const V hi = max(s, other), lo = min(s, other);
+      s = (((dirs >> j) & 1u) != 0) == kDescending ? hi : lo;
     }
   }
   return s;
@@ -80,10 +97,12 @@ __global__ void __launch_bounds__(kTopkWarps * 32)
   const int lane = threadIdx.x & 31;
   const int w = threadIdx.x >> 5;
   const unsigned lt = (1u << lane) - 1u;
+  const uint32_t dirs = bitonic_dirs(lane);
   const int ntiles = (MB + 32 * R - 1) / (32 * R);
-  const long long nrows = (long long)H * T;
-  for (long long r = (long long)blockIdx.x * kTopkWarps + w; r < nrows; r += (long long)gridDim.x * kTopkWarps) {
-    const float* row = score + r * (long long)MBp;   // rows are (h, t) in h-major order
+  // grid: x strides over the tokens, y over the heads (no division per row)
+  for (int h = blockIdx.y; h < H; h += gridDim.y)
+  for (long long t = (long long)blockIdx.x * kTopkWarps + w; t < T; t += (long long)gridDim.x * kTopkWarps) {
+    const float* row = score + ((long long)h * T + t) * (long long)MBp;   // rows are (h, t) in h-major order
     uint32_t key[R];
     // ---- 1. lane maxima over all tiles; the first tile stays in registers
     uint32_t lmax = 0;
@@ -92,7 +111,7 @@ __global__ void __launch_bounds__(kTopkWarps * 32)
 #pragma unroll
       for (int i = 0; i < R; ++i) lmax = max(lmax, key[i]);
     }
-    const uint32_t t0 = __shfl_sync(0xffffffffu, warp_sort<true>(lmax, lane), k - 1);
+    const uint32_t t0 = __shfl_sync(0xffffffffu, warp_sort<true>(lmax, dirs), k - 1);
     const uint32_t lo = t0 > 0 ? t0 : 1u;
     int cur = 0;   // the tile whose keys are in registers
     // ---- 2. candidates, compacted in index order (lane j's slot: the j-th);
@@ -113,15 +132,14 @@ __global__ void __launch_bounds__(kTopkWarps * 32)
         ncand += __popc(b);
       }
     }
-    const long long h = r / T, t = r - h * T;
-    int32_t* orow = out + (t * H + h) * k;
+    int32_t* orow = out + (t * H + h) * (long long)k;
     if (ncand <= 32) {
       __syncwarp();
       const unsigned long long word = lane < ncand ? s_cand[w][lane] : 0ull;
       __syncwarp();
       const uint32_t ck = (uint32_t)(word >> 32);   // 0 on lanes past the candidates
       // the k-th largest key; keys above it are kept, equal ones in index order
-      const uint32_t kk = __shfl_sync(0xffffffffu, warp_sort<true>(ck, lane), k - 1);
+      const uint32_t kk = __shfl_sync(0xffffffffu, warp_sort<true>(ck, dirs), k - 1);
       const bool gt = ck > kk;
       const bool eq = ck == kk && ck != 0u;
       const int ngt = __popc(__ballot_sync(0xffffffffu, gt));
@@ -166,7 +184,7 @@ __global__ void __launch_bounds__(kTopkWarps * 32)
         }
       }
       // ascending block indices, -1 tail
-      const int sidx = warp_sort<false>(lane < cnt ? li : 0x7fffffff, lane);
+      const int sidx = warp_sort<false>(lane < cnt ? li : 0x7fffffff, dirs);
       if (lane < k) orow[lane] = sidx == 0x7fffffff ? -1 : sidx;
     }
   }
@@ -175,11 +193,13 @@ __global__ void __launch_bounds__(kTopkWarps * 32)
 template <int R>
 cudaError_t launch_r(const float* score, int H, long long T, int MBp, int MB, int k, int32_t* out,
                      int num_sms, cudaStream_t s) {
-  const long long rows = (long long)H * T;
-  long long blocks = (rows + kTopkWarps - 1) / kTopkWarps;
-  const long long cap = (long long)num_sms * 8;   // 8 CTAs of 8 warps fill an SM
-  if (blocks > cap) blocks = cap;
-  topk_kernel<R><<<(unsigned)blocks, kTopkWarps * 32, 0, s>>>(score, H, T, MBp, MB, k, out);
+  // 8 CTAs of 8 warps fill an SM; the heads share that budget
+  long long bx = (T + kTopkWarps - 1) / kTopkWarps;
+  long long cap = (long long)num_sms * 8 / H;
+  if (cap < 1) cap = 1;
+  if (bx > cap) bx = cap;
+  const unsigned by = H < 65535 ? (unsigned)H : 65535u;
+  topk_kernel<R><<<dim3((unsigned)bx, by), kTopkWarps * 32, 0, s>>>(score, H, T, MBp, MB, k, out);
   return cudaGetLastError();
 }
 
