@@ -25,16 +25,25 @@ def _close(a, b):
     assert bool(((a[fin] - b[fin]).abs() <= ATOL + RTOL * b[fin].abs()).all())
 
 
-def test_noalloc_matches_workspace_entry_on_two_calls():
+KEYS = {
+    "bf16": (torch.bfloat16, None),
+    "int8": (torch.float16, torch.int8),          # tile and short-query kernels
+    "e4m3": (torch.float8_e4m3fn, torch.float8_e4m3fn),
+}
+
+
+@pytest.mark.parametrize("keys", sorted(KEYS))
+def test_noalloc_matches_workspace_entry_on_two_calls(keys):
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     import block_score_gb300 as bs
     lib = bs.load_library()
     dev = torch.device("cuda:0")
+    q_dtype, k_dtype = KEYS[keys]
     # a mixed batch: prefill tiles, single-token decode, an empty request, forced blocks
     case = synth.make_case([37, 1, 0, 4, 130], [290, 3000, 77, 4, 900], H_q=16, H_kv=2,
-                           layout="BBND", q_dtype=torch.bfloat16, MB=24, init_blocks=1,
-                           local_blocks=2, seed=901)
+                           layout="BBND", q_dtype=q_dtype, k_dtype=k_dtype, MB=24,
+                           init_blocks=1, local_blocks=2, seed=901)
     prep = bs.from_case(case, dev)
     ref = prep().clone().cpu()
     stream = torch.cuda.current_stream(dev)
