@@ -109,6 +109,21 @@ def test_large_tensor_sampled_rows(dev):
         assert out[t, h].tolist() == ref[t, h].tolist(), r
 
 
+def test_more_heads_than_one_grid_column(dev):
+    # 70,000 heads of one token: more than the 65,535 CTAs of the grid's y
+    # axis, so CTAs loop over heads; rows checked on a sample and at both ends
+    g = torch.Generator().manual_seed(6)
+    H, T, MB, MBp, k = 70000, 1, 20, 32, 4
+    score = torch.randn(H, T, MBp, generator=g)
+    score[:, :, MB:] = float("-inf")
+    out = gpu_topk(score, MB, k, dev)
+    rows = torch.randint(0, H * T, (2000,), generator=g).tolist() + list(range(65530, 65545)) + [H * T - 1]
+    ref = otk.block_topk(score, MB, k, rows=rows)
+    for r in rows:
+        h, t = divmod(r, T)
+        assert out[t, h].tolist() == ref[t, h].tolist(), r
+
+
 def test_gpu_scores_then_topk_by_property(dev):
     import block_score_gb300 as bs
     case = synth.config(3)
