@@ -110,6 +110,12 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const Params p) {
   // Let the score kernels start their prologue (barrier init, TMEM
   // allocation); they wait for this grid's completion before reading the plan.
   asm volatile("griddepcontrol.launch_dependents;");
+  // This grid is launched as a programmatic dependent of whatever precedes it
+  // on the stream, so its launch overlaps that kernel's last units; it reads
+  // nothing until the preceding kernel has completed (its request arrays may
+  // be that kernel's output, and a previous call's score kernel still reads
+  // the workspace).
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 
   __shared__ int s_warp[32];
   __shared__ unsigned long long s_work[2];
@@ -296,8 +302,20 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const Params p) {
 cudaError_t launch_plan(const Params& p, cudaStream_t s) {
   // small batches need few threads: fewer warps make every barrier cheaper
   const int threads = p.B <= 128 ? 128 : kPlanThreads;
-  plan_kernel<<<1, threads, 0, s>>>(p);
-  return cudaGetLastError();
+  // programmatic dependent of whatever precedes it on the stream: behind a
+  // previous call's score kernel, which triggers at its start, the plan is
+  // launched and resident before that kernel ends (see griddepcontrol.wait)
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(1);
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, plan_kernel, p);
 }
 
 }  // namespace msa
