@@ -423,6 +423,31 @@ def test_fp8_decoding_matches_torch_for_every_bit_pattern(dt):
     assert np.array_equal(got[~nan], ref[~nan])
 
 
+def test_fp16_decoding_matches_numpy_for_every_bit_pattern():
+    # all 65,536 binary16 patterns, decoded by numpy's IEEE half type: pins the
+    # normal, subnormal (exponent field 0), infinity and NaN branches
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ref = bits.view(np.float16).astype(np.float64)
+    got = np.array([oracle.decode(torch.float16, int(b)) for b in range(65536)])
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+    # the subnormal range on its own: m * 2^-24 for m in 1..1023, both signs
+    m = np.arange(1, 1024)
+    assert np.array_equal(got[m], m * 2.0 ** -24)
+    assert np.array_equal(got[0x8000 + m], -m * 2.0 ** -24)
+
+
+def test_bf16_decoding_matches_torch_for_every_bit_pattern():
+    # all 65,536 bfloat16 patterns, decoded by torch's bfloat16 type
+    bits = torch.arange(65536, dtype=torch.int32).to(torch.int16)
+    ref = bits.view(torch.bfloat16).to(torch.float64).numpy()
+    got = np.array([oracle.decode(torch.bfloat16, b & 0xFFFF) for b in range(65536)])
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+
+
 @pytest.mark.parametrize("layout", ["BBND", "BNBD", "TND"])
 @pytest.mark.parametrize("dt", [torch.float8_e4m3fn, torch.float8_e5m2])
 @pytest.mark.parametrize("mode", [0, 3])
