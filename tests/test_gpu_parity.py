@@ -135,6 +135,42 @@ def test_sparse_modes(dev, mode):
     assert_parity(out, oracle.oracle_full(case), what=f"mode{mode}")
 
 
+# int8 keys without the causal bound (sparse_mode 0, torch API guide sec. 4;
+# int8 path sec. 7.1): the short-query kernel (Lq * g <= 32 query rows) and the
+# tile kernel each have a mode-0 branch of their own
+INT8_MODE0 = [(layout, g) for layout in ("BBND", "TND") for g in (8, 4)]
+
+
+@pytest.mark.parametrize("layout,g", INT8_MODE0)
+def test_int8_keys_sparse_mode0(dev, layout, g):
+    # g=8: Lq 2, 3, 4 are short-class requests (16, 24, 32 query rows), Lq 5
+    # and 40 are tile-class; g=4 moves Lq 5..8 into the short class as well
+    H_kv = 2
+    q = [2, 3, 4, 1, 5, 40, 8, 0]
+    kv = [700, 129, 4000, 1, 260, 1500, 128, 50]
+    case = synth.make_case(q, kv, H_q=g * H_kv, H_kv=H_kv, layout=layout,
+                           q_dtype=torch.float16, k_dtype=torch.int8, sparse_mode=0,
+                           MB=40 if layout != "TND" else None, init_blocks=1,
+                           local_blocks=2, seed=340 + g + (layout == "TND"))
+    out, err, _ = run_gpu(case, dev)
+    assert err == 0
+    assert_parity(out, oracle.oracle_full(case), what=f"int8 mode0 {layout} g={g}")
+
+
+@pytest.mark.parametrize("layout", ["BBND", "TND"])
+def test_int8_unit_scale_bit_exact_mode0(dev, layout):
+    # integer queries, int8 keys, scale 1: exact in fp32, so bit-exact in mode 0
+    # for short-class (Lq 2..4 with g=8) and tile-class requests alike
+    case = synth.make_case([2, 4, 3, 1, 70], [300, 4100, 128, 9, 900], H_q=16, H_kv=2,
+                           layout=layout, q_dtype=torch.float16, k_dtype=torch.int8,
+                           q_kind="int_small", k_kind="int8_full", scale_const=1.0,
+                           sparse_mode=0, MB=33 if layout != "TND" else None,
+                           init_blocks=0, local_blocks=0, seed=350 + (layout == "TND"))
+    out, err, _ = run_gpu(case, dev)
+    assert err == 0
+    assert_parity(out, oracle.oracle_full(case), exact=True, what=f"int8 exact mode0 {layout}")
+
+
 def test_strided_cache_poisoned_gaps(dev):
     case = synth.make_case([20, 3], [500, 260], H_q=8, H_kv=1, layout="BBND",
                            q_dtype=torch.float16, q_kind="abs_randn", MB=6, page_gap=2,
