@@ -28,6 +28,7 @@ __all__ = [
     "msa_index_score", "msa_index_score_plan", "msa_index_score_run",
     "msa_index_score_workspace_size", "msa_index_score_out_shape", "msa_get_device_error",
     "MsaError", "library_path", "load_library", "DEVERR", "msa_index_score_noalloc",
+    "noalloc_device_error",
     "msa_block_topk",
 ]
 
@@ -93,14 +94,18 @@ def load_library():
     lib.msa_index_score_run.argtypes = [P, vp, vp, sz, vp]
     lib.msa_get_device_error.argtypes = [vp, ctypes.POINTER(ctypes.c_int32), vp]
     lib.msa_index_score_noalloc.argtypes = [P, vp, vp]
+    lib.msa_noalloc_device_error.argtypes = [ctypes.POINTER(ctypes.c_int32), vp]
     lib.msa_block_topk.argtypes = [vp, ctypes.c_int32, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32,
                                    ctypes.c_int32, vp, vp]
+    lib.msa_set_watchdog.argtypes = [ctypes.c_uint64, ctypes.c_int32]
+    lib.msa_set_watchdog.restype = ctypes.c_int
     lib.msa_status_string.restype = ctypes.c_char_p
     lib.msa_status_string.argtypes = [ctypes.c_int]
     lib.msa_last_error_message.restype = ctypes.c_char_p
     for name in ("msa_index_score_out_shape", "msa_index_score_workspace_size",
                  "msa_index_score", "msa_index_score_plan", "msa_index_score_run",
-                 "msa_get_device_error", "msa_index_score_noalloc", "msa_block_topk"):
+                 "msa_get_device_error", "msa_index_score_noalloc", "msa_noalloc_device_error",
+                 "msa_block_topk"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -292,10 +297,22 @@ def msa_index_score_noalloc(prepared: "Prepared", out: Optional[torch.Tensor] = 
     requests).  Calls that overlap on the GPU share that array and race, so
     keep them on one stream.  ``out`` defaults to ``prepared.out``.
     """
+    shape = tuple(prepared.shape)
     out = prepared.out if out is None else out
+    if (tuple(out.shape) != shape or out.dtype != torch.float32 or not out.is_contiguous()
+            or not out.is_cuda):
+        raise ValueError(f"out must be a contiguous float32 CUDA tensor of shape {shape}")
     _check(load_library().msa_index_score_noalloc(ctypes.byref(prepared.call.args),
                                                   out.data_ptr(), _stream_handle(stream)))
     return out
+
+
+def noalloc_device_error(stream=None) -> int:
+    """Device error bits left by the last ``msa_index_score_noalloc`` call on
+    the current device (synchronises ``stream``; 0 = clean)."""
+    bits = ctypes.c_int32(0)
+    _check(load_library().msa_noalloc_device_error(ctypes.byref(bits), _stream_handle(stream)))
+    return int(bits.value)
 
 
 def msa_block_topk(score: torch.Tensor, k: int = 16, MB: Optional[int] = None,

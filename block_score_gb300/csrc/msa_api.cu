@@ -125,6 +125,12 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
+// Watchdog controls (msa_set_watchdog): limit of one on-chip pipeline wait
+// (0 = default) and the test stall.
+constexpr uint64_t kDefaultWaitLimitNs = 4000000000ull;   // 4 s: far above any legitimate wait
+std::atomic<uint64_t> g_wait_limit_ns{0};
+std::atomic<int32_t> g_wait_stall{0};
+
 int sm_count(int dev) {
   static std::atomic<int> cache[64];   // per device; threads that race store the same value
   if (dev >= 0 && dev < 64) {
@@ -167,7 +173,10 @@ msa_status_t fill_params(const msa_index_score_args* a, float* out, void* ws, ms
   p.scale = a->scale;
   p.out = out;
   p.ws = static_cast<uint8_t*>(ws);
-  p.wait_limit_ns = 4000000000ull;   // 4 s: far above any legitimate wait
+  const uint64_t lim = g_wait_limit_ns.load(std::memory_order_relaxed);
+  p.wait_limit_ns = lim ? lim : kDefaultWaitLimitNs;
+  p.stall = g_wait_stall.load(std::memory_order_relaxed) ? 1 : 0;
+  p.pad_ = 0;
   return MSA_OK;
 }
 
@@ -300,6 +309,31 @@ msa_status_t make_maps(const msa_index_score_args* a, const msa::Params& p, CUte
 
 namespace msa {
 void set_last_error_message(const char* msg) { snprintf(g_msg, sizeof g_msg, "%s", msg); }
+
+uint64_t current_context_id() {
+  typedef CUresult (*GetCurrentFn)(CUcontext*);
+  typedef CUresult (*GetIdFn)(CUcontext, unsigned long long*);
+  static GetCurrentFn get_current = nullptr;
+  static GetIdFn get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<GetCurrentFn>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<GetIdFn>(p);
+  });
+  if (!get_current || !get_id) return 0;
+  CUcontext c = nullptr;
+  if (get_current(&c) != CUDA_SUCCESS || !c) return 0;
+  unsigned long long id = 0;
+  if (get_id(c, &id) != CUDA_SUCCESS) return 0;
+  return (uint64_t)id + 1;
+}
 }  // namespace msa
 
 extern "C" {
@@ -450,5 +484,11 @@ const char* msa_status_string(msa_status_t st) {
 }
 
 const char* msa_last_error_message(void) { return g_msg; }
+
+msa_status_t msa_set_watchdog(uint64_t wait_limit_ns, int32_t stall) {
+  g_wait_limit_ns.store(wait_limit_ns, std::memory_order_relaxed);
+  g_wait_stall.store(stall ? 1 : 0, std::memory_order_relaxed);
+  return MSA_OK;
+}
 
 }  // extern "C"

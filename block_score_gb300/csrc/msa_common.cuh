@@ -2,6 +2,7 @@
 // block-score library: workspace (plan) layout, kernel parameters, unit
 // descriptors.  Nothing here is part of the public ABI.
 #pragma once
+#include <atomic>
 #include <cstddef>
 #include <cstdint>
 #include <cuda_runtime.h>
@@ -84,6 +85,8 @@ struct Params {
   float* out;
   uint8_t* ws;
   uint64_t wait_limit_ns;  // bound of every on-chip wait
+  int32_t stall;           // nonzero: the MMA helper first waits on a barrier nothing completes
+  int32_t pad_;
 };
 
 // One work unit as handed from the scheduler thread to the other roles.
@@ -105,6 +108,24 @@ static_assert(sizeof(UnitDesc) == 64, "UnitDesc is 64 bytes");
 
 // Record the message returned by msa_last_error_message() on this host thread.
 void set_last_error_message(const char* msg);
+
+// Unique id (+1) of the CUDA context current on this host thread, 0 if there
+// is none or the driver cannot say.  Per-device host caches are keyed by it:
+// a device reset or another context on the same device invalidates them.
+uint64_t current_context_id();
+
+// Raise a kernel's dynamic shared-memory limit, once per device context.
+// `done[dev]` holds the context id it was last raised for; host threads that
+// race both set it, which is harmless.
+template <class Kern>
+inline cudaError_t ensure_smem_limit(Kern kern, int bytes, std::atomic<uint64_t> (&done)[64], int dev) {
+  const uint64_t ctx = current_context_id();
+  const bool cached = ctx != 0 && dev >= 0 && dev < 64;
+  if (cached && done[dev].load(std::memory_order_relaxed) == ctx) return cudaSuccess;
+  const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && cached) done[dev].store(ctx, std::memory_order_relaxed);
+  return e;
+}
 
 // Host-side launchers (defined in the .cu files).
 cudaError_t launch_plan(const Params& p, cudaStream_t s);

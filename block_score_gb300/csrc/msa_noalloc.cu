@@ -11,8 +11,10 @@
 // The array is a file-scope __device__ object of MSA_NOALLOC_WORKSPACE_BYTES
 // bytes: every GPU that loads the library holds it until the process exits.
 // In host code the array's name is only a host-side stand-in, so its device
-// address is looked up with cudaGetSymbolAddress on the first call on each
-// device (with that device current) and cached.
+// address is looked up with cudaGetSymbolAddress with the device current and
+// cached per device, together with the id of the CUDA context it was looked
+// up in: after a device reset, or in another context on the same device, the
+// module is loaded afresh and the address is looked up again.
 #include <cuda_runtime.h>
 
 #include <cstdio>
@@ -29,38 +31,40 @@ static_assert(kScratchBytes == MSA_NOALLOC_WORKSPACE_BYTES, "header constant out
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 
 constexpr int kMaxDevices = 64;
+struct Resolved {
+  uint64_t ctx;   // context id the address belongs to (0: none yet)
+  void* addr;
+};
 std::mutex g_mu;
-void* g_scratch_addr[kMaxDevices] = {};
+Resolved g_scratch[kMaxDevices] = {};
 
-// Device address of the scratch array on the current device (first use per
-// device resolves it while that device is current).
+msa_status_t cuda_error(cudaError_t e, const char* what) {
+  char msg[256];
+  snprintf(msg, sizeof msg, "%s: %s", what, cudaGetErrorString(e));
+  msa::set_last_error_message(msg);
+  return MSA_ERR_CUDA;
+}
+
+// Device address of the scratch array in the current device's context.
 msa_status_t scratch_address(void** addr) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) {
-    char msg[256];
-    snprintf(msg, sizeof msg, "cudaGetDevice: %s", cudaGetErrorString(e));
-    msa::set_last_error_message(msg);
-    return MSA_ERR_CUDA;
-  }
+  if (e != cudaSuccess) return cuda_error(e, "cudaGetDevice");
   if (dev < 0 || dev >= kMaxDevices) {
     msa::set_last_error_message("device ordinal beyond the no-alloc entry point's table");
     return MSA_ERR_UNSUPPORTED;
   }
   std::lock_guard<std::mutex> lock(g_mu);
-  if (!g_scratch_addr[dev]) {
+  const uint64_t ctx = msa::current_context_id();
+  if (ctx == 0 || g_scratch[dev].ctx != ctx) {
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-    if (e != cudaSuccess || !p) {
-      char msg[256];
-      snprintf(msg, sizeof msg, "cudaGetSymbolAddress(no-alloc scratch): %s",
-               cudaGetErrorString(e));
-      msa::set_last_error_message(msg);
-      return MSA_ERR_CUDA;
-    }
-    g_scratch_addr[dev] = p;
+    if (e != cudaSuccess || !p) return cuda_error(e, "cudaGetSymbolAddress(no-alloc scratch)");
+    // the lookup makes the device's primary context current if none was
+    g_scratch[dev].ctx = msa::current_context_id();
+    g_scratch[dev].addr = p;
   }
-  *addr = g_scratch_addr[dev];
+  *addr = g_scratch[dev].addr;
   return MSA_OK;
 }
 
@@ -85,4 +89,15 @@ extern "C" msa_status_t msa_index_score_noalloc(const msa_index_score_args* args
   msa_status_t st = scratch_address(&ws);
   if (st != MSA_OK) return st;
   return msa_index_score(args, out, ws, kScratchBytes, stream);
+}
+
+extern "C" msa_status_t msa_noalloc_device_error(int32_t* bits, msa_stream_t stream) {
+  if (!bits) {
+    msa::set_last_error_message("bits is NULL");
+    return MSA_ERR_INVALID_ARG;
+  }
+  void* ws = nullptr;
+  msa_status_t st = scratch_address(&ws);
+  if (st != MSA_OK) return st;
+  return msa_get_device_error(ws, bits, stream);
 }

@@ -77,6 +77,12 @@ struct WaitCtl {
 
 constexpr int kDevErrTimeout = 0x10;
 
+// Bound of the teardown drains (in-flight TMA loads, queued MMAs) that a CTA
+// waits out before it exits.  Fixed and long, independent of the pipeline-wait
+// limit: copies and MMAs that are already issued always complete, and the CTA
+// must not exit while one can still write its shared or tensor memory.
+constexpr uint64_t kDrainLimitNs = 4000000000ull;
+
 // Wait until the phase with the given parity has completed.  Returns false
 // (and leaves the abort flag set) if the CTA is aborting or the limit passed.
 static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, const WaitCtl& ctl) {

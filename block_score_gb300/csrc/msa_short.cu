@@ -5,15 +5,12 @@ namespace msa {
 
 cudaError_t launch_short_i8(const void* tq, const void* tk, const Params& p, cudaStream_t s) {
   auto kern = short_kernel<false>;
-  static bool configured[64] = {};   // per device; setting it twice is harmless
+  static std::atomic<uint64_t> configured[64];   // per device: context the limit was raised in
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev >= 64 || !configured[dev]) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Short8::bytes);
-    if (e != cudaSuccess) return e;
-    if (dev < 64) configured[dev] = true;
-  }
+  e = ensure_smem_limit(kern, (int)Short8::bytes, configured, dev);
+  if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)p.num_sms);
   cfg.blockDim = dim3(Short8::kThreads);

@@ -330,13 +330,13 @@ __global__ void __launch_bounds__(Short8::kThreads, 1)
       for (uint32_t j = n_k > (uint32_t)S ? n_k - S : 0; j < n_k; ++j) {
         const uint32_t st = j % S, ph = (j / S) & 1u;
         const uint64_t t0 = global_timer_ns();
-        while (!mbar_try_wait(b_st_full + 8 * st, ph) && global_timer_ns() - t0 < p.wait_limit_ns) {
+        while (!mbar_try_wait(b_st_full + 8 * st, ph) && global_timer_ns() - t0 < kDrainLimitNs) {
         }
       }
       for (uint32_t j = n_q > (uint32_t)C::kQBufs ? n_q - C::kQBufs : 0; j < n_q; ++j) {
         const uint32_t st = j % C::kQBufs, ph = (j / C::kQBufs) & 1u;
         const uint64_t t0 = global_timer_ns();
-        while (!mbar_try_wait(b_q_full + 8 * st, ph) && global_timer_ns() - t0 < p.wait_limit_ns) {
+        while (!mbar_try_wait(b_q_full + 8 * st, ph) && global_timer_ns() - t0 < kDrainLimitNs) {
         }
       }
     }
@@ -381,7 +381,7 @@ __global__ void __launch_bounds__(Short8::kThreads, 1)
     if (lane == 0 && issued) {
       tc_commit(b_drain);
       const uint64_t t0 = global_timer_ns();
-      while (!mbar_try_wait(b_drain, 0) && global_timer_ns() - t0 < p.wait_limit_ns) {
+      while (!mbar_try_wait(b_drain, 0) && global_timer_ns() - t0 < kDrainLimitNs) {
       }
     }
     __syncwarp();
@@ -392,7 +392,10 @@ __global__ void __launch_bounds__(Short8::kThreads, 1)
     // passes the item to the MMA warp.  Every path out of the loop ends with
     // exactly one stop code, so the MMA warp's barrier waits always pair up.
     uint32_t ss = 0, sph = 0, qb = 0, qph = 0, it = 0;
-    for (;;) {
+    // watchdog test: the drain barrier's first phase completes only after the
+    // MMA warp's last commit, which waits for this warp, so the wait runs out
+    const bool go = !p.stall || warp_wait(b_drain, 0, ctl);
+    for (; go;) {
       if (!warp_wait(b_sched_full + 8 * ss, sph, ctl)) break;
       const UnitDesc d = ring[ss];
       __syncwarp();

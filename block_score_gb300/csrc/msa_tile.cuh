@@ -343,13 +343,13 @@ __global__ void __launch_bounds__(TileCfg<KI8>::kThreads, 1)
       for (uint32_t j = n_k > kRing ? n_k - kRing : 0; j < n_k; ++j) {
         const uint32_t st = j % kRing, ph = (j / kRing) & 1u;
         const uint64_t t0 = global_timer_ns();
-        while (!mbar_try_wait(kfull + 8 * st, ph) && global_timer_ns() - t0 < p.wait_limit_ns) {
+        while (!mbar_try_wait(kfull + 8 * st, ph) && global_timer_ns() - t0 < kDrainLimitNs) {
         }
       }
       for (uint32_t j = n_q > (uint32_t)L::kQBufs ? n_q - L::kQBufs : 0; j < n_q; ++j) {
         const uint32_t st = j % L::kQBufs, ph = (j / L::kQBufs) & 1u;
         const uint64_t t0 = global_timer_ns();
-        while (!mbar_try_wait(b_q_full + 8 * st, ph) && global_timer_ns() - t0 < p.wait_limit_ns) {
+        while (!mbar_try_wait(b_q_full + 8 * st, ph) && global_timer_ns() - t0 < kDrainLimitNs) {
         }
       }
     }
@@ -398,7 +398,7 @@ __global__ void __launch_bounds__(TileCfg<KI8>::kThreads, 1)
       // every MMA of this CTA has landed before TMEM is released
       tc_commit(b_drain);
       const uint64_t t0 = global_timer_ns();
-      while (!mbar_try_wait(b_drain, 0) && global_timer_ns() - t0 < p.wait_limit_ns) {
+      while (!mbar_try_wait(b_drain, 0) && global_timer_ns() - t0 < kDrainLimitNs) {
       }
     }
     __syncwarp();
@@ -409,7 +409,10 @@ __global__ void __launch_bounds__(TileCfg<KI8>::kThreads, 1)
     // slot on.  Every path out of the loop ends with exactly one stop code,
     // so the MMA warp's barrier waits always pair up.
     uint32_t ss = 0, sph = 0, qb = 0, qph = 0, ks = 0, kph = 0, ab = 0, aph = 0;
-    for (;;) {
+    // watchdog test: the drain barrier's first phase completes only after the
+    // MMA warp's last commit, which waits for this warp, so the wait runs out
+    const bool go = !p.stall || warp_wait(b_drain, 0, ctl);
+    for (; go;) {
       if (!warp_wait(b_sched_full + 8 * ss, sph, ctl)) break;
       const UnitDesc d = ring[ss];
       __syncwarp();
@@ -680,15 +683,12 @@ template <bool KI8, bool BF16, int F8>
 inline cudaError_t launch_tile(const void* tq, const void* tk, const Params& p, cudaStream_t s) {
   using L = TileLayout<KI8>;
   auto kern = tile_kernel<KI8, BF16, F8>;
-  static bool configured[64] = {};   // per device; setting it twice is harmless
+  static std::atomic<uint64_t> configured[64];   // per device: context the limit was raised in
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev >= 64 || !configured[dev]) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::bytes);
-    if (e != cudaSuccess) return e;
-    if (dev < 64) configured[dev] = true;
-  }
+  e = ensure_smem_limit(kern, (int)L::bytes, configured, dev);
+  if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)p.num_sms);
   cfg.blockDim = dim3(TileCfg<KI8>::kThreads);

@@ -176,17 +176,26 @@ msa_status_t msa_index_score_run(const msa_index_score_args *args, float *out, v
  * - The first call on a device looks up the array's device address
  *   (cudaGetSymbolAddress) with that device current and caches it; make that
  *   first call before any stream capture on that device.
+ *   The cache is keyed by the CUDA context as well: after a device reset,
+ *   or when another context is current on that device, the next call looks
+ *   the address up again (again outside any stream capture).
  * - Every call uses the same array and leaves its contents behind; each call
  *   clears the parts that must start at zero (work counter, error word) itself.
  * - Calls whose kernels overlap on the GPU (different streams, or several
  *   host threads) race on the array: order them, e.g. on one stream.
- * - The device error word of these calls lives in the library's array and is
- *   not readable through msa_get_device_error.
+ * - The device error word of these calls lives in the library's array; read
+ *   it with msa_noalloc_device_error.
  */
 #define MSA_NOALLOC_MAX_BATCH 1024
 #define MSA_NOALLOC_WORKSPACE_BYTES 41216
 msa_status_t msa_index_score_noalloc(const msa_index_score_args *args, float *out,
                                      msa_stream_t stream);
+
+/* Synchronise `stream` and read the device error word that the last
+ * msa_index_score_noalloc call on the current device left in the library's
+ * array (MSA_DEVERR_* bits; 0 = clean).  Allocates nothing.  Returns MSA_OK,
+ * MSA_ERR_INVALID_ARG for a NULL `bits`, or MSA_ERR_CUDA if the copy fails. */
+msa_status_t msa_noalloc_device_error(int32_t *bits, msa_stream_t stream);
 
 /*
  * Block top-k selection, the consumer of the block scores (MiniMax Sparse
@@ -222,6 +231,22 @@ msa_status_t msa_block_topk(const float *score, int32_t H, int64_t T, int32_t MB
  * by the last call (MSA_DEVERR_* bits; 0 = clean).  Returns MSA_OK, or
  * MSA_ERR_CUDA if the copy fails. */
 msa_status_t msa_get_device_error(const void *workspace, int32_t *bits, msa_stream_t stream);
+
+/*
+ * Watchdog of the score kernels (process-wide; applies to the calls enqueued
+ * after it is set).  Every on-chip pipeline wait has a wall-clock limit,
+ * `wait_limit_ns` (0 restores the default of 4 s, far above any legitimate
+ * wait).  A wait that runs past it records MSA_DEVERR_TIMEOUT; the kernel then
+ * lets its in-flight copies and tensor-core work finish, frees its tensor
+ * memory and returns instead of hanging, and that call's scores are
+ * incomplete.
+ *
+ * `stall` != 0 is for tests of that path: in every CTA of the score kernels
+ * the warp that feeds the tensor-core issuer first waits on a barrier that
+ * nothing completes, as a lost copy would leave it, so the limit runs out on
+ * every call.  Set it back to 0 for normal calls.  Returns MSA_OK.
+ */
+msa_status_t msa_set_watchdog(uint64_t wait_limit_ns, int32_t stall);
 
 /* Static description of a status code. */
 const char *msa_status_string(msa_status_t status);
