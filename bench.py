@@ -2,14 +2,18 @@
 
 One step = one full call of the op (plan kernel + persistent tensor-core score
 kernel) over one resident batch of synthetic inputs.  Default workload: the
-batched decode case (B=64 single-token requests, H_q=16, H_kv=1, D=P=128,
-kv_len uniform in [1024, 65536], BBND bf16 paged cache, 545 MB of keys).
+long-context prefill (B=1, T=16384 query tokens at kv_len=131072, H_q=64,
+H_kv=8, D=P=128, bf16, a randomly permuted [1, 1100] block table; output
+[64, 16384, 1104] fp32, 4.63 GB; 3.3e13 flop).  The same run also measures
+the other four workloads (tiny prefill, batched decode, varlen chunked
+prefill, int8 mixed) and the int8 decode subset as sub-records.
 
 Prints ONE JSON line (rank 0).  ``value`` is microseconds per call for the
 whole job (lower is better); the line also carries TFLOP/s, K-cache GB/s, the
-roofline of the dominant kernel, the CPU oracle timed on the host cores, an
-end-to-end figure through the C ABI with host buffers, and the SM clocks seen
-during the timed region.
+roofline of the dominant kernel (timed with CUDA events in the same
+clock-sampled window as the calls), the CPU oracle timed on the host cores,
+an end-to-end figure through the C ABI with host buffers, and the SM clocks
+seen during the timed region.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 1..5]
     python bench.py --impl reference ...   # the CPU oracle as the reference arm
@@ -41,7 +45,11 @@ L2_BYTES = 126 * 1024 * 1024   # GB300 L2 (spec: ~129 MB); inputs below it are c
 import synth  # noqa: E402
 
 METRIC = "MsaIndexScore µs/call, TFLOP/s and K-cache GB/s vs GB300 roofline (1 GPU)"
-DEFAULT_WORKLOAD = 2
+DEFAULT_WORKLOAD = 5
+# calls per timed pass when --steps is not given (about 0.2-0.6 s of GPU time each)
+DEFAULT_STEPS = {1: 5000, 2: 2000, 3: 300, 4: 400, 5: 30}
+DEFAULT_STEPS_DECODE_SUBSET = 5000
+SUB_WORKLOADS = [(1, False), (2, False), (3, False), (4, False), (4, True)]
 DTYPE_NAME = {torch.float16: "f16", torch.bfloat16: "bf16", torch.int8: "i8",
               torch.float8_e4m3fn: "e4m3", torch.float8_e5m2: "e5m2"}
 FP8 = {"e4m3": torch.float8_e4m3fn, "e5m2": torch.float8_e5m2}
@@ -281,7 +289,8 @@ def cpu_oracle_baseline(case, target_s: float = 12.0):
 
 
 def make_workload(args):
-    case = synth.config(args.workload, layout=args.layout)
+    case = synth.config(args.workload, layout=args.layout,
+                        q_len=getattr(args, "q_len", None) if args.workload == 5 else None)
     if args.decode_subset:
         case = synth.decode_subset(case)
     if args.fp8:
@@ -296,9 +305,19 @@ def make_workload(args):
 
 
 def workload_key(args) -> str:
+    q = getattr(args, "q_len", None)
     return (f"cfg{args.workload}" + ("_decode" if args.decode_subset else "")
+            + (f"_q{q}" if q and args.workload == 5 else "")
             + (f"_{args.layout.lower()}" if args.layout else "")
             + (f"_{args.fp8}" if args.fp8 else ""))
+
+
+def default_steps(args) -> int:
+    if args.steps is not None:
+        return args.steps
+    if args.decode_subset:
+        return DEFAULT_STEPS_DECODE_SUBSET
+    return DEFAULT_STEPS[args.workload]
 
 
 def run_reference(args):
@@ -317,10 +336,11 @@ def run_reference(args):
     n = int(min(rows_total, max(len(probe), 1.0 / per_row)))
     step = max(1, rows_total // n)
     rows = list(range(0, rows_total, step))
+    steps = args.steps if args.steps is not None else 5
     for _ in range(args.warmup):
         oracle.oracle_rows(case, rows)
     times = []
-    for _ in range(args.steps):
+    for _ in range(steps):
         t0 = time.perf_counter()
         oracle.oracle_rows(case, rows)
         times.append(time.perf_counter() - t0)
@@ -331,7 +351,7 @@ def run_reference(args):
               "scaled by row count")
     line = {
         "impl": "reference", "metric": METRIC, "value": us, "unit": "us/call",
-        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "n_gpus": ws, "steps": steps, "warmup": args.warmup,
         "ms_per_step": statistics.mean(times) * 1e3, "higher_is_better": False,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": config_block(case, workload_key(args)),
@@ -348,13 +368,120 @@ def run_reference(args):
 
 def config_block(case, workload):
     kb = algorithmic_work(case)["k_bytes"]
+    total_in = kb + case.query.numel() * case.query.element_size()
     return {"workload": f"{workload}:{case.name}", "B": case.B, "T": case.T,
             "H_q": case.H_q, "H_kv": case.H_kv, "D": case.D, "P": case.P, "MB": case.MB,
             "layout": case.layout, "k_dtype": DTYPE_NAME[case.key.dtype],
             "sparse_mode": case.sparse_mode, "init_blocks": case.init_blocks,
             "local_blocks": case.local_blocks,
-            "l2": (f"inputs larger than L2: K cache {kb / 1e6:.0f} MB > 129 MB"
-                   if kb > 129e6 else "inputs fit in L2 (no flush; latency-bound case)")}
+            "l2": (f"inputs larger than L2 (no flush): K cache {kb / 1e6:.0f} MB > 129 MB"
+                   if kb > 129e6 else
+                   (f"inputs larger than L2 (no flush): K + Q {total_in / 1e6:.0f} MB > 129 MB"
+                    if total_in > 129e6 else
+                    "inputs fit in L2 (no flush; launch- or latency-bound case)"))}
+
+
+def roofline_of(case, work, kern_ms, peaks, traffic):
+    """Roofline record of the dominant kernel from its per-launch duration."""
+    kern_s = kern_ms / 1e3
+    hbm_gbs_kernel = work["bytes"] / kern_s / 1e9
+    tflops_kernel = work["flops"] / kern_s / 1e12
+    bound = "hbm" if work["bytes"] / (peaks["hbm_gbs"] * 1e9) >= \
+        work["flops"] / (peaks["bf16_tflops"] * 1e12) else "tensor"
+    if bound == "hbm":
+        roof = {"bound": "hbm", "achieved": hbm_gbs_kernel, "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": hbm_gbs_kernel / peaks["hbm_gbs"],
+                "traffic": traffic, "peak_source": peaks["source"] + " hbm_gbs"}
+    elif case.query.element_size() == 1:
+        # FP8 operands: the measured bf16 peak times the nominal dense ratio 4.5 / 2.25
+        pk = peaks["bf16_tflops"] * 2.0
+        roof = {"bound": "tensor", "achieved": tflops_kernel, "peak": pk, "unit": "TFLOP/s",
+                "frac": tflops_kernel / pk, "traffic": traffic,
+                "peak_source": peaks["source"] + " bf16_tflops (burst) x 2 (nominal fp8 / bf16)"}
+    else:
+        pk = peaks["bf16_tflops"]
+        roof = {"bound": "tensor", "achieved": tflops_kernel, "peak": pk, "unit": "TFLOP/s",
+                "frac": tflops_kernel / pk, "traffic": traffic,
+                "peak_source": peaks["source"] + " bf16_tflops (burst)",
+                "frac_of_sustained": tflops_kernel / peaks["bf16_tflops_sustained"]}
+    roof["kernel"] = dominant_kernel(case)
+    roof["kernel_us"] = kern_ms * 1e3
+    roof["algorithmic_bytes"] = work["bytes"]
+    roof["algorithmic_flops"] = work["flops"]
+    return roof
+
+
+def measure(case, key, steps, warmup, device, stream, peaks, ws, traffic=None):
+    """Time one workload: pass A (K back-to-back calls, events at the ends)
+    gives the per-call time; pass B (K calls with events before each call and
+    around its score launches) gives the dominant kernel's per-launch time and,
+    from the same events, its own per-call time, so a launch never reads longer
+    than the call it belongs to.  Both passes run inside one clock-sampled
+    window."""
+    import block_score_gb300 as bs
+    work = algorithmic_work(case)
+    # the caller knows its requests' query lengths (as a serving loop does)
+    prep = bs.from_case(case, device, max_seqlen_q=max(case.q_lens) if case.q_lens else None)
+    # correctness gate before timing (the parity tests are the full check)
+    prep(stream)
+    if prep.device_error(stream):
+        raise RuntimeError(f"{key}: device error during the first call")
+    for _ in range(warmup):
+        prep(stream)
+    torch.cuda.synchronize(device)
+
+    sampler = ClockSampler(device.index if device.index is not None else 0)
+    sampler.start()
+    time.sleep(0.25)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev_b = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(3)) for _ in range(steps)]
+    barrier(ws)
+    torch.cuda.synchronize(device)
+    sampler.mark("start")
+    # pass A: back-to-back calls; the score kernel's launch overlaps the plan
+    ev0.record(stream)
+    for _ in range(steps):
+        prep(stream)
+    ev1.record(stream)
+    # pass B: events before each call and around its score launches
+    for i in range(steps):
+        ev_b[i][0].record(stream)
+        prep.plan(stream)
+        ev_b[i][1].record(stream)
+        prep.run(stream)
+        ev_b[i][2].record(stream)
+    torch.cuda.synchronize(device)
+    sampler.mark("stop")
+    sampler.stop()
+    barrier(ws)
+    total_ms = ev0.elapsed_time(ev1)
+    kern_ms = statistics.mean(b.elapsed_time(c) for _, b, c in ev_b)
+    call_b_ms = statistics.mean(a.elapsed_time(c) for a, _, c in ev_b)
+    step_ms, us_per_call = whole_job_us_per_call(total_ms / steps, ws, device)
+    kern_ms = max_over_ranks(kern_ms, ws, device)
+    call_b_ms = max_over_ranks(call_b_ms, ws, device)
+    if prep.device_error(stream):
+        raise RuntimeError(f"{key}: device error during the timed region")
+    call_s = step_ms / 1e3
+    roof = roofline_of(case, work, kern_ms, peaks, traffic)
+    roof["kernel_timing"] = ("CUDA events around the score launches of each call (tile "
+                             "kernel, plus the short-query kernel for int8 keys) after its "
+                             "plan, in a second pass of K calls inside the same clock-sampled "
+                             "window as the per-call timing")
+    roof["call_us_same_pass"] = call_b_ms * 1e3
+    rec = {
+        "workload": f"{key}:{case.name}", "value": us_per_call, "unit": "us/call",
+        "steps": steps, "ms_per_step": step_ms,
+        "tflops": work["flops"] / call_s / 1e12,
+        "k_cache_gbs": work["k_bytes"] / call_s / 1e9,
+        "frac_hbm": (work["bytes"] / call_s / 1e9) / peaks["hbm_gbs"],
+        "frac_tensor": work["flops"] / call_s / 1e12 /
+        (peaks["bf16_tflops"] * (2.0 if case.query.element_size() == 1 else 1.0)),
+        "roofline": roof,
+        "gpu_launches": launches_per_call(case) * steps,
+        "clocks": sampler.summary(),
+    }
+    return rec, prep
 
 
 def run_ours(args):
@@ -367,116 +494,65 @@ def run_ours(args):
     torch.cuda.set_device(device)
     import block_score_gb300 as bs
     bs.load_library()
-
-    case = make_workload(args)
-    work = algorithmic_work(case)
     peaks = load_peaks()
-    if args.traffic is None:
-        args.traffic = recorded_traffic(workload_key(args), dominant_kernel(case))
-    # the caller knows its requests' query lengths (as a serving loop does)
-    prep = bs.from_case(case, device, max_seqlen_q=max(case.q_lens) if case.q_lens else None)
     stream = torch.cuda.current_stream(device)
 
-    # correctness gate before timing (the parity tests are the full check)
-    prep()
-    if prep.device_error(stream):
-        raise RuntimeError("device error during the first call")
-
-    for _ in range(args.warmup):
-        prep(stream)
-    torch.cuda.synchronize(device)
-
-    sampler = ClockSampler(local)
-    sampler.start()
-    time.sleep(0.3)
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    # timed region: K back-to-back calls of the op (plan + score kernel), events
-    # only at its ends so the score kernel's launch overlaps the plan kernel
-    barrier(ws)
-    torch.cuda.synchronize(device)
-    sampler.mark("start")
-    ev0.record(stream)
-    for _ in range(args.steps):
-        prep(stream)
-    ev1.record(stream)
-    torch.cuda.synchronize(device)
-    sampler.mark("stop")
-    barrier(ws)
-    total_ms = ev0.elapsed_time(ev1)
-    # dominant kernel: a second pass of K calls with events around each
-    # score-kernel launch, on the launching stream
-    ev_k = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-            for _ in range(args.steps)]
-    torch.cuda.synchronize(device)
-    for i in range(args.steps):
-        prep.plan(stream)
-        ev_k[i][0].record(stream)
-        prep.run(stream)
-        ev_k[i][1].record(stream)
-    torch.cuda.synchronize(device)
-    sampler.stop()
-    kern_ms = statistics.mean(a.elapsed_time(b) for a, b in ev_k)
-    step_ms, us_per_call = whole_job_us_per_call(total_ms / args.steps, ws, device)
-    kern_ms = max_over_ranks(kern_ms, ws, device)
-    if prep.device_error(stream):
-        raise RuntimeError("device error during the timed region")
+    case = make_workload(args)
+    key = workload_key(args)
+    steps = default_steps(args)
+    traffic = args.traffic
+    if traffic is None:
+        traffic = recorded_traffic(key, dominant_kernel(case))
+    head, prep = measure(case, key, steps, args.warmup, device, stream, peaks, ws, traffic)
 
     # end to end through the C ABI with host buffers: H2D of the inputs, the
     # call, D2H of the scores, every step
-    e2e = e2e_run(case, device, stream, args)
+    e2e = e2e_run(case, device, stream, args, steps=min(steps, 5 if case.T * case.H_q > 1e6 else 20))
     # the block top-k selection over this call's scores (the scores' consumer;
     # not part of the metric above)
-    topk = topk_run(prep.out, case.MB, 16, device, stream, peaks, min(args.steps, 200))
-
-    call_s = step_ms / 1e3
-    kern_s = kern_ms / 1e3
-    tflops = work["flops"] / call_s / 1e12
-    kgbs = work["k_bytes"] / call_s / 1e9
-    hbm_gbs_kernel = work["bytes"] / kern_s / 1e9
-    tflops_kernel = work["flops"] / kern_s / 1e12
-    dominant_bound = "hbm" if work["bytes"] / (peaks["hbm_gbs"] * 1e9) >= \
-        work["flops"] / (peaks["bf16_tflops"] * 1e12) else "tensor"
-    if dominant_bound == "hbm":
-        roof = {"bound": "hbm", "achieved": hbm_gbs_kernel, "peak": peaks["hbm_gbs"],
-                "unit": "GB/s", "frac": hbm_gbs_kernel / peaks["hbm_gbs"],
-                "traffic": args.traffic, "peak_source": peaks["source"] + " hbm_gbs"}
-    elif case.query.element_size() == 1:
-        # FP8 operands: the measured bf16 peak times the nominal dense ratio 4.5 / 2.25
-        pk = peaks["bf16_tflops"] * 2.0
-        roof = {"bound": "tensor", "achieved": tflops_kernel, "peak": pk, "unit": "TFLOP/s",
-                "frac": tflops_kernel / pk, "traffic": args.traffic,
-                "peak_source": peaks["source"] + " bf16_tflops (burst) x 2 (nominal fp8 / bf16)"}
-    else:
-        pk = peaks["bf16_tflops"]
-        roof = {"bound": "tensor", "achieved": tflops_kernel, "peak": pk, "unit": "TFLOP/s",
-                "frac": tflops_kernel / pk, "traffic": args.traffic,
-                "peak_source": peaks["source"] + " bf16_tflops (burst)"}
-    roof["kernel"] = dominant_kernel(case)
-    roof["kernel_timing"] = ("second pass of K calls with CUDA events around the score "
-                             "launches of each call (tile kernel, plus the short-query "
-                             "kernel for int8 keys), after its plan")
-    roof["kernel_us"] = kern_ms * 1e3
-    roof["algorithmic_bytes"] = work["bytes"]
-    roof["algorithmic_flops"] = work["flops"]
+    topk = topk_run(prep.out, case.MB, 16, device, stream, peaks, min(steps * 5, 200))
+    del prep
+    torch.cuda.empty_cache()
 
     line = {
-        "metric": METRIC, "value": us_per_call, "unit": "us/call", "n_gpus": ws,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
+        "metric": METRIC, "value": head["value"], "unit": "us/call", "n_gpus": ws,
+        "steps": steps, "warmup": args.warmup, "ms_per_step": head["ms_per_step"],
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
         "dtype": DTYPE_NAME[case.query.dtype] if case.key.dtype != torch.int8 else "f16xi8",
         "data": "synthetic (seeded; shapes and length mix of the workload recipe)",
-        "config": config_block(case, workload_key(args)),
-        "tflops": tflops, "k_cache_gbs": kgbs,
-        "frac_hbm": (work["bytes"] / call_s / 1e9) / peaks["hbm_gbs"],
-        "frac_tensor": tflops / (peaks["bf16_tflops"] * (2.0 if case.query.element_size() == 1 else 1.0)),
-        "roofline": roof,
+        "config": config_block(case, key),
+        "tflops": head["tflops"], "k_cache_gbs": head["k_cache_gbs"],
+        "frac_hbm": head["frac_hbm"], "frac_tensor": head["frac_tensor"],
+        "roofline": head["roofline"],
         "e2e": e2e,
         "topk": topk,
-        "gpu_launches": launches_per_call(case) * args.steps,
-        "clocks": sampler.summary(),
+        "gpu_launches": head["gpu_launches"],
+        "clocks": head["clocks"],
     }
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_oracle_baseline(case)
+    del case
+
+    # the other workloads (and the int8 decode subset), each measured the same way
+    if not args.no_sub and args.workload == DEFAULT_WORKLOAD and not args.decode_subset \
+            and args.layout is None and args.fp8 is None and getattr(args, "q_len", None) is None:
+        subs = []
+        for n, dsub in SUB_WORKLOADS:
+            sa = argparse.Namespace(workload=n, decode_subset=dsub, layout=None, fp8=None,
+                                    q_len=None, steps=None)
+            scase = make_workload(sa)
+            skey = workload_key(sa)
+            rec, sprep = measure(scase, skey, default_steps(sa), args.warmup, device, stream,
+                                 peaks, ws, recorded_traffic(skey, dominant_kernel(scase)))
+            del sprep
+            rec["e2e"] = e2e_run(scase, device, stream, args, steps=20)
+            if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+                rec["cpu_baseline"] = cpu_oracle_baseline(scase, target_s=3.0)
+            rec["config"] = config_block(scase, skey)
+            subs.append(rec)
+            del scase
+            torch.cuda.empty_cache()
+        line["sub_workloads"] = subs
     if rank == 0:
         print(json.dumps(line), flush=True)
     if ws > 1:
@@ -508,7 +584,7 @@ def topk_run(score, MB: int, k: int, device, stream, peaks, steps: int):
             "inputs_in_l2": nbytes < L2_BYTES, "kernel": "topk_kernel"}
 
 
-def e2e_run(case, device, stream, args):
+def e2e_run(case, device, stream, args, steps=None):
     """Same metric through the public call with pinned host inputs."""
     import block_score_gb300 as bs
     host = {}
@@ -532,7 +608,7 @@ def e2e_run(case, device, stream, args):
                        local_blocks=case.local_blocks,
                        max_blocks=case.MB if case.layout == "TND" else None,
                        max_seqlen_q=max(case.q_lens) if case.q_lens else None)
-    out_host = torch.empty(prep.shape, dtype=torch.float32).pin_memory()
+    out_host = torch.empty(prep.shape, dtype=torch.float32, pin_memory=True)
     h2d = sum(v.numel() * v.element_size() for v in host.values() if v is not None)
     h2d += host_key_base.numel() * host_key_base.element_size()
     d2h = out_host.numel() * 4
@@ -545,7 +621,7 @@ def e2e_run(case, device, stream, args):
         prep(stream)
         out_host.copy_(prep.out, non_blocking=True)
 
-    steps = max(1, min(args.steps, 20))
+    steps = max(1, steps if steps is not None else 20)
     for _ in range(min(args.warmup, 3)):
         step()
     torch.cuda.synchronize(device)
@@ -563,8 +639,9 @@ def e2e_run(case, device, stream, args):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
-    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=None,
+                    help="calls per timed pass (default: per workload, ~0.2-0.6 s of GPU time)")
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", type=int, default=DEFAULT_WORKLOAD, choices=[1, 2, 3, 4, 5])
     ap.add_argument("--decode-subset", action="store_true",
@@ -573,6 +650,10 @@ def main(argv=None):
                     help="draw the workload's keys in another layout (same lengths)")
     ap.add_argument("--fp8", choices=sorted(FP8), default=None,
                     help="run the (fp16 / bf16) workload with FP8 query and keys")
+    ap.add_argument("--q-len", type=int, default=None,
+                    help="workload 5 only: its last Q_LEN query positions (profiler captures)")
+    ap.add_argument("--no-sub", action="store_true",
+                    help="measure the selected workload only (no sub-records)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--traffic", type=float, default=None,
                     help="DRAM bytes per launch of the score kernel from an ncu capture")

@@ -255,12 +255,16 @@ def _randint(gen, lo, hi):
     return int(torch.randint(lo, hi + 1, (1,), generator=gen).item())
 
 
-def config(n: int, seed: Optional[int] = None, layout: Optional[str] = None) -> MsaCase:
+def config(n: int, seed: Optional[int] = None, layout: Optional[str] = None,
+           q_len: Optional[int] = None) -> MsaCase:
     """Workload ``n`` (1..5) with its default seed ``1234 + n``.
 
     ``layout`` (optional) stores the same lengths in another key layout
     (BBND, BNBD or packed TND; for TND, MB becomes the longest request's block
     count); the drawn values then differ, the shapes and lengths do not.
+    ``q_len`` (workload 5 only) cuts the long prefill to its last ``q_len``
+    query positions at the same kv_len (a smaller case of the same kernel, for
+    profiler captures).
     """
     seed = 1234 + n if seed is None else seed
     g = torch.Generator().manual_seed(seed)
@@ -312,7 +316,8 @@ def config(n: int, seed: Optional[int] = None, layout: Optional[str] = None) -> 
                          k_kind="int8_full", MB=256, sparse_mode=3,
                          init_blocks=0, local_blocks=1, seed=seed + 1, name=name)
     if n == 5:
-        return build([16384], [131072], H_q=64, H_kv=8, layout="BBND",
+        return build([16384 if q_len is None else int(q_len)], [131072], H_q=64, H_kv=8,
+                         layout="BBND",
                          q_dtype=torch.bfloat16, MB=1100, NP=1024, sparse_mode=3,
                          init_blocks=4, local_blocks=8, start_loc=[1023],
                          seed=seed + 1, name=name)
