@@ -28,6 +28,23 @@ Readings where the pages are silent (listed in the design notes):
 The selection is written as the definition: filter, sort by (score
 descending, index ascending), cut at k, sort the cut by index.  A library
 sort is the only primitive; no blocking or reordering beyond that.
+
+Per-group selection (:func:`group_topk`), the same notes, section 4.3
+(Equation (3): every query head of a GQA group uses the group's index set)
+and the checklist of section 10 (items 7-9: one independent selection per
+GQA group shared by its heads; each query's own block added and occupying a
+slot; indices deduplicated, ascending, -1 only in the tail).  Readings where
+the pages leave the step open (listed in the design notes):
+
+* the group ranks blocks by its group score, the maximum over the group's g
+  index heads of their block scores (the op computes one score row per index
+  head; the paper's index branch has one index head per group, where this
+  maximum is that head's own score);
+* a query's own block is the block holding its position under the op's
+  rightDownCausal alignment, ``q_pos = kv_len - Lq + i``; it exists when
+  ``0 <= q_pos < kv_len`` (and its block is below MB).  With the local slot on,
+  it is always selected and the other k - 1 slots take the best remaining
+  blocks; without it the selection is the plain top-k of the group score.
 """
 from __future__ import annotations
 
@@ -61,4 +78,46 @@ def block_topk(score, MB: int, k: int, rows=None) -> np.ndarray:
     for r in it:
         h, t = divmod(int(r), T)
         out[t, h] = row_topk(sc[h, t], MB, k)
+    return out
+
+
+def local_blocks_of(case) -> np.ndarray:
+    """Each query token's own block (int64 ``[T]``, -1 where it has none)."""
+    P, MB = int(case.P), int(case.MB)
+    out = np.full(int(case.T), -1, dtype=np.int64)
+    t = 0
+    for Lq, L in zip(case.q_lens, case.kv_lens):
+        for i in range(Lq):
+            qpos = L - Lq + i
+            if 0 <= qpos < L and qpos // P < MB:
+                out[t + i] = qpos // P
+        t += Lq
+    return out
+
+
+def group_topk(score, g: int, MB: int, k: int, local=None, rows=None) -> np.ndarray:
+    """One selection per GQA group: ``[H, T, MBp]`` scores -> int32 ``[T, H // g, k]``.
+
+    ``local`` (optional, ``[T]``): each token's own block (-1: none); when
+    given, that block always takes one of the k slots.  ``rows`` (optional)
+    limits the work to the flat rows ``r * T + t``; the others stay -1.
+    """
+    sc = score.detach().cpu().numpy() if hasattr(score, "detach") else np.asarray(score)
+    H, T, MBp = sc.shape
+    R = H // g
+    gs = np.fmax.reduce(sc.reshape(R, g, T, MBp), axis=1)   # the group score: max over its heads
+    out = np.full((T, R, k), -1, dtype=np.int32)
+    it = range(R * T) if rows is None else rows
+    for flat in it:
+        r, t = divmod(int(flat), T)
+        row = gs[r, t]
+        loc = -1 if local is None else int(local[t])
+        if loc < 0:
+            out[t, r] = row_topk(row, MB, k)
+            continue
+        rest = np.array(row[:MB], dtype=np.float32, copy=True)
+        rest[loc] = np.float32(-np.inf)              # the local block is not a candidate twice
+        chosen = [c for c in row_topk(rest, MB, k - 1).tolist() if c >= 0] if k > 1 else []
+        chosen = sorted(chosen + [loc])
+        out[t, r, : len(chosen)] = chosen
     return out

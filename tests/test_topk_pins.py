@@ -113,3 +113,98 @@ def test_forced_blocks_are_selected():
             forced = np.nonzero(row[: case.MB] >= 1e28)[0]
             assert forced.size and forced.size <= 8
             assert set(forced.tolist()) <= set(out[t, h].tolist())
+
+
+# ---------------------------------------------------------------------------
+# per-GQA-group selection (MiniMax Sparse Attention notes, section 4.3
+# Equation (3), section 4.7 Equation (7), section 10 checklist items 7-9)
+
+GROUP_GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "group_topk_hand_example.json")
+
+
+def _group_golden():
+    spec = json.load(open(GROUP_GOLDEN))
+    H, T, MB, MBp = spec["H"], spec["T"], spec["MB"], spec["MBp"]
+    score = np.full((H, T, MBp), -np.inf, dtype=np.float32)
+    for key, vals in spec["rows"].items():
+        h, t = int(key[1]), int(key[3])
+        score[h, t, :MB] = [_v(x) for x in vals]
+    for key, cols in spec.get("padding_overrides", {}).items():
+        h, t = int(key[1]), int(key[3])
+        for c, v in cols.items():
+            score[h, t, int(c)] = v
+    return spec, score
+
+
+def test_group_hand_example():
+    spec, score = _group_golden()
+    g, MB, k = spec["g"], spec["MB"], spec["k"]
+    plain = otk.group_topk(score, g, MB, k)
+    local = otk.group_topk(score, g, MB, k, local=np.array(spec["local"]))
+    assert plain.shape == (spec["T"], spec["H"] // g, k)
+    for key, exp in spec["expect_plain"].items():
+        assert plain[int(key[3]), int(key[1])].tolist() == exp, key
+    for key, exp in spec["expect_local"].items():
+        assert local[int(key[3]), int(key[1])].tolist() == exp, key
+    k4 = otk.group_topk(score, g, MB, 4)
+    assert k4[1, 0].tolist() == spec["k4_plain_r0t1"]
+
+
+@pytest.mark.parametrize("g", [1, 2, 8])
+def test_group_selection_matches_torch_amax_then_topk(g):
+    # the group score by torch.amax over the group's heads, the selection by
+    # torch.topk: the same sets on rows without ties
+    gen = torch.Generator().manual_seed(70 + g)
+    R, T, MB, MBp, k = 3, 4, 200, 208, 16
+    score = torch.randn(R * g, T, MBp, generator=gen)
+    score[:, :, MB:] = 1e30                           # padding columns never count
+    out = otk.group_topk(score.numpy(), g, MB, k)
+    gs = score.reshape(R, g, T, MBp).amax(dim=1)[:, :, :MB]
+    for r in range(R):
+        for t in range(T):
+            want = sorted(torch.topk(gs[r, t], k).indices.tolist())
+            assert out[t, r].tolist() == want
+
+
+def test_group_selection_ignores_head_order_inside_a_group():
+    gen = torch.Generator().manual_seed(77)
+    g, R, T, MBp = 4, 2, 3, 64
+    score = torch.randn(R * g, T, MBp, generator=gen).numpy()
+    perm = np.concatenate([r * g + np.random.default_rng(r).permutation(g) for r in range(R)])
+    a = otk.group_topk(score, g, 60, 8)
+    b = otk.group_topk(score[perm], g, 60, 8)
+    assert np.array_equal(a, b)
+
+
+def test_group_of_one_head_is_the_per_head_selection():
+    gen = torch.Generator().manual_seed(78)
+    score = torch.randn(5, 6, 48, generator=gen).numpy()
+    assert np.array_equal(otk.group_topk(score, 1, 40, 7), otk.block_topk(score, 40, 7))
+
+
+def test_local_slot_keeps_the_own_block_and_the_best_others():
+    gen = torch.Generator().manual_seed(79)
+    g, R, T, MB, MBp, k = 2, 2, 8, 90, 96, 16
+    score = torch.randn(R * g, T, MBp, generator=gen)
+    local = np.array([0, 5, 89, 44, 44, 3, 88, 17])
+    out = otk.group_topk(score.numpy(), g, MB, k, local=local)
+    gs = score.reshape(R, g, T, MBp).amax(dim=1)[:, :, :MB]
+    for r in range(R):
+        for t in range(T):
+            row = out[t, r].tolist()
+            assert row == sorted(set(row)) and len(row) == k      # ascending, no repeats
+            assert int(local[t]) in row
+            rest = gs[r, t].clone()
+            rest[int(local[t])] = -float("inf")
+            best = set(torch.topk(rest, k - 1).indices.tolist())
+            assert set(row) == best | {int(local[t])}
+
+
+def test_own_block_of_each_query_token():
+    # rightDownCausal positions: q_pos = kv_len - Lq + i, block q_pos // P
+    case = make_case([3, 1, 0, 2], [300, 129, 50, 1], H_q=2, H_kv=1, P=128, D=16,
+                     layout="BBND", q_dtype=torch.float16, MB=4, seed=80)
+    loc = otk.local_blocks_of(case).tolist()
+    # request 0: q_pos 297, 298, 299 -> block 2; request 1: q_pos 128 -> block 1;
+    # request 3: q_pos -1 (no key at or before it) and 0 -> none, block 0
+    assert loc == [2, 2, 2, 1, -1, 0]
