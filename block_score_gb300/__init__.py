@@ -97,6 +97,8 @@ def load_library():
     lib.msa_noalloc_device_error.argtypes = [ctypes.POINTER(ctypes.c_int32), vp]
     lib.msa_block_topk.argtypes = [vp, ctypes.c_int32, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32,
                                    ctypes.c_int32, vp, vp]
+    lib.msa_index_score_topk_workspace_size.argtypes = [P, ctypes.c_int32, ctypes.POINTER(sz)]
+    lib.msa_index_score_topk.argtypes = [P, ctypes.c_int32, ctypes.c_int32, vp, vp, vp, sz, vp]
     lib.msa_set_watchdog.argtypes = [ctypes.c_uint64, ctypes.c_int32]
     lib.msa_set_watchdog.restype = ctypes.c_int
     lib.msa_status_string.restype = ctypes.c_char_p
@@ -105,7 +107,7 @@ def load_library():
     for name in ("msa_index_score_out_shape", "msa_index_score_workspace_size",
                  "msa_index_score", "msa_index_score_plan", "msa_index_score_run",
                  "msa_get_device_error", "msa_index_score_noalloc", "msa_noalloc_device_error",
-                 "msa_block_topk"):
+                 "msa_block_topk", "msa_index_score_topk_workspace_size", "msa_index_score_topk"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -393,6 +395,43 @@ class Prepared:
 
     def device_error(self, stream=None) -> int:
         return msa_get_device_error(self.workspace, stream)
+
+    def select_workspace_bytes(self, k: int) -> int:
+        n = ctypes.c_size_t()
+        _check(load_library().msa_index_score_topk_workspace_size(ctypes.byref(self.call.args),
+                                                                  int(k), ctypes.byref(n)))
+        return int(n.value)
+
+    def topk(self, k: int = 16, local_slot: bool = True, scores: bool = True,
+             indices: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+             stream=None) -> torch.Tensor:
+        """Scores (into ``self.out`` when ``scores``) and the fused per-GQA-group
+        selection: int32 ``[T, H_kv, k]``, ascending block indices, -1 tail.
+
+        ``local_slot``: each query token's own block always takes a slot.
+        ``workspace`` (optional) is reused across calls when given; it must hold
+        ``select_workspace_bytes(k)`` bytes."""
+        T, H_kv = int(self.call.args.T), int(self.call.args.H_kv)
+        shape = (T, H_kv, int(k))
+        if indices is None:
+            indices = torch.empty(shape, dtype=torch.int32, device=self.out.device)
+        elif tuple(indices.shape) != shape or indices.dtype != torch.int32 or not indices.is_contiguous():
+            raise ValueError(f"indices must be a contiguous int32 tensor of shape {shape}")
+        nbytes = self.select_workspace_bytes(k)
+        if workspace is None:
+            workspace = torch.empty(nbytes, dtype=torch.uint8, device=self.out.device)
+        elif workspace.numel() * workspace.element_size() < nbytes:
+            raise ValueError(f"workspace needs {nbytes} bytes")
+        self.select_workspace = workspace
+        _check(load_library().msa_index_score_topk(
+            ctypes.byref(self.call.args), int(k), 1 if local_slot else 0,
+            self.out.data_ptr() if scores else None, indices.data_ptr(), workspace.data_ptr(),
+            workspace.numel() * workspace.element_size(), _stream_handle(stream)))
+        return indices
+
+    def select_device_error(self, stream=None) -> int:
+        """Device error bits of the last ``topk`` call (its workspace holds them)."""
+        return msa_get_device_error(self.select_workspace, stream)
 
 
 def msa_index_score_plan(prepared: Prepared, stream=None):

@@ -176,7 +176,51 @@ msa_status_t fill_params(const msa_index_score_args* a, float* out, void* ws, ms
   const uint64_t lim = g_wait_limit_ns.load(std::memory_order_relaxed);
   p.wait_limit_ns = lim ? lim : kDefaultWaitLimitNs;
   p.stall = g_wait_stall.load(std::memory_order_relaxed) ? 1 : 0;
+  p.topk_k = 0;
+  p.cand = nullptr;
+  p.cand_parts = 0;
+  p.chunk_min[0] = p.chunk_min[1] = 0;
   p.pad_ = 0;
+  return MSA_OK;
+}
+
+// Fused per-group selection: the partial lists of all rows (T x H_kv rows,
+// 2 per KV chunk of a tile, k keys of 8 bytes each) are kept within
+// kCandBudget bytes by capping the KV chunks of a tile (the plan's chunk floor).
+constexpr int64_t kCandBudget = 64ll << 20;
+
+struct SelectPlan {
+  int32_t chunks;         // KV chunks per tile at most
+  int32_t parts;          // partial lists per row
+  int32_t chunk_min[2];   // plan chunk floors (tile class: multiple of 8, short class: of 4)
+  size_t plan_bytes;      // the score plan's workspace
+  size_t cand_bytes;      // the partial lists
+};
+
+SelectPlan select_plan(const msa_index_score_args* a, int k) {
+  SelectPlan sp;
+  const int64_t mbp = round16(a->MB);
+  const int64_t most = (mbp + 3) / 4;               // chunks of the smallest chunk size (4 blocks)
+  const int64_t per_chunk = a->T * (int64_t)a->H_kv * 2 * k * 8;
+  int64_t c = per_chunk > 0 ? kCandBudget / per_chunk : most;
+  c = c < 1 ? 1 : (c > most ? most : c);
+  const int64_t floor_blocks = (mbp + c - 1) / c;
+  sp.chunks = (int32_t)c;
+  sp.parts = (int32_t)(2 * c);
+  sp.chunk_min[0] = (int32_t)((floor_blocks + 7) / 8 * 8);
+  sp.chunk_min[1] = (int32_t)((floor_blocks + 3) / 4 * 4);
+  sp.plan_bytes = msa::workspace_bytes_for(a->B);
+  sp.cand_bytes = (size_t)(a->T * (int64_t)a->H_kv * sp.parts * k) * 8;
+  return sp;
+}
+
+msa_status_t validate_select(const msa_index_score_args* a, int k) {
+  if (k < 1 || k > msa::kTopkMax)
+    return fail(MSA_ERR_INVALID_ARG, "k must be in [1, %d]", msa::kTopkMax);
+  const int g = a->H_q / a->H_kv;
+  if (32 % g != 0)
+    return fail(MSA_ERR_UNSUPPORTED,
+                "the fused per-group selection needs H_q / H_kv in {1, 2, 4, 8, 16, 32} (got %d)", g);
   return MSA_OK;
 }
 
@@ -442,6 +486,48 @@ msa_status_t msa_index_score(const msa_index_score_args* args, float* out, void*
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if ((st = launch_plan_checked(p, s)) != MSA_OK) return st;
   return launch_score_checked(args, p, s);
+}
+
+msa_status_t msa_index_score_topk_workspace_size(const msa_index_score_args* args, int32_t k,
+                                                 size_t* bytes) {
+  msa_status_t st = validate(args);
+  if (st != MSA_OK) return st;
+  if ((st = validate_select(args, k)) != MSA_OK) return st;
+  if (!bytes) return fail(MSA_ERR_INVALID_ARG, "bytes is NULL");
+  const SelectPlan sp = select_plan(args, k);
+  *bytes = sp.plan_bytes + sp.cand_bytes;
+  return MSA_OK;
+}
+
+msa_status_t msa_index_score_topk(const msa_index_score_args* args, int32_t k, int32_t local_slot,
+                                  float* out, int32_t* indices, void* workspace,
+                                  size_t workspace_bytes, msa_stream_t stream) {
+  g_msg[0] = 0;
+  msa_status_t st = validate(args);
+  if (st != MSA_OK) return st;
+  if ((st = validate_select(args, k)) != MSA_OK) return st;
+  if (args->T == 0 || args->B == 0) return MSA_OK;
+  if (!indices || !aligned(indices, 4)) return fail(MSA_ERR_INVALID_ARG, "indices must be a 4-byte aligned pointer");
+  if (out && !aligned(out, 16)) return fail(MSA_ERR_INVALID_ARG, "out must be 16-byte aligned (or NULL)");
+  const SelectPlan sp = select_plan(args, k);
+  if (!workspace) return fail(MSA_ERR_WORKSPACE, "workspace is NULL");
+  if (!aligned(workspace, 256)) return fail(MSA_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+  if (workspace_bytes < sp.plan_bytes + sp.cand_bytes)
+    return fail(MSA_ERR_WORKSPACE, "workspace needs %zu bytes, got %zu", sp.plan_bytes + sp.cand_bytes,
+                workspace_bytes);
+  msa::Params p;
+  if ((st = fill_params(args, out, workspace, p)) != MSA_OK) return st;
+  p.topk_k = k;
+  p.cand = reinterpret_cast<uint64_t*>(static_cast<uint8_t*>(workspace) + sp.plan_bytes);
+  p.cand_parts = sp.parts;
+  p.chunk_min[0] = sp.chunk_min[0];
+  p.chunk_min[1] = sp.chunk_min[1];
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if ((st = launch_plan_checked(p, s)) != MSA_OK) return st;
+  if ((st = launch_score_checked(args, p, s)) != MSA_OK) return st;
+  cudaError_t e = msa::launch_group_select(p, local_slot ? 1 : 0, indices, s);
+  if (e != cudaSuccess) return cuda_fail(e, "selection kernel launch");
+  return MSA_OK;
 }
 
 msa_status_t msa_block_topk(const float* score, int32_t H, int64_t T, int32_t MBp, int32_t MB,

@@ -86,8 +86,17 @@ struct Params {
   uint8_t* ws;
   uint64_t wait_limit_ns;  // bound of every on-chip wait
   int32_t stall;           // nonzero: the MMA helper first waits on a barrier nothing completes
+  // fused per-group selection (msa_index_score_topk); zero / null otherwise
+  int32_t topk_k;          // blocks per selection (1..kTopkMax)
+  uint64_t* cand;          // partial selections: [T][H_kv][cand_parts][topk_k] candidate keys
+  int32_t cand_parts;      // partial lists per (token, group) row: 2 per KV chunk
+  int32_t chunk_min[2];    // lower bound of each class's KV chunk (caps the chunks per tile)
   int32_t pad_;
 };
+
+// Blocks per selection that the fused per-group selection supports (the
+// pages' selector fixes 16).
+constexpr int kTopkMax = 16;
 
 // One work unit as handed from the scheduler thread to the other roles.
 struct alignas(16) UnitDesc {
@@ -102,9 +111,58 @@ struct alignas(16) UnitDesc {
   int32_t kbase;     // TND key row base
   int32_t sl;        // start_loc of the request
   int32_t pg0, pg1;  // paged layouts: block_table entries of blocks c0 and c0 + 1 (if computed)
-  int32_t pad;
+  int32_t ch;        // KV chunk index of the unit within its query tile
 };
 static_assert(sizeof(UnitDesc) == 64, "UnitDesc is 64 bytes");
+
+__host__ __device__ __forceinline__ int cdiv(int a, int b) { return (a + b - 1) / b; }
+
+// One request as the plan sees it, read and validated from the per-request
+// arrays (the plan kernel and the per-group selection merge both use it, so
+// they agree on every request's class and KV chunk count).
+struct ReqScratch {
+  int Lq, L, t0, kbase, ntiles, nbc_max, cls;
+};
+
+__device__ inline ReqScratch read_request(const Params& p, int b, int& err) {
+  ReqScratch r;
+  const int64_t q0 = p.cu_q[b], q1 = p.cu_q[b + 1];
+  if ((b == 0 && q0 != 0) || q1 < q0 || q0 < 0 || q1 > p.T || (b == p.B - 1 && q1 != p.T))
+    err |= kErrCuQ;
+  int64_t lo = q0 < 0 ? 0 : (q0 > p.T ? p.T : q0);
+  int64_t hi = q1 < lo ? lo : (q1 > p.T ? p.T : q1);
+  r.t0 = (int)lo;
+  r.Lq = (int)(hi - lo);
+  // a host length bound that this request breaks: the launch may have left
+  // out the kernel that would have scored it
+  if (p.max_q > 0 && r.Lq > p.max_q) err |= kErrCuQ;
+  int64_t L;
+  if (p.layout == 2) {
+    const int64_t k0 = p.cu_k[b], k1 = p.cu_k[b + 1];
+    if ((b == 0 && k0 != 0) || k1 < k0 || k0 < 0 || k1 > p.NP) err |= kErrCuK;
+    int64_t a = k0 < 0 ? 0 : (k0 > p.NP ? p.NP : k0);
+    int64_t e = k1 < a ? a : (k1 > p.NP ? p.NP : k1);
+    r.kbase = (int)a;
+    L = e - a;
+  } else {
+    L = p.kv_len[b];
+    r.kbase = 0;
+    if (L < 0) {
+      err |= kErrKvLen;
+      L = 0;
+    }
+  }
+  const int64_t nb = (L + kP - 1) / kP;
+  if (nb > p.MB) err |= kErrKvLen;
+  r.L = (int)(L > 0x7fffffff ? 0x7fffffff : L);
+  // short class (int8 keys): every query row of the request fits the N side
+  // of one MMA; 16-bit keys stream through the tile kernel at HBM speed
+  r.cls = (p.k_int8 && r.Lq > 0 && (int64_t)r.Lq * p.g <= kShortRows) ? 1 : 0;
+  r.ntiles = r.cls ? 1 : cdiv(r.Lq, p.np);
+  // the last query row sees the most blocks: q_pos = L - 1 in both modes
+  r.nbc_max = L > 0 ? (int)(nb < p.MB ? nb : p.MB) : 0;
+  return r;
+}
 
 // Record the message returned by msa_last_error_message() on this host thread.
 void set_last_error_message(const char* msg);
@@ -131,6 +189,8 @@ inline cudaError_t ensure_smem_limit(Kern kern, int bytes, std::atomic<uint64_t>
 cudaError_t launch_plan(const Params& p, cudaStream_t s);
 cudaError_t launch_topk(const float* score, int H, long long T, int MBp, int MB, int k, int32_t* out,
                         int num_sms, cudaStream_t s);
+// The score launchers run the fused-selection variant of their kernel when
+// p.topk_k > 0.
 cudaError_t launch_score_16(const void* tmap_q, const void* tmap_k, const Params& p, bool bf16,
                             cudaStream_t s);
 cudaError_t launch_score_f8(const void* tmap_q, const void* tmap_k, const Params& p, bool e5m2,
@@ -139,5 +199,7 @@ cudaError_t launch_score_i8(const void* tmap_q, const void* tmap_k, const Params
                             cudaStream_t s);
 cudaError_t launch_short_i8(const void* tmap_q, const void* tmap_k, const Params& p,
                             cudaStream_t s);
+// Merge of the partial selections into [T, H_kv, k] indices (after the score kernels).
+cudaError_t launch_group_select(const Params& p, int local_slot, int32_t* out, cudaStream_t s);
 
 }  // namespace msa

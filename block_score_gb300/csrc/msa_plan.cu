@@ -19,8 +19,6 @@ namespace {
 
 constexpr int kPlanThreads = 1024;
 
-__device__ __forceinline__ int cdiv(int a, int b) { return (a + b - 1) / b; }
-
 // Inclusive block scan of one value per thread (blockDim.x threads, a
 // multiple of 32 and at most 1024).
 __device__ int block_incl_scan(int v, int* s_warp) {
@@ -46,50 +44,6 @@ __device__ int block_incl_scan(int v, int* s_warp) {
   if (warp > 0) v += s_warp[warp - 1];
   __syncthreads();
   return v;
-}
-
-struct ReqScratch {
-  int Lq, L, t0, kbase, ntiles, nbc_max, cls;
-};
-
-__device__ ReqScratch read_request(const Params& p, int b, int& err) {
-  ReqScratch r;
-  const int64_t q0 = p.cu_q[b], q1 = p.cu_q[b + 1];
-  if ((b == 0 && q0 != 0) || q1 < q0 || q0 < 0 || q1 > p.T || (b == p.B - 1 && q1 != p.T))
-    err |= kErrCuQ;
-  int64_t lo = q0 < 0 ? 0 : (q0 > p.T ? p.T : q0);
-  int64_t hi = q1 < lo ? lo : (q1 > p.T ? p.T : q1);
-  r.t0 = (int)lo;
-  r.Lq = (int)(hi - lo);
-  // a host length bound that this request breaks: the launch may have left
-  // out the kernel that would have scored it
-  if (p.max_q > 0 && r.Lq > p.max_q) err |= kErrCuQ;
-  int64_t L;
-  if (p.layout == 2) {
-    const int64_t k0 = p.cu_k[b], k1 = p.cu_k[b + 1];
-    if ((b == 0 && k0 != 0) || k1 < k0 || k0 < 0 || k1 > p.NP) err |= kErrCuK;
-    int64_t a = k0 < 0 ? 0 : (k0 > p.NP ? p.NP : k0);
-    int64_t e = k1 < a ? a : (k1 > p.NP ? p.NP : k1);
-    r.kbase = (int)a;
-    L = e - a;
-  } else {
-    L = p.kv_len[b];
-    r.kbase = 0;
-    if (L < 0) {
-      err |= kErrKvLen;
-      L = 0;
-    }
-  }
-  const int64_t nb = (L + kP - 1) / kP;
-  if (nb > p.MB) err |= kErrKvLen;
-  r.L = (int)(L > 0x7fffffff ? 0x7fffffff : L);
-  // short class (int8 keys): every query row of the request fits the N side
-  // of one MMA; 16-bit keys stream through the tile kernel at HBM speed
-  r.cls = (p.k_int8 && r.Lq > 0 && (int64_t)r.Lq * p.g <= kShortRows) ? 1 : 0;
-  r.ntiles = r.cls ? 1 : cdiv(r.Lq, p.np);
-  // the last query row sees the most blocks: q_pos = L - 1 in both modes
-  r.nbc_max = L > 0 ? (int)(nb < p.MB ? nb : p.MB) : 0;
-  return r;
 }
 
 __device__ int chunk_for(unsigned long long work, int num_sms, int MBp, int gran) {
@@ -173,8 +127,9 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const Params p) {
     if (nreq[1]) atomicAdd(&s_nreq[1], nreq[1]);
   }
   __syncthreads();
-  const int chunk0 = chunk_for(s_work[0], p.num_sms, p.MBp, 8);
-  const int chunk1 = chunk_for(s_work[1], p.num_sms, p.MBp, 4);
+  // a caller-side floor (the fused selection bounds the KV chunks of a tile)
+  const int chunk0 = max(chunk_for(s_work[0], p.num_sms, p.MBp, 8), min(p.chunk_min[0], p.MBp));
+  const int chunk1 = max(chunk_for(s_work[1], p.num_sms, p.MBp, 4), min(p.chunk_min[1], p.MBp));
   const int n0 = s_nreq[0];
 
   if (small) {

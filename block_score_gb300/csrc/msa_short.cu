@@ -3,8 +3,9 @@
 
 namespace msa {
 
-cudaError_t launch_short_i8(const void* tq, const void* tk, const Params& p, cudaStream_t s) {
-  auto kern = short_kernel<false>;
+template <bool TOPK>
+cudaError_t launch_short_variant(const void* tq, const void* tk, const Params& p, cudaStream_t s) {
+  auto kern = short_kernel<false, TOPK>;
   static std::atomic<uint64_t> configured[64];   // per device: context the limit was raised in
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -23,6 +24,12 @@ cudaError_t launch_short_i8(const void* tq, const void* tk, const Params& p, cud
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kern, *static_cast<const CUtensorMap*>(tq),
                             *static_cast<const CUtensorMap*>(tk), p);
+}
+
+// The plain scores, or the fused per-group selection when p.topk_k > 0.
+cudaError_t launch_short_i8(const void* tq, const void* tk, const Params& p, cudaStream_t s) {
+  return p.topk_k > 0 ? launch_short_variant<true>(tq, tk, p, s)
+                      : launch_short_variant<false>(tq, tk, p, s);
 }
 
 }  // namespace msa

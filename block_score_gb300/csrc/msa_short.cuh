@@ -89,6 +89,21 @@ struct Short8 {
 };
 
 static_assert(Short8::bytes <= 232448, "shared memory per CTA");
+// Regions in address order without overlap (nothing but mbarrier operations
+// and tcgen05.commit touches the barrier words); swizzled tiles 1 KiB aligned.
+static_assert(Short8::q_off % 1024 == 0 && Short8::k_off % 1024 == 0 &&
+                  Short8::kQBytes % 1024 == 0 && Short8::kPageBytes % 1024 == 0 &&
+                  Short8::q_off + Short8::kQBufs * Short8::kQBytes <= Short8::k_off &&
+                  kRawBytes + kRawScaleBytes <= Short8::kPageBytes &&
+                  Short8::k_off + Short8::kStages * Short8::kStageBytes <= Short8::red_off &&
+                  Short8::red_off + Short8::red_bytes <= Short8::ring_off &&
+                  Short8::ring_off + kSched * sizeof(UnitDesc) <= Short8::req_off &&
+                  Short8::req_off + Short8::kReqCache * sizeof(ReqInfo) <= Short8::pfx_off &&
+                  Short8::pfx_off + Short8::kReqCache * 4 <= Short8::bar_off &&
+                  Short8::bar_off % 8 == 0 &&
+                  Short8::bar_off + Short8::n_bars * 8 <= Short8::misc_off &&
+                  Short8::misc_off + 16 + 8 * Short8::kStages <= Short8::end,
+              "short-query kernel shared-memory layout");
 // A converter writes page p's scale into column p % kScCols once the MMAs of
 // the item kA back are done; by then the epilogue has read every page up to
 // (kA + kD) items back, so the ring never overwrites an unread scale.
@@ -110,7 +125,12 @@ __device__ __forceinline__ float warp_transpose_max32(float (&v)[32], int lane) 
   return v[0];
 }
 
-template <bool BF16>
+// TOPK: the fused per-group selection.  The combine warp keeps, per query
+// position, a running top-kTopkMax list of the group score (the max over the
+// position's g head lanes, g dividing 32) over every block of a unit and
+// writes it as the unit's partial list (part 2 * chunk; part 2 * chunk + 1 is
+// written empty); the scores are stored only if p.out is not null.
+template <bool BF16, bool TOPK = false>
 __global__ void __launch_bounds__(Short8::kThreads, 1)
     short_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                  const Params p) {
@@ -534,7 +554,9 @@ __global__ void __launch_bounds__(Short8::kThreads, 1)
     // four partial maxima of each computed block, the local-mask constants, the
     // fill of the other columns, and 16-byte stores of 4 blocks at a time.
     const float ninf = __int_as_float(0xff800000);
+    const bool write_out = p.out != nullptr;
     uint32_t ss = 0, sph = 0, rr = 0, rph = 0;
+    TopList sel;
     for (;;) {
       if (!warp_wait(b_sched_full + 8 * ss, sph, ctl)) break;
       const UnitDesc d = ring[ss];
@@ -544,6 +566,13 @@ __global__ void __launch_bounds__(Short8::kThreads, 1)
       if (!d.live) break;
       const int rows = d.Lq * p.g;                        // valid query rows (<= 32)
       const bool row_valid = lane < rows;
+      if constexpr (TOPK) sel.clear();
+      auto select = [&](float m, int col) {
+        if constexpr (TOPK) {
+          const float gm = group_max(row_valid ? m : ninf, p.g);
+          if (col < p.MB) sel.insert(cand_key(gm, col));
+        }
+      };
       const int pos = lane / p.g;
       const int h = d.hk * p.g + (lane - pos * p.g);
       float* orow = p.out + ((int64_t)h * p.T + (d.t0 + pos)) * (int64_t)p.MBp;
@@ -572,6 +601,8 @@ __global__ void __launch_bounds__(Short8::kThreads, 1)
         // local mask after the max; a lone last block's partner is a fill column
         if (forced(beta)) m0 = fill_value(beta);
         if (beta + 1 >= d.b1 || forced(beta + 1)) m1 = fill_value(beta + 1);
+        select(m0, beta);
+        select(m1, beta + 1);
         // 16-byte stores of 4 columns (units start on multiples of 4)
         if ((beta & 3) == 0) {
           v[0] = m0;
@@ -579,11 +610,22 @@ __global__ void __launch_bounds__(Short8::kThreads, 1)
         } else {
           v[2] = m0;
           v[3] = m1;
-          if (row_valid) __stcs(reinterpret_cast<float4*>(orow + (beta - 2)), make_float4(v[0], v[1], v[2], v[3]));
+          if (row_valid && write_out)
+            __stcs(reinterpret_cast<float4*>(orow + (beta - 2)), make_float4(v[0], v[1], v[2], v[3]));
         }
       }
       if (!ok) break;
-      if (row_valid) {
+      if constexpr (TOPK) {
+        // the forced columns past the computed pairs, then this unit's partial list
+        if (live_kv) insert_forced(sel, beta, min(d.c1, p.MB), p.init_blocks, lo, d.sl);
+        const int hl = lane - pos * p.g;
+        if (row_valid && hl == 0 && 2 * d.ch + 1 < p.cand_parts) {
+          sel.store(cand_row(p, d.t0 + pos, d.hk, 2 * d.ch), p.topk_k);
+          uint64_t* empty = cand_row(p, d.t0 + pos, d.hk, 2 * d.ch + 1);
+          for (int i = 0; i < p.topk_k; ++i) empty[i] = 0ull;
+        }
+      }
+      if (row_valid && write_out) {
         if (beta & 3) {   // an open group of 4 (beta is even): close it with fill columns
           v[2] = fill_value(beta);
           v[3] = fill_value(beta + 1);

@@ -99,6 +99,27 @@ struct TileLayout {
 static_assert(TileLayout<false>::bytes <= 232448, "shared memory per CTA");
 static_assert(TileLayout<true>::bytes <= 232448, "shared memory per CTA");
 
+// Every writer of shared memory stays inside its own region, so nothing but
+// mbarrier operations and tcgen05.commit ever touches the barrier words:
+// regions in address order without overlap, 128-byte-swizzled operand tiles
+// on 1 KiB boundaries, and each copy no larger than its destination.
+template <bool KI8>
+constexpr bool tile_layout_ok() {
+  using L = TileLayout<KI8>;
+  using C = TileCfg<KI8>;
+  return L::q_off % 1024 == 0 && L::k_off % 1024 == 0 && L::raw_off % 1024 == 0 &&
+         kRawStride % 1024 == 0 && L::kSlotBytes % 1024 == 0 &&
+         L::q_off + L::kQBufs * kTileBytes <= L::k_off &&                 // Q box: <= 128 rows x 256 B
+         L::k_off + C::kSlots * L::kSlotBytes <= L::raw_off &&            // K slot: 2 pages x 16 KiB
+         L::raw_off + C::kRaw * kRawStride <= L::sc_off &&                // raw page + scales
+         kRawBytes + kRawScaleBytes <= kRawStride &&
+         L::sc_off + C::kScPairs * 256 * 4 <= L::ring_off &&              // [pair][page][token] fp32
+         L::ring_off + kSched * sizeof(UnitDesc) <= L::bar_off &&
+         L::bar_off % 8 == 0 && L::bar_off + L::n_bars * 8 <= L::misc_off &&
+         L::misc_off + 16 + 4 * C::kRaw <= L::end && L::end + 1024 <= L::bytes;
+}
+static_assert(tile_layout_ok<false>() && tile_layout_ok<true>(), "tile kernel shared-memory layout");
+
 // A claim costs an atomic and a chain of dependent L2 round trips (the search
 // over the unit prefix sums, the request record, the first table entries):
 // about 5,000 cycles while HBM is saturated, as long as a few FP8 block pairs
@@ -117,7 +138,12 @@ constexpr uint32_t kCodeLive = 1, kCodeFirst = 2, kCodeLast = 4, kCodeLone = 8, 
 // 1 = FP8 E4M3 query and keys; 2 = FP8 E5M2.  An FP8 row of 128 elements is
 // one 128-byte swizzle row, so a query tile is one box and a pair of pages
 // fills one K slot; four kind::f8f6f4 MMAs (K = 32) cover the head dimension.
-template <bool KI8, bool BF16, int F8 = 0>
+// TOPK: the fused per-group selection.  Each epilogue thread keeps a running
+// top-kTopkMax list of its query position's group score (the max over the
+// position's g head rows, g dividing 32) over the blocks its group drains,
+// and writes it as one partial list per unit; the scores are stored only if
+// p.out is not null.
+template <bool KI8, bool BF16, int F8 = 0, bool TOPK = false>
 __global__ void __launch_bounds__(TileCfg<KI8>::kThreads, 1)
     tile_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const Params p) {
@@ -452,7 +478,9 @@ __global__ void __launch_bounds__(TileCfg<KI8>::kThreads, 1)
     const int rows = p.g * p.np;
     const int pos = r / p.g;
     const int hl = r - pos * p.g;
+    const bool write_out = p.out != nullptr;
     uint32_t ss = 0, sph = 0, ab = 0, aph = 0, sc = 0, scph = 0;
+    TopList sel;
     for (;;) {
       if (!warp_wait(b_sched_full + 8 * ss, sph, ctl)) break;
       const UnitDesc d = ring[ss];
@@ -479,6 +507,14 @@ __global__ void __launch_bounds__(TileCfg<KI8>::kThreads, 1)
       auto forced = [&](int beta) -> bool {
         return live_kv && (beta < p.init_blocks || (beta >= lo && beta <= d.sl));
       };
+      // fused selection: the group score of this position for block col
+      auto select = [&](float m, int col) {
+        if constexpr (TOPK) {
+          const float gm = group_max(valid ? m : ninf, p.g);
+          if (col < p.MB) sel.insert(cand_key(gm, col));
+        }
+      };
+      if constexpr (TOPK) sel.clear();
       bool ok = true;
       int beta = d.c0;
       for (; beta < d.b1; beta += 2) {
@@ -528,14 +564,32 @@ __global__ void __launch_bounds__(TileCfg<KI8>::kThreads, 1)
           // lone last block's partner column is a fill column
           const int col = beta + b;
           if (col >= d.b1 || forced(col)) mb = fill_value(col);
-          if (valid) __stcs(orow + col, mb);
+          if (valid && write_out) __stcs(orow + col, mb);
+          select(mb, col);
           continue;
         }
         const int col = beta + grp;        // this group's block of the pair
         const bool has = col < d.b1;       // else a lone last block's partner (a fill column)
         const bool ld = warp_valid && has;
         float m = ninf;
-        {
+        if constexpr (TOPK) {
+          // two 64-column pieces: the running selection holds the registers
+          // that the other half of a 128-column load would take
+#pragma unroll
+          for (int hf = 0; hf < 2; ++hf) {
+            float x[64];
+            if (ld) {
+              tmem_ld64(t_lane + a * 256u + (uint32_t)grp * 128u + 64u * hf, x);
+              tmem_wait_ld();
+            }
+            if (hf == 1) {
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(b_acc_empty + 8 * a);
+            }
+            if (ld && valid) m = fmaxf(m, masked_max<64>(x, lim - col * kP - 64 * hf));
+          }
+        } else {
           float x[128];
           if (ld) {
             tmem_ld128(t_lane + a * 256u + (uint32_t)grp * 128u, x);
@@ -549,13 +603,23 @@ __global__ void __launch_bounds__(TileCfg<KI8>::kThreads, 1)
         }
         // local mask after the max: forced blocks take their constant
         if (!has || forced(col)) m = fill_value(col);
-        if (valid) __stcs(orow + col, m);
+        if (valid && write_out) __stcs(orow + col, m);
+        select(m, col);
       }
       if (!ok) break;
+      // one partial selection per (unit, epilogue group): part 2 * chunk + group
+      const bool store_sel = valid && hl == 0 && 2 * d.ch + 1 < p.cand_parts;
+      if constexpr (TOPK) {
+        if (grp != 0 && store_sel) sel.store(cand_row(p, d.t0 + pos, d.hk, 2 * d.ch + 1), p.topk_k);
+      }
       // columns past the computed pairs (group 0): pairs up to a multiple of
       // 8, then whole groups of closed-form values
       if (grp != 0) continue;
-      if (valid) {
+      if constexpr (TOPK) {
+        if (live_kv) insert_forced(sel, beta, min(d.c1, p.MB), p.init_blocks, lo, d.sl);
+        if (store_sel) sel.store(cand_row(p, d.t0 + pos, d.hk, 2 * d.ch), p.topk_k);
+      }
+      if (valid && write_out) {
         for (; (beta & 7) && beta < d.c1; beta += 2)
           __stcs(reinterpret_cast<float2*>(orow + beta), make_float2(fill_value(beta), fill_value(beta + 1)));
         for (; beta < d.c1; beta += 8) {
@@ -679,10 +743,10 @@ __global__ void __launch_bounds__(TileCfg<KI8>::kThreads, 1)
 
 // Launch one instantiation: persistent grid of one CTA per SM, programmatic
 // dependent launch after the plan kernel.
-template <bool KI8, bool BF16, int F8>
-inline cudaError_t launch_tile(const void* tq, const void* tk, const Params& p, cudaStream_t s) {
+template <bool KI8, bool BF16, int F8, bool TOPK>
+inline cudaError_t launch_tile_variant(const void* tq, const void* tk, const Params& p, cudaStream_t s) {
   using L = TileLayout<KI8>;
-  auto kern = tile_kernel<KI8, BF16, F8>;
+  auto kern = tile_kernel<KI8, BF16, F8, TOPK>;
   static std::atomic<uint64_t> configured[64];   // per device: context the limit was raised in
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -701,6 +765,13 @@ inline cudaError_t launch_tile(const void* tq, const void* tk, const Params& p, 
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kern, *static_cast<const CUtensorMap*>(tq),
                             *static_cast<const CUtensorMap*>(tk), p);
+}
+
+// The plain scores, or the fused per-group selection when p.topk_k > 0.
+template <bool KI8, bool BF16, int F8>
+inline cudaError_t launch_tile(const void* tq, const void* tk, const Params& p, cudaStream_t s) {
+  return p.topk_k > 0 ? launch_tile_variant<KI8, BF16, F8, true>(tq, tk, p, s)
+                      : launch_tile_variant<KI8, BF16, F8, false>(tq, tk, p, s);
 }
 
 }  // namespace msa

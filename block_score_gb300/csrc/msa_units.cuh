@@ -83,6 +83,7 @@ __device__ __forceinline__ void unit_of_request(const Params& p, const ReqInfo& 
   d.b1 = max(d.c0, min(d.c1, nbc));
   d.kbase = ri.kbase;
   d.sl = ri.sl;
+  d.ch = ch;
   // the first pair's pages, so the producer can start the unit's loads at once
   d.pg0 = d.pg1 = 0;
   if (p.layout != 2 && d.b1 > d.c0) {
@@ -165,6 +166,67 @@ __device__ __forceinline__ float masked_max(const float (&x)[N], int climit) {
     }
   }
   return fmax3(a0, a1, fmaxf(a2, a3));
+}
+
+// ------------------------------------------------ fused per-group selection --
+// A candidate is one (score, block) pair packed into 64 bits so that one
+// unsigned comparison ranks it: the score's order-preserving bits above, the
+// complement of the block index below (a larger score first, then the
+// smaller block).  0 is "no candidate" (-inf, NaN): below every real key.
+__device__ __forceinline__ uint64_t cand_key(float x, int beta) {
+  if (!(x > __int_as_float(0xff800000))) return 0ull;
+  const uint32_t u = __float_as_uint(x);
+  const uint32_t o = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+  return ((uint64_t)o << 32) | (uint64_t)(0xffffffffu - (uint32_t)beta);
+}
+
+__device__ __forceinline__ int cand_block(uint64_t key) {
+  return (int)(0xffffffffu - (uint32_t)(key & 0xffffffffull));
+}
+
+// Running selection of one row: the kTopkMax largest keys seen, descending
+// (unused entries 0).  Insertion into a sorted list, branch-free per entry:
+// new[i] = max(v[i], min(v[i-1], x)).
+struct TopList {
+  uint64_t v[kTopkMax];
+  __device__ __forceinline__ void clear() {
+#pragma unroll
+    for (int i = 0; i < kTopkMax; ++i) v[i] = 0ull;
+  }
+  __device__ __forceinline__ void insert(uint64_t x) {
+    if (x > v[kTopkMax - 1]) {
+#pragma unroll
+      for (int i = kTopkMax - 1; i > 0; --i) v[i] = max(v[i], min(v[i - 1], x));
+      v[0] = max(v[0], x);
+    }
+  }
+  // the first k entries to dst (one partial list)
+  __device__ __forceinline__ void store(uint64_t* dst, int k) const {
+#pragma unroll
+    for (int i = 0; i < kTopkMax; ++i)
+      if (i < k) dst[i] = v[i];
+  }
+};
+
+// Max over the g consecutive lanes that hold the g heads of one query
+// position (g divides 32, so the lanes of a position form an aligned group).
+__device__ __forceinline__ float group_max(float m, int g) {
+  for (int o = 1; o < g; o <<= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  return m;
+}
+
+// The forced columns of the local mask within [c_lo, c_hi) (a request with
+// kv_len > 0): init blocks take 1e30, the window [lo, sl] 1e29 (it wins).
+__device__ __forceinline__ void insert_forced(TopList& sel, int c_lo, int c_hi, int init_blocks,
+                                              int lo, int sl) {
+  for (int c = c_lo; c < min(c_hi, init_blocks); ++c)
+    if (!(c >= lo && c <= sl)) sel.insert(cand_key(1e30f, c));
+  for (int c = max(c_lo, lo); c < min(c_hi, sl + 1); ++c) sel.insert(cand_key(1e29f, c));
+}
+
+// Partial list `part` of row (token t, group hk).
+__device__ __forceinline__ uint64_t* cand_row(const Params& p, int64_t t, int hk, int part) {
+  return p.cand + ((t * p.H_kv + hk) * (int64_t)p.cand_parts + part) * (int64_t)p.topk_k;
 }
 
 }  // namespace msa

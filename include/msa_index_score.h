@@ -227,6 +227,45 @@ msa_status_t msa_noalloc_device_error(int32_t *bits, msa_stream_t stream);
 msa_status_t msa_block_topk(const float *score, int32_t H, int64_t T, int32_t MBp, int32_t MB,
                             int32_t k, int32_t *out, msa_stream_t stream);
 
+/*
+ * Block scores with the per-GQA-group block selection fused into the score
+ * kernels (MiniMax Sparse Attention notes, section 4.3 Equation (3): the
+ * heads of a GQA group share one index set; section 4.7 Equation (7) and the
+ * selector contract: top-k blocks, indices ascending, -1 tail; section 10,
+ * checklist items 7-9).  The scores are computed exactly as by
+ * msa_index_score; the selection never reads them back from memory.
+ *
+ *   k           blocks per selection, 1 <= k <= 16 (the pages' selector fixes 16).
+ *   local_slot  nonzero: each query token's own block -- the block holding its
+ *               position kv_len - Lq + i under the rightDownCausal alignment,
+ *               when 0 <= that position < kv_len -- always takes one of the k
+ *               slots; the other k - 1 go to the best remaining blocks.  Zero:
+ *               the plain top-k of the group score.
+ *   out         device fp32 [H_q, T, RoundUp(MB, 16)] for the scores, or NULL
+ *               to compute the selection without storing the scores.
+ *   indices     device int32 [T, H_kv, k], written completely: for token t
+ *               and group r (the query heads r*g .. r*g+g-1, g = H_q / H_kv),
+ *               the selected blocks in ascending order, then -1.
+ *   workspace   device memory of msa_index_score_topk_workspace_size() bytes
+ *               (256-byte aligned, caller-owned, need not be initialised): the
+ *               plan and each row's partial selections (at most 64 MiB of them).
+ *
+ * The group score of block beta is the maximum over the group's g index heads
+ * of score[h, t, beta]; a block is a candidate when beta < MB and that score
+ * is above -inf.  Equal group scores rank the smaller block first.  Forced
+ * blocks of the local mask (1e30 / 1e29) outrank every dot product.
+ *
+ * Errors: as msa_index_score, plus MSA_ERR_INVALID_ARG for k outside [1, 16]
+ * or a NULL `indices`, and MSA_ERR_UNSUPPORTED when g = H_q / H_kv does not
+ * divide 32 (the heads of a position are combined inside one warp).
+ * Asynchronous on `stream`; T == 0 or B == 0 enqueues nothing.
+ */
+msa_status_t msa_index_score_topk_workspace_size(const msa_index_score_args *args, int32_t k,
+                                                 size_t *bytes);
+msa_status_t msa_index_score_topk(const msa_index_score_args *args, int32_t k, int32_t local_slot,
+                                  float *out, int32_t *indices, void *workspace,
+                                  size_t workspace_bytes, msa_stream_t stream);
+
 /* Synchronise `stream` and read the device error word left in `workspace`
  * by the last call (MSA_DEVERR_* bits; 0 = clean).  Returns MSA_OK, or
  * MSA_ERR_CUDA if the copy fails. */
