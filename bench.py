@@ -509,8 +509,9 @@ def run_ours(args):
     # call, D2H of the scores, every step
     e2e = e2e_run(case, device, stream, args, steps=min(steps, 5 if case.T * case.H_q > 1e6 else 20))
     # the block top-k selection over this call's scores (the scores' consumer;
-    # not part of the metric above)
+    # not part of the metric above), and the fused per-group selection
     topk = topk_run(prep.out, case.MB, 16, device, stream, peaks, min(steps * 5, 200))
+    fused = fused_select_run(case, prep, device, stream, min(steps, 30), head, topk)
     del prep
     torch.cuda.empty_cache()
 
@@ -526,6 +527,7 @@ def run_ours(args):
         "roofline": head["roofline"],
         "e2e": e2e,
         "topk": topk,
+        "fused_select": fused,
         "gpu_launches": head["gpu_launches"],
         "clocks": head["clocks"],
     }
@@ -544,6 +546,8 @@ def run_ours(args):
             skey = workload_key(sa)
             rec, sprep = measure(scase, skey, default_steps(sa), args.warmup, device, stream,
                                  peaks, ws, recorded_traffic(skey, dominant_kernel(scase)))
+            rec["topk"] = topk_run(sprep.out, scase.MB, 16, device, stream, peaks, 200)
+            rec["fused_select"] = fused_select_run(scase, sprep, device, stream, 30, rec, rec["topk"])
             del sprep
             rec["e2e"] = e2e_run(scase, device, stream, args, steps=20)
             if rank == 0 and ws == 1 and not args.no_cpu_baseline:
@@ -559,6 +563,35 @@ def run_ours(args):
         import torch.distributed as dist
         dist.destroy_process_group()
     return 0
+
+
+def fused_select_run(case, prep, device, stream, steps, head, topk):
+    """The fused per-group selection (msa_index_score_topk, k = 16, own-block
+    slot on), with and without storing the scores: microseconds per call of
+    the whole op, against one score call plus the unfused top-k over its
+    scores."""
+    if 32 % (case.H_q // case.H_kv):
+        return None
+    res = {"k": 16, "local_slot": True, "groups": case.H_kv,
+           "rows": case.T * case.H_kv, "unfused_us": head["value"] + topk["us_per_call"]}
+    ws = torch.empty(prep.select_workspace_bytes(16), dtype=torch.uint8, device=device)
+    idx = torch.empty((case.T, case.H_kv, 16), dtype=torch.int32, device=device)
+    for scores in (True, False):
+        for _ in range(3):
+            prep.topk(16, True, scores, idx, ws, stream)
+        torch.cuda.synchronize(device)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            prep.topk(16, True, scores, idx, ws, stream)
+        e1.record(stream)
+        torch.cuda.synchronize(device)
+        res["with_scores_us" if scores else "without_scores_us"] = e0.elapsed_time(e1) / steps * 1e3
+    if prep.select_device_error(stream):
+        raise RuntimeError("device error in the fused selection")
+    res["workspace_bytes"] = ws.numel()
+    res["launches_per_call"] = launches_per_call(case) + 1
+    return res
 
 
 def topk_run(score, MB: int, k: int, device, stream, peaks, steps: int):

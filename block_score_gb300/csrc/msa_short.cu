@@ -3,7 +3,7 @@
 
 namespace msa {
 
-template <bool TOPK>
+template <int TOPK>
 cudaError_t launch_short_variant(const void* tq, const void* tk, const Params& p, cudaStream_t s) {
   auto kern = short_kernel<false, TOPK>;
   static std::atomic<uint64_t> configured[64];   // per device: context the limit was raised in
@@ -28,8 +28,8 @@ cudaError_t launch_short_variant(const void* tq, const void* tk, const Params& p
 
 // The plain scores, or the fused per-group selection when p.topk_k > 0.
 cudaError_t launch_short_i8(const void* tq, const void* tk, const Params& p, cudaStream_t s) {
-  return p.topk_k > 0 ? launch_short_variant<true>(tq, tk, p, s)
-                      : launch_short_variant<false>(tq, tk, p, s);
+  if (p.topk_k <= 0) return launch_short_variant<0>(tq, tk, p, s);
+  return p.g >= 8 ? launch_short_variant<2>(tq, tk, p, s) : launch_short_variant<16>(tq, tk, p, s);
 }
 
 }  // namespace msa

@@ -38,6 +38,7 @@
 //   warp 12       MMA helper: waits for each item's operands
 #pragma once
 #include <cstdint>
+#include <type_traits>
 #include <cuda.h>
 #include <cuda_fp16.h>
 
@@ -125,12 +126,14 @@ __device__ __forceinline__ float warp_transpose_max32(float (&v)[32], int lane) 
   return v[0];
 }
 
-// TOPK: the fused per-group selection.  The combine warp keeps, per query
-// position, a running top-kTopkMax list of the group score (the max over the
-// position's g head lanes, g dividing 32) over every block of a unit and
-// writes it as the unit's partial list (part 2 * chunk; part 2 * chunk + 1 is
-// written empty); the scores are stored only if p.out is not null.
-template <bool BF16, bool TOPK = false>
+// TOPK: the fused per-group selection (0 = off).  The combine warp keeps,
+// per query position, a running top-kTopkMax list of the group score (the max
+// over the position's g head lanes, g dividing 32) over every block of a unit
+// and writes it as the unit's partial list (part 2 * chunk; part 2 * chunk + 1
+// is written empty); the scores are stored only if p.out is not null.
+// TOPK = 2: the list is spread over 8 lanes of the position (g >= 8);
+// TOPK = 16: every lane of the position holds the whole list.
+template <bool BF16, int TOPK = 0>
 __global__ void __launch_bounds__(Short8::kThreads, 1)
     short_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                  const Params p) {
@@ -556,7 +559,8 @@ __global__ void __launch_bounds__(Short8::kThreads, 1)
     const float ninf = __int_as_float(0xff800000);
     const bool write_out = p.out != nullptr;
     uint32_t ss = 0, sph = 0, rr = 0, rph = 0;
-    TopList sel;
+    using Sel = std::conditional_t<TOPK == 2, TopList2, TopList>;
+    Sel sel;
     for (;;) {
       if (!warp_wait(b_sched_full + 8 * ss, sph, ctl)) break;
       const UnitDesc d = ring[ss];
@@ -566,12 +570,10 @@ __global__ void __launch_bounds__(Short8::kThreads, 1)
       if (!d.live) break;
       const int rows = d.Lq * p.g;                        // valid query rows (<= 32)
       const bool row_valid = lane < rows;
-      if constexpr (TOPK) sel.clear();
+      if constexpr (TOPK != 0) sel.clear();
+      const int hl = lane - (lane / p.g) * p.g;
       auto select = [&](float m, int col) {
-        if constexpr (TOPK) {
-          const float gm = group_max(row_valid ? m : ninf, p.g);
-          if (col < p.MB) sel.insert(cand_key(gm, col));
-        }
+        if constexpr (TOPK != 0) select_block(sel, m, row_valid, col, p.MB, hl, p.g);
       };
       const int pos = lane / p.g;
       const int h = d.hk * p.g + (lane - pos * p.g);
@@ -615,14 +617,15 @@ __global__ void __launch_bounds__(Short8::kThreads, 1)
         }
       }
       if (!ok) break;
-      if constexpr (TOPK) {
-        // the forced columns past the computed pairs, then this unit's partial list
-        if (live_kv) insert_forced(sel, beta, min(d.c1, p.MB), p.init_blocks, lo, d.sl);
-        const int hl = lane - pos * p.g;
-        if (row_valid && hl == 0 && 2 * d.ch + 1 < p.cand_parts) {
-          sel.store(cand_row(p, d.t0 + pos, d.hk, 2 * d.ch), p.topk_k);
-          uint64_t* empty = cand_row(p, d.t0 + pos, d.hk, 2 * d.ch + 1);
-          for (int i = 0; i < p.topk_k; ++i) empty[i] = 0ull;
+      if constexpr (TOPK != 0) {
+        // the forced columns past the computed pairs, then this unit's partial
+        // list (and an empty second list: every unit owns two parts)
+        if (live_kv) insert_forced(sel, beta, min(d.c1, p.MB), p.init_blocks, lo, d.sl, hl, p.g);
+        if (row_valid && 2 * d.ch + 1 < p.cand_parts) {
+          sel.store(cand_row(p, d.t0 + pos, d.hk, 2 * d.ch), p.topk_k, hl);
+          Sel none;
+          none.clear();
+          none.store(cand_row(p, d.t0 + pos, d.hk, 2 * d.ch + 1), p.topk_k, hl);
         }
       }
       if (row_valid && write_out) {

@@ -41,6 +41,7 @@
 // TMEM: two 256-column accumulators.
 #pragma once
 #include <cstdint>
+#include <type_traits>
 #include <cuda.h>
 #include <cuda_fp16.h>
 
@@ -138,12 +139,15 @@ constexpr uint32_t kCodeLive = 1, kCodeFirst = 2, kCodeLast = 4, kCodeLone = 8, 
 // 1 = FP8 E4M3 query and keys; 2 = FP8 E5M2.  An FP8 row of 128 elements is
 // one 128-byte swizzle row, so a query tile is one box and a pair of pages
 // fills one K slot; four kind::f8f6f4 MMAs (K = 32) cover the head dimension.
-// TOPK: the fused per-group selection.  Each epilogue thread keeps a running
-// top-kTopkMax list of its query position's group score (the max over the
-// position's g head rows, g dividing 32) over the blocks its group drains,
+// TOPK: the fused per-group selection (0 = off).  The epilogue keeps a
+// running top-kTopkMax list of each query position's group score (the max over
+// the position's g head rows, g dividing 32) over the blocks its group drains,
 // and writes it as one partial list per unit; the scores are stored only if
-// p.out is not null.
-template <bool KI8, bool BF16, int F8 = 0, bool TOPK = false>
+// p.out is not null.  TOPK = 2: the list is spread over 8 lanes of the
+// position (g >= 8), so the 128-column TMEM load of a block still fits the
+// registers; TOPK = 16: every lane holds the whole list (g < 8) and a block is
+// loaded in two 64-column pieces.
+template <bool KI8, bool BF16, int F8 = 0, int TOPK = 0>
 __global__ void __launch_bounds__(TileCfg<KI8>::kThreads, 1)
     tile_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const Params p) {
@@ -480,7 +484,8 @@ __global__ void __launch_bounds__(TileCfg<KI8>::kThreads, 1)
     const int hl = r - pos * p.g;
     const bool write_out = p.out != nullptr;
     uint32_t ss = 0, sph = 0, ab = 0, aph = 0, sc = 0, scph = 0;
-    TopList sel;
+    using Sel = std::conditional_t<TOPK == 2, TopList2, TopList>;
+    Sel sel;
     for (;;) {
       if (!warp_wait(b_sched_full + 8 * ss, sph, ctl)) break;
       const UnitDesc d = ring[ss];
@@ -509,12 +514,9 @@ __global__ void __launch_bounds__(TileCfg<KI8>::kThreads, 1)
       };
       // fused selection: the group score of this position for block col
       auto select = [&](float m, int col) {
-        if constexpr (TOPK) {
-          const float gm = group_max(valid ? m : ninf, p.g);
-          if (col < p.MB) sel.insert(cand_key(gm, col));
-        }
+        if constexpr (TOPK != 0) select_block(sel, m, valid, col, p.MB, hl, p.g);
       };
-      if constexpr (TOPK) sel.clear();
+      if constexpr (TOPK != 0) sel.clear();
       bool ok = true;
       int beta = d.c0;
       for (; beta < d.b1; beta += 2) {
@@ -572,7 +574,7 @@ __global__ void __launch_bounds__(TileCfg<KI8>::kThreads, 1)
         const bool has = col < d.b1;       // else a lone last block's partner (a fill column)
         const bool ld = warp_valid && has;
         float m = ninf;
-        if constexpr (TOPK) {
+        if constexpr (TOPK == 16) {
           // two 64-column pieces: the running selection holds the registers
           // that the other half of a 128-column load would take
 #pragma unroll
@@ -608,16 +610,16 @@ __global__ void __launch_bounds__(TileCfg<KI8>::kThreads, 1)
       }
       if (!ok) break;
       // one partial selection per (unit, epilogue group): part 2 * chunk + group
-      const bool store_sel = valid && hl == 0 && 2 * d.ch + 1 < p.cand_parts;
-      if constexpr (TOPK) {
-        if (grp != 0 && store_sel) sel.store(cand_row(p, d.t0 + pos, d.hk, 2 * d.ch + 1), p.topk_k);
+      const bool store_sel = valid && 2 * d.ch + 1 < p.cand_parts;
+      if constexpr (TOPK != 0) {
+        if (grp != 0 && store_sel) sel.store(cand_row(p, d.t0 + pos, d.hk, 2 * d.ch + 1), p.topk_k, hl);
       }
       // columns past the computed pairs (group 0): pairs up to a multiple of
       // 8, then whole groups of closed-form values
       if (grp != 0) continue;
-      if constexpr (TOPK) {
-        if (live_kv) insert_forced(sel, beta, min(d.c1, p.MB), p.init_blocks, lo, d.sl);
-        if (store_sel) sel.store(cand_row(p, d.t0 + pos, d.hk, 2 * d.ch), p.topk_k);
+      if constexpr (TOPK != 0) {
+        if (live_kv) insert_forced(sel, beta, min(d.c1, p.MB), p.init_blocks, lo, d.sl, hl, p.g);
+        if (store_sel) sel.store(cand_row(p, d.t0 + pos, d.hk, 2 * d.ch), p.topk_k, hl);
       }
       if (valid && write_out) {
         for (; (beta & 7) && beta < d.c1; beta += 2)
@@ -743,7 +745,7 @@ __global__ void __launch_bounds__(TileCfg<KI8>::kThreads, 1)
 
 // Launch one instantiation: persistent grid of one CTA per SM, programmatic
 // dependent launch after the plan kernel.
-template <bool KI8, bool BF16, int F8, bool TOPK>
+template <bool KI8, bool BF16, int F8, int TOPK>
 inline cudaError_t launch_tile_variant(const void* tq, const void* tk, const Params& p, cudaStream_t s) {
   using L = TileLayout<KI8>;
   auto kern = tile_kernel<KI8, BF16, F8, TOPK>;
@@ -770,8 +772,9 @@ inline cudaError_t launch_tile_variant(const void* tq, const void* tk, const Par
 // The plain scores, or the fused per-group selection when p.topk_k > 0.
 template <bool KI8, bool BF16, int F8>
 inline cudaError_t launch_tile(const void* tq, const void* tk, const Params& p, cudaStream_t s) {
-  return p.topk_k > 0 ? launch_tile_variant<KI8, BF16, F8, true>(tq, tk, p, s)
-                      : launch_tile_variant<KI8, BF16, F8, false>(tq, tk, p, s);
+  if (p.topk_k <= 0) return launch_tile_variant<KI8, BF16, F8, 0>(tq, tk, p, s);
+  return p.g >= 8 ? launch_tile_variant<KI8, BF16, F8, 2>(tq, tk, p, s)
+                  : launch_tile_variant<KI8, BF16, F8, 16>(tq, tk, p, s);
 }
 
 }  // namespace msa

@@ -184,8 +184,11 @@ __device__ __forceinline__ int cand_block(uint64_t key) {
   return (int)(0xffffffffu - (uint32_t)(key & 0xffffffffull));
 }
 
-// Running selection of one row: the kTopkMax largest keys seen, descending
-// (unused entries 0).  Insertion into a sorted list, branch-free per entry:
+// Running selection of one query position's group score: the kTopkMax
+// largest keys seen, in descending order (unused entries 0).
+//
+// TopList keeps the whole list in every lane of the position (32 registers;
+// any g).  Insertion into a sorted list, branch-free per entry:
 // new[i] = max(v[i], min(v[i-1], x)).
 struct TopList {
   uint64_t v[kTopkMax];
@@ -193,18 +196,45 @@ struct TopList {
 #pragma unroll
     for (int i = 0; i < kTopkMax; ++i) v[i] = 0ull;
   }
-  __device__ __forceinline__ void insert(uint64_t x) {
+  // the list's smallest entry: a key at or below it changes nothing
+  __device__ __forceinline__ uint64_t threshold() const { return v[kTopkMax - 1]; }
+  // x: the position's key (the same in all its lanes); whole warp
+  __device__ __forceinline__ void insert(uint64_t x, int /*hl*/, int /*g*/) {
     if (x > v[kTopkMax - 1]) {
 #pragma unroll
       for (int i = kTopkMax - 1; i > 0; --i) v[i] = max(v[i], min(v[i - 1], x));
       v[0] = max(v[0], x);
     }
   }
-  // the first k entries to dst (one partial list)
-  __device__ __forceinline__ void store(uint64_t* dst, int k) const {
+  __device__ __forceinline__ void store(uint64_t* dst, int k, int hl) const {
+    if (hl != 0) return;
 #pragma unroll
     for (int i = 0; i < kTopkMax; ++i)
       if (i < k) dst[i] = v[i];
+  }
+};
+
+// TopList2 spreads the list over the first 8 lanes of a position with g >= 8
+// head lanes: lane j (0 <= j < 8) holds entries 2j and 2j+1, so a thread
+// spends 6 registers on it.  The same per-entry rule; entry 2j-1 comes from
+// the lane before.  Lanes j >= 8 (g = 16, 32) carry values nobody reads.
+struct TopList2 {
+  uint64_t a, b;      // entries 2j, 2j+1
+  uint64_t thr;       // entry 15, the same in every lane of the position
+  __device__ __forceinline__ void clear() { a = b = thr = 0ull; }
+  __device__ __forceinline__ uint64_t threshold() const { return thr; }
+  __device__ __forceinline__ void insert(uint64_t x, int hl, int g) {
+    uint64_t up = __shfl_up_sync(0xffffffffu, b, 1, g);
+    if (hl == 0) up = ~0ull;
+    const uint64_t nb = max(b, min(a, x));
+    a = max(a, min(up, x));
+    b = nb;
+    thr = __shfl_sync(0xffffffffu, b, 7, g);
+  }
+  __device__ __forceinline__ void store(uint64_t* dst, int k, int hl) const {
+    if (hl >= kTopkMax / 2) return;
+    if (2 * hl < k) dst[2 * hl] = a;
+    if (2 * hl + 1 < k) dst[2 * hl + 1] = b;
   }
 };
 
@@ -215,13 +245,28 @@ __device__ __forceinline__ float group_max(float m, int g) {
   return m;
 }
 
+// One block of a position: `m` is this lane's row score of block col.  A
+// warp vote first: when no lane's own score beats its list's threshold, no
+// group score can, and the shuffles and the insertion are skipped.  Whole warp.
+template <class Sel>
+__device__ __forceinline__ void select_block(Sel& sel, float m, bool row_valid, int col, int MB,
+                                             int hl, int g) {
+  const uint64_t own = (row_valid && col < MB) ? cand_key(m, col) : 0ull;
+  if (__any_sync(0xffffffffu, own > sel.threshold())) {
+    const float gm = group_max(row_valid ? m : __int_as_float(0xff800000), g);
+    sel.insert(col < MB ? cand_key(gm, col) : 0ull, hl, g);
+  }
+}
+
 // The forced columns of the local mask within [c_lo, c_hi) (a request with
 // kv_len > 0): init blocks take 1e30, the window [lo, sl] 1e29 (it wins).
-__device__ __forceinline__ void insert_forced(TopList& sel, int c_lo, int c_hi, int init_blocks,
-                                              int lo, int sl) {
+// Whole warp (the ranges are the same in every lane).
+template <class Sel>
+__device__ __forceinline__ void insert_forced(Sel& sel, int c_lo, int c_hi, int init_blocks,
+                                              int lo, int sl, int hl, int g) {
   for (int c = c_lo; c < min(c_hi, init_blocks); ++c)
-    if (!(c >= lo && c <= sl)) sel.insert(cand_key(1e30f, c));
-  for (int c = max(c_lo, lo); c < min(c_hi, sl + 1); ++c) sel.insert(cand_key(1e29f, c));
+    if (!(c >= lo && c <= sl)) sel.insert(cand_key(1e30f, c), hl, g);
+  for (int c = max(c_lo, lo); c < min(c_hi, sl + 1); ++c) sel.insert(cand_key(1e29f, c), hl, g);
 }
 
 // Partial list `part` of row (token t, group hk).
