@@ -54,7 +54,11 @@ class _Args(ctypes.Structure):
         ("start_loc", ctypes.c_void_p), ("scale", ctypes.c_void_p),
         ("sparse_mode", ctypes.c_int32), ("init_blocks", ctypes.c_int32),
         ("local_blocks", ctypes.c_int32), ("fill_value", ctypes.c_float),
+        ("q_scale", ctypes.c_void_p), ("k_scale", ctypes.c_void_p),
+        ("fp4_format", ctypes.c_int32),
     ]
+
+_FP4_FORMAT = {"mx": 0, "nv": 1}
 
 
 def build(force: bool = False) -> str:
@@ -111,13 +115,14 @@ def _make_args(case, fill_value: float, keep: list) -> _Args:
         page_stride = int(k.stride(0))
     keep += [q, k]
     a = _Args()
+    fp4 = getattr(case, "fp4", None)
     a.query = q.data_ptr()
-    a.q_dtype = _DT[q.dtype]
+    a.q_dtype = 5 if fp4 else _DT[q.dtype]
     a.T = int(q.shape[0])
     a.H_q = int(q.shape[1])
-    a.D = int(q.shape[2])
+    a.D = int(q.shape[2]) * (2 if fp4 else 1)      # FP4: two elements per byte
     a.key = k.data_ptr()
-    a.k_dtype = _DT[k.dtype]
+    a.k_dtype = 5 if fp4 else _DT[k.dtype]
     a.layout = _LAYOUT[layout]
     a.NP = int(k.shape[0])
     if layout == "BBND":
@@ -147,6 +152,10 @@ def _make_args(case, fill_value: float, keep: list) -> _Args:
     a.init_blocks = int(case.init_blocks)
     a.local_blocks = int(case.local_blocks)
     a.fill_value = float(fill_value)
+    if fp4:
+        a.q_scale = ptr(case.q_scale, torch.uint8)
+        a.k_scale = ptr(case.k_scale, torch.uint8)
+        a.fp4_format = _FP4_FORMAT[fp4]
     return a
 
 
@@ -181,9 +190,11 @@ def oracle_rows(case, rows: Sequence[int], nthreads: int = 0,
     return out
 
 
-def decode(dtype: torch.dtype, bits: int) -> float:
-    """The oracle's decoding of one element bit pattern of ``dtype``."""
-    return float(_load().msa_oracle_decode(_DT[dtype], bits))
+def decode(dtype, bits: int) -> float:
+    """The oracle's decoding of one element bit pattern of ``dtype`` (a torch
+    dtype, or "e2m1" for an FP4 code / "e8m0" for an MX scale byte)."""
+    code = {"e2m1": 5, "e8m0": 6}.get(dtype) if isinstance(dtype, str) else _DT[dtype]
+    return float(_load().msa_oracle_decode(code, bits))
 
 
 def oracle_threads(nthreads: int = 0) -> int:

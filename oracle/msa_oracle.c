@@ -35,9 +35,16 @@
  *
  * Element types: 0 = fp16, 1 = bf16, 2 = int8 (keys only), 3 = fp8 e4m3fn,
  * 4 = fp8 e5m2 (query and key of the same FP8 type, no scale: torch API guide,
- * sec. 4 and 7.2).  The FP8 decodings follow the OCP 8-bit floating point
- * formats (E4M3: bias 7, no infinities, S.1111.111 is NaN; E5M2: bias 15,
- * IEEE-style infinities and NaNs).
+ * sec. 4 and 7.2), 5 = FP4 E2M1 with group scales, query and key alike (the
+ * block-scaled FP4 indexer of the MiniMax Sparse Attention notes, sec. 8.2:
+ * MXFP4 = E2M1 values with one E8M0 scale per 32 elements, NVFP4 = E2M1
+ * values with one E4M3 scale per 16 elements).  The FP8 decodings follow the
+ * OCP 8-bit floating point formats (E4M3: bias 7, no infinities, S.1111.111 is
+ * NaN; E5M2: bias 15, IEEE-style infinities and NaNs); E2M1 and E8M0 follow
+ * the OCP Microscaling (MX) formats (E2M1: bias 1, no infinities or NaN;
+ * E8M0: 2^(e - 127), 0xFF is NaN).  An FP4 row of D elements is D/2 bytes,
+ * element 2i in the low nibble of byte i; each element is dequantised as
+ * value * scale of its group before the dot product, all in fp64 (exact).
  * Layouts: 0 = BBND [NP,P,H_kv,D], 1 = BNBD [NP,H_kv,P,D], 2 = TND [T2,H_kv,D].
  */
 #include <math.h>
@@ -68,6 +75,11 @@ typedef struct {
     const float *scale;         /* int8: paged [NP, H_kv, P]; TND [T2, H_kv] */
     int32_t sparse_mode, init_blocks, local_blocks;
     float fill_value;
+    /* FP4 (type 5) group scales, one byte per group of G elements:
+     * query [T, H_q, D/G]; key paged [NP, H_kv, P, D/G], TND [T2, H_kv, D/G] */
+    const uint8_t *q_scale;
+    const uint8_t *k_scale;
+    int32_t fp4_format;         /* 0: MXFP4 (E8M0, G = 32); 1: NVFP4 (E4M3, G = 16) */
 } msa_oracle_args;
 
 /* IEEE binary16 -> double, from the format's definition (1/5/10 bits). */
@@ -121,6 +133,33 @@ static double e5m2_to_double(uint8_t b)
     return s ? -v : v;
 }
 
+/* FP4 E2M1 -> double: 1/2/1 bits, bias 1, no infinities or NaN. */
+static double e2m1_to_double(uint8_t c)
+{
+    int s = (c >> 3) & 1, e = (c >> 1) & 3, m = c & 1;
+    double v = e == 0 ? ldexp((double)m, -1)           /* subnormal: (m/2) * 2^0 */
+                      : ldexp((double)(m + 2), e - 2); /* (1 + m/2) * 2^(e-1) */
+    return s ? -v : v;
+}
+
+/* E8M0 scale -> double: 2^(e - 127); 0xFF is NaN. */
+static double e8m0_to_double(uint8_t b)
+{
+    return b == 0xFF ? NAN : ldexp(1.0, (int)b - 127);
+}
+
+/* Element d of an FP4 row that starts at byte `row`, dequantised by the
+ * scale of its group (scales of the row start at `srow`). */
+static double fp4_elem(const uint8_t *base, int64_t row, const uint8_t *scales, int64_t srow,
+                       int d, int32_t fmt)
+{
+    const uint8_t byte = base[row + d / 2];
+    const double v = e2m1_to_double((uint8_t)((d & 1) ? (byte >> 4) : (byte & 15)));
+    const int G = fmt ? 16 : 32;
+    const uint8_t sb = scales[srow + d / G];
+    return v * (fmt ? e4m3_to_double(sb) : e8m0_to_double(sb));
+}
+
 static double load_elem(const void *base, int32_t dtype, int64_t idx)
 {
     if (dtype == 2)
@@ -142,17 +181,25 @@ static int request_of(const msa_oracle_args *a, int64_t t)
     return -1;
 }
 
-/* Element offset of key row j (logical position in request b), head hk.
- * Returns -1 if the row cannot be addressed (bad table entry). */
+/* Storage elements of one row of D values: D, or D/2 bytes for FP4. */
+static int64_t row_units(const msa_oracle_args *a)
+{
+    return a->k_dtype == 5 ? a->D / 2 : a->D;
+}
+
+/* Storage offset of key row j (logical position in request b), head hk; the
+ * row's scale index (int8: one per row; FP4: the row's first group scale is
+ * scale_idx * D/G).  Returns -1 if the row cannot be addressed (bad table entry). */
 static int64_t key_offset(const msa_oracle_args *a, int b, int64_t j, int hk,
                           int64_t *scale_idx)
 {
+    const int64_t ru = row_units(a);
     if (a->layout == 2) {                                   /* TND */
         int64_t row = (int64_t)a->cu_k[b] + j;
         if (row < 0 || row >= a->NP)
             return -1;
         *scale_idx = row * a->H_kv + hk;
-        return (row * a->H_kv + hk) * (int64_t)a->D;
+        return (row * a->H_kv + hk) * ru;
     }
     int64_t beta = j / a->P, off = j % a->P;
     int64_t page = a->block_table[(int64_t)b * a->MB + beta];
@@ -160,8 +207,8 @@ static int64_t key_offset(const msa_oracle_args *a, int b, int64_t j, int hk,
         return -1;
     *scale_idx = (page * a->H_kv + hk) * (int64_t)a->P + off;
     if (a->layout == 0)                                      /* BBND */
-        return page * a->page_stride + (off * a->H_kv + hk) * (int64_t)a->D;
-    return page * a->page_stride + ((int64_t)hk * a->P + off) * (int64_t)a->D;  /* BNBD */
+        return page * a->page_stride + (off * a->H_kv + hk) * ru;
+    return page * a->page_stride + ((int64_t)hk * a->P + off) * ru;  /* BNBD */
 }
 
 /* One output row (h, t): MBp values. Returns 0, or 1 if a needed key row could
@@ -182,7 +229,8 @@ static int oracle_row(const msa_oracle_args *a, int h, int64_t t, float *dst)
                                      : (int64_t)a->kv_len[b];
     const int64_t i = t - a->cu_q[b];
     const int64_t qpos = a->sparse_mode == 3 ? L - Lq + i : INT64_MAX;
-    const int64_t qrow = (t * a->H_q + h) * (int64_t)a->D;
+    const int64_t qrow = (t * a->H_q + h) * row_units(a);
+    const int64_t ng = a->fp4_format ? a->D / 16 : a->D / 32;   /* FP4 groups per row */
 
     for (int64_t beta = 0; beta < a->MB; ++beta) {
         double best = 0.0;
@@ -197,9 +245,17 @@ static int oracle_row(const msa_oracle_args *a, int h, int64_t t, float *dst)
                 continue;
             }
             double s = 0.0;                                  /* DOT */
-            for (int d = 0; d < a->D; ++d)
-                s += load_elem(a->query, a->q_dtype, qrow + d) *
-                     load_elem(a->key, a->k_dtype, koff + d);
+            if (a->k_dtype == 5) {                           /* FP4: dequantised values */
+                for (int d = 0; d < a->D; ++d)
+                    s += fp4_elem((const uint8_t *)a->query, qrow, a->q_scale,
+                                  (t * a->H_q + h) * ng, d, a->fp4_format) *
+                         fp4_elem((const uint8_t *)a->key, koff, a->k_scale, sidx * ng, d,
+                                  a->fp4_format);
+            } else {
+                for (int d = 0; d < a->D; ++d)
+                    s += load_elem(a->query, a->q_dtype, qrow + d) *
+                         load_elem(a->key, a->k_dtype, koff + d);
+            }
             if (a->k_dtype == 2)
                 s *= (double)a->scale[sidx];                 /* DEQUANT (column scale) */
             if (!any || s > best)                            /* MAX */
@@ -281,11 +337,14 @@ int msa_oracle_threads(int nthreads)
 #endif
 }
 
-/* Decode one element of the given type (for tests of the decoders). */
+/* Decode one element of the given type (for tests of the decoders); 5 is an
+ * E2M1 code (low nibble), 6 an E8M0 scale byte. */
 double msa_oracle_decode(int32_t dtype, uint32_t bits)
 {
     if (dtype == 2) return (double)(int8_t)(uint8_t)bits;
     if (dtype == 3) return e4m3_to_double((uint8_t)bits);
     if (dtype == 4) return e5m2_to_double((uint8_t)bits);
+    if (dtype == 5) return e2m1_to_double((uint8_t)(bits & 15));
+    if (dtype == 6) return e8m0_to_double((uint8_t)bits);
     return dtype == 1 ? bf16_to_double((uint16_t)bits) : half_to_double((uint16_t)bits);
 }

@@ -32,11 +32,11 @@ from typing import List, Optional, Sequence
 import torch
 
 __all__ = [
-    "MsaCase", "make_case", "config", "CONFIG_NAMES", "FILL_KINDS",
+    "MsaCase", "make_case", "make_fp4_case", "config", "CONFIG_NAMES", "FILL_KINDS",
 ]
 
 FILL_KINDS = ("randn", "randn01", "int_small", "int8_full", "onehot_d0",
-              "abs_randn")
+              "abs_randn", "bytes")
 
 
 @dataclasses.dataclass
@@ -60,6 +60,11 @@ class MsaCase:
     # bookkeeping of what was drawn (host ints, for reports and sampling)
     q_lens: List[int] = dataclasses.field(default_factory=list)
     kv_lens: List[int] = dataclasses.field(default_factory=list)
+    # FP4 inputs ("mx" / "nv"): query and key hold packed E2M1 codes (two per
+    # byte, element 2i in the low nibble), with one scale byte per group
+    fp4: Optional[str] = None
+    q_scale: Optional[torch.Tensor] = None     # [T, H_q, D/G] uint8
+    k_scale: Optional[torch.Tensor] = None     # paged [NP, H_kv, P, D/G]; TND [T2, H_kv, D/G]
 
     @property
     def T(self) -> int:
@@ -71,7 +76,7 @@ class MsaCase:
 
     @property
     def D(self) -> int:
-        return int(self.query.shape[2])
+        return int(self.query.shape[2]) * (2 if self.fp4 else 1)
 
     @property
     def H_kv(self) -> int:
@@ -111,6 +116,9 @@ def _draw(shape, kind: str, dtype: torch.dtype, gen: torch.Generator) -> torch.T
     elif kind == "onehot_d0":
         x = torch.zeros(shape, dtype=torch.float32)
         x[..., 0] = 1.0
+    elif kind == "bytes":
+        # every byte pattern equally likely (packed FP4 codes: two per byte)
+        return torch.randint(0, 256, shape, generator=gen, dtype=torch.int32).to(torch.uint8)
     else:
         raise ValueError(f"unknown value kind {kind!r}")
     if dtype == torch.int8:
@@ -322,6 +330,42 @@ def config(n: int, seed: Optional[int] = None, layout: Optional[str] = None,
                          init_blocks=4, local_blocks=8, start_loc=[1023],
                          seed=seed + 1, name=name)
     raise ValueError(f"no workload {n}")
+
+
+# scale bytes drawn for FP4 cases: E8M0 codes 2^-6 .. 2^6 (MXFP4) and E4M3
+# values 0.25 .. 4.5 (NVFP4, codes 0x28 .. 0x49), per group of 32 / 16 elements
+FP4_SCALE_CODES = {"mx": (121, 133), "nv": (0x28, 0x49)}
+FP4_GROUP = {"mx": 32, "nv": 16}
+
+
+def make_fp4_case(q_lens: Sequence[int], kv_lens: Sequence[int], *, fmt: str, H_q: int,
+                  H_kv: int, D: int = 128, scale_codes=None, seed: int = 0,
+                  name: str = "fp4_case", **kw) -> MsaCase:
+    """An FP4 case: uniformly random packed E2M1 codes for the query and the
+    key cache (any layout of ``make_case``), random group scale bytes.
+
+    ``fmt`` is "mx" (E8M0 scale per 32 elements) or "nv" (E4M3 scale per 16).
+    The key scales are kept in logical page order: paged [NP, H_kv, P, D/G],
+    TND [T2, H_kv, D/G]; the query scales are [T, H_q, D/G].  ``scale_codes``
+    (lo, hi) overrides the drawn scale byte range (inclusive).
+    """
+    if fmt not in FP4_GROUP:
+        raise ValueError(f"fp4 format {fmt!r}")
+    base = make_case(q_lens, kv_lens, H_q=H_q, H_kv=H_kv, D=D // 2, q_dtype=torch.uint8,
+                     k_dtype=torch.uint8, q_kind="bytes", k_kind="bytes", seed=seed, name=name,
+                     **kw)
+    ng = D // FP4_GROUP[fmt]
+    lo, hi = scale_codes if scale_codes is not None else FP4_SCALE_CODES[fmt]
+    gen = torch.Generator().manual_seed(int(seed) + 7777)
+
+    def codes(shape):
+        return torch.randint(lo, hi + 1, shape, generator=gen, dtype=torch.int32).to(torch.uint8)
+    q_scale = codes((base.T, H_q, ng))
+    if base.layout == "TND":
+        k_scale = codes((int(base.key.shape[0]), H_kv, ng))
+    else:
+        k_scale = codes((int(base.key.shape[0]), H_kv, base.P, ng))
+    return dataclasses.replace(base, fp4=fmt, q_scale=q_scale, k_scale=k_scale)
 
 
 def decode_subset(case: MsaCase) -> MsaCase:

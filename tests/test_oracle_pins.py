@@ -15,6 +15,7 @@ Definition: feature request "MsaIndexScore" (gitcode.com/cann/ops-transformer
 issues/4117, "calculation"); local mask / shape / modes: torch API guide
 "CANN ops-transformer ... msa_index_score", sec. 2, 4, 5.
 """
+import dataclasses
 import json
 import math
 import os
@@ -216,6 +217,7 @@ def test_closed_form_int8_scale_index_and_order():
 # ---------------------------------------------------------------------------
 
 def _compare_with_bruteforce(case, exact=False):
+    """Compare the C oracle with the dense formulation; returns the oracle's output."""
     out = oracle.oracle_full(case).numpy()
     bf = bruteforce.block_scores(case)
     assert out.shape == bf.shape
@@ -229,6 +231,7 @@ def _compare_with_bruteforce(case, exact=False):
         # one rounding to fp32 of the same fp64 value (sums may differ in order)
         err = np.abs(out[fin].astype(np.float64) - bf[fin])
         assert (err <= np.abs(bf[fin]) * 2.0 ** -23 + 1e-30).all()
+    return out
 
 
 @pytest.mark.parametrize("layout", ["BBND", "BNBD", "TND"])
@@ -471,3 +474,90 @@ def test_fp8_one_hot_reads_the_key_value():
     for beta in range(3):
         lo, hi = beta * 128, min(300, beta * 128 + 128)
         assert out[0, 0, beta] == np.float32(keys[lo:hi, 0, 0].max())
+
+
+# ---------------------------------------------------------------------------
+# FP4 inputs (MiniMax Sparse Attention notes, section 8.2: MXFP4 = E2M1 values
+# with an E8M0 scale per 32 elements, NVFP4 = E2M1 values with an E4M3 scale
+# per 16); formats as defined by the OCP Microscaling (MX) specification
+
+# E2M1 by code 0..15: +0, 0.5, 1, 1.5, 2, 3, 4, 6, then the same negated
+E2M1_TABLE = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0,
+              -0.0, -0.5, -1.0, -1.5, -2.0, -3.0, -4.0, -6.0]
+
+
+def test_e2m1_decoding_matches_the_format_table():
+    got = [oracle.decode("e2m1", c) for c in range(16)]
+    assert got == E2M1_TABLE
+    assert [np.signbit(x) for x in got] == [c >= 8 for c in range(16)]
+
+
+def test_e2m1_decoding_matches_torch_e4m3_of_the_same_value():
+    # every E2M1 value is an E4M3 value: same sign, exponent e - 1 + 7, mantissa
+    # bit m as the top of three (code 1, 0.5, is the normal E4M3 0.5); torch
+    # decodes those bytes
+    def as_e4m3(c):
+        s, e, m = c >> 3, (c >> 1) & 3, c & 1
+        if e == 0:
+            mag = 0 if m == 0 else (6 << 3)              # 0, or 0.5 = 2^(6-7)
+        else:
+            mag = ((e + 6) << 3) | (m << 2)
+        return (s << 7) | mag
+    b = torch.tensor([as_e4m3(c) for c in range(16)], dtype=torch.uint8)
+    ref = b.view(torch.float8_e4m3fn).to(torch.float64).tolist()
+    assert [oracle.decode("e2m1", c) for c in range(16)] == ref
+
+
+def test_e8m0_decoding_matches_torch_for_every_bit_pattern():
+    bits = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    ref = bits.view(torch.float8_e8m0fnu).to(torch.float64).numpy()
+    got = np.array([oracle.decode("e8m0", b) for b in range(256)])
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan) and nan.sum() == 1
+    assert np.array_equal(got[~nan], ref[~nan])
+
+
+@pytest.mark.parametrize("layout", ["BBND", "BNBD", "TND"])
+@pytest.mark.parametrize("fmt", ["mx", "nv"])
+@pytest.mark.parametrize("mode", [0, 3])
+def test_fp4_oracle_matches_dense_amax(layout, fmt, mode):
+    from synth import make_fp4_case
+    case = make_fp4_case([5, 0, 3, 9, 1], [900, 6, 0, 9, 1000], fmt=fmt, H_q=6, H_kv=3,
+                         layout=layout, sparse_mode=mode, init_blocks=1, local_blocks=1,
+                         MB=8 if layout != "TND" else None, seed=60 + mode)
+    out = _compare_with_bruteforce(case)
+    real = np.isfinite(out) & (np.abs(out) < 1e28)
+    assert real.sum() > 100                       # most blocks are real scores, not forced
+
+
+def test_fp4_with_unit_scales_equals_the_fp16_oracle_on_the_decoded_values():
+    # E8M0 code 127 is 1.0: the block scores are those of the E2M1 values
+    # themselves, which fp16 holds exactly, so the fp16 oracle must agree bit
+    # for bit
+    from synth import make_fp4_case
+    case = make_fp4_case([7, 1], [400, 130], fmt="mx", H_q=4, H_kv=2, layout="BBND", MB=4,
+                         scale_codes=(127, 127), seed=61)
+    table = torch.tensor(E2M1_TABLE, dtype=torch.float16)
+
+    def unpack(p):
+        b = p.to(torch.int64)
+        return table[torch.stack([b & 15, b >> 4], dim=-1).flatten(-2)]
+    f16 = dataclasses.replace(case, query=unpack(case.query), key=unpack(case.key), fp4=None,
+                              q_scale=None, k_scale=None)
+    assert torch.equal(oracle.oracle_full(case), oracle.oracle_full(f16))
+
+
+def test_fp4_group_scales_apply_to_their_own_elements():
+    # query = +1 everywhere (code 2) with unit scales; key = +1 everywhere with
+    # the scale of group gi of token j equal to 2^gi (MXFP4, 4 groups of 32):
+    # every dot product is 32 * (1 + 2 + 4 + 8) = 480, and a wrong group or
+    # element index would change it
+    from synth import make_fp4_case
+    case = make_fp4_case([3], [200], fmt="mx", H_q=2, H_kv=1, layout="BNBD", MB=2,
+                         sparse_mode=0, init_blocks=0, local_blocks=0, seed=62)
+    case.query.fill_(0x22)
+    case.key.fill_(0x22)
+    case.q_scale.fill_(127)
+    case.k_scale.copy_(torch.tensor([127, 128, 129, 130], dtype=torch.uint8).expand_as(case.k_scale))
+    out = oracle.oracle_full(case)
+    assert torch.all(out[:, :, :2] == 480.0)
