@@ -42,6 +42,8 @@ DEVERR = {0x01: "cu_seqlens_q", 0x02: "kv_len", 0x04: "cu_seqlens_k",
 _DT = {torch.float16: 0, torch.bfloat16: 1, torch.int8: 2,
        torch.float8_e4m3fn: 3, torch.float8_e5m2: 4}
 _LAYOUT = {"BBND": 0, "BNBD": 1, "TND": 2}
+MSA_E2M1 = 5
+FP4_FORMATS = {"mx": 0, "nv": 1}
 
 
 class MsaError(RuntimeError):
@@ -99,6 +101,8 @@ def load_library():
                                    ctypes.c_int32, vp, vp]
     lib.msa_index_score_topk_workspace_size.argtypes = [P, ctypes.c_int32, ctypes.POINTER(sz)]
     lib.msa_index_score_topk.argtypes = [P, ctypes.c_int32, ctypes.c_int32, vp, vp, vp, sz, vp]
+    lib.msa_index_score_fp4_workspace_size.argtypes = [P, ctypes.c_int32, ctypes.POINTER(sz)]
+    lib.msa_index_score_fp4.argtypes = [P, ctypes.c_int32, vp, vp, vp, vp, sz, vp]
     lib.msa_set_watchdog.argtypes = [ctypes.c_uint64, ctypes.c_int32]
     lib.msa_set_watchdog.restype = ctypes.c_int
     lib.msa_status_string.restype = ctypes.c_char_p
@@ -107,7 +111,8 @@ def load_library():
     for name in ("msa_index_score_out_shape", "msa_index_score_workspace_size",
                  "msa_index_score", "msa_index_score_plan", "msa_index_score_run",
                  "msa_get_device_error", "msa_index_score_noalloc", "msa_noalloc_device_error",
-                 "msa_block_topk", "msa_index_score_topk_workspace_size", "msa_index_score_topk"):
+                 "msa_block_topk", "msa_index_score_topk_workspace_size", "msa_index_score_topk",
+                 "msa_index_score_fp4_workspace_size", "msa_index_score_fp4"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -147,7 +152,7 @@ class _Call:
 
     def __init__(self, query, key, start_loc, block_table, scale, actual_seq_qlen,
                  actual_seq_klen, layout_key, sparse_mode, init_blocks, local_blocks,
-                 max_blocks, max_seqlen_q=None):
+                 max_blocks, max_seqlen_q=None, fp4=None):
         layout = str(layout_key).upper()
         if layout not in _LAYOUT:
             raise ValueError(f"layout_key must be one of TND/BBND/BNBD, got {layout_key!r}")
@@ -205,13 +210,15 @@ class _Call:
             self.kv_len, self.cu_k = klen, None
             MB = int(self.block_table.shape[1])
         a = _Args()
+        if fp4 is not None and (query.dtype != torch.uint8 or key.dtype != torch.uint8):
+            raise ValueError("FP4 query and key are uint8 tensors of packed E2M1 codes")
         a.query = _ptr(query)
-        a.q_dtype = _DT.get(query.dtype, -1)
+        a.q_dtype = MSA_E2M1 if fp4 is not None else _DT.get(query.dtype, -1)
         a.T = int(query.shape[0])
         a.H_q = int(query.shape[1])
-        a.D = int(query.shape[2])
+        a.D = int(query.shape[2]) * (2 if fp4 is not None else 1)   # FP4: two codes per byte
         a.key_cache = _ptr(key)
-        a.k_dtype = _DT.get(key.dtype, -1)
+        a.k_dtype = MSA_E2M1 if fp4 is not None else _DT.get(key.dtype, -1)
         a.layout = _LAYOUT[layout]
         a.NP = int(NP)
         a.P = int(P)
@@ -246,9 +253,10 @@ class _Call:
 
 def _prepare(query, key, start_loc, block_table, scale, actual_seq_qlen, actual_seq_klen,
              layout_key, sparse_mode, init_blocks, local_blocks, max_blocks,
-             max_seqlen_q=None) -> _Call:
+             max_seqlen_q=None, fp4=None) -> _Call:
     return _Call(query, key, start_loc, block_table, scale, actual_seq_qlen, actual_seq_klen,
-                 layout_key, sparse_mode, init_blocks, local_blocks, max_blocks, max_seqlen_q)
+                 layout_key, sparse_mode, init_blocks, local_blocks, max_blocks, max_seqlen_q,
+                 fp4)
 
 
 def msa_index_score(query: torch.Tensor, key: torch.Tensor, start_loc: torch.Tensor, *,
@@ -358,25 +366,53 @@ def msa_index_score_workspace_size(query, key, start_loc, **kw) -> int:
 
 
 class Prepared:
-    """Arguments marshalled once, for repeated plan/run calls (benchmarks)."""
+    """Arguments marshalled once, for repeated plan/run calls (benchmarks).
+
+    FP4 inputs: ``fp4="mx"`` or ``"nv"`` with uint8 ``query`` / ``key`` of
+    packed E2M1 codes and the group scale bytes ``q_scale`` / ``k_scale``
+    (see ``msa_index_score_fp4`` in the C header); the call then goes through
+    the FP4 entry point."""
 
     def __init__(self, query, key, start_loc, **kw):
         kw = dict(kw)
+        fp4 = kw.pop("fp4", None)
+        q_scale, k_scale = kw.pop("q_scale", None), kw.pop("k_scale", None)
+        if fp4 is not None and fp4 not in FP4_FORMATS:
+            raise ValueError(f"fp4 must be one of {sorted(FP4_FORMATS)}")
         self.call = _prepare(query, key, start_loc, kw.pop("block_table", None),
                              kw.pop("scale", None), kw.pop("actual_seq_qlen", None),
                              kw.pop("actual_seq_klen", None), kw.pop("layout_key", "BBND"),
                              kw.pop("sparse_mode", 3), kw.pop("init_blocks", 0),
                              kw.pop("local_blocks", 1), kw.pop("max_blocks", None),
-                             kw.pop("max_seqlen_q", None))
+                             kw.pop("max_seqlen_q", None), fp4)
         if kw:
             raise TypeError(f"unknown arguments {sorted(kw)}")
+        self.fp4 = fp4
+        if fp4 is not None:
+            if q_scale is None or k_scale is None:
+                raise ValueError("FP4 inputs need q_scale and k_scale")
+            if q_scale.dtype != torch.uint8 or k_scale.dtype != torch.uint8:
+                raise ValueError("q_scale and k_scale are uint8 scale bytes")
+            self.q_scale, self.k_scale = q_scale.contiguous(), k_scale.contiguous()
         self.shape = self.call.out_shape()
-        self.ws_bytes = self.call.workspace_bytes()
+        if fp4 is not None:
+            n = ctypes.c_size_t()
+            _check(load_library().msa_index_score_fp4_workspace_size(
+                ctypes.byref(self.call.args), FP4_FORMATS[fp4], ctypes.byref(n)))
+            self.ws_bytes = int(n.value)
+        else:
+            self.ws_bytes = self.call.workspace_bytes()
         dev = query.device
         self.out = torch.empty(self.shape, dtype=torch.float32, device=dev)
         self.workspace = torch.empty(self.ws_bytes, dtype=torch.uint8, device=dev)
 
     def __call__(self, stream=None) -> torch.Tensor:
+        if self.fp4 is not None:
+            _check(load_library().msa_index_score_fp4(
+                ctypes.byref(self.call.args), FP4_FORMATS[self.fp4], self.q_scale.data_ptr(),
+                self.k_scale.data_ptr(), self.out.data_ptr(), self.workspace.data_ptr(),
+                self.ws_bytes, _stream_handle(stream)))
+            return self.out
         _check(load_library().msa_index_score(ctypes.byref(self.call.args), self.out.data_ptr(),
                                               self.workspace.data_ptr(), self.ws_bytes,
                                               _stream_handle(stream)))
@@ -468,7 +504,10 @@ def from_case(case, device, max_seqlen_q: Optional[int] = None) -> Prepared:
     else:
         key_dev = key.to(device)
     klen = case.cu_seqlens_k if case.layout == "TND" else case.kv_len
-    return Prepared(case.query.to(device), key_dev, mv(case.start_loc),
+    fp4 = {}
+    if getattr(case, "fp4", None):
+        fp4 = dict(fp4=case.fp4, q_scale=mv(case.q_scale), k_scale=mv(case.k_scale))
+    return Prepared(case.query.to(device), key_dev, mv(case.start_loc), **fp4,
                     block_table=mv(case.block_table), scale=mv(case.scale),
                     actual_seq_qlen=mv(case.cu_seqlens_q), actual_seq_klen=mv(klen),
                     layout_key=case.layout, sparse_mode=case.sparse_mode,

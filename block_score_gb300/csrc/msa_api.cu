@@ -37,18 +37,32 @@ int64_t round16(int64_t x) { return (x + 15) / 16 * 16; }
 
 bool is_f8(msa_dtype_t t) { return t == MSA_E4M3 || t == MSA_E5M2; }
 
-int elem_size(msa_dtype_t t) { return (t == MSA_I8 || is_f8(t)) ? 1 : 2; }
+int elem_size(msa_dtype_t t) { return (t == MSA_I8 || is_f8(t) || t == MSA_E2M1) ? 1 : 2; }
+
+// Storage elements of one key row of D values (FP4: two values per byte).
+int64_t row_elems(const msa_index_score_args* a) {
+  return a->k_dtype == MSA_E2M1 ? a->D / 2 : a->D;
+}
 
 // Host-side checks; everything that can be judged without reading device memory.
-msa_status_t validate(const msa_index_score_args* a) {
+// `fp4`: the call is msa_index_score_fp4 (E2M1 query and key, scales given apart).
+msa_status_t validate(const msa_index_score_args* a, bool fp4 = false) {
   if (!a) return fail(MSA_ERR_INVALID_ARG, "args is NULL");
+  if (fp4 != (a->q_dtype == MSA_E2M1 || a->k_dtype == MSA_E2M1)) {
+    if (fp4) return fail(MSA_ERR_INVALID_ARG, "msa_index_score_fp4 takes E2M1 query and key");
+    return fail(MSA_ERR_INVALID_ARG, "E2M1 (FP4) inputs go through msa_index_score_fp4");
+  }
   if (a->layout != MSA_LAYOUT_BBND && a->layout != MSA_LAYOUT_BNBD && a->layout != MSA_LAYOUT_TND)
     return fail(MSA_ERR_INVALID_ARG, "layout must be BBND, BNBD or TND");
   if (a->sparse_mode != 0 && a->sparse_mode != 3)
     return fail(MSA_ERR_INVALID_ARG, "sparse_mode must be 0 or 3");
-  if (a->q_dtype != MSA_F16 && a->q_dtype != MSA_BF16 && !is_f8(a->q_dtype))
+  if (a->q_dtype != MSA_F16 && a->q_dtype != MSA_BF16 && !is_f8(a->q_dtype) && !fp4)
     return fail(MSA_ERR_INVALID_ARG, "query dtype must be fp16, bf16, fp8 e4m3 or fp8 e5m2");
-  if (is_f8(a->q_dtype) || is_f8(a->k_dtype)) {
+  if (fp4) {
+    if (a->q_dtype != MSA_E2M1 || a->k_dtype != MSA_E2M1)
+      return fail(MSA_ERR_INVALID_ARG, "FP4 query and key must both be E2M1");
+    if (a->scale) return fail(MSA_ERR_INVALID_ARG, "FP4 inputs take their group scales, not scale");
+  } else if (is_f8(a->q_dtype) || is_f8(a->k_dtype)) {
     if (a->k_dtype != a->q_dtype)
       return fail(MSA_ERR_INVALID_ARG, "fp8 query and key must be of the same fp8 type");
     if (a->scale) return fail(MSA_ERR_INVALID_ARG, "fp8 inputs take no scale");
@@ -83,13 +97,13 @@ msa_status_t validate(const msa_index_score_args* a) {
     if (a->block_table) return fail(MSA_ERR_INVALID_ARG, "TND takes no block_table");
     if (!a->cu_seqlens_k || a->kv_len)
       return fail(MSA_ERR_INVALID_ARG, "TND takes cu_seqlens_k [B+1] and no kv_len");
-    if (a->page_stride != (int64_t)a->H_kv * a->D)
+    if (a->page_stride != (int64_t)a->H_kv * row_elems(a))
       return fail(MSA_ERR_INVALID_ARG, "TND key must be contiguous");
   } else {
     if (a->B > 0 && !a->block_table) return fail(MSA_ERR_INVALID_ARG, "paged layout needs block_table");
     if (a->B > 0 && !a->kv_len) return fail(MSA_ERR_INVALID_ARG, "paged layout needs kv_len [B]");
     if (a->cu_seqlens_k) return fail(MSA_ERR_INVALID_ARG, "cu_seqlens_k is for TND only");
-    if (a->page_stride < (int64_t)a->P * a->H_kv * a->D)
+    if (a->page_stride < (int64_t)a->P * a->H_kv * row_elems(a))
       return fail(MSA_ERR_INVALID_ARG, "page_stride smaller than a compact page");
     if ((a->page_stride * es) % 16 != 0)
       return fail(MSA_ERR_UNSUPPORTED, "page stride must be a multiple of 16 bytes");
@@ -180,6 +194,8 @@ msa_status_t fill_params(const msa_index_score_args* a, float* out, void* ws, ms
   p.cand = nullptr;
   p.cand_parts = 0;
   p.chunk_min[0] = p.chunk_min[1] = 0;
+  p.k_scale8 = nullptr;
+  p.fp4_ng = 0;
   p.pad_ = 0;
   return MSA_OK;
 }
@@ -284,14 +300,21 @@ CUresult encode_cached(EncodeTiledFn enc, CUtensorMap* m, CUtensorMapDataType dt
   return r;
 }
 
+// fp4_q16: FP4 call, the dequantised query (fp16 for NVFP4, bf16 for MXFP4)
+// that the tile kernel reads, else NULL.
 msa_status_t make_maps(const msa_index_score_args* a, const msa::Params& p, CUtensorMap* tq,
-                       CUtensorMap* tk, CUtensorMap* tq_short, CUtensorMap* tk_short) {
+                       CUtensorMap* tk, CUtensorMap* tq_short, CUtensorMap* tk_short,
+                       const void* fp4_q16 = nullptr, bool fp4_nv = false) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return fail(MSA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  const bool fp4 = fp4_q16 != nullptr;
   const bool f8 = is_f8(a->q_dtype);
-  const CUtensorMapDataType qdt = f8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+  const CUtensorMapDataType qdt = fp4 ? (fp4_nv ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16)
+                                  : f8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
                                   : a->q_dtype == MSA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                                            : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  const void* qbase = fp4 ? fp4_q16 : a->query;
   const cuuint64_t qsz = f8 ? 1 : 2;
   // query [T, H_q, D]: dims (D, H_q, T); a box is (128 bytes of D, g, positions):
   // one GQA group x a run of positions, 128-byte swizzled
@@ -300,7 +323,7 @@ msa_status_t make_maps(const msa_index_score_args* a, const msa::Params& p, CUte
     cuuint64_t strides[2] = {(cuuint64_t)a->D * qsz, (cuuint64_t)a->H_q * a->D * qsz};
     cuuint32_t box[3] = {(cuuint32_t)(128 / qsz), (cuuint32_t)p.g, (cuuint32_t)positions};
     cuuint32_t es[3] = {1, 1, 1};
-    CUresult r = encode_cached(enc, m, qdt, 3, const_cast<void*>(a->query), dims, strides, box, es,
+    CUresult r = encode_cached(enc, m, qdt, 3, const_cast<void*>(qbase), dims, strides, box, es,
                                CU_TENSOR_MAP_SWIZZLE_128B);
     if (r != CUDA_SUCCESS) return fail(MSA_ERR_CUDA, "%s tensor map: CUresult %d", what, (int)r);
     return MSA_OK;
@@ -308,32 +331,35 @@ msa_status_t make_maps(const msa_index_score_args* a, const msa::Params& p, CUte
   // one 128-token key page of one kv head; dims ordered by increasing stride
   auto kmap = [&](CUtensorMap* m, bool swizzle_int8, const char* what) -> msa_status_t {
     const bool i8 = a->k_dtype == MSA_I8;
-    const bool byte = i8 || f8;                  // one-byte elements: a 128-element row is 128 bytes
+    const bool byte = i8 || f8 || fp4;           // one-byte elements: a 128-element row is 128 bytes
     const cuuint64_t esz = byte ? 1 : 2;
     const CUtensorMapDataType kdt = byte ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : qdt;
     cuuint64_t dims[4];
     cuuint64_t strides[3];
     cuuint32_t box[4];
-    const cuuint32_t bx = byte ? 128 : 64;
+    // FP4: a row is 64 bytes of packed codes (the whole row in one box)
+    const cuuint32_t bx = fp4 ? 64 : (byte ? 128 : 64);
+    const cuuint64_t dx = fp4 ? (cuuint64_t)a->D / 2 : (cuuint64_t)a->D;   // row elements in storage
     if (a->layout == MSA_LAYOUT_BNBD) {         // [NP, H_kv, P, D]
-      dims[0] = a->D; dims[1] = a->P; dims[2] = a->H_kv; dims[3] = a->NP;
-      strides[0] = a->D * esz; strides[1] = (cuuint64_t)a->P * a->D * esz;
+      dims[0] = dx; dims[1] = a->P; dims[2] = a->H_kv; dims[3] = a->NP;
+      strides[0] = dx * esz; strides[1] = (cuuint64_t)a->P * dx * esz;
       strides[2] = (cuuint64_t)a->page_stride * esz;
       box[0] = bx; box[1] = 128; box[2] = 1; box[3] = 1;
     } else if (a->layout == MSA_LAYOUT_BBND) {  // [NP, P, H_kv, D]
-      dims[0] = a->D; dims[1] = a->H_kv; dims[2] = a->P; dims[3] = a->NP;
-      strides[0] = a->D * esz; strides[1] = (cuuint64_t)a->H_kv * a->D * esz;
+      dims[0] = dx; dims[1] = a->H_kv; dims[2] = a->P; dims[3] = a->NP;
+      strides[0] = dx * esz; strides[1] = (cuuint64_t)a->H_kv * dx * esz;
       strides[2] = (cuuint64_t)a->page_stride * esz;
       box[0] = bx; box[1] = 1; box[2] = 128; box[3] = 1;
     } else {                                    // TND [T2, H_kv, D]
-      dims[0] = a->D; dims[1] = a->H_kv; dims[2] = a->NP; dims[3] = 1;
-      strides[0] = a->D * esz; strides[1] = (cuuint64_t)a->H_kv * a->D * esz;
-      strides[2] = (cuuint64_t)a->NP * a->H_kv * a->D * esz;
+      dims[0] = dx; dims[1] = a->H_kv; dims[2] = a->NP; dims[3] = 1;
+      strides[0] = dx * esz; strides[1] = (cuuint64_t)a->H_kv * dx * esz;
+      strides[2] = (cuuint64_t)a->NP * a->H_kv * dx * esz;
       box[0] = bx; box[1] = 1; box[2] = 128; box[3] = 1;
     }
     cuuint32_t es[4] = {1, 1, 1, 1};
-    const CUtensorMapSwizzle sw =
-        (!i8 || swizzle_int8) ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE;
+    const CUtensorMapSwizzle sw = fp4 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                  : (!i8 || swizzle_int8) ? CU_TENSOR_MAP_SWIZZLE_128B
+                                                          : CU_TENSOR_MAP_SWIZZLE_NONE;
     CUresult r = encode_cached(enc, m, kdt, 4, const_cast<void*>(a->key_cache), dims, strides,
                                box, es, sw);
     if (r != CUDA_SUCCESS) return fail(MSA_ERR_CUDA, "%s tensor map: CUresult %d", what, (int)r);
@@ -385,7 +411,8 @@ extern "C" {
 int32_t msa_abi_version(void) { return MSA_ABI_VERSION; }
 
 msa_status_t msa_index_score_out_shape(const msa_index_score_args* args, int64_t shape[3]) {
-  msa_status_t st = validate(args);
+  // the same shape for FP4 inputs (validated by their own entry point's rules)
+  msa_status_t st = validate(args, args && args->q_dtype == MSA_E2M1);
   if (st != MSA_OK) return st;
   if (!shape) return fail(MSA_ERR_INVALID_ARG, "shape is NULL");
   shape[0] = args->H_q;
@@ -527,6 +554,58 @@ msa_status_t msa_index_score_topk(const msa_index_score_args* args, int32_t k, i
   if ((st = launch_score_checked(args, p, s)) != MSA_OK) return st;
   cudaError_t e = msa::launch_group_select(p, local_slot ? 1 : 0, indices, s);
   if (e != cudaSuccess) return cuda_fail(e, "selection kernel launch");
+  return MSA_OK;
+}
+
+size_t fp4_query_bytes(const msa_index_score_args* a) {
+  return ((size_t)a->T * a->H_q * a->D * 2 + 255) / 256 * 256;
+}
+
+msa_status_t msa_index_score_fp4_workspace_size(const msa_index_score_args* args, int32_t format,
+                                                size_t* bytes) {
+  msa_status_t st = validate(args, true);
+  if (st != MSA_OK) return st;
+  if (format != MSA_FP4_MX && format != MSA_FP4_NV)
+    return fail(MSA_ERR_INVALID_ARG, "format must be MSA_FP4_MX or MSA_FP4_NV");
+  if (!bytes) return fail(MSA_ERR_INVALID_ARG, "bytes is NULL");
+  *bytes = msa::workspace_bytes_for(args->B) + fp4_query_bytes(args);
+  return MSA_OK;
+}
+
+msa_status_t msa_index_score_fp4(const msa_index_score_args* args, int32_t format,
+                                 const uint8_t* q_scale, const uint8_t* k_scale, float* out,
+                                 void* workspace, size_t workspace_bytes, msa_stream_t stream) {
+  g_msg[0] = 0;
+  msa_status_t st = validate(args, true);
+  if (st != MSA_OK) return st;
+  if (format != MSA_FP4_MX && format != MSA_FP4_NV)
+    return fail(MSA_ERR_INVALID_ARG, "format must be MSA_FP4_MX or MSA_FP4_NV");
+  if (args->T == 0 || args->B == 0) return MSA_OK;
+  if (!q_scale || !k_scale) return fail(MSA_ERR_INVALID_ARG, "q_scale and k_scale are required");
+  if (!aligned(q_scale, 16) || !aligned(k_scale, 16))
+    return fail(MSA_ERR_INVALID_ARG, "q_scale and k_scale must be 16-byte aligned");
+  if (!out || !aligned(out, 16)) return fail(MSA_ERR_INVALID_ARG, "out must be a 16-byte aligned pointer");
+  const size_t plan_bytes = msa::workspace_bytes_for(args->B);
+  if (!workspace) return fail(MSA_ERR_WORKSPACE, "workspace is NULL");
+  if (!aligned(workspace, 256)) return fail(MSA_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+  if (workspace_bytes < plan_bytes + fp4_query_bytes(args))
+    return fail(MSA_ERR_WORKSPACE, "workspace needs %zu bytes, got %zu",
+                plan_bytes + fp4_query_bytes(args), workspace_bytes);
+  const bool nv = format == MSA_FP4_NV;
+  msa::Params p;
+  if ((st = fill_params(args, out, workspace, p)) != MSA_OK) return st;
+  p.k_scale8 = k_scale;
+  p.fp4_ng = args->D / (nv ? 16 : 32);
+  void* q16 = static_cast<uint8_t*>(workspace) + plan_bytes;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = msa::launch_fp4_dequant_query(static_cast<const uint8_t*>(args->query), q_scale,
+                                                args->T * (int64_t)args->H_q, nv, q16, s);
+  if (e != cudaSuccess) return cuda_fail(e, "FP4 query dequantisation launch");
+  if ((st = launch_plan_checked(p, s)) != MSA_OK) return st;
+  CUtensorMap tq, tk;
+  if ((st = make_maps(args, p, &tq, &tk, nullptr, nullptr, q16, nv)) != MSA_OK) return st;
+  e = msa::launch_score_fp4(&tq, &tk, p, nv, s);
+  if (e != cudaSuccess) return cuda_fail(e, "score kernel launch");
   return MSA_OK;
 }
 

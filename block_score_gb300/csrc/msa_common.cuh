@@ -91,6 +91,10 @@ struct Params {
   uint64_t* cand;          // partial selections: [T][H_kv][cand_parts][topk_k] candidate keys
   int32_t cand_parts;      // partial lists per (token, group) row: 2 per KV chunk
   int32_t chunk_min[2];    // lower bound of each class's KV chunk (caps the chunks per tile)
+  // FP4 keys (msa_index_score_fp4): group scale bytes of the key cache, in
+  // logical page order (paged [NP, H_kv, P, D/G]; TND [T2, H_kv, D/G])
+  const uint8_t* k_scale8;
+  int32_t fp4_ng;          // scale bytes per row: D/32 (MXFP4) or D/16 (NVFP4)
   int32_t pad_;
 };
 
@@ -199,6 +203,13 @@ cudaError_t launch_score_i8(const void* tmap_q, const void* tmap_k, const Params
                             cudaStream_t s);
 cudaError_t launch_short_i8(const void* tmap_q, const void* tmap_k, const Params& p,
                             cudaStream_t s);
+// FP4 keys: the tile kernel with E2M1 pages dequantised into 16-bit operands
+// (nv: E4M3 scales per 16 elements, fp16 operands; else E8M0 per 32, bf16).
+cudaError_t launch_score_fp4(const void* tmap_q, const void* tmap_k, const Params& p, bool nv,
+                             cudaStream_t s);
+// FP4 queries [T, H_q, D/2] with scales [T, H_q, D/G] -> 16-bit [T, H_q, D] (exact).
+cudaError_t launch_fp4_dequant_query(const uint8_t* q, const uint8_t* q_scale, int64_t rows, bool nv,
+                                     void* out, cudaStream_t s);
 // Merge of the partial selections into [T, H_kv, k] indices (after the score kernels).
 cudaError_t launch_group_select(const Params& p, int local_slot, int32_t* out, cudaStream_t s);
 

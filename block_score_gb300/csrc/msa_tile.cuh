@@ -147,11 +147,16 @@ constexpr uint32_t kCodeLive = 1, kCodeFirst = 2, kCodeLast = 4, kCodeLone = 8, 
 // position (g >= 8), so the 128-column TMEM load of a block still fits the
 // registers; TOPK = 16: every lane holds the whole list (g < 8) and a block is
 // loaded in two 64-column pieces.
-template <bool KI8, bool BF16, int F8 = 0, int TOPK = 0>
+// KF4 (with KI8): FP4 key pages instead of int8, 1 = NVFP4 (E4M3 scale per 16
+// elements, fp16 operands), 2 = MXFP4 (E8M0 scale per 32, bf16 operands): the
+// converters dequantise each E2M1 element by its group scale exactly, so the
+// epilogue has no per-token scale to apply.
+template <bool KI8, bool BF16, int F8 = 0, int TOPK = 0, int KF4 = 0>
 __global__ void __launch_bounds__(TileCfg<KI8>::kThreads, 1)
     tile_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const Params p) {
   static_assert(F8 == 0 || !KI8, "FP8 operands come with FP8 keys");
+  static_assert(KF4 == 0 || KI8, "FP4 pages go through the converter warps");
   constexpr bool kF8 = F8 != 0;
   constexpr int kHalves = kF8 ? 1 : 2;             // K slots (and Q boxes) per pair of blocks
   using Cfg = TileCfg<KI8>;
@@ -341,11 +346,20 @@ __global__ void __launch_bounds__(TileCfg<KI8>::kThreads, 1)
               raw_page[ks] = paged ? page[j] : tok[j];
               const uint32_t rdst = sbase + L::raw_off + ks * kRawStride;
               const bool with_scale = paged && (int64_t)page[j] < p.NP;
-              mbar_arrive_expect_tx(b_raw_full + 8 * ks, kRawBytes + (with_scale ? kRawScaleBytes : 0u));
+              // int8: a 16 KiB page and its 128 fp32 token scales; FP4: an 8 KiB
+              // page and its tokens' group scale bytes
+              const uint32_t data_bytes = KF4 ? kRawBytes / 2 : kRawBytes;
+              const uint32_t sc_bytes = KF4 ? (uint32_t)(kP * p.fp4_ng) : kRawScaleBytes;
+              mbar_arrive_expect_tx(b_raw_full + 8 * ks, data_bytes + (with_scale ? sc_bytes : 0u));
               tma_k(rdst, &tm_k, b_raw_full + 8 * ks, 0, tok[j], d.hk, page[j], p.layout, pol_k);
-              if (with_scale)
-                bulk_load(rdst + kRawBytes, p.scale + ((int64_t)page[j] * p.H_kv + d.hk) * kP,
-                          kRawScaleBytes, b_raw_full + 8 * ks);
+              if (with_scale) {
+                if constexpr (KF4 != 0)
+                  bulk_load(rdst + kRawBytes, p.k_scale8 + ((int64_t)page[j] * p.H_kv + d.hk) * kP * p.fp4_ng,
+                            sc_bytes, b_raw_full + 8 * ks);
+                else
+                  bulk_load(rdst + kRawBytes, p.scale + ((int64_t)page[j] * p.H_kv + d.hk) * kP,
+                            kRawScaleBytes, b_raw_full + 8 * ks);
+              }
               ++n_k;
               if (++ks == R) { ks = 0; kph ^= 1; }
             }
@@ -548,14 +562,16 @@ __global__ void __launch_bounds__(TileCfg<KI8>::kThreads, 1)
               if (lane == 0) mbar_arrive(b_acc_empty + 8 * a);
             }
             if (ld && valid) {
-              const float4* sv = reinterpret_cast<const float4*>(scale_s + s * 256 + b * 128 + hq * 32);
+              if constexpr (KF4 == 0) {               // FP4: the scales are in the operands
+                const float4* sv = reinterpret_cast<const float4*>(scale_s + s * 256 + b * 128 + hq * 32);
 #pragma unroll
-              for (int c = 0; c < 8; ++c) {
-                const float4 s4 = sv[c];
-                x[4 * c + 0] *= s4.x;
-                x[4 * c + 1] *= s4.y;
-                x[4 * c + 2] *= s4.z;
-                x[4 * c + 3] *= s4.w;
+                for (int c = 0; c < 8; ++c) {
+                  const float4 s4 = sv[c];
+                  x[4 * c + 0] *= s4.x;
+                  x[4 * c + 1] *= s4.y;
+                  x[4 * c + 2] *= s4.z;
+                  x[4 * c + 3] *= s4.w;
+                }
               }
               mb = fmaxf(mb, masked_max<32>(x, lim - (beta + b) * kP - 32 * hq));
             }
@@ -665,6 +681,7 @@ __global__ void __launch_bounds__(TileCfg<KI8>::kThreads, 1)
         const int nblk = beta + 1 < d.b1 ? 2 : 1;
         uint32_t rs[2];
         float sv[2] = {0.f, 0.f};
+        uint2 gsc[2] = {make_uint2(0u, 0u), make_uint2(0u, 0u)};   // FP4: this token's group scale bytes
         for (int j = cgp; j < nblk && ok; j += Cfg::kCvtGroups) {
           const uint32_t rpage = rc + (uint32_t)j;   // the page's place in the raw ring
           rs[j] = rpage % R;
@@ -673,7 +690,23 @@ __global__ void __launch_bounds__(TileCfg<KI8>::kThreads, 1)
           // keys, a global load issued now so that it overlaps the conversion
           const uint8_t* src = smem + L::raw_off + rs[j] * kRawStride;
           const int page = raw_page[rs[j]];
-          if (p.layout == 2) {
+          if constexpr (KF4 != 0) {
+            // FP4: the group scales of token ct (4 bytes MXFP4, 8 bytes NVFP4);
+            // the epilogue's token scale is 1
+            sv[j] = 1.f;
+            const uint8_t* g = nullptr;
+            if (p.layout == 2) {
+              const int64_t row = (int64_t)page + ct;
+              if (row < (int64_t)d.kbase + d.L && row < p.NP)
+                g = p.k_scale8 + (row * p.H_kv + d.hk) * (int64_t)p.fp4_ng;
+            } else if (page >= 0 && (int64_t)page < p.NP) {
+              g = src + kRawBytes + ct * p.fp4_ng;
+            }
+            if (g) {
+              if constexpr (KF4 == 1) gsc[j] = *reinterpret_cast<const uint2*>(g);
+              else gsc[j].x = *reinterpret_cast<const uint32_t*>(g);
+            }
+          } else if (p.layout == 2) {
             const int64_t row = (int64_t)page + ct;      // page holds the first key row here
             if (row < (int64_t)d.kbase + d.L && row < p.NP) sv[j] = __ldg(p.scale + row * p.H_kv + d.hk);
           } else if (page >= 0 && (int64_t)page < p.NP) {
@@ -689,29 +722,57 @@ __global__ void __launch_bounds__(TileCfg<KI8>::kThreads, 1)
           for (int j = cgp; j < nblk; j += Cfg::kCvtGroups) {
             const uint8_t* src = smem + L::raw_off + rs[j] * kRawStride;
             uint8_t* dst = smem + L::k_off + k * L::kSlotBytes + j * kHalfBytes;
-            int4 raw[4];
-#pragma unroll
-            for (int t = 0; t < 4; ++t) {
-              const int row = wq * 32 + t * 8 + rsub;
-              const int c = 4 * x + ci;
-              raw[t] = *reinterpret_cast<const int4*>(src + row * 128 + ((c ^ (row & 7)) << 4));
-            }
-#pragma unroll
-            for (int t = 0; t < 4; ++t) {
-              const int row = wq * 32 + t * 8 + rsub;
-              uint32_t hv[8];
-              int8x4_to_half4((uint32_t)raw[t].x, hv[0], hv[1]);
-              int8x4_to_half4((uint32_t)raw[t].y, hv[2], hv[3]);
-              int8x4_to_half4((uint32_t)raw[t].z, hv[4], hv[5]);
-              int8x4_to_half4((uint32_t)raw[t].w, hv[6], hv[7]);
-              // 16 fp16 values = output chunks 2ci, 2ci + 1 of the 128-byte row
+            if constexpr (KF4 != 0) {
+              // FP4: thread = token row ct; half x = elements 64x .. 64x+63 =
+              // bytes 32x .. 32x+31 of the 64-byte row (64-byte swizzled: chunk
+              // c at (c ^ ((row >> 1) & 3)) * 16), written as 8 chunks of 8
+              // 16-bit values into the 128-byte swizzled operand row
+              const int row = ct;
+              const int sw = (row >> 1) & 3;
+              const uint4 in0 = *reinterpret_cast<const uint4*>(src + row * 64 + (((2 * x) ^ sw) << 4));
+              const uint4 in1 = *reinterpret_cast<const uint4*>(src + row * 64 + (((2 * x + 1) ^ sw) << 4));
+              const uint32_t wv[8] = {in0.x, in0.y, in0.z, in0.w, in1.x, in1.y, in1.z, in1.w};
               uint8_t* rowp = dst + row * 128;
-              const int ca = (2 * ci + (odd_first ? 1 : 0)) ^ (row & 7);
-              const int cb = (2 * ci + (odd_first ? 0 : 1)) ^ (row & 7);
-              const uint4 lo = make_uint4(hv[0], hv[1], hv[2], hv[3]);
-              const uint4 hi = make_uint4(hv[4], hv[5], hv[6], hv[7]);
-              *reinterpret_cast<uint4*>(rowp + (ca << 4)) = odd_first ? hi : lo;
-              *reinterpret_cast<uint4*>(rowp + (cb << 4)) = odd_first ? lo : hi;
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                uint4 o;
+                if constexpr (KF4 == 1) {
+                  // NVFP4: group (64x + 8i) / 16 = 4x + i / 2 of 8 scale bytes
+                  const int gi = 4 * x + (i >> 1);
+                  const uint32_t sb = ((gi < 4 ? gsc[j].x : gsc[j].y) >> (8 * (gi & 3))) & 0xffu;
+                  o = fp4x8_to_f16(wv[i], e4m3_scale2(sb));
+                } else {
+                  // MXFP4: group (64x + 8i) / 32 = 2x + i / 4 of 4 scale bytes
+                  const uint32_t sb = (gsc[j].x >> (8 * (2 * x + (i >> 2)))) & 0xffu;
+                  o = fp4x8_to_bf16(wv[i], e8m0_scale(sb));
+                }
+                *reinterpret_cast<uint4*>(rowp + ((i ^ (row & 7)) << 4)) = o;
+              }
+            } else {
+              int4 raw[4];
+#pragma unroll
+              for (int t = 0; t < 4; ++t) {
+                const int row = wq * 32 + t * 8 + rsub;
+                const int c = 4 * x + ci;
+                raw[t] = *reinterpret_cast<const int4*>(src + row * 128 + ((c ^ (row & 7)) << 4));
+              }
+#pragma unroll
+              for (int t = 0; t < 4; ++t) {
+                const int row = wq * 32 + t * 8 + rsub;
+                uint32_t hv[8];
+                int8x4_to_half4((uint32_t)raw[t].x, hv[0], hv[1]);
+                int8x4_to_half4((uint32_t)raw[t].y, hv[2], hv[3]);
+                int8x4_to_half4((uint32_t)raw[t].z, hv[4], hv[5]);
+                int8x4_to_half4((uint32_t)raw[t].w, hv[6], hv[7]);
+                // 16 fp16 values = output chunks 2ci, 2ci + 1 of the 128-byte row
+                uint8_t* rowp = dst + row * 128;
+                const int ca = (2 * ci + (odd_first ? 1 : 0)) ^ (row & 7);
+                const int cb = (2 * ci + (odd_first ? 0 : 1)) ^ (row & 7);
+                const uint4 lo = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+                const uint4 hi = make_uint4(hv[4], hv[5], hv[6], hv[7]);
+                *reinterpret_cast<uint4*>(rowp + (ca << 4)) = odd_first ? hi : lo;
+                *reinterpret_cast<uint4*>(rowp + (cb << 4)) = odd_first ? lo : hi;
+              }
             }
           }
           fence_proxy_async_smem();
@@ -745,10 +806,10 @@ __global__ void __launch_bounds__(TileCfg<KI8>::kThreads, 1)
 
 // Launch one instantiation: persistent grid of one CTA per SM, programmatic
 // dependent launch after the plan kernel.
-template <bool KI8, bool BF16, int F8, int TOPK>
+template <bool KI8, bool BF16, int F8, int TOPK, int KF4 = 0>
 inline cudaError_t launch_tile_variant(const void* tq, const void* tk, const Params& p, cudaStream_t s) {
   using L = TileLayout<KI8>;
-  auto kern = tile_kernel<KI8, BF16, F8, TOPK>;
+  auto kern = tile_kernel<KI8, BF16, F8, TOPK, KF4>;
   static std::atomic<uint64_t> configured[64];   // per device: context the limit was raised in
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);

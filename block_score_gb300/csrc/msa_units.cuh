@@ -3,7 +3,9 @@
 #pragma once
 #include <cstdint>
 #include <cuda.h>
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 
 #include "msa_common.cuh"
 #include "msa_ptx.cuh"
@@ -41,6 +43,58 @@ __device__ __forceinline__ void int8x4_to_half4(uint32_t w, uint32_t& lo, uint32
   const __half2 rb = __hsub2(*reinterpret_cast<const __half2*>(&b), bias);
   lo = *reinterpret_cast<const uint32_t*>(&ra);
   hi = *reinterpret_cast<const uint32_t*>(&rb);
+}
+
+// ------------------------------------------------------------- FP4 (E2M1) --
+// An E2M1 code (sign, 2 exponent bits with bias 1, 1 mantissa bit) placed so
+// that its exponent and mantissa bits land at the bottom of a binary16
+// exponent field reads as 2^-14 times its value (exponent 0 reads as a
+// binary16 subnormal, which is again 2^-14 times the E2M1 subnormal m/2), so
+// one exact multiplication by 2^14 gives the value.  The same placement in
+// binary32 reads as 2^-126 times the value.
+
+// 8 E2M1 codes (a 32-bit word, element 2i in the low nibble of byte i) times
+// an NVFP4 group scale (E4M3, as binary16) -> 8 binary16 values.  Exact: every
+// product of an E2M1 value and an E4M3 value is a binary16 number.
+__device__ __forceinline__ uint4 fp4x8_to_f16(uint32_t w, __half2 scale2) {
+  const __half2 two14 = __half2half2(__ushort_as_half((unsigned short)0x7400));
+  uint32_t r[4];
+#pragma unroll
+  for (int b = 0; b < 4; ++b) {
+    const uint32_t byte = (w >> (8 * b)) & 0xffu;
+    const uint32_t y = (byte & 0x0fu) | ((byte & 0xf0u) << 12);   // nibbles at bits 0 and 16
+    const uint32_t h = ((y & 0x00070007u) << 9) | ((y & 0x00080008u) << 12);
+    const __half2 v = __hmul2(__hmul2(*reinterpret_cast<const __half2*>(&h), two14), scale2);
+    r[b] = *reinterpret_cast<const uint32_t*>(&v);
+  }
+  return make_uint4(r[0], r[1], r[2], r[3]);
+}
+
+// 8 E2M1 codes times an MXFP4 group scale 2^(e-127) (E8M0 code e, given as
+// binary32) -> 8 bfloat16 values.  Exact while the products stay in bfloat16's
+// normal range (E8M0 codes 2 .. 252).
+__device__ __forceinline__ uint4 fp4x8_to_bf16(uint32_t w, float scale) {
+  uint32_t r[4];
+#pragma unroll
+  for (int b = 0; b < 4; ++b) {
+    const uint32_t lo = (w >> (8 * b)) & 0x0fu, hi = (w >> (8 * b + 4)) & 0x0fu;
+    const float flo = __uint_as_float(((lo & 7u) << 22) | ((lo & 8u) << 28)) * 0x1p126f * scale;
+    const float fhi = __uint_as_float(((hi & 7u) << 22) | ((hi & 8u) << 28)) * 0x1p126f * scale;
+    const __nv_bfloat162 v = __floats2bfloat162_rn(flo, fhi);
+    r[b] = *reinterpret_cast<const uint32_t*>(&v);
+  }
+  return make_uint4(r[0], r[1], r[2], r[3]);
+}
+
+// Group scale bytes as the converters' multipliers.
+__device__ __forceinline__ __half2 e4m3_scale2(uint32_t byte) {
+  const __half h = __half(__nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)byte, __NV_E4M3));
+  return __half2half2(h);
+}
+__device__ __forceinline__ float e8m0_scale(uint32_t byte) {
+  // 2^(e-127): the code is a binary32 exponent field; 0 is 2^-127 (subnormal), 255 NaN
+  return byte == 0xffu ? __uint_as_float(0x7fc00000u)
+                       : (byte ? __uint_as_float(byte << 23) : __uint_as_float(0x00400000u));
 }
 
 // K page tile load.  The tensor map's dimensions are ordered by increasing

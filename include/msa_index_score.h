@@ -67,7 +67,13 @@ typedef enum { MSA_LAYOUT_BBND = 0, MSA_LAYOUT_BNBD = 1, MSA_LAYOUT_TND = 2 } ms
  * query and key must be of the same FP8 type and take no scale (torch API
  * guide "CANN ops-transformer ... msa_index_score", sec. 4 and 7.2; on this
  * GPU they run on tcgen05 kind::f8f6f4 with fp32 accumulation). */
-typedef enum { MSA_F16 = 0, MSA_BF16 = 1, MSA_I8 = 2, MSA_E4M3 = 3, MSA_E5M2 = 4 } msa_dtype_t;
+typedef enum { MSA_F16 = 0, MSA_BF16 = 1, MSA_I8 = 2, MSA_E4M3 = 3, MSA_E5M2 = 4,
+               MSA_E2M1 = 5 /* FP4, two codes per byte: msa_index_score_fp4 only */ } msa_dtype_t;
+
+/* FP4 group-scale formats (MiniMax Sparse Attention notes, sec. 8.2, "FP4
+ * Indexer"): MXFP4 = E2M1 values with one E8M0 scale byte per 32 elements;
+ * NVFP4 = E2M1 values with one E4M3 scale byte per 16 elements. */
+typedef enum { MSA_FP4_MX = 0, MSA_FP4_NV = 1 } msa_fp4_format_t;
 
 /* Bits of the device error word (msa_get_device_error). */
 #define MSA_DEVERR_CU_Q        0x01  /* cu_seqlens_q[0] != 0, decreasing, cu_seqlens_q[B] != T, or a query length above a nonzero max_seqlen_q */
@@ -265,6 +271,39 @@ msa_status_t msa_index_score_topk_workspace_size(const msa_index_score_args *arg
 msa_status_t msa_index_score_topk(const msa_index_score_args *args, int32_t k, int32_t local_slot,
                                   float *out, int32_t *indices, void *workspace,
                                   size_t workspace_bytes, msa_stream_t stream);
+
+/*
+ * Block scores of an FP4 index branch (the block-scaled FP4 indexer of the
+ * MiniMax Sparse Attention notes, sec. 8.2: E2M1 values with group scales,
+ * fp32 block scores; its results approximate the real-valued index score, so
+ * top-k orders need not match a 16-bit indexer's).  Computes exactly what
+ * msa_index_score computes, on the dequantised values
+ *     q~[t, h, d] = e2m1(q) * scale(q_scale[t, h, d / G])
+ *     k~[j, hk, d] = e2m1(k) * scale(k_scale[.., d / G])   (G = 32 MX, 16 NV)
+ * with fp32 accumulation (every dequantised value is exact in the 16-bit
+ * operand type: fp16 for NVFP4, bf16 for MXFP4 with E8M0 codes 2 .. 252).
+ *
+ *   args      q_dtype = k_dtype = MSA_E2M1, args->scale = NULL.  query
+ *             [T, H_q, D/2] bytes; key_cache BBND [NP, P, H_kv, D/2], BNBD
+ *             [NP, H_kv, P, D/2] (page_stride in bytes) or TND [T2, H_kv, D/2];
+ *             element 2i of a row is the low nibble of byte i.  D = 128.
+ *   format    MSA_FP4_MX or MSA_FP4_NV.
+ *   q_scale   device bytes [T, H_q, D/G], 16-byte aligned.
+ *   k_scale   device bytes in logical page order: paged [NP, H_kv, P, D/G]
+ *             (compact, even when key_cache has a page stride), TND
+ *             [T2, H_kv, D/G]; 16-byte aligned.
+ *   out       as msa_index_score.
+ *   workspace msa_index_score_fp4_workspace_size() bytes (256-byte aligned,
+ *             caller-owned): the plan and the dequantised query.
+ *
+ * Errors as msa_index_score, plus MSA_ERR_INVALID_ARG for a bad format or a
+ * missing or misaligned scale array.  Asynchronous on `stream`.
+ */
+msa_status_t msa_index_score_fp4_workspace_size(const msa_index_score_args *args, int32_t format,
+                                                size_t *bytes);
+msa_status_t msa_index_score_fp4(const msa_index_score_args *args, int32_t format,
+                                 const uint8_t *q_scale, const uint8_t *k_scale, float *out,
+                                 void *workspace, size_t workspace_bytes, msa_stream_t stream);
 
 /* Synchronise `stream` and read the device error word left in `workspace`
  * by the last call (MSA_DEVERR_* bits; 0 = clean).  Returns MSA_OK, or

@@ -32,7 +32,7 @@ from typing import List, Optional, Sequence
 import torch
 
 __all__ = [
-    "MsaCase", "make_case", "make_fp4_case", "config", "CONFIG_NAMES", "FILL_KINDS",
+    "MsaCase", "make_case", "make_fp4_case", "to_fp4", "config", "CONFIG_NAMES", "FILL_KINDS",
 ]
 
 FILL_KINDS = ("randn", "randn01", "int_small", "int8_full", "onehot_d0",
@@ -366,6 +366,31 @@ def make_fp4_case(q_lens: Sequence[int], kv_lens: Sequence[int], *, fmt: str, H_
     else:
         k_scale = codes((int(base.key.shape[0]), H_kv, base.P, ng))
     return dataclasses.replace(base, fp4=fmt, q_scale=q_scale, k_scale=k_scale)
+
+
+def to_fp4(case: MsaCase, fmt: str, seed: Optional[int] = None) -> MsaCase:
+    """The same workload (lengths, table, layout, page order) with FP4 inputs:
+    random packed E2M1 codes in place of the query and key values and random
+    group scale bytes (see ``make_fp4_case``).  The key must be compact."""
+    if fmt not in FP4_GROUP:
+        raise ValueError(f"fp4 format {fmt!r}")
+    gen = torch.Generator().manual_seed(4321 if seed is None else int(seed))
+    D = case.D
+    kshape = tuple(case.key.shape[:-1]) + (D // 2,)
+    q = torch.randint(0, 256, (case.T, case.H_q, D // 2), generator=gen, dtype=torch.int32).to(torch.uint8)
+    k = torch.randint(0, 256, kshape, generator=gen, dtype=torch.int32).to(torch.uint8)
+    ng = D // FP4_GROUP[fmt]
+    lo, hi = FP4_SCALE_CODES[fmt]
+
+    def codes(shape):
+        return torch.randint(lo, hi + 1, shape, generator=gen, dtype=torch.int32).to(torch.uint8)
+    if case.layout == "TND":
+        k_scale = codes((kshape[0], case.H_kv, ng))
+    else:
+        k_scale = codes((kshape[0], case.H_kv, case.P, ng))
+    return dataclasses.replace(case, query=q, key=k, scale=None, fp4=fmt,
+                               q_scale=codes((case.T, case.H_q, ng)), k_scale=k_scale,
+                               name=f"{case.name}_fp4{fmt}")
 
 
 def decode_subset(case: MsaCase) -> MsaCase:

@@ -155,3 +155,23 @@ def test_python_binding_unsqueezes_3d_bbnd_key():
 ])
 def test_block_topk_host_validation(lib, H, T, MBp, MB, k, status):
     assert lib.msa_block_topk(None, H, T, MBp, MB, k, None, None) == status
+
+
+def test_fp4_host_rules(lib):
+    # E2M1 (FP4) query and key: page_stride counts bytes (D/2 per row); the
+    # output shape is the usual one; the 16-bit entry points refuse FP4 args
+    fp4 = dict(q_dtype=5, k_dtype=5, page_stride=128 * 64)
+    st, shape = _shape(lib, _args(**fp4))
+    assert st == 0 and shape == (8, 32, 16)
+    n = ctypes.c_size_t()
+    assert lib.msa_index_score_fp4_workspace_size(ctypes.byref(_args(**fp4)), 1, ctypes.byref(n)) == 0
+    plan = ctypes.c_size_t()
+    assert lib.msa_index_score_workspace_size(ctypes.byref(_args()), ctypes.byref(plan)) == 0
+    assert n.value == plan.value + 32 * 8 * 128 * 2           # + the dequantised query
+    assert lib.msa_index_score_fp4_workspace_size(ctypes.byref(_args(**fp4)), 7, ctypes.byref(n)) == 1
+    assert lib.msa_index_score_workspace_size(ctypes.byref(_args(**fp4)), ctypes.byref(n)) == 1
+    # one side FP4 only, a scale, a stride below a compact FP4 page
+    for over in (dict(q_dtype=5, k_dtype=1, page_stride=128 * 64), dict(fp4, scale=16),
+                 dict(fp4, page_stride=100)):
+        assert lib.msa_index_score_fp4_workspace_size(ctypes.byref(_args(**over)), 0,
+                                                      ctypes.byref(n)) == 1
