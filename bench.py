@@ -49,7 +49,10 @@ DEFAULT_WORKLOAD = 5
 # calls per timed pass when --steps is not given (about 0.2-0.6 s of GPU time each)
 DEFAULT_STEPS = {1: 5000, 2: 2000, 3: 300, 4: 400, 5: 30}
 DEFAULT_STEPS_DECODE_SUBSET = 5000
-SUB_WORKLOADS = [(1, False), (2, False), (3, False), (4, False), (4, True)]
+# (workload, decode subset, FP4 format): the other workloads, the int8 decode
+# subset, and FP4 inputs on the batched decode and the varlen prefill
+SUB_WORKLOADS = [(1, False, None), (2, False, None), (3, False, None), (4, False, None),
+                 (4, True, None), (2, False, "nv"), (3, False, "mx")]
 DTYPE_NAME = {torch.float16: "f16", torch.bfloat16: "bf16", torch.int8: "i8",
               torch.float8_e4m3fn: "e4m3", torch.float8_e5m2: "e5m2"}
 FP8 = {"e4m3": torch.float8_e4m3fn, "e5m2": torch.float8_e5m2}
@@ -62,7 +65,10 @@ def algorithmic_work(case):
     """FLOPs = 2*D*sum over (h,t) of visible keys; bytes = visible K once per kv head
     (+ int8 scale) + Q + the fp32 output + the table entries read."""
     D, P = case.D, case.P
-    es_k = case.key.element_size()
+    fp4 = getattr(case, "fp4", None)
+    # bytes of one key row of D values: FP4 codes are half a byte each, plus
+    # one scale byte per group of 32 (MXFP4) or 16 (NVFP4)
+    row_k = (D // 2 + D // (32 if fp4 == "mx" else 16)) if fp4 else D * case.key.element_size()
     vis_rows = 0
     k_tokens = 0
     tab = 0
@@ -78,10 +84,10 @@ def algorithmic_work(case):
         k_tokens += L
         tab += -(-L // P)
     flops = 2.0 * D * case.H_q * vis_rows
-    k_bytes = k_tokens * case.H_kv * D * es_k
+    k_bytes = k_tokens * case.H_kv * row_k
     if case.key.dtype == torch.int8:
         k_bytes += k_tokens * case.H_kv * 4
-    q_bytes = case.T * case.H_q * D * case.query.element_size()
+    q_bytes = case.T * case.H_q * (row_k if fp4 else D * case.query.element_size())
     out_bytes = case.H_q * case.T * case.MBp * 4
     total = k_bytes + q_bytes + out_bytes + 4 * tab
     return {"flops": flops, "k_bytes": k_bytes, "q_bytes": q_bytes, "out_bytes": out_bytes,
@@ -123,6 +129,8 @@ def launches_per_call(case) -> int:
     length bound puts every request on the short path, and, for int8 keys with
     a query-row group of at most 32, the short-query kernel."""
     g = case.H_q // case.H_kv
+    if getattr(case, "fp4", None):
+        return 3            # query dequantisation, plan, tile kernel
     short_ok = case.key.dtype == torch.int8 and g <= 32
     max_q = max(case.q_lens) if case.q_lens else 0
     tile = not (short_ok and max_q > 0 and max_q * g <= 32)
@@ -293,6 +301,11 @@ def make_workload(args):
                         q_len=getattr(args, "q_len", None) if args.workload == 5 else None)
     if args.decode_subset:
         case = synth.decode_subset(case)
+    if getattr(args, "fp4", None):
+        # the same workload (lengths, table, pages) with FP4 query and keys
+        if case.key.dtype == torch.int8:
+            raise SystemExit("--fp4 applies to the fp16 / bf16 workloads")
+        return synth.to_fp4(case, args.fp4)
     if args.fp8:
         # the same workload with FP8 query and keys of one type (no scale):
         # the 16-bit draws rounded to FP8
@@ -309,7 +322,8 @@ def workload_key(args) -> str:
     return (f"cfg{args.workload}" + ("_decode" if args.decode_subset else "")
             + (f"_q{q}" if q and args.workload == 5 else "")
             + (f"_{args.layout.lower()}" if args.layout else "")
-            + (f"_{args.fp8}" if args.fp8 else ""))
+            + (f"_{args.fp8}" if args.fp8 else "")
+            + (f"_fp4{args.fp4}" if getattr(args, "fp4", None) else ""))
 
 
 def default_steps(args) -> int:
@@ -366,12 +380,21 @@ def run_reference(args):
     return 0
 
 
+def dtype_name(case) -> str:
+    """The arithmetic type the path computes in."""
+    fp4 = getattr(case, "fp4", None)
+    if fp4:
+        return "e2m1 codes x group scales, dequantised to " + ("f16" if fp4 == "nv" else "bf16")
+    return DTYPE_NAME[case.query.dtype] if case.key.dtype != torch.int8 else "f16xi8"
+
+
 def config_block(case, workload):
     kb = algorithmic_work(case)["k_bytes"]
     total_in = kb + case.query.numel() * case.query.element_size()
     return {"workload": f"{workload}:{case.name}", "B": case.B, "T": case.T,
             "H_q": case.H_q, "H_kv": case.H_kv, "D": case.D, "P": case.P, "MB": case.MB,
-            "layout": case.layout, "k_dtype": DTYPE_NAME[case.key.dtype],
+            "layout": case.layout,
+            "k_dtype": ("fp4" + case.fp4) if getattr(case, "fp4", None) else DTYPE_NAME[case.key.dtype],
             "sparse_mode": case.sparse_mode, "init_blocks": case.init_blocks,
             "local_blocks": case.local_blocks,
             "l2": (f"inputs larger than L2 (no flush): K cache {kb / 1e6:.0f} MB > 129 MB"
@@ -404,6 +427,9 @@ def roofline_of(case, work, kern_ms, peaks, traffic):
                 "frac": tflops_kernel / pk, "traffic": traffic,
                 "peak_source": peaks["source"] + " bf16_tflops (burst)",
                 "frac_of_sustained": tflops_kernel / peaks["bf16_tflops_sustained"]}
+    if getattr(case, "fp4", None) and roof["bound"] == "tensor":
+        roof["peak_source"] += ("; FP4 operands are dequantised to 16-bit and multiplied on the "
+                                "16-bit tensor path, whose peak applies")
     roof["kernel"] = dominant_kernel(case)
     roof["kernel_us"] = kern_ms * 1e3
     roof["algorithmic_bytes"] = work["bytes"]
@@ -519,7 +545,7 @@ def run_ours(args):
         "metric": METRIC, "value": head["value"], "unit": "us/call", "n_gpus": ws,
         "steps": steps, "warmup": args.warmup, "ms_per_step": head["ms_per_step"],
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
-        "dtype": DTYPE_NAME[case.query.dtype] if case.key.dtype != torch.int8 else "f16xi8",
+        "dtype": dtype_name(case),
         "data": "synthetic (seeded; shapes and length mix of the workload recipe)",
         "config": config_block(case, key),
         "tflops": head["tflops"], "k_cache_gbs": head["k_cache_gbs"],
@@ -537,11 +563,12 @@ def run_ours(args):
 
     # the other workloads (and the int8 decode subset), each measured the same way
     if not args.no_sub and args.workload == DEFAULT_WORKLOAD and not args.decode_subset \
-            and args.layout is None and args.fp8 is None and getattr(args, "q_len", None) is None:
+            and args.layout is None and args.fp8 is None and args.fp4 is None \
+            and getattr(args, "q_len", None) is None:
         subs = []
-        for n, dsub in SUB_WORKLOADS:
+        for n, dsub, fp4 in SUB_WORKLOADS:
             sa = argparse.Namespace(workload=n, decode_subset=dsub, layout=None, fp8=None,
-                                    q_len=None, steps=None)
+                                    fp4=fp4, q_len=None, steps=None)
             scase = make_workload(sa)
             skey = workload_key(sa)
             rec, sprep = measure(scase, skey, default_steps(sa), args.warmup, device, stream,
@@ -570,7 +597,7 @@ def fused_select_run(case, prep, device, stream, steps, head, topk):
     slot on), with and without storing the scores: microseconds per call of
     the whole op, against one score call plus the unfused top-k over its
     scores."""
-    if 32 % (case.H_q // case.H_kv):
+    if 32 % (case.H_q // case.H_kv) or getattr(case, "fp4", None):
         return None
     res = {"k": 16, "local_slot": True, "groups": case.H_kv,
            "rows": case.T * case.H_kv, "unfused_us": head["value"] + topk["us_per_call"]}
@@ -622,8 +649,8 @@ def e2e_run(case, device, stream, args, steps=None):
     import block_score_gb300 as bs
     host = {}
     for name in ("query", "block_table", "cu_seqlens_q", "kv_len", "cu_seqlens_k",
-                 "start_loc", "scale"):
-        t = getattr(case, name)
+                 "start_loc", "scale", "q_scale", "k_scale"):
+        t = getattr(case, name, None)
         host[name] = None if t is None else t.contiguous().pin_memory()
     key = case.key
     base = key
@@ -640,7 +667,9 @@ def e2e_run(case, device, stream, args, steps=None):
                        sparse_mode=case.sparse_mode, init_blocks=case.init_blocks,
                        local_blocks=case.local_blocks,
                        max_blocks=case.MB if case.layout == "TND" else None,
-                       max_seqlen_q=max(case.q_lens) if case.q_lens else None)
+                       max_seqlen_q=max(case.q_lens) if case.q_lens else None,
+                       **(dict(fp4=case.fp4, q_scale=dev["q_scale"], k_scale=dev["k_scale"])
+                          if getattr(case, "fp4", None) else {}))
     out_host = torch.empty(prep.shape, dtype=torch.float32, pin_memory=True)
     h2d = sum(v.numel() * v.element_size() for v in host.values() if v is not None)
     h2d += host_key_base.numel() * host_key_base.element_size()
@@ -683,6 +712,8 @@ def main(argv=None):
                     help="draw the workload's keys in another layout (same lengths)")
     ap.add_argument("--fp8", choices=sorted(FP8), default=None,
                     help="run the (fp16 / bf16) workload with FP8 query and keys")
+    ap.add_argument("--fp4", choices=["mx", "nv"], default=None,
+                    help="run the (fp16 / bf16) workload with FP4 query and keys (MXFP4 / NVFP4)")
     ap.add_argument("--q-len", type=int, default=None,
                     help="workload 5 only: its last Q_LEN query positions (profiler captures)")
     ap.add_argument("--no-sub", action="store_true",

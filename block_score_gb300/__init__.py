@@ -103,6 +103,8 @@ def load_library():
     lib.msa_index_score_topk.argtypes = [P, ctypes.c_int32, ctypes.c_int32, vp, vp, vp, sz, vp]
     lib.msa_index_score_fp4_workspace_size.argtypes = [P, ctypes.c_int32, ctypes.POINTER(sz)]
     lib.msa_index_score_fp4.argtypes = [P, ctypes.c_int32, vp, vp, vp, vp, sz, vp]
+    lib.msa_index_score_fp4_plan.argtypes = [P, ctypes.c_int32, vp, vp, sz, vp]
+    lib.msa_index_score_fp4_run.argtypes = [P, ctypes.c_int32, vp, vp, vp, sz, vp]
     lib.msa_set_watchdog.argtypes = [ctypes.c_uint64, ctypes.c_int32]
     lib.msa_set_watchdog.restype = ctypes.c_int
     lib.msa_status_string.restype = ctypes.c_char_p
@@ -112,7 +114,8 @@ def load_library():
                  "msa_index_score", "msa_index_score_plan", "msa_index_score_run",
                  "msa_get_device_error", "msa_index_score_noalloc", "msa_noalloc_device_error",
                  "msa_block_topk", "msa_index_score_topk_workspace_size", "msa_index_score_topk",
-                 "msa_index_score_fp4_workspace_size", "msa_index_score_fp4"):
+                 "msa_index_score_fp4_workspace_size", "msa_index_score_fp4",
+                 "msa_index_score_fp4_plan", "msa_index_score_fp4_run"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -419,11 +422,22 @@ class Prepared:
         return self.out
 
     def plan(self, stream=None):
+        if self.fp4 is not None:
+            _check(load_library().msa_index_score_fp4_plan(
+                ctypes.byref(self.call.args), FP4_FORMATS[self.fp4], self.q_scale.data_ptr(),
+                self.workspace.data_ptr(), self.ws_bytes, _stream_handle(stream)))
+            return
         _check(load_library().msa_index_score_plan(ctypes.byref(self.call.args),
                                                    self.workspace.data_ptr(), self.ws_bytes,
                                                    _stream_handle(stream)))
 
     def run(self, stream=None) -> torch.Tensor:
+        if self.fp4 is not None:
+            _check(load_library().msa_index_score_fp4_run(
+                ctypes.byref(self.call.args), FP4_FORMATS[self.fp4], self.k_scale.data_ptr(),
+                self.out.data_ptr(), self.workspace.data_ptr(), self.ws_bytes,
+                _stream_handle(stream)))
+            return self.out
         _check(load_library().msa_index_score_run(ctypes.byref(self.call.args),
                                                   self.out.data_ptr(), self.workspace.data_ptr(),
                                                   self.ws_bytes, _stream_handle(stream)))

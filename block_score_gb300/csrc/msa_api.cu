@@ -572,41 +572,89 @@ msa_status_t msa_index_score_fp4_workspace_size(const msa_index_score_args* args
   return MSA_OK;
 }
 
-msa_status_t msa_index_score_fp4(const msa_index_score_args* args, int32_t format,
-                                 const uint8_t* q_scale, const uint8_t* k_scale, float* out,
-                                 void* workspace, size_t workspace_bytes, msa_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// Shared checks and parameters of the FP4 entry points.
+msa_status_t prepare_fp4(const msa_index_score_args* args, int32_t format, const uint8_t* q_scale,
+                         const uint8_t* k_scale, float* out, bool need_out, void* workspace,
+                         size_t workspace_bytes, msa::Params& p, bool& empty, void** q16) {
   g_msg[0] = 0;
   msa_status_t st = validate(args, true);
   if (st != MSA_OK) return st;
   if (format != MSA_FP4_MX && format != MSA_FP4_NV)
     return fail(MSA_ERR_INVALID_ARG, "format must be MSA_FP4_MX or MSA_FP4_NV");
-  if (args->T == 0 || args->B == 0) return MSA_OK;
-  if (!q_scale || !k_scale) return fail(MSA_ERR_INVALID_ARG, "q_scale and k_scale are required");
-  if (!aligned(q_scale, 16) || !aligned(k_scale, 16))
-    return fail(MSA_ERR_INVALID_ARG, "q_scale and k_scale must be 16-byte aligned");
-  if (!out || !aligned(out, 16)) return fail(MSA_ERR_INVALID_ARG, "out must be a 16-byte aligned pointer");
+  empty = args->T == 0 || args->B == 0;
+  if (empty) return MSA_OK;
+  if (q_scale && !aligned(q_scale, 16)) return fail(MSA_ERR_INVALID_ARG, "q_scale must be 16-byte aligned");
+  if (k_scale && !aligned(k_scale, 16)) return fail(MSA_ERR_INVALID_ARG, "k_scale must be 16-byte aligned");
+  if (need_out && (!out || !aligned(out, 16)))
+    return fail(MSA_ERR_INVALID_ARG, "out must be a 16-byte aligned pointer");
   const size_t plan_bytes = msa::workspace_bytes_for(args->B);
   if (!workspace) return fail(MSA_ERR_WORKSPACE, "workspace is NULL");
   if (!aligned(workspace, 256)) return fail(MSA_ERR_WORKSPACE, "workspace must be 256-byte aligned");
   if (workspace_bytes < plan_bytes + fp4_query_bytes(args))
     return fail(MSA_ERR_WORKSPACE, "workspace needs %zu bytes, got %zu",
                 plan_bytes + fp4_query_bytes(args), workspace_bytes);
-  const bool nv = format == MSA_FP4_NV;
-  msa::Params p;
   if ((st = fill_params(args, out, workspace, p)) != MSA_OK) return st;
   p.k_scale8 = k_scale;
-  p.fp4_ng = args->D / (nv ? 16 : 32);
-  void* q16 = static_cast<uint8_t*>(workspace) + plan_bytes;
+  p.fp4_ng = args->D / (format == MSA_FP4_NV ? 16 : 32);
+  *q16 = static_cast<uint8_t*>(workspace) + plan_bytes;
+  return MSA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+msa_status_t msa_index_score_fp4_plan(const msa_index_score_args* args, int32_t format,
+                                      const uint8_t* q_scale, void* workspace,
+                                      size_t workspace_bytes, msa_stream_t stream) {
+  msa::Params p;
+  bool empty = false;
+  void* q16 = nullptr;
+  msa_status_t st = prepare_fp4(args, format, q_scale, nullptr, nullptr, false, workspace,
+                                workspace_bytes, p, empty, &q16);
+  if (st != MSA_OK || empty) return st;
+  if (!q_scale) return fail(MSA_ERR_INVALID_ARG, "q_scale is required");
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = msa::launch_fp4_dequant_query(static_cast<const uint8_t*>(args->query), q_scale,
-                                                args->T * (int64_t)args->H_q, nv, q16, s);
+                                                args->T * (int64_t)args->H_q,
+                                                format == MSA_FP4_NV, q16, s);
   if (e != cudaSuccess) return cuda_fail(e, "FP4 query dequantisation launch");
-  if ((st = launch_plan_checked(p, s)) != MSA_OK) return st;
+  return launch_plan_checked(p, s);
+}
+
+msa_status_t msa_index_score_fp4_run(const msa_index_score_args* args, int32_t format,
+                                     const uint8_t* k_scale, float* out, void* workspace,
+                                     size_t workspace_bytes, msa_stream_t stream) {
+  msa::Params p;
+  bool empty = false;
+  void* q16 = nullptr;
+  msa_status_t st = prepare_fp4(args, format, nullptr, k_scale, out, true, workspace,
+                                workspace_bytes, p, empty, &q16);
+  if (st != MSA_OK || empty) return st;
+  if (!k_scale) return fail(MSA_ERR_INVALID_ARG, "k_scale is required");
+  const bool nv = format == MSA_FP4_NV;
   CUtensorMap tq, tk;
   if ((st = make_maps(args, p, &tq, &tk, nullptr, nullptr, q16, nv)) != MSA_OK) return st;
-  e = msa::launch_score_fp4(&tq, &tk, p, nv, s);
+  cudaError_t e = msa::launch_score_fp4(&tq, &tk, p, nv, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "score kernel launch");
   return MSA_OK;
+}
+
+msa_status_t msa_index_score_fp4(const msa_index_score_args* args, int32_t format,
+                                 const uint8_t* q_scale, const uint8_t* k_scale, float* out,
+                                 void* workspace, size_t workspace_bytes, msa_stream_t stream) {
+  g_msg[0] = 0;
+  if (args && args->T > 0 && args->B > 0 && (!q_scale || !k_scale))
+    return fail(MSA_ERR_INVALID_ARG, "q_scale and k_scale are required");
+  if (args && args->T > 0 && args->B > 0 && (!out || !aligned(out, 16)))
+    return fail(MSA_ERR_INVALID_ARG, "out must be a 16-byte aligned pointer");
+  msa_status_t st = msa_index_score_fp4_plan(args, format, q_scale, workspace, workspace_bytes, stream);
+  if (st != MSA_OK) return st;
+  return msa_index_score_fp4_run(args, format, k_scale, out, workspace, workspace_bytes, stream);
 }
 
 msa_status_t msa_block_topk(const float* score, int32_t H, int64_t T, int32_t MBp, int32_t MB,

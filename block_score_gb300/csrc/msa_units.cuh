@@ -46,42 +46,72 @@ __device__ __forceinline__ void int8x4_to_half4(uint32_t w, uint32_t& lo, uint32
 }
 
 // ------------------------------------------------------------- FP4 (E2M1) --
-// An E2M1 code (sign, 2 exponent bits with bias 1, 1 mantissa bit) placed so
-// that its exponent and mantissa bits land at the bottom of a binary16
-// exponent field reads as 2^-14 times its value (exponent 0 reads as a
-// binary16 subnormal, which is again 2^-14 times the E2M1 subnormal m/2), so
-// one exact multiplication by 2^14 gives the value.  The same placement in
-// binary32 reads as 2^-126 times the value.
+// Codes c0..c7 of a 32-bit word sit in its nibbles 0..7 (element 2i in the
+// low nibble of byte i).  The 3 magnitude bits of four codes (one 16-bit half
+// of the word, masked with 0x7777) are exactly four byte selectors of a
+// byte permute, so one prmt looks four magnitudes up in an 8-entry table; the
+// sign bits (bits 4n+3) are the top bits of the bytes of w << 4 (even codes)
+// and of w (odd codes), which prmt's sign-replicating selectors spread into
+// whole bytes.
 
-// 8 E2M1 codes (a 32-bit word, element 2i in the low nibble of byte i) times
-// an NVFP4 group scale (E4M3, as binary16) -> 8 binary16 values.  Exact: every
-// product of an E2M1 value and an E4M3 value is a binary16 number.
+// prmt with the default mode: a selector nibble with its top bit set
+// replicates the sign bit of the selected byte.
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t r;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
+  return r;
+}
+
+// 0x00 / 0xff per code: the signs of codes 4h .. 4h+3 of w
+__device__ __forceinline__ uint32_t fp4_sign_bytes(uint32_t w, int h) {
+  return prmt(w << 4, w, h ? 0xFBEAu : 0xD9C8u);
+}
+
+// 8 E2M1 codes times an NVFP4 group scale (E4M3, as binary16) -> 8 binary16
+// values: each code becomes the E4M3 byte of the same value (magnitudes 0,
+// 0.5, 1, 1.5, 2, 3, 4, 6 are 0x00 0x30 0x38 0x3c 0x40 0x44 0x48 0x4c), the
+// hardware converts E4M3 pairs to binary16, one multiplication applies the
+// scale.  Exact: every product of an E2M1 value and an E4M3 value is a
+// binary16 number.
 __device__ __forceinline__ uint4 fp4x8_to_f16(uint32_t w, __half2 scale2) {
-  const __half2 two14 = __half2half2(__ushort_as_half((unsigned short)0x7400));
   uint32_t r[4];
 #pragma unroll
-  for (int b = 0; b < 4; ++b) {
-    const uint32_t byte = (w >> (8 * b)) & 0xffu;
-    const uint32_t y = (byte & 0x0fu) | ((byte & 0xf0u) << 12);   // nibbles at bits 0 and 16
-    const uint32_t h = ((y & 0x00070007u) << 9) | ((y & 0x00080008u) << 12);
-    const __half2 v = __hmul2(__hmul2(*reinterpret_cast<const __half2*>(&h), two14), scale2);
-    r[b] = *reinterpret_cast<const uint32_t*>(&v);
+  for (int h = 0; h < 2; ++h) {
+    const uint32_t mag = prmt(0x3C383000u, 0x4C484440u, (w >> (16 * h)) & 0x7777u);
+    const uint32_t e4 = mag | (fp4_sign_bytes(w, h) & 0x80808080u);
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      const __half2_raw hr =
+          __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(e4 >> (16 * q)), __NV_E4M3);
+      const __half2 v = __hmul2(__half2(hr), scale2);
+      r[2 * h + q] = *reinterpret_cast<const uint32_t*>(&v);
+    }
   }
   return make_uint4(r[0], r[1], r[2], r[3]);
 }
 
-// 8 E2M1 codes times an MXFP4 group scale 2^(e-127) (E8M0 code e, given as
-// binary32) -> 8 bfloat16 values.  Exact while the products stay in bfloat16's
-// normal range (E8M0 codes 2 .. 252).
-__device__ __forceinline__ uint4 fp4x8_to_bf16(uint32_t w, float scale) {
+// 8 E2M1 codes times an MXFP4 group scale 2^(e-127) (E8M0 code e, as a
+// bfloat16 power of two) -> 8 bfloat16 values: two table lookups give the
+// high and low bytes of each magnitude's bfloat16 pattern (0.5 0x3f00, 1
+// 0x3f80, 1.5 0x3fc0, 2 0x4000, 3 0x4040, 4 0x4080, 6 0x40c0), two permutes
+// interleave them into pairs, the sign goes to bit 15, one multiplication
+// applies the scale.  Exact while the products stay in bfloat16's normal
+// range (E8M0 codes 2 .. 252).
+__device__ __forceinline__ uint4 fp4x8_to_bf16(uint32_t w, __nv_bfloat162 scale2) {
   uint32_t r[4];
 #pragma unroll
-  for (int b = 0; b < 4; ++b) {
-    const uint32_t lo = (w >> (8 * b)) & 0x0fu, hi = (w >> (8 * b + 4)) & 0x0fu;
-    const float flo = __uint_as_float(((lo & 7u) << 22) | ((lo & 8u) << 28)) * 0x1p126f * scale;
-    const float fhi = __uint_as_float(((hi & 7u) << 22) | ((hi & 8u) << 28)) * 0x1p126f * scale;
-    const __nv_bfloat162 v = __floats2bfloat162_rn(flo, fhi);
-    r[b] = *reinterpret_cast<const uint32_t*>(&v);
+  for (int h = 0; h < 2; ++h) {
+    const uint32_t sel = (w >> (16 * h)) & 0x7777u;
+    const uint32_t hb = prmt(0x3F3F3F00u, 0x40404040u, sel);
+    const uint32_t lb = prmt(0xC0800000u, 0xC0804000u, sel);
+    const uint32_t sg = fp4_sign_bytes(w, h);
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      const uint32_t bits = prmt(lb, hb, q ? 0x7362u : 0x5140u) |
+                            (prmt(sg, sg, q ? 0x3020u : 0x1000u) & 0x80008000u);
+      const __nv_bfloat162 v = __hmul2(*reinterpret_cast<const __nv_bfloat162*>(&bits), scale2);
+      r[2 * h + q] = *reinterpret_cast<const uint32_t*>(&v);
+    }
   }
   return make_uint4(r[0], r[1], r[2], r[3]);
 }
@@ -91,10 +121,11 @@ __device__ __forceinline__ __half2 e4m3_scale2(uint32_t byte) {
   const __half h = __half(__nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)byte, __NV_E4M3));
   return __half2half2(h);
 }
-__device__ __forceinline__ float e8m0_scale(uint32_t byte) {
-  // 2^(e-127): the code is a binary32 exponent field; 0 is 2^-127 (subnormal), 255 NaN
-  return byte == 0xffu ? __uint_as_float(0x7fc00000u)
-                       : (byte ? __uint_as_float(byte << 23) : __uint_as_float(0x00400000u));
+__device__ __forceinline__ __nv_bfloat162 e8m0_scale2(uint32_t byte) {
+  // 2^(e-127): the code is a bfloat16 exponent field; 0 is 2^-127 (subnormal), 255 NaN
+  const uint32_t b = byte == 0xffu ? 0x7fc0u : (byte ? (byte << 7) : 0x0040u);
+  const uint32_t b2 = b | (b << 16);
+  return *reinterpret_cast<const __nv_bfloat162*>(&b2);
 }
 
 // K page tile load.  The tensor map's dimensions are ordered by increasing

@@ -305,6 +305,16 @@ msa_status_t msa_index_score_fp4(const msa_index_score_args *args, int32_t forma
                                  const uint8_t *q_scale, const uint8_t *k_scale, float *out,
                                  void *workspace, size_t workspace_bytes, msa_stream_t stream);
 
+/* The two halves of msa_index_score_fp4, on the same stream and workspace:
+ * _plan dequantises the query into the workspace and writes the work plan;
+ * _run launches the tile kernel that reads the key cache and writes `out`. */
+msa_status_t msa_index_score_fp4_plan(const msa_index_score_args *args, int32_t format,
+                                      const uint8_t *q_scale, void *workspace,
+                                      size_t workspace_bytes, msa_stream_t stream);
+msa_status_t msa_index_score_fp4_run(const msa_index_score_args *args, int32_t format,
+                                     const uint8_t *k_scale, float *out, void *workspace,
+                                     size_t workspace_bytes, msa_stream_t stream);
+
 /* Synchronise `stream` and read the device error word left in `workspace`
  * by the last call (MSA_DEVERR_* bits; 0 = clean).  Returns MSA_OK, or
  * MSA_ERR_CUDA if the copy fails. */
