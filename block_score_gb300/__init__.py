@@ -52,6 +52,12 @@ class MsaError(RuntimeError):
         self.status = status
 
 
+class _SparseArgs(ctypes.Structure):
+    """msa_sparse_attention_args of the C header."""
+    _fields_ = [("value_cache", ctypes.c_void_p), ("selection", ctypes.c_void_p),
+                ("k", ctypes.c_int32), ("sm_scale", ctypes.c_float)]
+
+
 class _Args(ctypes.Structure):
     # field order and types follow msa_index_score_args in include/msa_index_score.h
     _fields_ = [
@@ -104,6 +110,9 @@ def load_library():
     lib.msa_index_score_fp4_workspace_size.argtypes = [P, ctypes.c_int32, ctypes.POINTER(sz)]
     lib.msa_index_score_fp4.argtypes = [P, ctypes.c_int32, vp, vp, vp, vp, sz, vp]
     lib.msa_index_score_fp4_plan.argtypes = [P, ctypes.c_int32, vp, vp, sz, vp]
+    SA = ctypes.POINTER(_SparseArgs)
+    lib.msa_sparse_attention_workspace_size.argtypes = [P, SA, ctypes.POINTER(sz)]
+    lib.msa_sparse_attention.argtypes = [P, SA, vp, vp, vp, sz, vp]
     lib.msa_index_score_fp4_run.argtypes = [P, ctypes.c_int32, vp, vp, vp, sz, vp]
     lib.msa_set_watchdog.argtypes = [ctypes.c_uint64, ctypes.c_int32]
     lib.msa_set_watchdog.restype = ctypes.c_int
@@ -115,7 +124,8 @@ def load_library():
                  "msa_get_device_error", "msa_index_score_noalloc", "msa_noalloc_device_error",
                  "msa_block_topk", "msa_index_score_topk_workspace_size", "msa_index_score_topk",
                  "msa_index_score_fp4_workspace_size", "msa_index_score_fp4",
-                 "msa_index_score_fp4_plan", "msa_index_score_fp4_run"):
+                 "msa_index_score_fp4_plan", "msa_index_score_fp4_run",
+                 "msa_sparse_attention_workspace_size", "msa_sparse_attention"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -478,6 +488,48 @@ class Prepared:
             self.out.data_ptr() if scores else None, indices.data_ptr(), workspace.data_ptr(),
             workspace.numel() * workspace.element_size(), _stream_handle(stream)))
         return indices
+
+    def sparse_attention(self, value: torch.Tensor, selection: torch.Tensor,
+                         sm_scale: float = 0.0, out: Optional[torch.Tensor] = None,
+                         lse: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                         stream=None):
+        """The sparse main branch over the selected blocks (see
+        ``msa_sparse_attention`` in the C header): this object's query and key
+        cache are the main branch's; ``value`` has the key cache's layout,
+        shape, dtype and strides; ``selection`` is int32 ``[T, H_kv, k]``.
+        Returns ``(out [T, H_q, D] fp32, lse [T, H_q] fp32)``."""
+        key = self.call.key
+        if (tuple(value.shape) != tuple(key.shape) or value.stride() != key.stride()
+                or value.dtype != key.dtype or not value.is_cuda):
+            raise ValueError("value must match the key cache's shape, strides and dtype")
+        if selection.dtype != torch.int32 or selection.dim() != 3 or not selection.is_contiguous():
+            raise ValueError("selection must be a contiguous int32 tensor [T, H_kv, k]")
+        T, H_q = int(self.call.args.T), int(self.call.args.H_q)
+        D = int(self.call.args.D)
+        sa = _SparseArgs()
+        sa.value_cache = value.data_ptr()
+        sa.selection = selection.data_ptr()
+        sa.k = int(selection.shape[2])
+        sa.sm_scale = float(sm_scale)
+        n = ctypes.c_size_t()
+        _check(load_library().msa_sparse_attention_workspace_size(
+            ctypes.byref(self.call.args), ctypes.byref(sa), ctypes.byref(n)))
+        if workspace is None or workspace.numel() * workspace.element_size() < n.value:
+            workspace = torch.empty(n.value, dtype=torch.uint8, device=value.device)
+        self.sparse_workspace = workspace
+        if out is None:
+            out = torch.empty((T, H_q, D), dtype=torch.float32, device=value.device)
+        if lse is None:
+            lse = torch.empty((T, H_q), dtype=torch.float32, device=value.device)
+        _check(load_library().msa_sparse_attention(
+            ctypes.byref(self.call.args), ctypes.byref(sa), out.data_ptr(), lse.data_ptr(),
+            workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+            _stream_handle(stream)))
+        return out, lse
+
+    def sparse_device_error(self, stream=None) -> int:
+        """Device error bits of the last ``sparse_attention`` call."""
+        return msa_get_device_error(self.sparse_workspace, stream)
 
     def select_device_error(self, stream=None) -> int:
         """Device error bits of the last ``topk`` call (its workspace holds them)."""

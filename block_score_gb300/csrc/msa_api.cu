@@ -6,6 +6,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <cmath>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -655,6 +656,112 @@ msa_status_t msa_index_score_fp4(const msa_index_score_args* args, int32_t forma
   msa_status_t st = msa_index_score_fp4_plan(args, format, q_scale, workspace, workspace_bytes, stream);
   if (st != MSA_OK) return st;
   return msa_index_score_fp4_run(args, format, k_scale, out, workspace, workspace_bytes, stream);
+}
+
+}  // extern "C"
+
+namespace {
+
+// Workspace of a sparse-attention call, each array 256-byte aligned.
+struct SparseLayout {
+  size_t header, cnt, row_ptr, cursor, unit_ptr, qidx, units, o_part, lse_part, bytes;
+  int64_t rows, entries;
+};
+
+size_t up256(size_t x) { return (x + 255) / 256 * 256; }
+
+SparseLayout sparse_layout(const msa_index_score_args* a, int k) {
+  SparseLayout l;
+  l.rows = (int64_t)a->H_kv * a->B * a->MB;
+  l.entries = a->T * (int64_t)a->H_kv * k;
+  size_t off = 0;
+  l.header = off;   off += 256;
+  l.cnt = off;      off += up256(4 * (size_t)l.rows);
+  l.row_ptr = off;  off += up256(4 * (size_t)(l.rows + 1));
+  l.cursor = off;   off += up256(4 * (size_t)l.rows);
+  l.unit_ptr = off; off += up256(4 * (size_t)(l.rows + 1));
+  l.qidx = off;     off += up256(4 * (size_t)l.entries);
+  l.units = off;    off += up256(16 * (size_t)l.entries);
+  l.o_part = off;   off += up256(4 * (size_t)a->T * a->H_q * k * a->D);
+  l.lse_part = off; off += up256(4 * (size_t)a->T * a->H_q * k);
+  l.bytes = off;
+  return l;
+}
+
+msa_status_t validate_sparse(const msa_index_score_args* a, const msa_sparse_attention_args* sa) {
+  msa_status_t st = validate(a);
+  if (st != MSA_OK) return st;
+  if (!sa) return fail(MSA_ERR_INVALID_ARG, "sparse attention args are NULL");
+  if (a->q_dtype != MSA_F16 && a->q_dtype != MSA_BF16)
+    return fail(MSA_ERR_INVALID_ARG, "sparse attention takes fp16 or bf16 query, keys and values");
+  if (sa->k < 1 || sa->k > 32) return fail(MSA_ERR_INVALID_ARG, "k must be in [1, 32]");
+  if (!(sa->sm_scale >= 0.f)) return fail(MSA_ERR_INVALID_ARG, "sm_scale must be >= 0 (0: 1/sqrt(D))");
+  if (a->T > 0 && a->B > 0) {
+    if (!sa->value_cache || !sa->selection)
+      return fail(MSA_ERR_INVALID_ARG, "value_cache and selection are required");
+    if (!aligned(sa->value_cache, 16)) return fail(MSA_ERR_INVALID_ARG, "value_cache must be 16-byte aligned");
+    if (!aligned(sa->selection, 4)) return fail(MSA_ERR_INVALID_ARG, "selection must be 4-byte aligned");
+  }
+  return MSA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+msa_status_t msa_sparse_attention_workspace_size(const msa_index_score_args* args,
+                                                 const msa_sparse_attention_args* sa,
+                                                 size_t* bytes) {
+  msa_status_t st = validate_sparse(args, sa);
+  if (st != MSA_OK) return st;
+  if (!bytes) return fail(MSA_ERR_INVALID_ARG, "bytes is NULL");
+  *bytes = sparse_layout(args, sa->k).bytes;
+  return MSA_OK;
+}
+
+msa_status_t msa_sparse_attention(const msa_index_score_args* args,
+                                  const msa_sparse_attention_args* sa, float* out, float* lse,
+                                  void* workspace, size_t workspace_bytes, msa_stream_t stream) {
+  g_msg[0] = 0;
+  msa_status_t st = validate_sparse(args, sa);
+  if (st != MSA_OK) return st;
+  if (args->T == 0 || args->B == 0) return MSA_OK;
+  if (!out || !aligned(out, 16)) return fail(MSA_ERR_INVALID_ARG, "out must be a 16-byte aligned pointer");
+  if (lse && !aligned(lse, 4)) return fail(MSA_ERR_INVALID_ARG, "lse must be 4-byte aligned");
+  const SparseLayout lo = sparse_layout(args, sa->k);
+  if (!workspace) return fail(MSA_ERR_WORKSPACE, "workspace is NULL");
+  if (!aligned(workspace, 256)) return fail(MSA_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+  if (workspace_bytes < lo.bytes)
+    return fail(MSA_ERR_WORKSPACE, "workspace needs %zu bytes, got %zu", lo.bytes, workspace_bytes);
+  if (lo.entries > 0x7fffffffLL) return fail(MSA_ERR_UNSUPPORTED, "T * H_kv * k too large");
+  msa::SparseParams sp;
+  if ((st = fill_params(args, nullptr, workspace, sp.p)) != MSA_OK) return st;
+  uint8_t* w = static_cast<uint8_t*>(workspace);
+  sp.query = args->query;
+  sp.sel = sa->selection;
+  sp.k = sa->k;
+  sp.qpu = msa::kTileRows / sp.p.g;
+  sp.sm_scale = sa->sm_scale > 0.f ? sa->sm_scale : 1.0f / sqrtf((float)args->D);
+  sp.pad_ = 0;
+  sp.rows = lo.rows;
+  sp.cnt = reinterpret_cast<int32_t*>(w + lo.cnt);
+  sp.row_ptr = reinterpret_cast<int32_t*>(w + lo.row_ptr);
+  sp.cursor = reinterpret_cast<int32_t*>(w + lo.cursor);
+  sp.unit_ptr = reinterpret_cast<int32_t*>(w + lo.unit_ptr);
+  sp.qidx = reinterpret_cast<int32_t*>(w + lo.qidx);
+  sp.units = reinterpret_cast<int4*>(w + lo.units);
+  sp.o_part = reinterpret_cast<float*>(w + lo.o_part);
+  sp.lse_part = reinterpret_cast<float*>(w + lo.lse_part);
+  // K and V pages through the key cache's tensor-map recipe
+  CUtensorMap tq, tk, tv;
+  if ((st = make_maps(args, sp.p, &tq, &tk, nullptr, nullptr)) != MSA_OK) return st;
+  msa_index_score_args va = *args;
+  va.key_cache = sa->value_cache;
+  if ((st = make_maps(&va, sp.p, &tq, &tv, nullptr, nullptr)) != MSA_OK) return st;
+  cudaError_t e = msa::launch_sparse_attention(&tk, &tv, sp, args->q_dtype == MSA_BF16, out, lse,
+                                               reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "sparse attention launch");
+  return MSA_OK;
 }
 
 msa_status_t msa_block_topk(const float* score, int32_t H, int64_t T, int32_t MBp, int32_t MB,

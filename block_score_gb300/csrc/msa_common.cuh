@@ -18,6 +18,7 @@ constexpr int kErrKvLen = 0x02;
 constexpr int kErrCuK = 0x04;
 constexpr int kErrBlockTable = 0x08;
 constexpr int kErrTimeout = 0x10;
+constexpr int kErrSelection = 0x20;   // a selection row out of range, repeated or not ascending
 
 // Requests are split into two classes, each consumed by its own kernel:
 //   class 0 ("tile" class): query tiles of floor(128/g) positions x g heads,
@@ -170,6 +171,31 @@ __device__ inline ReqScratch read_request(const Params& p, int b, int& err) {
 
 // Record the message returned by msa_last_error_message() on this host thread.
 void set_last_error_message(const char* msg);
+
+// Sparse main-branch attention (msa_sparse_attention): the block-score call's
+// parameters for the query, the key / value layout and the request arrays, plus
+// the selection and the workspace arrays of the CSR build and the partials.
+struct SparseParams {
+  Params p;                // p.ws: the workspace header
+  const void* query;       // [T, H_q, D] fp16 / bf16
+  const int32_t* sel;      // [T, H_kv, k] logical blocks, ascending, -1 tail
+  int32_t k;
+  int32_t qpu;             // queries per unit: floor(128 / g)
+  float sm_scale;
+  int32_t pad_;
+  int64_t rows;            // block -> query lists: H_kv * B * MB
+  int32_t* cnt;            // [rows] list lengths
+  int32_t* row_ptr;        // [rows + 1]
+  int32_t* cursor;         // [rows] scatter positions
+  int32_t* unit_ptr;       // [rows + 1] first unit of each list
+  int32_t* qidx;           // [T * H_kv * k] token * k + slot, grouped by list
+  int4* units;             // [T * H_kv * k] {list, first entry, entries, 0}
+  float* o_part;           // [T, H_q, k, D] per-block outputs, normalised
+  float* lse_part;         // [T, H_q, k] per-block natural log-sum-exp
+};
+
+cudaError_t launch_sparse_attention(const void* tm_k, const void* tm_v, const SparseParams& sp,
+                                    bool bf16, float* out, float* lse, cudaStream_t s);
 
 // Unique id (+1) of the CUDA context current on this host thread, 0 if there
 // is none or the driver cannot say.  Per-device host caches are keyed by it:

@@ -81,6 +81,7 @@ typedef enum { MSA_FP4_MX = 0, MSA_FP4_NV = 1 } msa_fp4_format_t;
 #define MSA_DEVERR_CU_K        0x04  /* TND: cu_seqlens_k[0] != 0, decreasing, or beyond T2 */
 #define MSA_DEVERR_BLOCK_TABLE 0x08  /* a block_table entry that is read lies outside [0, NP) */
 #define MSA_DEVERR_TIMEOUT     0x10  /* an on-chip pipeline wait ran past its limit (kernel returned early) */
+#define MSA_DEVERR_SELECTION   0x20  /* sparse attention: a selection entry >= MB, repeated, or not ascending */
 
 typedef struct {
     /* query: [T, H_q, D] contiguous, fp16 or bf16 ("TND" query of the guide, sec. 4). */
@@ -314,6 +315,58 @@ msa_status_t msa_index_score_fp4_plan(const msa_index_score_args *args, int32_t 
 msa_status_t msa_index_score_fp4_run(const msa_index_score_args *args, int32_t format,
                                      const uint8_t *k_scale, float *out, void *workspace,
                                      size_t workspace_bytes, msa_stream_t stream);
+
+/*
+ * Sparse main branch (MiniMax Sparse Attention notes, sec. 4.8 Equation (8)):
+ * softmax attention of every query head over the keys of the blocks its GQA
+ * group selected (sec. 4.3 Equation (3)), computed KV-outer in two phases
+ * (sec. 4.11, 5.5-5.10): the selection is inverted into block -> query lists,
+ * every selected block's K and V pages are loaded once per unit of gathered
+ * queries and give one partial (output, log-sum-exp) per (query, head, block),
+ * and the partials are merged exactly:
+ *
+ *   out[t, h, :] = sum_{j in S} softmax_j(s_j) V[j, h / g, :],  s_j = sm_scale <Q[t, h], K[j, h / g]>
+ *   lse[t, h]    = log sum_{j in S} exp(s_j)
+ *
+ * S holds the keys j of the blocks listed in selection[t, h / g, :] (logical
+ * block indices of the token's request; -1 entries and blocks at or beyond
+ * ceil(kv_len / P) are skipped) that are visible to t: j < kv_len and, for
+ * sparse_mode 3, j <= kv_len - Lq + i.  A token with no such key gets out = 0
+ * and lse = -inf.
+ *
+ *   args   as for msa_index_score: query [T, H_q, D] fp16 / bf16 (the main
+ *          branch's query), key_cache the main branch's keys, layout, table,
+ *          lengths, sparse_mode; start_loc, init_blocks, local_blocks and
+ *          max_seqlen_q are not used; scale must be NULL.
+ *   sa     value_cache: device, the same layout, shape, dtype and page stride as
+ *          key_cache (one block table serves both); selection: device int32
+ *          [T, H_kv, k], ascending with a -1 tail (msa_index_score_topk writes
+ *          it); k in [1, 32]; sm_scale: 0 for 1 / sqrt(D).
+ *   out    device fp32 [T, H_q, D], 16-byte aligned.
+ *   lse    device fp32 [T, H_q], or NULL.
+ *   workspace  msa_sparse_attention_workspace_size() bytes (256-byte aligned,
+ *          caller-owned): the block -> query lists, the work units and the
+ *          per-block partials (T * H_q * k * (D + 1) floats).
+ *
+ * Errors: as msa_index_score, plus MSA_ERR_INVALID_ARG for a missing value
+ * cache or selection, k outside [1, 32] or a dtype other than fp16 / bf16.
+ * Selection rows that are out of range, repeated or not ascending set
+ * MSA_DEVERR_SELECTION (their outputs are then unspecified); read the error
+ * word with msa_get_device_error.  Asynchronous on `stream`.
+ */
+typedef struct {
+    const void *value_cache;
+    const int32_t *selection;
+    int32_t k;
+    float sm_scale;
+} msa_sparse_attention_args;
+
+msa_status_t msa_sparse_attention_workspace_size(const msa_index_score_args *args,
+                                                 const msa_sparse_attention_args *sa,
+                                                 size_t *bytes);
+msa_status_t msa_sparse_attention(const msa_index_score_args *args,
+                                  const msa_sparse_attention_args *sa, float *out, float *lse,
+                                  void *workspace, size_t workspace_bytes, msa_stream_t stream);
 
 /* Synchronise `stream` and read the device error word left in `workspace`
  * by the last call (MSA_DEVERR_* bits; 0 = clean).  Returns MSA_OK, or
