@@ -538,6 +538,7 @@ def run_ours(args):
     # not part of the metric above), and the fused per-group selection
     topk = topk_run(prep.out, case.MB, 16, device, stream, peaks, min(steps * 5, 200))
     fused = fused_select_run(case, prep, device, stream, min(steps, 30), head, topk)
+    sparse = sparse_run(case, prep, device, stream, peaks, min(steps, 10))
     del prep
     torch.cuda.empty_cache()
 
@@ -554,6 +555,7 @@ def run_ours(args):
         "e2e": e2e,
         "topk": topk,
         "fused_select": fused,
+        "sparse_attention": sparse,
         "gpu_launches": head["gpu_launches"],
         "clocks": head["clocks"],
     }
@@ -575,6 +577,8 @@ def run_ours(args):
                                  peaks, ws, recorded_traffic(skey, dominant_kernel(scase)))
             rec["topk"] = topk_run(sprep.out, scase.MB, 16, device, stream, peaks, 200)
             rec["fused_select"] = fused_select_run(scase, sprep, device, stream, 30, rec, rec["topk"])
+            if n == 3 and fp4 is None:
+                rec["sparse_attention"] = sparse_run(scase, sprep, device, stream, peaks, 20)
             del sprep
             rec["e2e"] = e2e_run(scase, device, stream, args, steps=20)
             if rank == 0 and ws == 1 and not args.no_cpu_baseline:
@@ -618,6 +622,83 @@ def fused_select_run(case, prep, device, stream, steps, head, topk):
         raise RuntimeError("device error in the fused selection")
     res["workspace_bytes"] = ws.numel()
     res["launches_per_call"] = launches_per_call(case) + 1
+    return res
+
+
+def sparse_work(case, sel):
+    """Algorithmic work of the sparse main branch for selection ``sel``
+    ``[T, H_kv, k]``: FLOPs = 4 * D * sum over (token, head) of the visible
+    keys in its selected blocks (S = Q K^T and O = P V); bytes = the query,
+    the K and V pages of every distinct selected (kv head, request, block)
+    once, the fp32 output and LSE."""
+    import numpy as np
+    sel = sel.cpu().numpy().astype(np.int64)
+    T, H_kv, k = sel.shape
+    g = case.H_q // case.H_kv
+    P, D = case.P, case.D
+    cu = case.cu_seqlens_q.tolist()
+    req = np.zeros(T, dtype=np.int64)
+    for b in range(len(cu) - 1):
+        req[cu[b]:cu[b + 1]] = b
+    L = np.asarray(case.kv_lens, dtype=np.int64)[req]                  # [T]
+    Lq = np.asarray(case.q_lens, dtype=np.int64)[req]
+    qpos = L - Lq + (np.arange(T) - np.asarray(cu[:-1], dtype=np.int64)[req])
+    last = np.minimum(L - 1, qpos) if case.sparse_mode == 3 else L - 1  # last visible key
+    nb = -(-L // P)
+    valid = (sel >= 0) & (sel < case.MB) & (sel < nb[:, None, None])
+    vis = np.clip(last[:, None, None] + 1 - sel * P, 0, P) * valid
+    flops = 4.0 * D * g * float(vis.sum())
+    blocks = set()
+    for r in range(H_kv):
+        t_idx, s_idx = np.nonzero(valid[:, r, :])
+        blocks.update(zip([r] * len(t_idx), req[t_idx].tolist(), sel[t_idx, r, s_idx].tolist()))
+    es = case.key.element_size()
+    nbytes = (case.T * case.H_q * D * case.query.element_size() + len(blocks) * 2 * P * D * es
+              + case.T * case.H_q * (D + 1) * 4)
+    return flops, nbytes, len(blocks)
+
+
+def sparse_run(case, prep, device, stream, peaks, steps: int):
+    """The sparse main branch (msa_sparse_attention) over the fused top-16
+    selection of this workload, the workload's query and keys as the main
+    branch's, random values of the key cache's layout: microseconds per call."""
+    if (case.key.dtype not in (torch.float16, torch.bfloat16) or getattr(case, "fp4", None)
+            or 32 % (case.H_q // case.H_kv)):
+        return None
+    sel = prep.topk(16, local_slot=True, scores=False, stream=stream)
+    key = prep.call.key
+    base = key
+    while base._base is not None:
+        base = base._base
+    gen = torch.Generator(device=device).manual_seed(99)
+    vbase = torch.randn(base.shape, generator=gen, device=device, dtype=torch.float32).to(key.dtype)
+    value = torch.as_strided(vbase, key.shape, key.stride(), key.storage_offset())
+    out, lse = prep.sparse_attention(value, sel, stream=stream)
+    for _ in range(2):
+        prep.sparse_attention(value, sel, out=out, lse=lse, workspace=prep.sparse_workspace,
+                              stream=stream)
+    torch.cuda.synchronize(device)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        prep.sparse_attention(value, sel, out=out, lse=lse, workspace=prep.sparse_workspace,
+                              stream=stream)
+    e1.record(stream)
+    torch.cuda.synchronize(device)
+    if prep.sparse_device_error(stream):
+        raise RuntimeError("device error in the sparse attention")
+    us = e0.elapsed_time(e1) / steps * 1e3
+    flops, nbytes, nblocks = sparse_work(case, sel)
+    tfl = flops / us / 1e6
+    gbs = nbytes / us / 1e3
+    bound = "tensor" if flops / (peaks["bf16_tflops"] * 1e12) >= nbytes / (peaks["hbm_gbs"] * 1e9) else "hbm"
+    res = {"k": 16, "selection": "fused per-group top-16 with the own-block slot",
+           "us_per_call": us, "tflops": tfl, "gbs": gbs, "algorithmic_flops": flops,
+           "algorithmic_bytes": nbytes, "selected_blocks": nblocks, "bound": bound,
+           "frac": (tfl / peaks["bf16_tflops"]) if bound == "tensor" else (gbs / peaks["hbm_gbs"]),
+           "partials_bytes": case.T * case.H_q * 16 * (case.D + 1) * 4 * 2,
+           "kernels": "count, scan, scatter, units, K1 (sparse_k1_kernel), K2 (combine); 2 memsets"}
+    del vbase, value, out, lse
     return res
 
 

@@ -752,13 +752,16 @@ msa_status_t msa_sparse_attention(const msa_index_score_args* args,
   sp.units = reinterpret_cast<int4*>(w + lo.units);
   sp.o_part = reinterpret_cast<float*>(w + lo.o_part);
   sp.lse_part = reinterpret_cast<float*>(w + lo.lse_part);
-  // K and V pages through the key cache's tensor-map recipe
-  CUtensorMap tq, tk, tv;
-  if ((st = make_maps(args, sp.p, &tq, &tk, nullptr, nullptr)) != MSA_OK) return st;
+  // K and V pages through the key cache's tensor-map recipe; the query map
+  // with a run of one position (a box is one query entry's g heads)
+  CUtensorMap tq, tk, tv, tq_unused;
+  msa::Params p1 = sp.p;
+  p1.np = 1;
+  if ((st = make_maps(args, p1, &tq, &tk, nullptr, nullptr)) != MSA_OK) return st;
   msa_index_score_args va = *args;
   va.key_cache = sa->value_cache;
-  if ((st = make_maps(&va, sp.p, &tq, &tv, nullptr, nullptr)) != MSA_OK) return st;
-  cudaError_t e = msa::launch_sparse_attention(&tk, &tv, sp, args->q_dtype == MSA_BF16, out, lse,
+  if ((st = make_maps(&va, p1, &tq_unused, &tv, nullptr, nullptr)) != MSA_OK) return st;
+  cudaError_t e = msa::launch_sparse_attention(&tq, &tk, &tv, sp, args->q_dtype == MSA_BF16, out, lse,
                                                reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "sparse attention launch");
   return MSA_OK;

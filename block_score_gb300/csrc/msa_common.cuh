@@ -194,8 +194,11 @@ struct SparseParams {
   float* lse_part;         // [T, H_q, k] per-block natural log-sum-exp
 };
 
-cudaError_t launch_sparse_attention(const void* tm_k, const void* tm_v, const SparseParams& sp,
-                                    bool bf16, float* out, float* lse, cudaStream_t s);
+// tm_q: the query map with a box of (64 columns, g heads, 1 position), read
+// when g is a multiple of 8; tm_k / tm_v: one 128-token page of one kv head.
+cudaError_t launch_sparse_attention(const void* tm_q, const void* tm_k, const void* tm_v,
+                                    const SparseParams& sp, bool bf16, float* out, float* lse,
+                                    cudaStream_t s);
 
 // Unique id (+1) of the CUDA context current on this host thread, 0 if there
 // is none or the driver cannot say.  Per-device host caches are keyed by it:

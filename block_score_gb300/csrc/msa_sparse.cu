@@ -169,33 +169,45 @@ __global__ void units_kernel(const SparseParams sp) {
 }
 
 // ------------------------------------------------------------------- K1 ----
+// Shared memory: two stages of {Q, K, V}, each a 128 x 128 16-bit tile stored
+// as two 16 KiB halves of 64 columns, 128-byte swizzled as TMA writes them
+// (Q: rows = query entry x head; K and V: rows = the block's tokens), then
+// one staging area per softmax warp for the O rows it writes out.
 struct K1Layout {
-  static constexpr uint32_t kTile = 32768;             // 128 x 128 16-bit operand (two 16 KiB halves)
-  static constexpr uint32_t kStage = 3 * kTile;        // Q, K, V (rows = tokens)
+  static constexpr uint32_t kTile = 32768;
+  static constexpr uint32_t kStage = 3 * kTile;          // Q, K, V
   static constexpr uint32_t stage_off = 0;
-  static constexpr uint32_t vt_off = 2 * kStage;       // V transposed: rows = dims, K-major over tokens
-  static constexpr uint32_t bar_off = vt_off + kTile;
-  static constexpr uint32_t n_bars = 4 * 2 + 9;
+  static constexpr uint32_t kORow = 128 + 16;            // 32 fp32 columns + a 16-byte pad
+  static constexpr uint32_t kOWarp = 32 * kORow;
+  static constexpr uint32_t ostage_off = 2 * kStage;
+  static constexpr uint32_t bar_off = ostage_off + 4 * kOWarp;
+  static constexpr uint32_t n_bars = 9 * 2 + 1;
   static constexpr uint32_t misc_off = bar_off + n_bars * 8;
   static constexpr uint32_t end = misc_off + 16;
   static constexpr uint32_t bytes = end + 1024;
 };
 static_assert(K1Layout::bytes <= 232448, "shared memory per CTA");
+static_assert(K1Layout::kStage % 1024 == 0 && K1Layout::ostage_off % 1024 == 0, "1 KiB aligned tiles");
 
-constexpr int kK1Threads = 320;       // 10 warps
-constexpr uint32_t kColS = 0, kColP = 128, kColO = 256;
+constexpr int kK1Threads = 256;       // 8 warps
+constexpr int kLoaderWarps = 2;
+// tensor memory: two buffers of [S (128 columns, P over its first 64) | O (128 columns)]
+constexpr uint32_t kBufCols = 256, kColO = 128;
 
-__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t (&r)[4]) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(addr)
-               : "memory");
-}
-
-__device__ __forceinline__ void stsm_x4(uint32_t addr, const uint32_t (&r)[4]) {
-  asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1, %2, %3, %4};" ::"r"(addr),
-               "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3])
-               : "memory");
+// Shared-memory descriptor of the V page as the B operand of O = P V in
+// MN-major form (N = the 128 head dims contiguous, K = tokens): 128-byte
+// swizzle atoms of 64 dims x 8 tokens; the next 64 dims are the tile's other
+// half (leading byte offset 16 KiB), the next 8 tokens 1 KiB further (stride
+// byte offset).  Slice kk covers tokens 16 kk .. 16 kk + 15.
+__device__ __forceinline__ uint64_t v_desc_mn(uint32_t tile_base, int kk) {
+  const uint32_t a = tile_base + (uint32_t)kk * 2048u;
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((a & 0x3FFFFu) >> 4);            // start address
+  d |= static_cast<uint64_t>(kHalfBytes >> 4) << 16;           // leading byte offset
+  d |= static_cast<uint64_t>(1024 >> 4) << 32;                 // stride byte offset
+  d |= static_cast<uint64_t>(1) << 46;                         // descriptor version
+  d |= static_cast<uint64_t>(2) << 61;                         // 128-byte swizzle
+  return d;
 }
 
 __device__ __forceinline__ float ex2(float x) {
@@ -213,15 +225,102 @@ __device__ __forceinline__ uint32_t pack2(float a, float b, bool bf16) {
   return *reinterpret_cast<const uint32_t*>(&v);
 }
 
-// Roles: warp 0 TMA producer (K and V pages), warp 1 TMEM owner + MMA issuer,
-// warps 2..5 softmax and partial stores (thread = MMA row = TMEM lane), warps
-// 6..9 loaders (gather the unit's query rows, transpose V into a K-major tile).
+// A unit: (kv head r, request b, block beta) and its query entries [e0, e0 + ne).
+struct UnitInfo {
+  int r, b, beta, e0, ne;
+};
+
+__device__ __forceinline__ UnitInfo unit_of(const SparseParams& sp, int4 d) {
+  UnitInfo ui;
+  const int64_t list = d.x;
+  ui.beta = (int)(list % sp.p.MB);
+  const int64_t rb = list / sp.p.MB;
+  ui.b = (int)(rb % sp.p.B);
+  ui.r = (int)(rb / sp.p.B);
+  ui.e0 = d.y;
+  ui.ne = d.z;
+  return ui;
+}
+
+__device__ __forceinline__ UnitInfo unit_info(const SparseParams& sp, int u) {
+  return unit_of(sp, __ldg(sp.units + u));
+}
+
+// What one MMA row (query entry row / g, head r * g + row % g) needs of a unit.
+struct RowInfo {
+  bool valid;
+  int64_t t;
+  int s, h;
+  int lim;          // last visible column of the block (-1: none)
+};
+
+// The loads behind a RowInfo, issued early (row_pre) and turned into the
+// RowInfo later (row_fin), so their latency hides under other work.
+struct RowPre {
+  bool valid;
+  int entry, t0, t1, kv0, kv1;   // query entry; cu_q[b], cu_q[b+1]; the request's KV bounds
+  int r, beta;
+};
+
+// The loads are unconditional, from indices clamped into range (a unit
+// descriptor of zeros reads entry 0 of request 0), so that no instruction
+// depends on a loaded value before row_fin.
+__device__ __forceinline__ RowPre row_pre(const SparseParams& sp, const UnitInfo& ui, int row) {
+  const Params& p = sp.p;
+  RowPre q;
+  q.valid = row < ui.ne * p.g;
+  q.r = ui.r;
+  q.beta = ui.beta;
+  const int e = ui.e0 + max(0, min(row / p.g, ui.ne - 1));
+  q.entry = __ldg(sp.qidx + e);
+  q.t0 = __ldg(p.cu_q + ui.b);
+  q.t1 = __ldg(p.cu_q + ui.b + 1);
+  if (p.layout == 2) {
+    q.kv0 = __ldg(p.cu_k + ui.b);
+    q.kv1 = __ldg(p.cu_k + ui.b + 1);
+  } else {
+    q.kv0 = 0;
+    q.kv1 = __ldg(p.kv_len + ui.b);
+  }
+  return q;
+}
+
+__device__ __forceinline__ RowInfo row_fin(const SparseParams& sp, const RowPre& q, int row) {
+  const Params& p = sp.p;
+  RowInfo ri;
+  ri.valid = q.valid;
+  ri.t = 0;
+  ri.s = ri.h = 0;
+  ri.lim = -1;
+  if (ri.valid) {
+    ri.t = q.entry / sp.k;
+    ri.s = q.entry - (int)(ri.t * sp.k);
+    ri.h = q.r * p.g + row % p.g;
+    int64_t L = (int64_t)q.kv1 - q.kv0;
+    if (L < 0) L = 0;
+    const int64_t Lq = (int64_t)q.t1 - q.t0;
+    int64_t last = L - 1;
+    if (p.sparse_mode == 3) last = min(last, L - Lq + (ri.t - q.t0));
+    const int64_t c = last - (int64_t)q.beta * kP;
+    ri.lim = c < 0 ? -1 : (c > kP - 1 ? kP - 1 : (int)c);
+  }
+  return ri;
+}
+
+// Roles: warp 0 TMA producer (the K and V pages, and the query rows when g is a
+// multiple of 8: one g-row box per query entry and half), warp 1 TMEM owner +
+// MMA issuer, warps 2..5 softmax and partial stores (thread = MMA row = TMEM
+// lane), warps 6..7 gather the query rows when g is not a multiple of 8.
 // Units are taken round-robin (unit i of CTA c is c + i * gridDim.x); every
-// role walks the same sequence, two stages of Q/K/V in flight.
-template <bool BF16>
+// role walks the same sequence.  Unit i uses stage i % 2 and tensor-memory
+// buffer i % 2.  Q and K of a stage are released when S = Q K^T is done, V
+// when O = P V is; the MMA warp issues S(i) before O(i-1), and the softmax
+// warps turn S(i) into P(i) before they store O(i-1), so the P V product of one
+// unit runs under the softmax of the next.
+template <bool BF16, bool QTMA>
 __global__ void __launch_bounds__(kK1Threads, 1)
-    sparse_k1_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                     const SparseParams sp) {
+    sparse_k1_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                     const __grid_constant__ CUtensorMap tm_v, const SparseParams sp) {
   using Lo = K1Layout;
   const Params& p = sp.p;
   extern __shared__ uint8_t smem_raw[];
@@ -229,19 +328,16 @@ __global__ void __launch_bounds__(kK1Threads, 1)
                                              ~static_cast<uintptr_t>(1023));
   const uint32_t sbase = smem_u32(smem);
   const uint32_t bars = sbase + Lo::bar_off;
-  const uint32_t b_k_full = bars;                 // [2] K page landed
+  const uint32_t b_k_full = bars;                 // [2] K page (and, by TMA, the query rows) landed
   const uint32_t b_v_full = b_k_full + 16;        // [2] V page landed
-  const uint32_t b_q_full = b_v_full + 16;        // [2] query rows written (4 loader warps)
-  const uint32_t b_stage_empty = b_q_full + 16;   // [2] the stage's last MMA done
-  const uint32_t b_s_full = b_stage_empty + 16;
-  const uint32_t b_s_empty = b_s_full + 8;        // 4 softmax warps read S
-  const uint32_t b_p_full = b_s_empty + 8;        // 4 softmax warps wrote P
-  const uint32_t b_o_full = b_p_full + 8;
-  const uint32_t b_o_empty = b_o_full + 8;        // 4 softmax warps read O
-  const uint32_t b_vt_full = b_o_empty + 8;       // 4 loader warps wrote V^T
-  const uint32_t b_vt_empty = b_vt_full + 8;      // the MMA reading V^T done
-  const uint32_t b_drain = b_vt_empty + 8;
-  const uint32_t b_spare = b_drain + 8;
+  const uint32_t b_q_full = b_v_full + 16;        // [2] query rows written (the loader warps)
+  const uint32_t b_kq_empty = b_q_full + 16;      // [2] the stage's Q K^T product done (Q, K free)
+  const uint32_t b_v_empty = b_kq_empty + 16;     // [2] the stage's P V product done (V free)
+  const uint32_t b_s_full = b_v_empty + 16;       // [2] S in the buffer
+  const uint32_t b_p_full = b_s_full + 16;        // [2] P written (4 softmax warps)
+  const uint32_t b_o_full = b_p_full + 16;        // [2] O in the buffer
+  const uint32_t b_o_empty = b_o_full + 16;       // [2] O read (4 softmax warps)
+  const uint32_t b_drain = b_o_empty + 16;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Lo::misc_off);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Lo::misc_off + 4);
 
@@ -251,20 +347,18 @@ __global__ void __launch_bounds__(kK1Threads, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(b_k_full + 8 * i, 1);
       mbar_init(b_v_full + 8 * i, 1);
-      mbar_init(b_q_full + 8 * i, 4);
-      mbar_init(b_stage_empty + 8 * i, 1);
+      mbar_init(b_q_full + 8 * i, kLoaderWarps);
+      mbar_init(b_kq_empty + 8 * i, 1);
+      mbar_init(b_v_empty + 8 * i, 1);
+      mbar_init(b_s_full + 8 * i, 1);
+      mbar_init(b_p_full + 8 * i, 4);
+      mbar_init(b_o_full + 8 * i, 1);
+      mbar_init(b_o_empty + 8 * i, 4);
     }
-    mbar_init(b_s_full, 1);
-    mbar_init(b_s_empty, 4);
-    mbar_init(b_p_full, 4);
-    mbar_init(b_o_full, 1);
-    mbar_init(b_o_empty, 4);
-    mbar_init(b_vt_full, 4);
-    mbar_init(b_vt_empty, 1);
     mbar_init(b_drain, 1);
-    mbar_init(b_spare, 1);
     *abort_flag = 0;
     fence_mbar_init();
+    if (QTMA) prefetch_tmap(&tm_q);
     prefetch_tmap(&tm_k);
     prefetch_tmap(&tm_v);
   }
@@ -281,103 +375,124 @@ __global__ void __launch_bounds__(kK1Threads, 1)
   const int n_units = hdr->n_units;
   WaitCtl ctl{abort_flag, &hdr->err, p.wait_limit_ns};
   const int g = p.g;
-
-  // unit -> (kv head, request, block, first list entry, entries)
-  auto unit_at = [&](int u, int& r, int& b, int& beta, int& e0, int& ne) {
-    const int4 d = __ldg(sp.units + u);
-    const int64_t list = d.x;
-    beta = (int)(list % p.MB);
-    const int64_t rb = list / p.MB;
-    b = (int)(rb % p.B);
-    r = (int)(rb / p.B);
-    e0 = d.y;
-    ne = d.z;
-  };
+  const int first = blockIdx.x, step = gridDim.x;
 
   if (warp == 0) {
     // -------------------------------------------------------- producer --
-    if (lane == 0) {
-      const bool paged = p.layout != 2;
-      const uint64_t pol = l2_policy_evict_last();      // a block's pages serve all its units
-      uint32_t n_issued[2] = {0, 0};
-      int i = 0;
-      for (int u = blockIdx.x; u < n_units; u += gridDim.x, ++i) {
-        const int st = i & 1;
-        const uint32_t ph = (uint32_t)(i >> 1) & 1u;
-        if (!mbar_wait(b_stage_empty + 8 * st, ph ^ 1, ctl)) break;
-        int r, b, beta, e0, ne;
-        unit_at(u, r, b, beta, e0, ne);
-        int page = 0, tok = 0;
-        if (paged) {
-          page = __ldg(p.block_table + (int64_t)b * p.MB + beta);
-          if (page < 0 || (int64_t)page >= p.NP) {
-            atomicOr(&hdr->err, kErrBlockTable);
-            page = (int32_t)(p.NP < 0x7fffffffLL ? p.NP : 0x7fffffffLL);   // out of bounds: zero fill
-          }
-        } else {
-          tok = __ldg(p.cu_k + b) + beta * kP;
+    const bool paged = p.layout != 2;
+    const uint64_t pol = l2_policy_evict_last();      // a block's pages serve all its units
+    uint32_t n_k[2] = {0, 0}, n_v[2] = {0, 0};
+    int i = 0;
+    for (int u = first; u < n_units; u += step, ++i) {
+      const int st = i & 1;
+      const uint32_t ph = (uint32_t)(i >> 1) & 1u;
+      const UnitInfo ui = unit_info(sp, u);
+      int page = 0, tok = 0;
+      if (paged) {
+        page = __ldg(p.block_table + (int64_t)ui.b * p.MB + ui.beta);
+        if (page < 0 || (int64_t)page >= p.NP) {
+          if (lane == 0) atomicOr(&hdr->err, kErrBlockTable);
+          page = (int32_t)(p.NP < 0x7fffffffLL ? p.NP : 0x7fffffffLL);   // out of bounds: zero fill
         }
-        const uint32_t st_base = sbase + Lo::stage_off + st * Lo::kStage;
-        mbar_arrive_expect_tx(b_k_full + 8 * st, Lo::kTile);
+      } else {
+        tok = __ldg(p.cu_k + ui.b) + ui.beta * kP;
+      }
+      // the unit's query tokens (entry / k), lane e holding entry e
+      int qt = 0;
+      if (QTMA && lane < ui.ne) qt = __ldg(sp.qidx + ui.e0 + lane) / sp.k;
+      const uint32_t st_base = sbase + Lo::stage_off + st * Lo::kStage;
+      if (!warp_wait(b_kq_empty + 8 * st, ph ^ 1u, ctl)) break;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(b_k_full + 8 * st,
+                              Lo::kTile + (QTMA ? (uint32_t)(ui.ne * g) * 2u * 128u : 0u));
         for (int x = 0; x < 2; ++x)
-          tma_k(st_base + Lo::kTile + x * kHalfBytes, &tm_k, b_k_full + 8 * st, 64 * x, tok, r, page,
+          tma_k(st_base + Lo::kTile + x * kHalfBytes, &tm_k, b_k_full + 8 * st, 64 * x, tok, ui.r, page,
                 p.layout, pol);
+      }
+      if (QTMA) {
+        // entry e's g heads land in rows e*g .. e*g+g-1 of each half (1 KiB aligned: g % 8 == 0)
+        for (int e = 0; e < ui.ne; ++e) {
+          const int t = __shfl_sync(0xffffffffu, qt, e);
+          if (lane == 0)
+            for (int x = 0; x < 2; ++x)
+              tma_load_3d(st_base + x * kHalfBytes + (uint32_t)(e * g) * 128u, &tm_q, b_k_full + 8 * st,
+                          64 * x, ui.r * g, t);
+        }
+      }
+      ++n_k[st];
+      if (!warp_wait(b_v_empty + 8 * st, ph ^ 1u, ctl)) break;
+      if (lane == 0) {
         mbar_arrive_expect_tx(b_v_full + 8 * st, Lo::kTile);
         for (int x = 0; x < 2; ++x)
-          tma_k(st_base + 2 * Lo::kTile + x * kHalfBytes, &tm_v, b_v_full + 8 * st, 64 * x, tok, r, page,
+          tma_k(st_base + 2 * Lo::kTile + x * kHalfBytes, &tm_v, b_v_full + 8 * st, 64 * x, tok, ui.r, page,
                 p.layout, pol);
-        ++n_issued[st];
       }
-      // teardown: the last load of each stage may still be in flight
+      ++n_v[st];
+    }
+    // teardown: the last loads of each stage may still be in flight
+    if (lane == 0) {
       for (int st = 0; st < 2; ++st) {
-        if (!n_issued[st]) continue;
-        const uint32_t ph = (n_issued[st] - 1) & 1u;
         const uint64_t t0 = global_timer_ns();
-        while (!(mbar_try_wait(b_k_full + 8 * st, ph) && mbar_try_wait(b_v_full + 8 * st, ph)) &&
-               global_timer_ns() - t0 < kDrainLimitNs) {
-        }
+        if (n_k[st])
+          while (!mbar_try_wait(b_k_full + 8 * st, (n_k[st] - 1) & 1u) && global_timer_ns() - t0 < kDrainLimitNs) {
+          }
+        if (n_v[st])
+          while (!mbar_try_wait(b_v_full + 8 * st, (n_v[st] - 1) & 1u) && global_timer_ns() - t0 < kDrainLimitNs) {
+          }
       }
     }
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------ MMA issuer --
-    constexpr uint32_t idesc = idesc_f16(BF16, 128, 128);
-    bool issued = false;
-    int i = 0;
-    for (int u = blockIdx.x; u < n_units; u += gridDim.x, ++i) {
-      const int st = i & 1;
-      const uint32_t ph2 = (uint32_t)(i >> 1) & 1u, ph1 = (uint32_t)i & 1u;
-      if (!warp_wait(b_k_full + 8 * st, ph2, ctl)) break;
-      if (!warp_wait(b_q_full + 8 * st, ph2, ctl)) break;
-      if (!warp_wait(b_s_empty, ph1 ^ 1, ctl)) break;
+    constexpr uint32_t idesc_s = idesc_f16(BF16, 128, 128);
+    constexpr uint32_t idesc_o = idesc_f16(BF16, 128, 128) | (1u << 16);   // B (V) MN-major
+    bool issued = false, ok = true;
+    // O(j) = P(j) V(j): P from tensor memory, V as loaded
+    auto pv = [&](int j) -> bool {
+      const int bj = j & 1;
+      const uint32_t phj = (uint32_t)(j >> 1) & 1u;
+      if (!warp_wait(b_p_full + 8 * bj, phj, ctl)) return false;
+      if (!warp_wait(b_v_full + 8 * bj, phj, ctl)) return false;
+      if (!warp_wait(b_o_empty + 8 * bj, phj ^ 1u, ctl)) return false;   // O(j-2) read
       tc_fence_after();
-      const uint32_t st_base = sbase + Lo::stage_off + st * Lo::kStage;
       if (lane == 0) {
-        // S = Q K^T: rows = (query, head), columns = the block's 128 tokens
+        const uint32_t buf = tmem_base + bj * kBufCols;
+        const uint32_t vt = sbase + Lo::stage_off + bj * Lo::kStage + 2 * Lo::kTile;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          tc_mma_f16(tmem_base + kColS, desc_at(st_base, kk), desc_at(st_base + Lo::kTile, kk), idesc,
-                     kk ? 1u : 0u);
-        tc_commit(b_s_full);
+          tc_mma_f16_ta(buf + kColO, buf + 8u * kk, v_desc_mn(vt, kk), idesc_o, kk ? 1u : 0u);
+        tc_commit(b_o_full + 8 * bj);
+        tc_commit(b_v_empty + 8 * bj);
       }
       __syncwarp();
-      if (!warp_wait(b_p_full, ph1, ctl)) break;
-      if (!warp_wait(b_vt_full, ph1, ctl)) break;
-      if (!warp_wait(b_o_empty, ph1 ^ 1, ctl)) break;
+      return true;
+    };
+    int i = 0;
+    for (int u = first; u < n_units; u += step, ++i) {
+      const int st = i & 1;
+      const uint32_t ph = (uint32_t)(i >> 1) & 1u;
+      // S(i) overwrites P(i-2) in this buffer: P(i-2) V(i-2) must be done
+      if (!warp_wait(b_k_full + 8 * st, ph, ctl) || (!QTMA && !warp_wait(b_q_full + 8 * st, ph, ctl)) ||
+          !warp_wait(b_v_empty + 8 * st, ph ^ 1u, ctl)) {
+        ok = false;
+        break;
+      }
       tc_fence_after();
       if (lane == 0) {
-        // O = P V: P (bf16 / fp16 pairs) from tensor memory, V^T K-major in shared memory
+        // S = Q K^T: rows = (query, head), columns = the block's 128 tokens
+        const uint32_t st_base = sbase + Lo::stage_off + st * Lo::kStage;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          tc_mma_f16_ta(tmem_base + kColO, tmem_base + kColP + 8u * kk,
-                        desc_at(sbase + Lo::vt_off, kk), idesc, kk ? 1u : 0u);
-        tc_commit(b_o_full);
-        tc_commit(b_vt_empty);
-        tc_commit(b_stage_empty + 8 * st);
+          tc_mma_f16(tmem_base + st * kBufCols, desc_at(st_base, kk), desc_at(st_base + Lo::kTile, kk),
+                     idesc_s, kk ? 1u : 0u);
+        tc_commit(b_s_full + 8 * st);
+        tc_commit(b_kq_empty + 8 * st);
       }
       __syncwarp();
       issued = true;
+      if (i > 0 && !pv(i - 1)) { ok = false; break; }
     }
+    if (ok && i > 0) pv(i - 1);
     if (lane == 0 && issued) {
       tc_commit(b_drain);
       const uint64_t t0 = global_timer_ns();
@@ -390,130 +505,153 @@ __global__ void __launch_bounds__(kK1Threads, 1)
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;              // MMA row = TMEM lane
     const uint32_t t_lane = tmem_base + ((uint32_t)(quarter * 32) << 16);
+    uint8_t* ostage = smem + Lo::ostage_off + quarter * Lo::kOWarp;
     const float ninf = __int_as_float(0xff800000);
     const float kscale = sp.sm_scale * 1.4426950408889634f;   // base-2 softmax
-    int i = 0;
-    for (int u = blockIdx.x; u < n_units; u += gridDim.x, ++i) {
-      const uint32_t ph1 = (uint32_t)i & 1u;
-      int r, b, beta, e0, ne;
-      unit_at(u, r, b, beta, e0, ne);
-      const bool valid = row < ne * g;
-      int64_t t = 0;
-      int s = 0, h = 0;
-      int lim = -1;                                    // last visible column of the block (-1: none)
-      if (valid) {
-        const int entry = __ldg(sp.qidx + e0 + row / g);
-        t = entry / sp.k;
-        s = entry - (int)(t * sp.k);
-        h = r * g + row % g;
-        const int64_t L = kv_length(sp, b);
-        const int64_t t0 = __ldg(p.cu_q + b);
-        const int64_t Lq = (int64_t)__ldg(p.cu_q + b + 1) - t0;
-        int64_t last = L - 1;
-        if (p.sparse_mode == 3) last = min(last, L - Lq + (t - t0));
-        const int64_t c = last - (int64_t)beta * kP;
-        lim = c < 0 ? -1 : (c > kP - 1 ? kP - 1 : (int)c);
-      }
-      if (!warp_wait(b_s_full, ph1, ctl)) break;
+    bool ok = true;
+    RowInfo prev{};                                    // the unit whose O is stored next
+    float prev_l = 0.f, prev_m = 0.f;
+    // store O(j) of the previous unit (normalised) and its LSE.  A quarter of
+    // the warp's 32 rows (32 columns each) at a time goes through the warp's
+    // staging area: each thread writes its row's 128 bytes, then every store
+    // instruction writes four whole 128-byte row segments.
+    auto store_o = [&](int j) -> bool {
+      const int bj = j & 1;
+      if (!warp_wait(b_o_full + 8 * bj, (uint32_t)(j >> 1) & 1u, ctl)) return false;
       tc_fence_after();
       float x[128];
-      tmem_ld128(t_lane + kColS, x);
+      tmem_ld128(t_lane + bj * kBufCols + kColO, x);
       tmem_wait_ld();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(b_s_empty);
-      float m = ninf;
+      if (lane == 0) mbar_arrive(b_o_empty + 8 * bj);
+      int64_t slot = -1;
+      float inv = 0.f;
+      if (prev.valid) {
+        const bool any = prev.lim >= 0;
+        slot = (prev.t * p.H_q + prev.h) * (int64_t)sp.k + prev.s;
+        inv = any ? 1.f / prev_l : 0.f;
+        // natural-log LSE of the block's visible keys
+        sp.lse_part[slot] = any ? (prev_m + __log2f(prev_l)) * 0.6931471805599453f : ninf;
+      }
+      const int rsub = lane >> 3, chunk = lane & 7;  // read-back: row rsub + 4 it, 16-byte chunk
+#pragma unroll
+      for (int qc = 0; qc < 4; ++qc) {
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const int col = 32 * qc + 4 * c;
+          *reinterpret_cast<float4*>(ostage + lane * Lo::kORow + 16 * c) =
+              make_float4(x[col] * inv, x[col + 1] * inv, x[col + 2] * inv, x[col + 3] * inv);
+        }
+        __syncwarp();
+#pragma unroll
+        for (int it = 0; it < 8; ++it) {
+          const int rr = 4 * it + rsub;
+          const int64_t sl = __shfl_sync(0xffffffffu, slot, rr);
+          const float4 v = *reinterpret_cast<const float4*>(ostage + rr * Lo::kORow + 16 * chunk);
+          if (sl >= 0) __stcs(reinterpret_cast<float4*>(sp.o_part + sl * kD + 32 * qc) + chunk, v);
+        }
+        __syncwarp();
+      }
+      return true;
+    };
+    int i = 0;
+    RowInfo cur = first < n_units ? row_fin(sp, row_pre(sp, unit_info(sp, first), row), row) : RowInfo{};
+    // unit descriptors are read at clamped indices (never past the last
+    // unit); whether a unit exists is decided from u alone
+    int4 d_next = n_units > 0 ? __ldg(sp.units + min(first + step, n_units - 1)) : make_int4(0, 0, 0, 0);
+    for (int u = first; u < n_units; u += step, ++i) {
+      const int bi = i & 1;
+      // the next unit's row loads and the unit after's descriptor, issued now
+      // and used after this unit's softmax and the previous unit's store
+      RowPre pre = row_pre(sp, unit_of(sp, d_next), row);
+      pre.valid = pre.valid && u + step < n_units;
+      const int4 d_after = __ldg(sp.units + min(u + 2 * step, n_units - 1));
+      if (!warp_wait(b_s_full + 8 * bi, (uint32_t)(i >> 1) & 1u, ctl)) { ok = false; break; }
+      tc_fence_after();
+      float x[128];
+      tmem_ld128(t_lane + bi * kBufCols, x);
+      tmem_wait_ld();
+      // row max over the visible columns (eight independent chains)
+      float mp[8];
+#pragma unroll
+      for (int a = 0; a < 8; ++a) mp[a] = ninf;
 #pragma unroll
       for (int c = 0; c < 128; ++c) {
-        x[c] = c <= lim ? x[c] * kscale : ninf;
-        m = fmaxf(m, x[c]);
+        x[c] = c <= cur.lim ? x[c] * kscale : ninf;
+        mp[c & 7] = fmaxf(mp[c & 7], x[c]);
       }
-      const bool any = lim >= 0;
-      float l = 0.f;
+      const float m = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
+                            fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
+      const bool any = cur.lim >= 0;
+      float lp[8];
+#pragma unroll
+      for (int a = 0; a < 8; ++a) lp[a] = 0.f;
       uint32_t pk[64];
 #pragma unroll
       for (int c = 0; c < 64; ++c) {
         const float a0 = any ? ex2(x[2 * c] - m) : 0.f;
         const float a1 = any ? ex2(x[2 * c + 1] - m) : 0.f;
-        l += a0 + a1;
+        lp[c & 7] += a0 + a1;
         pk[c] = pack2(a0, a1, BF16);
       }
-      tmem_st64(t_lane + kColP, pk);
+      const float l = ((lp[0] + lp[1]) + (lp[2] + lp[3])) + ((lp[4] + lp[5]) + (lp[6] + lp[7]));
+      // P over the first 64 columns of S (S is in registers now)
+      tmem_st64(t_lane + bi * kBufCols, pk);
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(b_p_full);
-      if (!warp_wait(b_o_full, ph1, ctl)) break;
-      tc_fence_after();
-      tmem_ld128(t_lane + kColO, x);
-      tmem_wait_ld();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(b_o_empty);
-      if (valid) {
-        const int64_t slot = (t * p.H_q + h) * (int64_t)sp.k + s;
-        float4* o = reinterpret_cast<float4*>(sp.o_part + slot * kD);
-        const float inv = any ? 1.f / l : 0.f;
-#pragma unroll
-        for (int c = 0; c < 32; ++c)
-          o[c] = make_float4(x[4 * c] * inv, x[4 * c + 1] * inv, x[4 * c + 2] * inv, x[4 * c + 3] * inv);
-        // natural-log LSE of the block's visible keys
-        sp.lse_part[slot] = any ? (m + __log2f(l)) * 0.6931471805599453f : ninf;
-      }
+      if (lane == 0) mbar_arrive(b_p_full + 8 * bi);
+      if (i > 0 && !store_o(i - 1)) { ok = false; break; }
+      prev = cur;
+      prev_l = l;
+      prev_m = m;
+      cur = row_fin(sp, pre, row);
+      d_next = d_after;
     }
-  } else {
+    if (ok && i > 0) store_o(i - 1);
+  } else if (!QTMA) {
     // --------------------------------------------------------- loaders --
-    const int wq = warp - 6;                           // 0..3
-    const int row = wq * 32 + lane;
+    // query rows (query entry row / g, head r * g + row % g); this warp takes
+    // rows (wq + 2 q) * 32 + lane, both rows' loads in flight before the stores
+    const int wq = warp - 6;                           // 0 .. kLoaderWarps-1
+    constexpr int kRows = 128 / (32 * kLoaderWarps);   // query rows per thread
     int i = 0;
-    for (int u = blockIdx.x; u < n_units; u += gridDim.x, ++i) {
+    for (int u = first; u < n_units; u += step, ++i) {
       const int st = i & 1;
-      const uint32_t ph2 = (uint32_t)(i >> 1) & 1u, ph1 = (uint32_t)i & 1u;
-      int r, b, beta, e0, ne;
-      unit_at(u, r, b, beta, e0, ne);
-      if (!warp_wait(b_stage_empty + 8 * st, ph2 ^ 1, ctl)) break;
-      const uint32_t st_base = sbase + Lo::stage_off + st * Lo::kStage;
+      const uint32_t ph = (uint32_t)(i >> 1) & 1u;
+      const UnitInfo ui = unit_info(sp, u);
+      const uint4* src[kRows];
+      bool have[kRows];
+#pragma unroll
+      for (int q = 0; q < kRows; ++q) {
+        const int row = (wq + kLoaderWarps * q) * 32 + lane;
+        have[q] = row < ui.ne * g;
+        const int64_t t = have[q] ? __ldg(sp.qidx + ui.e0 + row / g) / sp.k : 0;
+        src[q] = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(sp.query) +
+                                                (t * p.H_q + ui.r * g + row % g) * (int64_t)kD);
+      }
+      if (!warp_wait(b_kq_empty + 8 * st, ph ^ 1u, ctl)) break;
       uint8_t* qtile = smem + Lo::stage_off + st * Lo::kStage;
-      // the unit's query rows (query entry row / g, head r * g + row % g)
-      if (row < ne * g) {
-        const int entry = __ldg(sp.qidx + e0 + row / g);
-        const int64_t t = entry / sp.k;
-        const int h = r * g + row % g;
-        const uint4* src = reinterpret_cast<const uint4*>(
-            static_cast<const uint16_t*>(sp.query) + (t * p.H_q + h) * (int64_t)kD);
-        uint4 v[16];
+      uint4 v[kRows][16];
 #pragma unroll
-        for (int c = 0; c < 16; ++c) v[c] = __ldg(src + c);
+      for (int q = 0; q < kRows; ++q)
 #pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          const int half = c >> 3, ch = c & 7;
-          *reinterpret_cast<uint4*>(qtile + half * kHalfBytes + row * 128 + ((ch ^ (row & 7)) << 4)) = v[c];
+        for (int c = 0; c < 16; ++c) v[q][c] = have[q] ? __ldg(src[q] + c) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+      for (int q = 0; q < kRows; ++q) {
+        const int row = (wq + kLoaderWarps * q) * 32 + lane;
+        if (have[q]) {
+#pragma unroll
+          for (int c = 0; c < 16; ++c) {
+            const int half = c >> 3, ch = c & 7;
+            *reinterpret_cast<uint4*>(qtile + half * kHalfBytes + row * 128 + ((ch ^ (row & 7)) << 4)) = v[q][c];
+          }
         }
       }
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(b_q_full + 8 * st);
-      // V^T: 8x8 transposes, rows = tokens (V page) -> rows = dims (K-major over tokens)
-      if (!warp_wait(b_v_full + 8 * st, ph2, ctl)) break;
-      if (!warp_wait(b_vt_empty, ph1 ^ 1, ctl)) break;
-      const uint32_t vraw = st_base + 2 * Lo::kTile;
-      const uint32_t vt = sbase + Lo::vt_off;
-      const int mi = lane >> 3, ri = lane & 7;
-#pragma unroll 4
-      for (int combo = wq; combo < 64; combo += 4) {
-        const int a = combo & 15;                       // token group 8a .. 8a+7
-        const int hd = (combo >> 4) & 1;                // dims 0..63 / 64..127
-        const int c0 = (combo >> 5) * 4;                // dim chunks c0 .. c0+3 of the half
-        const uint32_t src = vraw + hd * kHalfBytes + (8 * a + ri) * 128 + (((c0 + mi) ^ ri) << 4);
-        const int dim = 64 * hd + 8 * (c0 + mi) + ri;
-        const uint32_t dst = vt + (a >> 3) * kHalfBytes + dim * 128 + (((a & 7) ^ ri) << 4);
-        uint32_t frag[4];
-        ldsm_x4_trans(src, frag);
-        stsm_x4(dst, frag);
-      }
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(b_vt_full);
     }
   }
 
@@ -566,7 +704,7 @@ __global__ void combine_kernel(const SparseParams sp, float* __restrict__ out,
 
 }  // namespace
 
-cudaError_t launch_sparse_attention(const void* tm_k, const void* tm_v, const SparseParams& sp,
+cudaError_t launch_sparse_attention(const void* tm_q, const void* tm_k, const void* tm_v, const SparseParams& sp,
                                     bool bf16, float* out, float* lse, cudaStream_t s) {
   const Params& p = sp.p;
   const int64_t th = p.T * (int64_t)p.H_kv;
@@ -580,13 +718,18 @@ cudaError_t launch_sparse_attention(const void* tm_k, const void* tm_v, const Sp
   units_kernel<<<(unsigned)((sp.rows + threads - 1) / threads), threads, 0, s>>>(sp);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
-  auto k1 = bf16 ? sparse_k1_kernel<true> : sparse_k1_kernel<false>;
-  static std::atomic<uint64_t> configured[2][64];
+  // query rows by TMA when a query entry's g rows start on a 1 KiB boundary
+  const bool qtma = p.g % 8 == 0;
+  auto k1 = bf16 ? (qtma ? sparse_k1_kernel<true, true> : sparse_k1_kernel<true, false>)
+                 : (qtma ? sparse_k1_kernel<false, true> : sparse_k1_kernel<false, false>);
+  static std::atomic<uint64_t> configured[4][64];
   int dev = 0;
   if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
-  if ((e = ensure_smem_limit(k1, (int)K1Layout::bytes, configured[bf16 ? 1 : 0], dev)) != cudaSuccess)
+  if ((e = ensure_smem_limit(k1, (int)K1Layout::bytes, configured[(bf16 ? 2 : 0) + (qtma ? 1 : 0)], dev)) !=
+      cudaSuccess)
     return e;
-  k1<<<(unsigned)p.num_sms, kK1Threads, K1Layout::bytes, s>>>(*static_cast<const CUtensorMap*>(tm_k),
+  k1<<<(unsigned)p.num_sms, kK1Threads, K1Layout::bytes, s>>>(*static_cast<const CUtensorMap*>(tm_q),
+                                                               *static_cast<const CUtensorMap*>(tm_k),
                                                                *static_cast<const CUtensorMap*>(tm_v), sp);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   const int64_t rows = p.T * (int64_t)p.H_q;
