@@ -696,7 +696,7 @@ def sparse_run(case, prep, device, stream, peaks, steps: int):
            "us_per_call": us, "tflops": tfl, "gbs": gbs, "algorithmic_flops": flops,
            "algorithmic_bytes": nbytes, "selected_blocks": nblocks, "bound": bound,
            "frac": (tfl / peaks["bf16_tflops"]) if bound == "tensor" else (gbs / peaks["hbm_gbs"]),
-           "partials_bytes": case.T * case.H_q * 16 * (case.D + 1) * 4 * 2,
+           "partials_bytes": case.T * case.H_q * 16 * (case.D * 2 + 4) * 2,
            "kernels": "count, scan, scatter, units, K1 (sparse_k1_kernel), K2 (combine); 2 memsets"}
     del vbase, value, out, lse
     return res

@@ -682,7 +682,7 @@ SparseLayout sparse_layout(const msa_index_score_args* a, int k) {
   l.unit_ptr = off; off += up256(4 * (size_t)(l.rows + 1));
   l.qidx = off;     off += up256(4 * (size_t)l.entries);
   l.units = off;    off += up256(16 * (size_t)l.entries);
-  l.o_part = off;   off += up256(4 * (size_t)a->T * a->H_q * k * a->D);
+  l.o_part = off;   off += up256(2 * (size_t)a->T * a->H_q * k * a->D);   // 16-bit partials
   l.lse_part = off; off += up256(4 * (size_t)a->T * a->H_q * k);
   l.bytes = off;
   return l;
@@ -750,7 +750,7 @@ msa_status_t msa_sparse_attention(const msa_index_score_args* args,
   sp.unit_ptr = reinterpret_cast<int32_t*>(w + lo.unit_ptr);
   sp.qidx = reinterpret_cast<int32_t*>(w + lo.qidx);
   sp.units = reinterpret_cast<int4*>(w + lo.units);
-  sp.o_part = reinterpret_cast<float*>(w + lo.o_part);
+  sp.o_part = reinterpret_cast<uint16_t*>(w + lo.o_part);
   sp.lse_part = reinterpret_cast<float*>(w + lo.lse_part);
   // K and V pages through the key cache's tensor-map recipe; the query map
   // with a run of one position (a box is one query entry's g heads)

@@ -13,7 +13,8 @@
 //               the 128 MMA rows (sec. 5.9), S = Q K^T on the tensor cores, a
 //               masked softmax of each row over the block's visible keys, O = P V
 //               with P read from tensor memory; each (query, head, selected
-//               block) gets a partial (O normalised by its own sum, LSE);
+//               block) gets a partial (O normalised by its own sum, in the
+//               input's 16-bit type; LSE in fp32);
 //   K2          per (query, head) the partials are merged by the exact
 //               log-sum-exp identity (sec. 5.10).
 //
@@ -177,10 +178,10 @@ struct K1Layout {
   static constexpr uint32_t kTile = 32768;
   static constexpr uint32_t kStage = 3 * kTile;          // Q, K, V
   static constexpr uint32_t stage_off = 0;
-  static constexpr uint32_t kORow = 128 + 16;            // 32 fp32 columns + a 16-byte pad
+  static constexpr uint32_t kORow = 64 + 16;             // 32 16-bit columns + a 16-byte pad
   static constexpr uint32_t kOWarp = 32 * kORow;
   static constexpr uint32_t ostage_off = 2 * kStage;
-  static constexpr uint32_t bar_off = ostage_off + 4 * kOWarp;
+  static constexpr uint32_t bar_off = ostage_off + 8 * kOWarp;
   static constexpr uint32_t n_bars = 9 * 2 + 1;
   static constexpr uint32_t misc_off = bar_off + n_bars * 8;
   static constexpr uint32_t end = misc_off + 16;
@@ -189,8 +190,8 @@ struct K1Layout {
 static_assert(K1Layout::bytes <= 232448, "shared memory per CTA");
 static_assert(K1Layout::kStage % 1024 == 0 && K1Layout::ostage_off % 1024 == 0, "1 KiB aligned tiles");
 
-constexpr int kK1Threads = 256;       // 8 warps
-constexpr int kLoaderWarps = 2;
+constexpr int kK1Threads = 352;       // 11 warps
+constexpr int kVWarp = 10;            // the V-page producer
 // tensor memory: two buffers of [S (128 columns, P over its first 64) | O (128 columns)]
 constexpr uint32_t kBufCols = 256, kColO = 128;
 
@@ -307,16 +308,19 @@ __device__ __forceinline__ RowInfo row_fin(const SparseParams& sp, const RowPre&
   return ri;
 }
 
-// Roles: warp 0 TMA producer (the K and V pages, and the query rows when g is a
-// multiple of 8: one g-row box per query entry and half), warp 1 TMEM owner +
-// MMA issuer, warps 2..5 softmax and partial stores (thread = MMA row = TMEM
-// lane), warps 6..7 gather the query rows when g is not a multiple of 8.
+// Roles: warp 0 producer of the K page and the query rows (the rows by TMA
+// when g is a multiple of 8, one g-row box per query entry and half, else
+// gathered by the warp's lanes), warp 10 producer of the V page, warp 1 TMEM
+// owner + MMA issuer, warps 2..9 two groups of four softmax warps (group =
+// unit index % 2) that also store the partials.
 // Units are taken round-robin (unit i of CTA c is c + i * gridDim.x); every
 // role walks the same sequence.  Unit i uses stage i % 2 and tensor-memory
-// buffer i % 2.  Q and K of a stage are released when S = Q K^T is done, V
-// when O = P V is; the MMA warp issues S(i) before O(i-1), and the softmax
-// warps turn S(i) into P(i) before they store O(i-1), so the P V product of one
-// unit runs under the softmax of the next.
+// buffer i % 2, which belong to softmax group i % 2.  Q and K of a stage are
+// released when S = Q K^T is done, V when O = P V is; the MMA warp issues S(i)
+// before O(i-1), and each softmax group turns S(i) into P(i) before it stores
+// O(i-2), so one group's softmax runs while the other stores and the tensor
+// core works on both.  (10 warps and more cap a thread at 168 registers, so a
+// softmax warp reads S in 64- and 32-column pieces and O in two halves.)
 template <bool BF16, bool QTMA>
 __global__ void __launch_bounds__(kK1Threads, 1)
     sparse_k1_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -330,7 +334,7 @@ __global__ void __launch_bounds__(kK1Threads, 1)
   const uint32_t bars = sbase + Lo::bar_off;
   const uint32_t b_k_full = bars;                 // [2] K page (and, by TMA, the query rows) landed
   const uint32_t b_v_full = b_k_full + 16;        // [2] V page landed
-  const uint32_t b_q_full = b_v_full + 16;        // [2] query rows written (the loader warps)
+  const uint32_t b_q_full = b_v_full + 16;        // [2] query rows written (gathered by the producer warp)
   const uint32_t b_kq_empty = b_q_full + 16;      // [2] the stage's Q K^T product done (Q, K free)
   const uint32_t b_v_empty = b_kq_empty + 16;     // [2] the stage's P V product done (V free)
   const uint32_t b_s_full = b_v_empty + 16;       // [2] S in the buffer
@@ -347,7 +351,7 @@ __global__ void __launch_bounds__(kK1Threads, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(b_k_full + 8 * i, 1);
       mbar_init(b_v_full + 8 * i, 1);
-      mbar_init(b_q_full + 8 * i, kLoaderWarps);
+      mbar_init(b_q_full + 8 * i, 1);
       mbar_init(b_kq_empty + 8 * i, 1);
       mbar_init(b_v_empty + 8 * i, 1);
       mbar_init(b_s_full + 8 * i, 1);
@@ -381,7 +385,7 @@ __global__ void __launch_bounds__(kK1Threads, 1)
     // -------------------------------------------------------- producer --
     const bool paged = p.layout != 2;
     const uint64_t pol = l2_policy_evict_last();      // a block's pages serve all its units
-    uint32_t n_k[2] = {0, 0}, n_v[2] = {0, 0};
+    uint32_t n_k[2] = {0, 0};
     int i = 0;
     for (int u = first; u < n_units; u += step, ++i) {
       const int st = i & 1;
@@ -419,15 +423,40 @@ __global__ void __launch_bounds__(kK1Threads, 1)
                           64 * x, ui.r * g, t);
         }
       }
-      ++n_k[st];
-      if (!warp_wait(b_v_empty + 8 * st, ph ^ 1u, ctl)) break;
-      if (lane == 0) {
-        mbar_arrive_expect_tx(b_v_full + 8 * st, Lo::kTile);
-        for (int x = 0; x < 2; ++x)
-          tma_k(st_base + 2 * Lo::kTile + x * kHalfBytes, &tm_v, b_v_full + 8 * st, 64 * x, tok, ui.r, page,
-                p.layout, pol);
+      if (!QTMA) {
+        // the unit's query rows (query entry row / g, head r * g + row % g):
+        // lane l takes rows l + 32 q, two rows' loads in flight at a time
+        uint8_t* qtile = smem + Lo::stage_off + st * Lo::kStage;
+#pragma unroll
+        for (int q0 = 0; q0 < 4; q0 += 2) {
+          uint4 v[2][16];
+#pragma unroll
+          for (int q = 0; q < 2; ++q) {
+            const int row = (q0 + q) * 32 + lane;
+            const bool have = row < ui.ne * g;
+            const int64_t t = have ? __ldg(sp.qidx + ui.e0 + row / g) / sp.k : 0;
+            const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(sp.query) +
+                                                              (t * p.H_q + ui.r * g + row % g) * (int64_t)kD);
+#pragma unroll
+            for (int c = 0; c < 16; ++c) v[q][c] = have ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
+          }
+#pragma unroll
+          for (int q = 0; q < 2; ++q) {
+            const int row = (q0 + q) * 32 + lane;
+            if (row < ui.ne * g) {
+#pragma unroll
+              for (int c = 0; c < 16; ++c) {
+                const int half = c >> 3, ch = c & 7;
+                *reinterpret_cast<uint4*>(qtile + half * kHalfBytes + row * 128 + ((ch ^ (row & 7)) << 4)) = v[q][c];
+              }
+            }
+          }
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(b_q_full + 8 * st);
       }
-      ++n_v[st];
+      ++n_k[st];
     }
     // teardown: the last loads of each stage may still be in flight
     if (lane == 0) {
@@ -436,9 +465,7 @@ __global__ void __launch_bounds__(kK1Threads, 1)
         if (n_k[st])
           while (!mbar_try_wait(b_k_full + 8 * st, (n_k[st] - 1) & 1u) && global_timer_ns() - t0 < kDrainLimitNs) {
           }
-        if (n_v[st])
-          while (!mbar_try_wait(b_v_full + 8 * st, (n_v[st] - 1) & 1u) && global_timer_ns() - t0 < kDrainLimitNs) {
-          }
+
       }
     }
     __syncwarp();
@@ -500,31 +527,66 @@ __global__ void __launch_bounds__(kK1Threads, 1)
       }
     }
     __syncwarp();
-  } else if (warp >= 2 && warp < 6) {
+  } else if (warp == kVWarp) {
+    // ------------------------------------------------------ V producer --
+    // The V page of unit i goes into stage i % 2 once O = P V of unit i - 2
+    // is done; a warp of its own, so that the K and query loads of the next
+    // units never wait behind it.
+    if (lane == 0) {
+      const bool paged = p.layout != 2;
+      const uint64_t pol = l2_policy_evict_last();
+      uint32_t n_v[2] = {0, 0};
+      int i = 0;
+      for (int u = first; u < n_units; u += step, ++i) {
+        const int st = i & 1;
+        const uint32_t ph = (uint32_t)(i >> 1) & 1u;
+        const UnitInfo ui = unit_info(sp, u);
+        int page = 0, tok = 0;
+        if (paged) {
+          page = __ldg(p.block_table + (int64_t)ui.b * p.MB + ui.beta);
+          if (page < 0 || (int64_t)page >= p.NP) page = (int32_t)(p.NP < 0x7fffffffLL ? p.NP : 0x7fffffffLL);
+        } else {
+          tok = __ldg(p.cu_k + ui.b) + ui.beta * kP;
+        }
+        if (!mbar_wait(b_v_empty + 8 * st, ph ^ 1u, ctl)) break;
+        mbar_arrive_expect_tx(b_v_full + 8 * st, Lo::kTile);
+        const uint32_t vdst = sbase + Lo::stage_off + st * Lo::kStage + 2 * Lo::kTile;
+        for (int x = 0; x < 2; ++x)
+          tma_k(vdst + x * kHalfBytes, &tm_v, b_v_full + 8 * st, 64 * x, tok, ui.r, page, p.layout, pol);
+        ++n_v[st];
+      }
+      // teardown: the last V load of each stage may still be in flight
+      for (int st = 0; st < 2; ++st) {
+        const uint64_t t0 = global_timer_ns();
+        if (n_v[st])
+          while (!mbar_try_wait(b_v_full + 8 * st, (n_v[st] - 1) & 1u) && global_timer_ns() - t0 < kDrainLimitNs) {
+          }
+      }
+    }
+    __syncwarp();
+  } else {
     // --------------------------------------------------------- softmax --
+    // Two groups of four warps take alternate units: group grp handles units
+    // i = grp, grp + 2, ... of this CTA, whose tensor-memory buffer is grp.
+    // Thread = MMA row = TMEM lane of the warp's quarter.
+    const int grp = (warp - 2) >> 2;
     const int quarter = warp & 3;
-    const int row = quarter * 32 + lane;              // MMA row = TMEM lane
-    const uint32_t t_lane = tmem_base + ((uint32_t)(quarter * 32) << 16);
-    uint8_t* ostage = smem + Lo::ostage_off + quarter * Lo::kOWarp;
+    const int row = quarter * 32 + lane;
+    const uint32_t t_s = tmem_base + ((uint32_t)(quarter * 32) << 16) + grp * kBufCols;   // S / P; O at + kColO
+    uint8_t* ostage = smem + Lo::ostage_off + (warp - 2) * Lo::kOWarp;
     const float ninf = __int_as_float(0xff800000);
     const float kscale = sp.sm_scale * 1.4426950408889634f;   // base-2 softmax
     bool ok = true;
     RowInfo prev{};                                    // the unit whose O is stored next
     float prev_l = 0.f, prev_m = 0.f;
-    // store O(j) of the previous unit (normalised) and its LSE.  A quarter of
-    // the warp's 32 rows (32 columns each) at a time goes through the warp's
-    // staging area: each thread writes its row's 128 bytes, then every store
-    // instruction writes four whole 128-byte row segments.
+    // store O(j) (j = the group's previous unit), normalised, and its LSE.  O
+    // comes out of tensor memory in two 64-column halves; each 32-column
+    // quarter of the warp's rows goes through the warp's staging area (each
+    // thread writes its row's 64 bytes), then every store instruction writes
+    // eight 64-byte row segments.
     auto store_o = [&](int j) -> bool {
-      const int bj = j & 1;
-      if (!warp_wait(b_o_full + 8 * bj, (uint32_t)(j >> 1) & 1u, ctl)) return false;
+      if (!warp_wait(b_o_full + 8 * grp, (uint32_t)(j >> 1) & 1u, ctl)) return false;
       tc_fence_after();
-      float x[128];
-      tmem_ld128(t_lane + bj * kBufCols + kColO, x);
-      tmem_wait_ld();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(b_o_empty + 8 * bj);
       int64_t slot = -1;
       float inv = 0.f;
       if (prev.valid) {
@@ -534,125 +596,111 @@ __global__ void __launch_bounds__(kK1Threads, 1)
         // natural-log LSE of the block's visible keys
         sp.lse_part[slot] = any ? (prev_m + __log2f(prev_l)) * 0.6931471805599453f : ninf;
       }
-      const int rsub = lane >> 3, chunk = lane & 7;  // read-back: row rsub + 4 it, 16-byte chunk
+      // the partial in the input's 16-bit type (fp16: clamped to the finite
+      // range; the exact value is at most max |V|, its rounding may step past it)
+      const float lim16 = BF16 ? 3.0e38f : 65504.f;
+      const int rsub = lane >> 2, chunk = lane & 3;  // read-back: row rsub + 8 it, 16-byte chunk
 #pragma unroll
-      for (int qc = 0; qc < 4; ++qc) {
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          const int col = 32 * qc + 4 * c;
-          *reinterpret_cast<float4*>(ostage + lane * Lo::kORow + 16 * c) =
-              make_float4(x[col] * inv, x[col + 1] * inv, x[col + 2] * inv, x[col + 3] * inv);
+      for (int hh = 0; hh < 2; ++hh) {
+        float x[64];
+        tmem_ld64(t_s + kColO + 64 * hh, x);
+        tmem_wait_ld();
+        if (hh == 1) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(b_o_empty + 8 * grp);
         }
-        __syncwarp();
 #pragma unroll
-        for (int it = 0; it < 8; ++it) {
-          const int rr = 4 * it + rsub;
-          const int64_t sl = __shfl_sync(0xffffffffu, slot, rr);
-          const float4 v = *reinterpret_cast<const float4*>(ostage + rr * Lo::kORow + 16 * chunk);
-          if (sl >= 0) __stcs(reinterpret_cast<float4*>(sp.o_part + sl * kD + 32 * qc) + chunk, v);
+        for (int qh = 0; qh < 2; ++qh) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int col = 32 * qh + 8 * c + 2 * e;
+              w[e] = pack2(fminf(fmaxf(x[col] * inv, -lim16), lim16), fminf(fmaxf(x[col + 1] * inv, -lim16), lim16),
+                           BF16);
+            }
+            *reinterpret_cast<uint4*>(ostage + lane * Lo::kORow + 16 * c) = make_uint4(w[0], w[1], w[2], w[3]);
+          }
+          __syncwarp();
+#pragma unroll
+          for (int it = 0; it < 4; ++it) {
+            const int rr = 8 * it + rsub;
+            const int64_t sl = __shfl_sync(0xffffffffu, slot, rr);
+            const uint4 v = *reinterpret_cast<const uint4*>(ostage + rr * Lo::kORow + 16 * chunk);
+            if (sl >= 0) __stcs(reinterpret_cast<uint4*>(sp.o_part + sl * kD + 64 * hh + 32 * qh) + chunk, v);
+          }
+          __syncwarp();
         }
-        __syncwarp();
       }
       return true;
     };
-    int i = 0;
-    RowInfo cur = first < n_units ? row_fin(sp, row_pre(sp, unit_info(sp, first), row), row) : RowInfo{};
+    const int u0 = first + grp * step, ustep = 2 * step;
+    int i = grp;
+    RowInfo cur = u0 < n_units ? row_fin(sp, row_pre(sp, unit_info(sp, u0), row), row) : RowInfo{};
     // unit descriptors are read at clamped indices (never past the last
     // unit); whether a unit exists is decided from u alone
-    int4 d_next = n_units > 0 ? __ldg(sp.units + min(first + step, n_units - 1)) : make_int4(0, 0, 0, 0);
-    for (int u = first; u < n_units; u += step, ++i) {
-      const int bi = i & 1;
-      // the next unit's row loads and the unit after's descriptor, issued now
-      // and used after this unit's softmax and the previous unit's store
+    int4 d_next = n_units > 0 ? __ldg(sp.units + min(u0 + ustep, n_units - 1)) : make_int4(0, 0, 0, 0);
+    for (int u = u0; u < n_units; u += ustep, i += 2) {
+      // the group's next unit's row loads and the descriptor of the one after,
+      // issued now and used after this unit's softmax and the previous store
       RowPre pre = row_pre(sp, unit_of(sp, d_next), row);
-      pre.valid = pre.valid && u + step < n_units;
-      const int4 d_after = __ldg(sp.units + min(u + 2 * step, n_units - 1));
-      if (!warp_wait(b_s_full + 8 * bi, (uint32_t)(i >> 1) & 1u, ctl)) { ok = false; break; }
+      pre.valid = pre.valid && u + ustep < n_units;
+      const int4 d_after = __ldg(sp.units + min(u + 2 * ustep, n_units - 1));
+      if (!warp_wait(b_s_full + 8 * grp, (uint32_t)(i >> 1) & 1u, ctl)) { ok = false; break; }
       tc_fence_after();
-      float x[128];
-      tmem_ld128(t_lane + bi * kBufCols, x);
-      tmem_wait_ld();
-      // row max over the visible columns (eight independent chains)
+      // pass 1: row max over the visible columns (eight independent chains)
       float mp[8];
 #pragma unroll
       for (int a = 0; a < 8; ++a) mp[a] = ninf;
 #pragma unroll
-      for (int c = 0; c < 128; ++c) {
-        x[c] = c <= cur.lim ? x[c] * kscale : ninf;
-        mp[c & 7] = fmaxf(mp[c & 7], x[c]);
+      for (int hh = 0; hh < 2; ++hh) {
+        float x[64];
+        tmem_ld64(t_s + 64 * hh, x);
+        tmem_wait_ld();
+#pragma unroll
+        for (int c = 0; c < 64; ++c)
+          if (64 * hh + c <= cur.lim) mp[c & 7] = fmaxf(mp[c & 7], x[c]);
       }
       const float m = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
-                            fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
+                            fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7]))) * kscale;
       const bool any = cur.lim >= 0;
+      // pass 2: p = 2^(s * scale - m) over each 32-column quarter; the 16
+      // packed pairs of quarter hq go to P columns 16 hq .. 16 hq + 15 (S
+      // columns this thread has already read)
       float lp[8];
 #pragma unroll
       for (int a = 0; a < 8; ++a) lp[a] = 0.f;
-      uint32_t pk[64];
 #pragma unroll
-      for (int c = 0; c < 64; ++c) {
-        const float a0 = any ? ex2(x[2 * c] - m) : 0.f;
-        const float a1 = any ? ex2(x[2 * c + 1] - m) : 0.f;
-        lp[c & 7] += a0 + a1;
-        pk[c] = pack2(a0, a1, BF16);
+      for (int hq = 0; hq < 4; ++hq) {
+        float x[32];
+        tmem_ld32(t_s + 32 * hq, x);
+        tmem_wait_ld();
+        uint32_t pk[16];
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          const int c0 = 32 * hq + 2 * c;
+          const float a0 = any && c0 <= cur.lim ? ex2(fmaf(x[2 * c], kscale, -m)) : 0.f;
+          const float a1 = any && c0 + 1 <= cur.lim ? ex2(fmaf(x[2 * c + 1], kscale, -m)) : 0.f;
+          lp[c & 7] += a0 + a1;
+          pk[c] = pack2(a0, a1, BF16);
+        }
+        tmem_st16(t_s + 16 * hq, pk);
       }
       const float l = ((lp[0] + lp[1]) + (lp[2] + lp[3])) + ((lp[4] + lp[5]) + (lp[6] + lp[7]));
-      // P over the first 64 columns of S (S is in registers now)
-      tmem_st64(t_lane + bi * kBufCols, pk);
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(b_p_full + 8 * bi);
-      if (i > 0 && !store_o(i - 1)) { ok = false; break; }
+      if (lane == 0) mbar_arrive(b_p_full + 8 * grp);
+      if (i >= 2 && !store_o(i - 2)) { ok = false; break; }
       prev = cur;
       prev_l = l;
       prev_m = m;
       cur = row_fin(sp, pre, row);
       d_next = d_after;
     }
-    if (ok && i > 0) store_o(i - 1);
-  } else if (!QTMA) {
-    // --------------------------------------------------------- loaders --
-    // query rows (query entry row / g, head r * g + row % g); this warp takes
-    // rows (wq + 2 q) * 32 + lane, both rows' loads in flight before the stores
-    const int wq = warp - 6;                           // 0 .. kLoaderWarps-1
-    constexpr int kRows = 128 / (32 * kLoaderWarps);   // query rows per thread
-    int i = 0;
-    for (int u = first; u < n_units; u += step, ++i) {
-      const int st = i & 1;
-      const uint32_t ph = (uint32_t)(i >> 1) & 1u;
-      const UnitInfo ui = unit_info(sp, u);
-      const uint4* src[kRows];
-      bool have[kRows];
-#pragma unroll
-      for (int q = 0; q < kRows; ++q) {
-        const int row = (wq + kLoaderWarps * q) * 32 + lane;
-        have[q] = row < ui.ne * g;
-        const int64_t t = have[q] ? __ldg(sp.qidx + ui.e0 + row / g) / sp.k : 0;
-        src[q] = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(sp.query) +
-                                                (t * p.H_q + ui.r * g + row % g) * (int64_t)kD);
-      }
-      if (!warp_wait(b_kq_empty + 8 * st, ph ^ 1u, ctl)) break;
-      uint8_t* qtile = smem + Lo::stage_off + st * Lo::kStage;
-      uint4 v[kRows][16];
-#pragma unroll
-      for (int q = 0; q < kRows; ++q)
-#pragma unroll
-        for (int c = 0; c < 16; ++c) v[q][c] = have[q] ? __ldg(src[q] + c) : make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
-      for (int q = 0; q < kRows; ++q) {
-        const int row = (wq + kLoaderWarps * q) * 32 + lane;
-        if (have[q]) {
-#pragma unroll
-          for (int c = 0; c < 16; ++c) {
-            const int half = c >> 3, ch = c & 7;
-            *reinterpret_cast<uint4*>(qtile + half * kHalfBytes + row * 128 + ((ch ^ (row & 7)) << 4)) = v[q][c];
-          }
-        }
-      }
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(b_q_full + 8 * st);
-    }
+    if (ok && i > grp) store_o(i - 2);
   }
 
   tc_fence_before();
@@ -666,6 +714,19 @@ __global__ void __launch_bounds__(kK1Threads, 1)
 // ------------------------------------------------------------------- K2 ----
 // Warp per (token, head): merges the partials of the token's selected blocks
 // with the log-sum-exp identity; lane l holds dims 4l .. 4l+3.
+__device__ __forceinline__ float4 load_partial(const uint16_t* src, bool bf16) {
+  const uint2 w = __ldcs(reinterpret_cast<const uint2*>(src));
+  if (bf16) {
+    const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w.x));
+    const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w.y));
+    return make_float4(a.x, a.y, b.x, b.y);
+  }
+  const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&w.x));
+  const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&w.y));
+  return make_float4(a.x, a.y, b.x, b.y);
+}
+
+template <bool BF16>
 __global__ void combine_kernel(const SparseParams sp, float* __restrict__ out,
                                float* __restrict__ lse) {
   const Params& p = sp.p;
@@ -688,7 +749,7 @@ __global__ void combine_kernel(const SparseParams sp, float* __restrict__ out,
     for (int s = 0; s < sp.k; ++s) {
       if (!entry_valid(__ldg(selrow + s), p.MB, L)) continue;
       const float w = __expf(sp.lse_part[rowid * sp.k + s] - mx);
-      const float4 o = reinterpret_cast<const float4*>(sp.o_part + (rowid * sp.k + s) * kD)[lane];
+      const float4 o = load_partial(sp.o_part + (rowid * sp.k + s) * kD + 4 * lane, BF16);
       acc.x += w * o.x;
       acc.y += w * o.y;
       acc.z += w * o.z;
@@ -733,7 +794,10 @@ cudaError_t launch_sparse_attention(const void* tm_q, const void* tm_k, const vo
                                                                *static_cast<const CUtensorMap*>(tm_v), sp);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   const int64_t rows = p.T * (int64_t)p.H_q;
-  if (rows > 0) combine_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(sp, out, lse);
+  if (rows > 0) {
+    if (bf16) combine_kernel<true><<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(sp, out, lse);
+    else combine_kernel<false><<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(sp, out, lse);
+  }
   return cudaGetLastError();
 }
 

@@ -346,7 +346,8 @@ msa_status_t msa_index_score_fp4_run(const msa_index_score_args *args, int32_t f
  *   lse    device fp32 [T, H_q], or NULL.
  *   workspace  msa_sparse_attention_workspace_size() bytes (256-byte aligned,
  *          caller-owned): the block -> query lists, the work units and the
- *          per-block partials (T * H_q * k * (D + 1) floats).
+ *          per-block partials (T * H_q * k * D outputs in the input's 16-bit
+ *          type and T * H_q * k fp32 log-sum-exps).
  *
  * Errors: as msa_index_score, plus MSA_ERR_INVALID_ARG for a missing value
  * cache or selection, k outside [1, 32] or a dtype other than fp16 / bf16.
