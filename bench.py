@@ -525,6 +525,14 @@ def run_ours(args):
 
     case = make_workload(args)
     key = workload_key(args)
+    if args.sparse_only:
+        # the sparse main branch alone on this workload (a profiler's target)
+        prep = bs.from_case(case, device)
+        rec = sparse_run(case, prep, device, stream, peaks, args.steps or 10)
+        if rank == 0:
+            print(json.dumps({"impl": "ours", "sparse_attention": rec, "config": config_block(case, key)}),
+                  flush=True)
+        return
     steps = default_steps(args)
     traffic = args.traffic
     if traffic is None:
@@ -800,6 +808,8 @@ def main(argv=None):
     ap.add_argument("--no-sub", action="store_true",
                     help="measure the selected workload only (no sub-records)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sparse-only", action="store_true",
+                    help="time only the sparse main branch (msa_sparse_attention) on the workload")
     ap.add_argument("--traffic", type=float, default=None,
                     help="DRAM bytes per launch of the score kernel from an ncu capture")
     args = ap.parse_args(argv)

@@ -73,25 +73,34 @@ __device__ __forceinline__ bool entry_valid(int beta, int MB, int64_t L) {
 }
 
 // ------------------------------------------------------------ CSR build ----
-// Thread per (token, kv head): validates the selection row and counts its
-// entries into the rows of the block -> query lists.
+// Thread per (kv head, token), tokens fastest: validates the selection row
+// and counts its entries into the rows of the block -> query lists.  Lanes of
+// a warp that name the same list (neighbouring tokens share most of their
+// blocks) add to it with one atomic.
 __global__ void count_kernel(const SparseParams sp) {
   const Params& p = sp.p;
   const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (idx >= p.T * (int64_t)p.H_kv) return;
-  const int64_t t = idx / p.H_kv;
-  const int r = (int)(idx - t * p.H_kv);
+  const bool live = idx < p.T * (int64_t)p.H_kv;
+  const int r = live ? (int)(idx / p.T) : 0;
+  const int64_t t = live ? idx - (int64_t)r * p.T : 0;
   const int b = request_search(p.cu_q, p.B, t);
   const int64_t L = kv_length(sp, b);
-  const int32_t* row = sp.sel + idx * sp.k;
+  const int32_t* row = sp.sel + (t * p.H_kv + r) * sp.k;
   SparseHeader* hdr = reinterpret_cast<SparseHeader*>(p.ws);
+  const int lane = threadIdx.x & 31;
   int prev = -1, err = 0;
   for (int s = 0; s < sp.k; ++s) {
-    const int beta = __ldg(row + s);
-    if (beta < 0) { prev = 0x7fffffff; continue; }      // -1 tail: nothing may follow
-    if (beta <= prev || beta >= p.MB) err = 1;           // not ascending, repeated, or beyond MB
-    prev = beta;
-    if (entry_valid(beta, p.MB, L)) atomicAdd(sp.cnt + ((int64_t)r * p.B + b) * p.MB + beta, 1);
+    const int beta = live ? __ldg(row + s) : -1;
+    if (beta < 0) {
+      prev = 0x7fffffff;                                 // -1 tail: nothing may follow
+    } else {
+      if (beta <= prev || beta >= p.MB) err = 1;         // not ascending, repeated, or beyond MB
+      prev = beta;
+    }
+    const bool valid = live && entry_valid(beta, p.MB, L);
+    const long long list = valid ? ((long long)r * p.B + b) * p.MB + beta : -1ll - lane;
+    const uint32_t peers = __match_any_sync(0xffffffffu, list);
+    if (valid && lane == __ffs(peers) - 1) atomicAdd(sp.cnt + list, __popc(peers));
   }
   if (err) atomicOr(&hdr->err, kErrSelection);
 }
@@ -139,22 +148,31 @@ __global__ void __launch_bounds__(1024) scan_kernel(const SparseParams sp) {
   }
 }
 
-// Thread per (token, kv head): writes token * k + slot into its blocks' lists.
+// Thread per (kv head, token), tokens fastest: writes token * k + slot into
+// its blocks' lists; lanes that name the same list take consecutive positions
+// from one atomic.
 __global__ void scatter_kernel(const SparseParams sp) {
   const Params& p = sp.p;
   const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (idx >= p.T * (int64_t)p.H_kv) return;
-  const int64_t t = idx / p.H_kv;
-  const int r = (int)(idx - t * p.H_kv);
+  const bool live = idx < p.T * (int64_t)p.H_kv;
+  const int r = live ? (int)(idx / p.T) : 0;
+  const int64_t t = live ? idx - (int64_t)r * p.T : 0;
   const int b = request_search(p.cu_q, p.B, t);
   const int64_t L = kv_length(sp, b);
-  const int32_t* row = sp.sel + idx * sp.k;
+  const int32_t* row = sp.sel + (t * p.H_kv + r) * sp.k;
+  const int lane = threadIdx.x & 31;
   for (int s = 0; s < sp.k; ++s) {
-    const int beta = __ldg(row + s);
-    if (!entry_valid(beta, p.MB, L)) continue;
-    const int64_t list = ((int64_t)r * p.B + b) * p.MB + beta;
-    const int pos = atomicAdd(sp.cursor + list, 1);
-    sp.qidx[pos] = (int32_t)(t * sp.k + s);
+    const int beta = live ? __ldg(row + s) : -1;
+    const bool valid = live && entry_valid(beta, p.MB, L);
+    const long long list = valid ? ((long long)r * p.B + b) * p.MB + beta : -1ll - lane;
+    const uint32_t peers = __match_any_sync(0xffffffffu, list);
+    if (valid) {
+      const int leader = __ffs(peers) - 1;
+      int base = 0;
+      if (lane == leader) base = atomicAdd(sp.cursor + list, __popc(peers));
+      base = __shfl_sync(peers, base, leader);
+      sp.qidx[base + __popc(peers & ((1u << lane) - 1u))] = (int32_t)(t * sp.k + s);
+    }
   }
 }
 
