@@ -126,15 +126,18 @@ def dominant_kernel(case) -> str:
 
 def launches_per_call(case) -> int:
     """Kernels one call launches: the plan, the tile kernel unless the host
-    length bound puts every request on the short path, and, for int8 keys with
-    a query-row group of at most 32, the short-query kernel."""
+    length bound puts every request on the short path (with int8 paged keys
+    preceded by the conversion of their pages into the fp16 mirror), and, for
+    int8 keys with a query-row group of at most 32, the short-query kernel."""
     g = case.H_q // case.H_kv
     if getattr(case, "fp4", None):
         return 3            # query dequantisation, plan, tile kernel
-    short_ok = case.key.dtype == torch.int8 and g <= 32
+    i8 = case.key.dtype == torch.int8
+    short_ok = i8 and g <= 32
     max_q = max(case.q_lens) if case.q_lens else 0
     tile = not (short_ok and max_q > 0 and max_q * g <= 32)
-    return 1 + (1 if tile else 0) + (1 if short_ok else 0)
+    mirror = tile and i8 and case.layout.upper() != "TND"
+    return 1 + (1 if tile else 0) + (1 if mirror else 0) + (1 if short_ok else 0)
 
 
 def recorded_traffic(workload_key: str, kernel: str):

@@ -376,6 +376,29 @@ msa_status_t make_maps(const msa_index_score_args* a, const msa::Params& p, CUte
   return MSA_OK;
 }
 
+// The fp16 mirror of an int8 paged key cache (query-tile requests read their
+// pages from it): [NP, H_kv, P, D] fp16, compact pages; 0 when not used.
+size_t mirror_bytes(const msa_index_score_args* a) {
+  if (!a || a->k_dtype != MSA_I8 || a->layout == MSA_LAYOUT_TND) return 0;
+  return (size_t)a->NP * (size_t)a->H_kv * (size_t)a->P * (size_t)a->D * 2;
+}
+
+// One 128-token page of one kv head of the mirror: box (64 elements, 128
+// tokens, 1, 1), 128-byte swizzled like a 16-bit key page.
+msa_status_t make_mirror_map(const msa_index_score_args* a, void* mirror, CUtensorMap* m) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return fail(MSA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  const cuuint64_t D = (cuuint64_t)a->D, P = (cuuint64_t)a->P;
+  cuuint64_t dims[4] = {D, P, (cuuint64_t)a->H_kv, (cuuint64_t)a->NP};
+  cuuint64_t strides[3] = {D * 2, P * D * 2, (cuuint64_t)a->H_kv * P * D * 2};
+  cuuint32_t box[4] = {64, 128, 1, 1};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  CUresult r = encode_cached(enc, m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, mirror, dims, strides, box, es,
+                             CU_TENSOR_MAP_SWIZZLE_128B);
+  if (r != CUDA_SUCCESS) return fail(MSA_ERR_CUDA, "key mirror tensor map: CUresult %d", (int)r);
+  return MSA_OK;
+}
+
 }  // namespace
 
 namespace msa {
@@ -426,7 +449,7 @@ msa_status_t msa_index_score_workspace_size(const msa_index_score_args* args, si
   msa_status_t st = validate(args);
   if (st != MSA_OK) return st;
   if (!bytes) return fail(MSA_ERR_INVALID_ARG, "bytes is NULL");
-  *bytes = msa::workspace_bytes_for(args->B);
+  *bytes = msa::workspace_bytes_for(args->B) + mirror_bytes(args);
   return MSA_OK;
 }
 
@@ -440,8 +463,10 @@ msa_status_t launch_plan_checked(const msa::Params& p, cudaStream_t s) {
   return MSA_OK;
 }
 
+// mirror: the fp16 copy of the int8 key pages in the workspace, or null (the
+// converter warps then convert each page per query tile).
 msa_status_t launch_score_checked(const msa_index_score_args* args, const msa::Params& p,
-                                  cudaStream_t s) {
+                                  cudaStream_t s, void* mirror = nullptr) {
   // short-query requests exist only for int8 keys and when a query row group
   // fits 32 MMA columns
   const bool short_ok = args->k_dtype == MSA_I8 && p.g <= msa::kShortRows;
@@ -456,7 +481,12 @@ msa_status_t launch_score_checked(const msa_index_score_args* args, const msa::P
       short_ok && args->max_seqlen_q > 0 && (int64_t)args->max_seqlen_q * p.g <= msa::kShortRows;
   cudaError_t e = cudaSuccess;
   if (!short_only) {
-    if (i8)
+    if (i8 && mirror) {
+      CUtensorMap tm;
+      if ((st = make_mirror_map(args, mirror, &tm)) != MSA_OK) return st;
+      e = msa::launch_i8_mirror(p, args->key_cache, args->page_stride, mirror, s);
+      if (e == cudaSuccess) e = msa::launch_score_i8_mirror(&tq, &tm, p, s);
+    } else if (i8)
       e = msa::launch_score_i8(&tq, &tk, p, s);
     else if (is_f8(args->q_dtype))
       e = msa::launch_score_f8(&tq, &tk, p, args->q_dtype == MSA_E5M2, s);
@@ -466,6 +496,14 @@ msa_status_t launch_score_checked(const msa_index_score_args* args, const msa::P
   if (e == cudaSuccess && short_ok) e = msa::launch_short_i8(&tqs, &tks, p, s);
   if (e != cudaSuccess) return cuda_fail(e, "score kernel launch");
   return MSA_OK;
+}
+
+// The mirror's place in a workspace of `bytes` (after the plan), or null if
+// it is not used or does not fit.
+void* mirror_in(const msa_index_score_args* args, void* ws, size_t bytes) {
+  const size_t m = mirror_bytes(args), plan = msa::workspace_bytes_for(args->B);
+  if (!m || !ws || bytes < plan + m) return nullptr;
+  return static_cast<uint8_t*>(ws) + plan;
 }
 
 // Shared front half of the entry points: validation, empty-call shortcut,
@@ -502,7 +540,8 @@ msa_status_t msa_index_score_run(const msa_index_score_args* args, float* out, v
   bool empty = false;
   msa_status_t st = prepare(args, out, true, workspace, workspace_bytes, p, empty);
   if (st != MSA_OK || empty) return st;
-  return launch_score_checked(args, p, reinterpret_cast<cudaStream_t>(stream));
+  return launch_score_checked(args, p, reinterpret_cast<cudaStream_t>(stream),
+                              mirror_in(args, workspace, workspace_bytes));
 }
 
 msa_status_t msa_index_score(const msa_index_score_args* args, float* out, void* workspace,
@@ -513,7 +552,7 @@ msa_status_t msa_index_score(const msa_index_score_args* args, float* out, void*
   if (st != MSA_OK || empty) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if ((st = launch_plan_checked(p, s)) != MSA_OK) return st;
-  return launch_score_checked(args, p, s);
+  return launch_score_checked(args, p, s, mirror_in(args, workspace, workspace_bytes));
 }
 
 msa_status_t msa_index_score_topk_workspace_size(const msa_index_score_args* args, int32_t k,
@@ -523,7 +562,8 @@ msa_status_t msa_index_score_topk_workspace_size(const msa_index_score_args* arg
   if ((st = validate_select(args, k)) != MSA_OK) return st;
   if (!bytes) return fail(MSA_ERR_INVALID_ARG, "bytes is NULL");
   const SelectPlan sp = select_plan(args, k);
-  *bytes = sp.plan_bytes + sp.cand_bytes;
+  const size_t mb = mirror_bytes(args);
+  *bytes = mb ? (sp.plan_bytes + sp.cand_bytes + 255) / 256 * 256 + mb : sp.plan_bytes + sp.cand_bytes;
   return MSA_OK;
 }
 
@@ -551,8 +591,13 @@ msa_status_t msa_index_score_topk(const msa_index_score_args* args, int32_t k, i
   p.chunk_min[0] = sp.chunk_min[0];
   p.chunk_min[1] = sp.chunk_min[1];
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  // the fp16 mirror of int8 key pages after the candidate lists (256-byte
+  // aligned), if it fits
+  const size_t mb = mirror_bytes(args);
+  const size_t moff = (sp.plan_bytes + sp.cand_bytes + 255) / 256 * 256;
+  void* mirror = mb && workspace_bytes >= moff + mb ? static_cast<uint8_t*>(workspace) + moff : nullptr;
   if ((st = launch_plan_checked(p, s)) != MSA_OK) return st;
-  if ((st = launch_score_checked(args, p, s)) != MSA_OK) return st;
+  if ((st = launch_score_checked(args, p, s, mirror)) != MSA_OK) return st;
   cudaError_t e = msa::launch_group_select(p, local_slot ? 1 : 0, indices, s);
   if (e != cudaSuccess) return cuda_fail(e, "selection kernel launch");
   return MSA_OK;

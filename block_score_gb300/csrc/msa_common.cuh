@@ -230,6 +230,13 @@ cudaError_t launch_score_f8(const void* tmap_q, const void* tmap_k, const Params
                             cudaStream_t s);
 cudaError_t launch_score_i8(const void* tmap_q, const void* tmap_k, const Params& p,
                             cudaStream_t s);
+// int8 keys read from their fp16 mirror (tmap_k maps the mirror, BNBD order)
+cudaError_t launch_score_i8_mirror(const void* tmap_q, const void* tmap_k, const Params& p,
+                                   cudaStream_t s);
+// The int8 key pages of the query-tile requests into the fp16 mirror [NP, H_kv, P, D]
+// (paged layouts; page_stride in elements of the int8 cache).
+cudaError_t launch_i8_mirror(const Params& p, const void* key, int64_t page_stride, void* mirror,
+                             cudaStream_t s);
 cudaError_t launch_short_i8(const void* tmap_q, const void* tmap_k, const Params& p,
                             cudaStream_t s);
 // FP4 keys: the tile kernel with E2M1 pages dequantised into 16-bit operands

@@ -51,11 +51,16 @@
 
 namespace msa {
 
-template <bool KI8>
+// Key modes: 0 = fp16 / bf16 / fp8 keys, 1 = int8 (or FP4) keys converted by
+// converter warps, 2 = int8 keys already converted into an fp16 copy of the
+// pages (the mirror; TMA straight into the K slots, the scales loaded beside).
+__host__ __device__ constexpr int tile_mode(bool ki8, bool km) { return ki8 ? 1 : (km ? 2 : 0); }
+
+template <int MODE>
 struct TileCfg;
 
 template <>
-struct TileCfg<false> {           // fp16 / bf16 / fp8 keys: TMA straight into the K slots
+struct TileCfg<0> {               // fp16 / bf16 / fp8 keys: TMA straight into the K slots
   static constexpr int kThreads = 384;         // the last warp feeds the MMA warp
   static constexpr int kSlots = 5;
   static constexpr int kRaw = 0;
@@ -66,7 +71,18 @@ struct TileCfg<false> {           // fp16 / bf16 / fp8 keys: TMA straight into t
 };
 
 template <>
-struct TileCfg<true> {            // int8 keys: raw pages, converters, scales
+struct TileCfg<2> {               // int8 keys from the fp16 mirror: TMA into the K slots, scales by bulk copy
+  static constexpr int kThreads = 384;         // the last warp feeds the MMA warp
+  static constexpr int kSlots = 4;             // one slot fewer than mode 0: room for the scale ring
+  static constexpr int kRaw = 0;
+  static constexpr int kScPairs = 4;
+  static constexpr int kGroups = 2;
+  static constexpr int kQBufs = 2;
+  static constexpr int kCvtGroups = 0;
+};
+
+template <>
+struct TileCfg<1> {               // int8 keys: raw pages, converters, scales
   static constexpr int kThreads = 640;         // the last warp feeds the MMA warp
   static constexpr int kCvtGroups = 2;         // page j of every pair by group j
   static constexpr int kSlots = 3;
@@ -76,9 +92,9 @@ struct TileCfg<true> {            // int8 keys: raw pages, converters, scales
   static constexpr int kQBufs = 1;             // the shared memory goes to the raw ring
 };
 
-template <bool KI8>
+template <int MODE>
 struct TileLayout {
-  using Cfg = TileCfg<KI8>;
+  using Cfg = TileCfg<MODE>;
   static constexpr int kQBufs = Cfg::kQBufs;
   static constexpr int kAcc = 2;                               // accumulators of 256 columns
   static constexpr int kGroups = Cfg::kGroups;                 // epilogue groups
@@ -97,17 +113,18 @@ struct TileLayout {
   static constexpr uint32_t bytes = end + 1024;                // + alignment slack
 };
 
-static_assert(TileLayout<false>::bytes <= 232448, "shared memory per CTA");
-static_assert(TileLayout<true>::bytes <= 232448, "shared memory per CTA");
+static_assert(TileLayout<0>::bytes <= 232448 && TileLayout<1>::bytes <= 232448 &&
+                  TileLayout<2>::bytes <= 232448,
+              "shared memory per CTA");
 
 // Every writer of shared memory stays inside its own region, so nothing but
 // mbarrier operations and tcgen05.commit ever touches the barrier words:
 // regions in address order without overlap, 128-byte-swizzled operand tiles
 // on 1 KiB boundaries, and each copy no larger than its destination.
-template <bool KI8>
+template <int MODE>
 constexpr bool tile_layout_ok() {
-  using L = TileLayout<KI8>;
-  using C = TileCfg<KI8>;
+  using L = TileLayout<MODE>;
+  using C = TileCfg<MODE>;
   return L::q_off % 1024 == 0 && L::k_off % 1024 == 0 && L::raw_off % 1024 == 0 &&
          kRawStride % 1024 == 0 && L::kSlotBytes % 1024 == 0 &&
          L::q_off + L::kQBufs * kTileBytes <= L::k_off &&                 // Q box: <= 128 rows x 256 B
@@ -119,7 +136,8 @@ constexpr bool tile_layout_ok() {
          L::bar_off % 8 == 0 && L::bar_off + L::n_bars * 8 <= L::misc_off &&
          L::misc_off + 16 + 4 * C::kRaw <= L::end && L::end + 1024 <= L::bytes;
 }
-static_assert(tile_layout_ok<false>() && tile_layout_ok<true>(), "tile kernel shared-memory layout");
+static_assert(tile_layout_ok<0>() && tile_layout_ok<1>() && tile_layout_ok<2>(),
+              "tile kernel shared-memory layout");
 
 // A claim costs an atomic and a chain of dependent L2 round trips (the search
 // over the unit prefix sums, the request record, the first table entries):
@@ -151,16 +169,21 @@ constexpr uint32_t kCodeLive = 1, kCodeFirst = 2, kCodeLast = 4, kCodeLone = 8, 
 // elements, fp16 operands), 2 = MXFP4 (E8M0 scale per 32, bf16 operands): the
 // converters dequantise each E2M1 element by its group scale exactly, so the
 // epilogue has no per-token scale to apply.
-template <bool KI8, bool BF16, int F8 = 0, int TOPK = 0, int KF4 = 0>
-__global__ void __launch_bounds__(TileCfg<KI8>::kThreads, 1)
+// KM (without KI8): int8 keys read from their fp16 mirror (tm_k maps the
+// mirror, BNBD order), the per-token scales bulk-copied by the producer into
+// the scale ring, the int8 epilogue.
+template <bool KI8, bool BF16, int F8 = 0, int TOPK = 0, int KF4 = 0, bool KM = false>
+__global__ void __launch_bounds__(TileCfg<tile_mode(KI8, KM)>::kThreads, 1)
     tile_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const Params p) {
   static_assert(F8 == 0 || !KI8, "FP8 operands come with FP8 keys");
   static_assert(KF4 == 0 || KI8, "FP4 pages go through the converter warps");
+  static_assert(!KM || (!KI8 && F8 == 0 && !BF16), "the int8 mirror: fp16 query, no converters");
   constexpr bool kF8 = F8 != 0;
   constexpr int kHalves = kF8 ? 1 : 2;             // K slots (and Q boxes) per pair of blocks
-  using Cfg = TileCfg<KI8>;
-  using L = TileLayout<KI8>;
+  constexpr int kMode = tile_mode(KI8, KM);
+  using Cfg = TileCfg<kMode>;
+  using L = TileLayout<kMode>;
   constexpr int PS = Cfg::kSlots;
   constexpr int R = Cfg::kRaw;
   constexpr int SC = Cfg::kScPairs;
@@ -218,7 +241,7 @@ __global__ void __launch_bounds__(TileCfg<KI8>::kThreads, 1)
       mbar_init(b_acc_empty + 8 * i, 4 * L::kGroups);
     }
     for (int i = 0; i < SC; ++i) {
-      mbar_init(b_sc_full + 8 * i, 4 * Cfg::kCvtGroups);
+      mbar_init(b_sc_full + 8 * i, KM ? 1 : 4 * Cfg::kCvtGroups);   // the producer, or the converter warps
       mbar_init(b_sc_empty + 8 * i, 4 * L::kGroups);
     }
     mbar_init(b_drain, 1);
@@ -288,8 +311,8 @@ __global__ void __launch_bounds__(TileCfg<KI8>::kThreads, 1)
       const uint32_t q_bytes = (uint32_t)kHalves * 128u * (uint32_t)(p.g * p.np);
       const bool paged = p.layout != 2;
       const int32_t page_oob = (int32_t)(p.NP < 0x7fffffffLL ? p.NP : 0x7fffffffLL);
-      uint32_t ss = 0, sph = 0, qb = 0, qph = 0, ks = 0, kph = 0;
-      uint32_t n_q = 0, n_k = 0;   // loads issued (for the teardown drain)
+      uint32_t ss = 0, sph = 0, qb = 0, qph = 0, ks = 0, kph = 0, scs = 0, scph = 0;
+      uint32_t n_q = 0, n_k = 0, n_sc = 0;   // loads issued (for the teardown drain)
       for (;;) {
         if (!mbar_wait(b_sched_full + 8 * ss, sph, ctl)) break;
         const UnitDesc d = ring[ss];
@@ -365,15 +388,40 @@ __global__ void __launch_bounds__(TileCfg<KI8>::kThreads, 1)
             }
           } else {
             // K half x of both pages into one slot: page j's 128 rows at j * 16 KiB
+            // (the mirror is in BNBD order)
             for (int x = 0; x < kHalves && ok; ++x) {
               if (!mbar_wait(b_k_empty + 8 * ks, kph ^ 1, ctl)) { ok = false; break; }
               const uint32_t kdst = sbase + L::k_off + ks * L::kSlotBytes;
               mbar_arrive_expect_tx(b_k_full + 8 * ks, (uint32_t)nblk * kHalfBytes);
               for (int j = 0; j < nblk; ++j)
                 tma_k(kdst + (uint32_t)j * kHalfBytes, &tm_k, b_k_full + 8 * ks, 64 * x, tok[j], d.hk,
-                      page[j], p.layout, pol_k);
+                      page[j], KM ? 1 : p.layout, pol_k);
               ++n_k;
               if (++ks == PS) { ks = 0; kph ^= 1; }
+            }
+            if constexpr (KM) {
+              // the pair's per-token scales into the scale ring (pages outside
+              // [0, NP) load as zeros above; their scales are written as zeros)
+              if (ok && !mbar_wait(b_sc_empty + 8 * scs, scph ^ 1, ctl)) ok = false;
+              if (ok) {
+                uint32_t sb = 0;
+                for (int j = 0; j < nblk; ++j) {
+                  if ((int64_t)page[j] < p.NP) {
+                    sb += kRawScaleBytes;
+                  } else {
+                    float* z = scale_s + scs * 256 + j * 128;
+                    for (int c = 0; c < 128; ++c) z[c] = 0.f;
+                  }
+                }
+                mbar_arrive_expect_tx(b_sc_full + 8 * scs, sb);
+                for (int j = 0; j < nblk; ++j)
+                  if ((int64_t)page[j] < p.NP)
+                    bulk_load(sbase + L::sc_off + (uint32_t)(scs * 256 + j * 128) * 4u,
+                              p.scale + ((int64_t)page[j] * p.H_kv + d.hk) * kP, kRawScaleBytes,
+                              b_sc_full + 8 * scs);
+                ++n_sc;
+                if (++scs == SC) { scs = 0; scph ^= 1; }
+              }
             }
           }
           if (!ok) break;
@@ -394,6 +442,14 @@ __global__ void __launch_bounds__(TileCfg<KI8>::kThreads, 1)
         const uint32_t st = j % L::kQBufs, ph = (j / L::kQBufs) & 1u;
         const uint64_t t0 = global_timer_ns();
         while (!mbar_try_wait(b_q_full + 8 * st, ph) && global_timer_ns() - t0 < kDrainLimitNs) {
+        }
+      }
+      if constexpr (KM) {
+        for (uint32_t j = n_sc > (uint32_t)SC ? n_sc - SC : 0; j < n_sc; ++j) {
+          const uint32_t st = j % SC, ph = (j / SC) & 1u;
+          const uint64_t t0 = global_timer_ns();
+          while (!mbar_try_wait(b_sc_full + 8 * st, ph) && global_timer_ns() - t0 < kDrainLimitNs) {
+          }
         }
       }
     }
@@ -538,6 +594,71 @@ __global__ void __launch_bounds__(TileCfg<KI8>::kThreads, 1)
         if (++ab == L::kAcc) { ab = 0; aph ^= 1; }
         if (!warp_wait(b_acc_full + 8 * a, a_ph, ctl)) { ok = false; break; }
         tc_fence_after();
+        if constexpr (KM) {
+          // this group's block of the pair from the fp16 mirror: the 16-bit
+          // path's TMEM loads, then DEQUANT (column multiply by the per-token
+          // scale) before the mask
+          const uint32_t s = sc, s_ph = scph;
+          if (++sc == SC) { sc = 0; scph ^= 1; }
+          if (!warp_wait(b_sc_full + 8 * s, s_ph, ctl)) { ok = false; break; }
+          const int col = beta + grp;
+          const bool has = col < d.b1;
+          const bool ld = warp_valid && has;
+          const float4* sv = reinterpret_cast<const float4*>(scale_s + s * 256 + grp * 128);
+          float m = ninf;
+          if constexpr (TOPK != 0) {          // the running selection holds registers
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+              float x[64];
+              if (ld) {
+                tmem_ld64(t_lane + a * 256u + (uint32_t)grp * 128u + 64u * hf, x);
+                tmem_wait_ld();
+              }
+              if (hf == 1) {
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(b_acc_empty + 8 * a);
+              }
+              if (ld && valid) {
+#pragma unroll
+                for (int c = 0; c < 16; ++c) {
+                  const float4 s4 = sv[16 * hf + c];
+                  x[4 * c + 0] *= s4.x;
+                  x[4 * c + 1] *= s4.y;
+                  x[4 * c + 2] *= s4.z;
+                  x[4 * c + 3] *= s4.w;
+                }
+                m = fmaxf(m, masked_max<64>(x, lim - col * kP - 64 * hf));
+              }
+            }
+          } else {
+            float x[128];
+            if (ld) {
+              tmem_ld128(t_lane + a * 256u + (uint32_t)grp * 128u, x);
+              tmem_wait_ld();
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(b_acc_empty + 8 * a);
+            if (ld && valid) {
+#pragma unroll
+              for (int c = 0; c < 32; ++c) {
+                const float4 s4 = sv[c];
+                x[4 * c + 0] *= s4.x;
+                x[4 * c + 1] *= s4.y;
+                x[4 * c + 2] *= s4.z;
+                x[4 * c + 3] *= s4.w;
+              }
+              m = masked_max<128>(x, lim - col * kP);
+            }
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(b_sc_empty + 8 * s);
+          if (!has || forced(col)) m = fill_value(col);
+          if (valid && write_out) __stcs(orow + col, m);
+          select(m, col);
+          continue;
+        }
         if constexpr (KI8) {
           // this group's block of the pair.  DEQUANT: column multiply by the
           // per-token scale, before the mask; 64-column pieces keep the
@@ -806,10 +927,10 @@ __global__ void __launch_bounds__(TileCfg<KI8>::kThreads, 1)
 
 // Launch one instantiation: persistent grid of one CTA per SM, programmatic
 // dependent launch after the plan kernel.
-template <bool KI8, bool BF16, int F8, int TOPK, int KF4 = 0>
+template <bool KI8, bool BF16, int F8, int TOPK, int KF4 = 0, bool KM = false>
 inline cudaError_t launch_tile_variant(const void* tq, const void* tk, const Params& p, cudaStream_t s) {
-  using L = TileLayout<KI8>;
-  auto kern = tile_kernel<KI8, BF16, F8, TOPK, KF4>;
+  using L = TileLayout<tile_mode(KI8, KM)>;
+  auto kern = tile_kernel<KI8, BF16, F8, TOPK, KF4, KM>;
   static std::atomic<uint64_t> configured[64];   // per device: context the limit was raised in
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -818,7 +939,7 @@ inline cudaError_t launch_tile_variant(const void* tq, const void* tk, const Par
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)p.num_sms);
-  cfg.blockDim = dim3(TileCfg<KI8>::kThreads);
+  cfg.blockDim = dim3(TileCfg<tile_mode(KI8, KM)>::kThreads);
   cfg.dynamicSmemBytes = L::bytes;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
@@ -831,11 +952,11 @@ inline cudaError_t launch_tile_variant(const void* tq, const void* tk, const Par
 }
 
 // The plain scores, or the fused per-group selection when p.topk_k > 0.
-template <bool KI8, bool BF16, int F8>
+template <bool KI8, bool BF16, int F8, bool KM = false>
 inline cudaError_t launch_tile(const void* tq, const void* tk, const Params& p, cudaStream_t s) {
-  if (p.topk_k <= 0) return launch_tile_variant<KI8, BF16, F8, 0>(tq, tk, p, s);
-  return p.g >= 8 ? launch_tile_variant<KI8, BF16, F8, 2>(tq, tk, p, s)
-                  : launch_tile_variant<KI8, BF16, F8, 16>(tq, tk, p, s);
+  if (p.topk_k <= 0) return launch_tile_variant<KI8, BF16, F8, 0, 0, KM>(tq, tk, p, s);
+  return p.g >= 8 ? launch_tile_variant<KI8, BF16, F8, 2, 0, KM>(tq, tk, p, s)
+                  : launch_tile_variant<KI8, BF16, F8, 16, 0, KM>(tq, tk, p, s);
 }
 
 }  // namespace msa

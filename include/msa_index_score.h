@@ -137,7 +137,13 @@ int32_t msa_abi_version(void);
 /* Output shape {H_q, T, RoundUp(MB, 16)} (guide sec. 5, 8.5).  Host-only, validates args. */
 msa_status_t msa_index_score_out_shape(const msa_index_score_args *args, int64_t shape[3]);
 
-/* Bytes of device workspace one call needs (>= 256, grows with B).  Host-only. */
+/* Bytes of device workspace one call needs (>= 256, grows with B).  Host-only.
+ * With int8 keys in a paged layout it also holds an fp16 copy of the key pages
+ * [NP, H_kv, P, D] (NP * H_kv * P * D * 2 bytes): the pages of requests scored
+ * by query tiles are converted into it once per call instead of once per tile
+ * (every int8 value is exact in fp16; the scale is applied to the dot products
+ * as before).  A workspace of only the plan's size (the value for 16-bit keys
+ * with the same B) is also accepted; those pages are then converted per tile. */
 msa_status_t msa_index_score_workspace_size(const msa_index_score_args *args, size_t *bytes);
 
 /*

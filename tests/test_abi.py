@@ -77,6 +77,20 @@ def test_out_shape_rounds_mb_to_16(lib):
     assert st == 0 and shape == (8, 32, 272)
 
 
+def test_workspace_holds_the_int8_key_mirror(lib):
+    # int8 paged keys: the plan plus an fp16 copy of the pages [NP, H_kv, P, D];
+    # TND int8 keys and 16-bit keys: the plan only
+    plan, i8, i8_tnd = ctypes.c_size_t(), ctypes.c_size_t(), ctypes.c_size_t()
+    assert lib.msa_index_score_workspace_size(ctypes.byref(_args()), ctypes.byref(plan)) == 0
+    a = _args(k_dtype=2, q_dtype=0, scale=16)
+    assert lib.msa_index_score_workspace_size(ctypes.byref(a), ctypes.byref(i8)) == 0
+    assert i8.value == plan.value + a.NP * a.H_kv * a.P * a.D * 2
+    t = _args(k_dtype=2, q_dtype=0, scale=16, layout=2, block_table=None, kv_len=None,
+              cu_seqlens_k=16, page_stride=128)
+    assert lib.msa_index_score_workspace_size(ctypes.byref(t), ctypes.byref(i8_tnd)) == 0
+    assert i8_tnd.value == plan.value
+
+
 def test_workspace_size_grows_with_batch(lib):
     n1, n2 = ctypes.c_size_t(), ctypes.c_size_t()
     assert lib.msa_index_score_workspace_size(ctypes.byref(_args(B=1)), ctypes.byref(n1)) == 0

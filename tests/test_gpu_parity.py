@@ -171,6 +171,25 @@ def test_int8_unit_scale_bit_exact_mode0(dev, layout):
     assert_parity(out, oracle.oracle_full(case), exact=True, what=f"int8 exact mode0 {layout}")
 
 
+@pytest.mark.parametrize("layout", ["BBND", "BNBD"])
+def test_int8_converter_path_without_mirror(dev, layout):
+    # a workspace with room for the plan only: query-tile requests convert each
+    # int8 page per tile in the converter warps instead of reading the fp16
+    # mirror; same bit-exact scores
+    import block_score_gb300 as bs
+    case = synth.make_case([2, 70, 1, 130], [300, 900, 128, 4100], H_q=16, H_kv=2,
+                           layout=layout, q_dtype=torch.float16, k_dtype=torch.int8,
+                           q_kind="int_small", k_kind="int8_full", scale_const=1.0,
+                           MB=33, init_blocks=1, local_blocks=2, seed=360)
+    prep = bs.from_case(case, dev)
+    mirror = case.key.shape[0] * case.H_kv * case.P * case.D * 2
+    assert prep.ws_bytes > mirror
+    prep.ws_bytes -= mirror
+    out = prep().cpu()
+    assert prep.device_error() == 0
+    assert_parity(out, oracle.oracle_full(case), exact=True, what=f"int8 converter path {layout}")
+
+
 def test_strided_cache_poisoned_gaps(dev):
     case = synth.make_case([20, 3], [500, 260], H_q=8, H_kv=1, layout="BBND",
                            q_dtype=torch.float16, q_kind="abs_randn", MB=6, page_gap=2,
