@@ -190,6 +190,22 @@ def test_int8_converter_path_without_mirror(dev, layout):
     assert_parity(out, oracle.oracle_full(case), exact=True, what=f"int8 converter path {layout}")
 
 
+@pytest.mark.parametrize("layout", ["BBND", "BNBD"])
+def test_int8_mirror_strided_cache(dev, layout):
+    # int8 keys in a paged cache with a gap page after every page (dim0 stride
+    # of two pages, the gaps filled with 127): the conversion into the fp16
+    # mirror reads each page through the page stride; integer query, unit
+    # scale, so the scores are exact
+    case = synth.make_case([70, 1, 130], [900, 300, 4100], H_q=16, H_kv=2, layout=layout,
+                           q_dtype=torch.float16, k_dtype=torch.int8, q_kind="int_small",
+                           k_kind="int8_full", scale_const=1.0, MB=33, page_gap=2,
+                           init_blocks=1, local_blocks=2, seed=370 + (layout == "BNBD"))
+    assert case.key.stride(0) == 2 * case.key[0].numel()
+    out, err, _ = run_gpu(case, dev)
+    assert err == 0
+    assert_parity(out, oracle.oracle_full(case), exact=True, what=f"int8 mirror strided {layout}")
+
+
 def test_strided_cache_poisoned_gaps(dev):
     case = synth.make_case([20, 3], [500, 260], H_q=8, H_kv=1, layout="BBND",
                            q_dtype=torch.float16, q_kind="abs_randn", MB=6, page_gap=2,

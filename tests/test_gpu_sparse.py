@@ -145,3 +145,34 @@ def test_sparse_attention_reports_a_bad_selection(dev):
     sel = torch.tensor([[[2, 1, -1]], [[0, 0, -1]], [[1, 3, -1]]], dtype=torch.int32, device=dev)
     prep.sparse_attention(value, sel)
     assert prep.sparse_device_error() & 0x20
+
+
+@pytest.mark.parametrize("n", [3, 5])
+def test_sparse_attention_benchmark_workload_sampled(dev, n):
+    # the bench's sparse record at full size (varlen prefill; long-context
+    # prefill, T = 16384 at kv_len 131072): the fused top-16 selection of the
+    # workload, random values in the key cache's layout, 256 sampled (token,
+    # head) rows against the oracle
+    import block_score_gb300 as bs
+    case = synth.config(n)
+    prep = bs.from_case(case, dev)
+    sel = prep.topk(16, local_slot=True, scores=False)
+    assert prep.select_device_error() == 0
+    value = value_like(case, seed=90 + n)
+    out, lse = prep.sparse_attention(to_dev(value, dev), sel)
+    assert prep.sparse_device_error() == 0
+    rng = np.random.default_rng(n)
+    rows = np.sort(rng.choice(case.T * case.H_q, 256, replace=False))
+    O_ref, L_ref = sparse_attention(case, value, sel.cpu(), rows=rows.tolist())
+    t, h = rows // case.H_q, rows % case.H_q
+    got_o = out.cpu().double().numpy()[t, h]
+    got_l = lse.cpu().double().numpy()[t, h]
+    ref_o, ref_l = O_ref[t, h], L_ref[t, h]
+    empty = np.isneginf(ref_l)
+    assert np.array_equal(np.isneginf(got_l), empty)
+    assert np.all(got_o[empty] == 0)
+    u = 2.0 ** -8 if value.dtype == torch.bfloat16 else 2.0 ** -11
+    dO = np.abs(got_o[~empty] - ref_o[~empty])
+    assert dO.max(initial=0) <= 2 * u * float(value.abs().max()) + 1e-5
+    dL = np.abs(got_l[~empty] - ref_l[~empty])
+    assert (dL <= 1e-4 + 1e-5 * np.abs(ref_l[~empty])).all()
