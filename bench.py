@@ -131,7 +131,10 @@ def launches_per_call(case) -> int:
     int8 keys with a query-row group of at most 32, the short-query kernel."""
     g = case.H_q // case.H_kv
     if getattr(case, "fp4", None):
-        return 3            # query dequantisation, plan, tile kernel
+        # query dequantisation, plan, tile kernel; a prefill-heavy call on paged
+        # keys (T * g >= 128 * B) also converts its key pages into the mirror
+        mirror = case.layout.upper() != "TND" and case.T * g >= 128 * case.B
+        return 4 if mirror else 3
     i8 = case.key.dtype == torch.int8
     short_ok = i8 and g <= 32
     max_q = max(case.q_lens) if case.q_lens else 0

@@ -383,9 +383,23 @@ size_t mirror_bytes(const msa_index_score_args* a) {
   return (size_t)a->NP * (size_t)a->H_kv * (size_t)a->P * (size_t)a->D * 2;
 }
 
+// FP4 paged keys: the same 16-bit mirror, used when the call has at least one
+// full query tile per request on average (T * g >= 128 * B); a decode-heavy
+// call reads each page about once, and the conversion would only add traffic.
+size_t fp4_mirror_bytes(const msa_index_score_args* a) {
+  if (!a || a->layout == MSA_LAYOUT_TND) return 0;
+  return (size_t)a->NP * (size_t)a->H_kv * (size_t)a->P * (size_t)a->D * 2;
+}
+
+bool fp4_mirror_pays(const msa_index_score_args* a) {
+  const int64_t g = a->H_kv > 0 ? a->H_q / a->H_kv : 1;
+  return a->T * g >= (int64_t)msa::kTileRows * a->B;
+}
+
 // One 128-token page of one kv head of the mirror: box (64 elements, 128
 // tokens, 1, 1), 128-byte swizzled like a 16-bit key page.
-msa_status_t make_mirror_map(const msa_index_score_args* a, void* mirror, CUtensorMap* m) {
+msa_status_t make_mirror_map(const msa_index_score_args* a, void* mirror, CUtensorMap* m,
+                             bool bf16 = false) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return fail(MSA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
   const cuuint64_t D = (cuuint64_t)a->D, P = (cuuint64_t)a->P;
@@ -393,8 +407,8 @@ msa_status_t make_mirror_map(const msa_index_score_args* a, void* mirror, CUtens
   cuuint64_t strides[3] = {D * 2, P * D * 2, (cuuint64_t)a->H_kv * P * D * 2};
   cuuint32_t box[4] = {64, 128, 1, 1};
   cuuint32_t es[4] = {1, 1, 1, 1};
-  CUresult r = encode_cached(enc, m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, mirror, dims, strides, box, es,
-                             CU_TENSOR_MAP_SWIZZLE_128B);
+  CUresult r = encode_cached(enc, m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                             4, mirror, dims, strides, box, es, CU_TENSOR_MAP_SWIZZLE_128B);
   if (r != CUDA_SUCCESS) return fail(MSA_ERR_CUDA, "key mirror tensor map: CUresult %d", (int)r);
   return MSA_OK;
 }
@@ -614,7 +628,8 @@ msa_status_t msa_index_score_fp4_workspace_size(const msa_index_score_args* args
   if (format != MSA_FP4_MX && format != MSA_FP4_NV)
     return fail(MSA_ERR_INVALID_ARG, "format must be MSA_FP4_MX or MSA_FP4_NV");
   if (!bytes) return fail(MSA_ERR_INVALID_ARG, "bytes is NULL");
-  *bytes = msa::workspace_bytes_for(args->B) + fp4_query_bytes(args);
+  *bytes = msa::workspace_bytes_for(args->B) + fp4_query_bytes(args) +
+           (fp4_mirror_pays(args) ? fp4_mirror_bytes(args) : 0);
   return MSA_OK;
 }
 
@@ -685,7 +700,23 @@ msa_status_t msa_index_score_fp4_run(const msa_index_score_args* args, int32_t f
   const bool nv = format == MSA_FP4_NV;
   CUtensorMap tq, tk;
   if ((st = make_maps(args, p, &tq, &tk, nullptr, nullptr, q16, nv)) != MSA_OK) return st;
-  cudaError_t e = msa::launch_score_fp4(&tq, &tk, p, nv, reinterpret_cast<cudaStream_t>(stream));
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  // prefill-heavy calls on paged keys: dequantise each page once into the
+  // 16-bit mirror after the query, then the 16-bit tile kernel (BNBD order)
+  const size_t mb = fp4_mirror_pays(args) ? fp4_mirror_bytes(args) : 0;
+  const size_t moff = msa::workspace_bytes_for(args->B) + fp4_query_bytes(args);
+  cudaError_t e;
+  if (mb && workspace_bytes >= moff + mb) {
+    void* mirror = static_cast<uint8_t*>(workspace) + moff;
+    CUtensorMap tm;
+    if ((st = make_mirror_map(args, mirror, &tm, !nv)) != MSA_OK) return st;
+    e = msa::launch_fp4_mirror(p, args->key_cache, args->page_stride, nv, mirror, s);
+    msa::Params pm = p;
+    pm.layout = 1;   // the mirror's order; the table and kv_len are read as before
+    if (e == cudaSuccess) e = msa::launch_score_16(&tq, &tm, pm, !nv, s);
+  } else {
+    e = msa::launch_score_fp4(&tq, &tk, p, nv, s);
+  }
   if (e != cudaSuccess) return cuda_fail(e, "score kernel launch");
   return MSA_OK;
 }

@@ -237,6 +237,10 @@ cudaError_t launch_score_i8_mirror(const void* tmap_q, const void* tmap_k, const
 // (paged layouts; page_stride in elements of the int8 cache).
 cudaError_t launch_i8_mirror(const Params& p, const void* key, int64_t page_stride, void* mirror,
                              cudaStream_t s);
+// The FP4 key pages of every request into the 16-bit mirror [NP, H_kv, P, D]
+// (fp16 for NVFP4, bf16 for MXFP4; paged layouts; page stride in bytes).
+cudaError_t launch_fp4_mirror(const Params& p, const void* key, int64_t page_stride_bytes, bool nv,
+                              void* mirror, cudaStream_t s);
 cudaError_t launch_short_i8(const void* tmap_q, const void* tmap_k, const Params& p,
                             cudaStream_t s);
 // FP4 keys: the tile kernel with E2M1 pages dequantised into 16-bit operands

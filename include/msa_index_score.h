@@ -301,7 +301,11 @@ msa_status_t msa_index_score_topk(const msa_index_score_args *args, int32_t k, i
  *             [T2, H_kv, D/G]; 16-byte aligned.
  *   out       as msa_index_score.
  *   workspace msa_index_score_fp4_workspace_size() bytes (256-byte aligned,
- *             caller-owned): the plan and the dequantised query.
+ *             caller-owned): the plan and the dequantised query, and for a
+ *             prefill-heavy call on paged keys (T * g >= 128 * B) a 16-bit copy
+ *             of the dequantised key pages [NP, H_kv, P, D], which lets every
+ *             page be dequantised once per call instead of once per query tile
+ *             (a workspace without it is accepted: the slower route then).
  *
  * Errors as msa_index_score, plus MSA_ERR_INVALID_ARG for a bad format or a
  * missing or misaligned scale array.  Asynchronous on `stream`.

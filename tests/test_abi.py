@@ -181,7 +181,15 @@ def test_fp4_host_rules(lib):
     assert lib.msa_index_score_fp4_workspace_size(ctypes.byref(_args(**fp4)), 1, ctypes.byref(n)) == 0
     plan = ctypes.c_size_t()
     assert lib.msa_index_score_workspace_size(ctypes.byref(_args()), ctypes.byref(plan)) == 0
-    assert n.value == plan.value + 32 * 8 * 128 * 2           # + the dequantised query
+    # + the dequantised query + (T * g >= 128 * B: a prefill-heavy call) the
+    # 16-bit mirror of the key pages [NP, H_kv, P, D]
+    assert n.value == plan.value + 32 * 8 * 128 * 2 + 8 * 1 * 128 * 128 * 2
+    # a decode-heavy call (T * g < 128 * B): no mirror
+    nd, pd = ctypes.c_size_t(), ctypes.c_size_t()
+    dec = dict(fp4, T=2, B=2)
+    assert lib.msa_index_score_fp4_workspace_size(ctypes.byref(_args(**dec)), 1, ctypes.byref(nd)) == 0
+    assert lib.msa_index_score_workspace_size(ctypes.byref(_args(T=2, B=2)), ctypes.byref(pd)) == 0
+    assert nd.value == pd.value + (2 * 8 * 128 * 2 + 255) // 256 * 256
     assert lib.msa_index_score_fp4_workspace_size(ctypes.byref(_args(**fp4)), 7, ctypes.byref(n)) == 1
     assert lib.msa_index_score_workspace_size(ctypes.byref(_args(**fp4)), ctypes.byref(n)) == 1
     # one side FP4 only, a scale, a stride below a compact FP4 page

@@ -110,3 +110,25 @@ def test_fp4_benchmark_workload_sampled(dev, n):
     ref = oracle.oracle_rows(case, rows)
     got = out.reshape(-1, out.shape[2])[torch.tensor(rows)]
     assert_parity(got, ref, what=f"cfg{n} fp4 sampled")
+
+
+@pytest.mark.parametrize("fmt", ["mx", "nv"])
+@pytest.mark.parametrize("mirror", [True, False])
+def test_fp4_mirror_and_converter_paths(dev, fmt, mirror):
+    # a prefill-heavy call: with the full workspace the key pages are
+    # dequantised once into the 16-bit mirror and scored by the 16-bit tile
+    # kernel; with room for the plan and the query only, the converter warps
+    # dequantise each page per query tile.  Unit scales: both bit-exact.
+    import block_score_gb300 as bs
+    unit = 127 if fmt == "mx" else 0x38
+    case = synth.make_fp4_case([200, 1, 70], [900, 300, 4100], fmt=fmt, H_q=16, H_kv=2,
+                               layout="BNBD", MB=33, scale_codes=(unit, unit),
+                               init_blocks=1, local_blocks=2, seed=420 + (fmt == "nv"))
+    prep = bs.from_case(case, dev)
+    mirror_bytes = case.key.shape[0] * case.H_kv * case.P * case.D * 2
+    assert prep.ws_bytes > mirror_bytes          # T * g >= 128 * B: the mirror is sized in
+    if not mirror:
+        prep.ws_bytes -= mirror_bytes
+    out = prep().cpu()
+    assert prep.device_error() == 0
+    assert_parity(out, oracle.oracle_full(case), exact=True, what=f"fp4 {fmt} mirror={mirror}")
