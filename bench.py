@@ -421,8 +421,9 @@ def roofline_of(case, work, kern_ms, peaks, traffic):
         roof = {"bound": "hbm", "achieved": hbm_gbs_kernel, "peak": peaks["hbm_gbs"],
                 "unit": "GB/s", "frac": hbm_gbs_kernel / peaks["hbm_gbs"],
                 "traffic": traffic, "peak_source": peaks["source"] + " hbm_gbs"}
-    elif case.query.element_size() == 1:
+    elif case.query.element_size() == 1 and not getattr(case, "fp4", None):
         # FP8 operands: the measured bf16 peak times the nominal dense ratio 4.5 / 2.25
+        # (FP4 codes are bytes too, but they are multiplied on the 16-bit path)
         pk = peaks["bf16_tflops"] * 2.0
         roof = {"bound": "tensor", "achieved": tflops_kernel, "peak": pk, "unit": "TFLOP/s",
                 "frac": tflops_kernel / pk, "traffic": traffic,
