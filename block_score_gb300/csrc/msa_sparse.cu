@@ -758,21 +758,44 @@ __global__ void combine_kernel(const SparseParams sp, float* __restrict__ out,
   const int64_t L = kv_length(sp, b);
   const int32_t* selrow = sp.sel + (t * p.H_kv + r) * sp.k;
   const float ninf = __int_as_float(0xff800000);
-  float mx = ninf;
-  for (int s = 0; s < sp.k; ++s)
-    if (entry_valid(__ldg(selrow + s), p.MB, L)) mx = fmaxf(mx, sp.lse_part[rowid * sp.k + s]);
+  // lane s (< k) reads slot s's selection entry and log-sum-exp; the row's
+  // maximum and every slot's weight come from one round of loads
+  const bool valid = lane < sp.k && entry_valid(__ldg(selrow + lane), p.MB, L);
+  const float ls = valid ? sp.lse_part[rowid * sp.k + lane] : ninf;
+  float mx = ls;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  const float wl = valid && mx > ninf ? __expf(ls - mx) : 0.f;
+  float wsum = wl;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, o);
+  const uint32_t vmask = __ballot_sync(0xffffffffu, valid && mx > ninf);
+  // the valid slots' partial rows, four loads in flight at a time (lane l
+  // holds dims 4l .. 4l+3)
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  float wsum = 0.f;
-  if (mx > ninf) {
-    for (int s = 0; s < sp.k; ++s) {
-      if (!entry_valid(__ldg(selrow + s), p.MB, L)) continue;
-      const float w = __expf(sp.lse_part[rowid * sp.k + s] - mx);
-      const float4 o = load_partial(sp.o_part + (rowid * sp.k + s) * kD + 4 * lane, BF16);
-      acc.x += w * o.x;
-      acc.y += w * o.y;
-      acc.z += w * o.z;
-      acc.w += w * o.w;
-      wsum += w;
+  const uint16_t* base = sp.o_part + rowid * sp.k * (int64_t)kD + 4 * lane;
+  uint32_t m = vmask;
+  while (m) {
+    int sl[4];
+    int n = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      sl[j] = m ? __ffs(m) - 1 : 0;
+      if (m) { m &= m - 1; ++n; }
+    }
+    float4 o[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      o[j] = j < n ? load_partial(base + (int64_t)sl[j] * kD, BF16) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float w = __shfl_sync(0xffffffffu, wl, sl[j]);
+      if (j < n) {
+        acc.x += w * o[j].x;
+        acc.y += w * o[j].y;
+        acc.z += w * o[j].z;
+        acc.w += w * o[j].w;
+      }
     }
   }
   const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
