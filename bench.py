@@ -100,7 +100,7 @@ KERNEL_SOURCES = {
     "tile_kernel": ["msa_tile.cuh", "msa_units.cuh", "msa_ptx.cuh", "msa_common.cuh",
                     "msa_score_16.cu", "msa_score_i8.cu", "msa_score_f8.cu"],
     "short_kernel": ["msa_short.cuh", "msa_units.cuh", "msa_ptx.cuh", "msa_common.cuh",
-                     "msa_short.cu"],
+                     "msa_short.cu", "msa_short_fp4.cu"],
 }
 
 
@@ -117,30 +117,33 @@ def kernel_source_hash(kernel: str) -> str:
 
 def dominant_kernel(case) -> str:
     """The kernel that does the work of a workload: the short-query kernel when
-    every request is a short int8 request, else the tile kernel."""
+    every request is a short request with int8 or FP4 keys, else the tile kernel."""
     g = case.H_q // case.H_kv
-    short = case.key.dtype == torch.int8 and all(
+    short = (case.key.dtype == torch.int8 or bool(getattr(case, "fp4", None))) and all(
         lq == 0 or lq * g <= 32 for lq in case.q_lens)
     return "short_kernel" if short and any(lq > 0 for lq in case.q_lens) else "tile_kernel"
 
 
 def launches_per_call(case) -> int:
-    """Kernels one call launches: the plan, the tile kernel unless the host
-    length bound puts every request on the short path (with int8 paged keys
-    preceded by the conversion of their pages into the fp16 mirror), and, for
-    int8 keys with a query-row group of at most 32, the short-query kernel."""
+    """Kernels one call launches: the plan (FP4: after the query
+    dequantisation), the tile kernel unless the host length bound puts every
+    request on the short path (with int8 paged keys, and FP4 paged keys of a
+    prefill-heavy call, preceded by the conversion of their pages into the
+    16-bit mirror), and, for int8 or FP4 keys with a query-row group of at
+    most 32, the short-query kernel."""
     g = case.H_q // case.H_kv
-    if getattr(case, "fp4", None):
-        # query dequantisation, plan, tile kernel; a prefill-heavy call on paged
-        # keys (T * g >= 128 * B) also converts its key pages into the mirror
-        mirror = case.layout.upper() != "TND" and case.T * g >= 128 * case.B
-        return 4 if mirror else 3
+    fp4 = bool(getattr(case, "fp4", None))
     i8 = case.key.dtype == torch.int8
-    short_ok = i8 and g <= 32
+    short_ok = (i8 or fp4) and g <= 32
     max_q = max(case.q_lens) if case.q_lens else 0
     tile = not (short_ok and max_q > 0 and max_q * g <= 32)
-    mirror = tile and i8 and case.layout.upper() != "TND"
-    return 1 + (1 if tile else 0) + (1 if mirror else 0) + (1 if short_ok else 0)
+    paged = case.layout.upper() != "TND"
+    if fp4:
+        mirror = tile and paged and case.T * g >= 128 * case.B
+    else:
+        mirror = tile and i8 and paged
+    return ((2 if fp4 else 1) + (1 if tile else 0) + (1 if mirror else 0)
+            + (1 if short_ok else 0))
 
 
 def recorded_traffic(workload_key: str, kernel: str):

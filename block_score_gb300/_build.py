@@ -18,7 +18,7 @@ OBJ = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libmsa_index_score.so")
 SOURCES = ["msa_api.cu", "msa_plan.cu", "msa_score_16.cu", "msa_score_i8.cu",
            "msa_short.cu", "msa_noalloc.cu", "msa_topk.cu", "msa_score_f8.cu", "msa_select.cu",
-           "msa_score_fp4.cu", "msa_sparse.cu", "msa_mirror.cu"]
+           "msa_score_fp4.cu", "msa_sparse.cu", "msa_mirror.cu", "msa_short_fp4.cu"]
 HEADERS = ["msa_common.cuh", "msa_ptx.cuh", "msa_units.cuh", "msa_tile.cuh", "msa_short.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

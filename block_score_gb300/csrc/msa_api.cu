@@ -174,7 +174,7 @@ msa_status_t fill_params(const msa_index_score_args* a, float* out, void* ws, ms
   p.MB = a->MB;
   p.MBp = (int32_t)round16(a->MB);
   p.layout = (int32_t)a->layout;
-  p.k_int8 = a->k_dtype == MSA_I8 ? 1 : 0;
+  p.short_cls = (a->k_dtype == MSA_I8 || a->k_dtype == MSA_E2M1) ? 1 : 0;
   p.sparse_mode = a->sparse_mode;
   p.init_blocks = a->init_blocks;
   p.local_blocks = a->local_blocks;
@@ -698,15 +698,24 @@ msa_status_t msa_index_score_fp4_run(const msa_index_score_args* args, int32_t f
   if (st != MSA_OK || empty) return st;
   if (!k_scale) return fail(MSA_ERR_INVALID_ARG, "k_scale is required");
   const bool nv = format == MSA_FP4_NV;
-  CUtensorMap tq, tk;
-  if ((st = make_maps(args, p, &tq, &tk, nullptr, nullptr, q16, nv)) != MSA_OK) return st;
+  // short-query requests (Lq * g <= 32 query rows) go to the short-query
+  // kernel, the others to the tile kernel; a host length bound that puts
+  // every request in the short class leaves the tile launch out
+  const bool short_ok = p.g <= msa::kShortRows;
+  const bool short_only =
+      short_ok && args->max_seqlen_q > 0 && (int64_t)args->max_seqlen_q * p.g <= msa::kShortRows;
+  CUtensorMap tq, tk, tqs, tks;
+  if ((st = make_maps(args, p, &tq, &tk, short_ok ? &tqs : nullptr, &tks, q16, nv)) != MSA_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  // prefill-heavy calls on paged keys: dequantise each page once into the
-  // 16-bit mirror after the query, then the 16-bit tile kernel (BNBD order)
+  // prefill-heavy calls on paged keys: dequantise the query-tile requests'
+  // pages once into the 16-bit mirror after the query, then the 16-bit tile
+  // kernel (BNBD order)
   const size_t mb = fp4_mirror_pays(args) ? fp4_mirror_bytes(args) : 0;
   const size_t moff = msa::workspace_bytes_for(args->B) + fp4_query_bytes(args);
-  cudaError_t e;
-  if (mb && workspace_bytes >= moff + mb) {
+  cudaError_t e = cudaSuccess;
+  if (short_only) {
+    // no query-tile request
+  } else if (mb && workspace_bytes >= moff + mb) {
     void* mirror = static_cast<uint8_t*>(workspace) + moff;
     CUtensorMap tm;
     if ((st = make_mirror_map(args, mirror, &tm, !nv)) != MSA_OK) return st;
@@ -717,6 +726,7 @@ msa_status_t msa_index_score_fp4_run(const msa_index_score_args* args, int32_t f
   } else {
     e = msa::launch_score_fp4(&tq, &tk, p, nv, s);
   }
+  if (e == cudaSuccess && short_ok) e = msa::launch_short_fp4(&tqs, &tks, p, nv, s);
   if (e != cudaSuccess) return cuda_fail(e, "score kernel launch");
   return MSA_OK;
 }

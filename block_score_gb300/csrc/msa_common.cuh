@@ -23,7 +23,7 @@ constexpr int kErrSelection = 0x20;   // a selection row out of range, repeated 
 // Requests are split into two classes, each consumed by its own kernel:
 //   class 0 ("tile" class): query tiles of floor(128/g) positions x g heads,
 //           QK^T with the query tile as the MMA's M side;
-//   class 1 ("short" class, int8 keys): Lq * g <= kShortRows, all query
+//   class 1 ("short" class, int8 or FP4 keys): Lq * g <= kShortRows, all query
 //           rows of the request as the MMA's N side against 128-token key
 //           pages (M side).
 constexpr int kShortRows = 32;
@@ -73,7 +73,7 @@ struct Params {
   int32_t np_short;            // positions the class-1 query box covers = floor(32 / g)
   int32_t B, MB, MBp;
   int32_t layout;          // 0 BBND, 1 BNBD, 2 TND
-  int32_t k_int8;          // keys are int8 (short-query class enabled)
+  int32_t short_cls;       // int8 or FP4 keys: the short-query class is enabled
   int32_t sparse_mode, init_blocks, local_blocks;
   int32_t max_q;            // host bound on every request's query length (0: none)
   int32_t num_sms;
@@ -160,9 +160,10 @@ __device__ inline ReqScratch read_request(const Params& p, int b, int& err) {
   const int64_t nb = (L + kP - 1) / kP;
   if (nb > p.MB) err |= kErrKvLen;
   r.L = (int)(L > 0x7fffffff ? 0x7fffffff : L);
-  // short class (int8 keys): every query row of the request fits the N side
-  // of one MMA; 16-bit keys stream through the tile kernel at HBM speed
-  r.cls = (p.k_int8 && r.Lq > 0 && (int64_t)r.Lq * p.g <= kShortRows) ? 1 : 0;
+  // short class (int8 or FP4 keys, converted per page): every query row of
+  // the request fits the N side of one MMA; 16-bit and FP8 keys stream
+  // through the tile kernel at HBM speed
+  r.cls = (p.short_cls && r.Lq > 0 && (int64_t)r.Lq * p.g <= kShortRows) ? 1 : 0;
   r.ntiles = r.cls ? 1 : cdiv(r.Lq, p.np);
   // the last query row sees the most blocks: q_pos = L - 1 in both modes
   r.nbc_max = L > 0 ? (int)(nb < p.MB ? nb : p.MB) : 0;
@@ -243,6 +244,10 @@ cudaError_t launch_fp4_mirror(const Params& p, const void* key, int64_t page_str
                               void* mirror, cudaStream_t s);
 cudaError_t launch_short_i8(const void* tmap_q, const void* tmap_k, const Params& p,
                             cudaStream_t s);
+// FP4 keys, short-query requests: the short-query kernel with E2M1 pages
+// dequantised into TMEM (nv: fp16 operands, else bf16).
+cudaError_t launch_short_fp4(const void* tmap_q, const void* tmap_k, const Params& p, bool nv,
+                             cudaStream_t s);
 // FP4 keys: the tile kernel with E2M1 pages dequantised into 16-bit operands
 // (nv: E4M3 scales per 16 elements, fp16 operands; else E8M0 per 32, bf16).
 cudaError_t launch_score_fp4(const void* tmap_q, const void* tmap_k, const Params& p, bool nv,

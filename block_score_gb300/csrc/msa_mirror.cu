@@ -13,8 +13,9 @@
 // them, sec. 7.1).
 //
 // The mirror keeps the cache's page indices, in BNBD order [NP, H_kv, P, D]
-// fp16 with compact pages.  Requests of the short-query class (Lq * g <= 32)
-// are scored from the int8 pages by the short-query kernel and are skipped.
+// 16-bit with compact pages.  Requests of the short-query class (Lq * g <= 32)
+// are scored from the int8 or FP4 pages by the short-query kernel and are
+// skipped.
 #include <cstdint>
 #include <cuda_runtime.h>
 
@@ -69,7 +70,7 @@ __global__ void __launch_bounds__(256)
   const int b = (int)(blockIdx.x / (unsigned)p.MB);
   const int beta = (int)(blockIdx.x - (unsigned)b * (unsigned)p.MB);
   const int64_t Lq = (int64_t)__ldg(p.cu_q + b + 1) - __ldg(p.cu_q + b);
-  if (Lq <= 0) return;
+  if (Lq <= 0 || Lq * p.g <= kShortRows) return;       // no query rows, or a short-query request
   const int64_t L = __ldg(p.kv_len + b);
   if (L <= 0) return;
   const int64_t nb = (L + kP - 1) / kP;
@@ -90,7 +91,7 @@ __global__ void __launch_bounds__(256)
       mirror[di] = fp4x8_to_f16(codes, e4m3_scale2(sb));
     } else {
       const uint32_t sb = __ldg(p.k_scale8 + srow * (kD / 32) + (w >> 2));
-      mirror[di] = fp4x8_to_bf16(codes, e8m0_scale2(sb));
+      mirror[di] = fp4x8_to_bf16(codes, e8m0_scale(sb));
     }
   }
 }

@@ -30,7 +30,7 @@ __global__ void fp4_dequant_query_kernel(const uint8_t* __restrict__ q,
     out[i] = fp4x8_to_f16(codes, e4m3_scale2(sb));
   } else {
     const uint32_t sb = __ldg(q_scale + row * 4 + (w >> 2));
-    out[i] = fp4x8_to_bf16(codes, e8m0_scale2(sb));
+    out[i] = fp4x8_to_bf16(codes, e8m0_scale(sb));
   }
 }
 

@@ -1,5 +1,5 @@
-// Persistent block-score kernel for short-query requests with int8 keys
-// (Lq * g <= 32 query rows: decode and speculative decode), sm_103a.
+// Persistent block-score kernel for short-query requests with int8 or FP4
+// keys (Lq * g <= 32 query rows: decode and speculative decode), sm_103a.
 //
 // The MMA is turned around with respect to the tile kernel: the 128 tokens of
 // one key page are the M side and the request's query rows are the N side,
@@ -15,6 +15,11 @@
 // page (TMA, 128-byte swizzle), convert one token row per thread and store it
 // straight into tensor memory, where the MMA reads its A operand; the token's
 // scale goes into a TMEM column that the epilogue reads with the accumulator.
+// FP4 pages (E2M1 codes, 64-byte rows, 64-byte swizzle, with their group
+// scale bytes) take the same route: a converter dequantises its token row
+// exactly into the 16-bit operand type (fp16 for NVFP4, bf16 for MXFP4; the
+// MiniMax Sparse Attention notes, sec. 8.2, "FP4 Indexer") and there is no
+// per-token scale.
 //
 // Pipeline granularity.  Per page there is little arithmetic, and an mbarrier
 // wait costs a warp ~100-150 cycles even when the phase is already complete.
@@ -37,6 +42,7 @@
 //   warps 8..11   converters (one token quarter of both pages of an item)
 //   warp 12       MMA helper: waits for each item's operands
 #pragma once
+#include <atomic>
 #include <cstdint>
 #include <type_traits>
 #include <cuda.h>
@@ -49,11 +55,16 @@
 namespace msa {
 
 struct Short8 {
-  static constexpr int kThreads = 416;
   static constexpr int kCombineWarp = 3;
   static constexpr int kEpiW0 = 4;
   static constexpr int kCvtW0 = 8;
-  static constexpr int kHelperWarp = 12;
+  // converter warp sets (set s converts pages s, s + kCvtSets, ... of an item);
+  // more sets put more than four warps on a sub-partition, which caps the
+  // registers of every warp at 96
+  static constexpr int kCvtSets = 1;
+  static constexpr int kCvtWarps = 4 * kCvtSets;
+  static constexpr int kHelperWarp = kCvtW0 + kCvtWarps;
+  static constexpr int kThreads = 32 * (kHelperWarp + 1);
   static constexpr uint32_t kMmaBar = 1;                 // named barrier: helper -> MMA warp
   // item codes passed through that barrier (0 = no more items)
   static constexpr uint32_t kCodeLive = 1, kCodeTwo = 2, kCodeNarrow = 4, kCodeLast = 8;
@@ -133,12 +144,18 @@ __device__ __forceinline__ float warp_transpose_max32(float (&v)[32], int lane) 
 // is written empty); the scores are stored only if p.out is not null.
 // TOPK = 2: the list is spread over 8 lanes of the position (g >= 8);
 // TOPK = 16: every lane of the position holds the whole list.
-template <bool BF16, int TOPK = 0>
+// KF4: FP4 key pages instead of int8, 1 = NVFP4 (E4M3 scale per 16 elements,
+// fp16 operands), 2 = MXFP4 (E8M0 scale per 32, bf16 operands).
+template <bool BF16, int TOPK = 0, int KF4 = 0>
 __global__ void __launch_bounds__(Short8::kThreads, 1)
     short_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                  const Params p) {
   using C = Short8;
   constexpr int S = C::kStages;
+  static_assert(KF4 == 0 || BF16 == (KF4 == 2), "FP4 operand type: fp16 for NVFP4, bf16 for MXFP4");
+  constexpr bool kTokScale = KF4 == 0;                   // int8: DEQUANT by the per-token scale
+  // bytes of one page in a stage: int8 16 KiB, FP4 8 KiB of codes
+  constexpr uint32_t kData = KF4 ? kRawBytes / 2 : kRawBytes;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -166,8 +183,8 @@ __global__ void __launch_bounds__(Short8::kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  // readers of each unit descriptor: producer, MMA helper, combine, 4 epilogue, 4 converter warps
-  constexpr int kConsumers = 11;
+  // readers of each unit descriptor: producer, MMA helper, combine, 4 epilogue, the converter warps
+  constexpr int kConsumers = 7 + C::kCvtWarps;
 
   asm volatile("griddepcontrol.launch_dependents;");
   if (threadIdx.x == 0) {
@@ -181,10 +198,10 @@ __global__ void __launch_bounds__(Short8::kThreads, 1)
     }
     for (int i = 0; i < S; ++i) {
       mbar_init(b_st_full + 8 * i, 1);
-      mbar_init(b_st_empty + 8 * i, 4);
+      mbar_init(b_st_empty + 8 * i, C::kCvtWarps);
     }
     for (int i = 0; i < C::kA; ++i) {
-      mbar_init(b_a_full + 8 * i, 4);
+      mbar_init(b_a_full + 8 * i, C::kCvtWarps);
       mbar_init(b_a_free + 8 * i, 1);
     }
     for (int i = 0; i < C::kD; ++i) {
@@ -283,6 +300,9 @@ __global__ void __launch_bounds__(Short8::kThreads, 1)
       const uint32_t q_bytes = 2u * 128u * (uint32_t)(p.g * p.np_short);
       const bool paged = p.layout != 2;
       const int page_oob = (int)(p.NP < 0x7fffffffLL ? p.NP : 0x7fffffffLL);
+      // a page's scales: 128 fp32 token scales (int8) or 128 rows of FP4
+      // group scale bytes (4 MXFP4, 8 NVFP4)
+      const uint32_t sc_bytes = KF4 ? (uint32_t)(kP * p.fp4_ng) : kRawScaleBytes;
       uint32_t ss = 0, sph = 0, qb = 0, qph = 0, ks = 0, kph = 0;
       uint32_t n_q = 0, n_k = 0;
       for (;;) {
@@ -333,16 +353,21 @@ __global__ void __launch_bounds__(Short8::kThreads, 1)
               pg[j] = tok;
             }
             raw_page[2 * ks + j] = pg[j];
-            bytes += kRawBytes + (with_scale[j] ? kRawScaleBytes : 0u);
+            bytes += kData + (with_scale[j] ? sc_bytes : 0u);
           }
           mbar_arrive_expect_tx(b_st_full + 8 * ks, bytes);
           for (int j = 0; j < npg; ++j) {
             const uint32_t pdst = dst + (uint32_t)j * C::kPageBytes;
             tma_k(pdst, &tm_k, b_st_full + 8 * ks, 0, paged ? 0 : pg[j], d.hk, paged ? pg[j] : 0,
                   p.layout, pol_k);
-            if (with_scale[j])
-              bulk_load(pdst + kRawBytes, p.scale + ((int64_t)pg[j] * p.H_kv + d.hk) * kP,
-                        kRawScaleBytes, b_st_full + 8 * ks);
+            if (with_scale[j]) {
+              if constexpr (KF4 != 0)
+                bulk_load(pdst + kRawBytes, p.k_scale8 + ((int64_t)pg[j] * p.H_kv + d.hk) * kP * p.fp4_ng,
+                          sc_bytes, b_st_full + 8 * ks);
+              else
+                bulk_load(pdst + kRawBytes, p.scale + ((int64_t)pg[j] * p.H_kv + d.hk) * kP,
+                          kRawScaleBytes, b_st_full + 8 * ks);
+            }
           }
           ++n_k;
           if (++ks == S) { ks = 0; kph ^= 1; }
@@ -487,8 +512,8 @@ __global__ void __launch_bounds__(Short8::kThreads, 1)
         // page p's scale sits in column p % kScCols; items hold pages 2it, 2it + 1
         const uint32_t dcol = t_lane + C::kDCol0 + ds * (2u * C::kN);
         const uint32_t scol = t_lane + C::kScCol0;
-        const float sc0 = tmem_ld1(scol + (2u * it) % C::kScCols);
-        const float sc1 = tmem_ld1(scol + (2u * it + 1u) % C::kScCols);
+        const float sc0 = kTokScale ? tmem_ld1(scol + (2u * it) % C::kScCols) : 1.f;
+        const float sc1 = kTokScale ? tmem_ld1(scol + (2u * it + 1u) % C::kScCols) : 1.f;
         float* rslot = red + rr * (4 * 2 * C::kN) + quarter * (2 * C::kN);
         if (narrow) {
           // both pages' 16 columns in one 32-wide transpose: lane c < 16 gets
@@ -501,10 +526,12 @@ __global__ void __launch_bounds__(Short8::kThreads, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive(b_d_free + 8 * ds);
           if (all_visible(beta, two)) {
+            if constexpr (kTokScale) {
 #pragma unroll
-            for (int c = 0; c < 16; ++c) {
-              x[c] *= sc0;                                       // DEQUANT
-              x[16 + c] *= sc1;
+              for (int c = 0; c < 16; ++c) {
+                x[c] *= sc0;                                     // DEQUANT
+                x[16 + c] *= sc1;
+              }
             }
           } else {
             const int n0 = first_row(beta), n1 = two ? first_row(beta + 1) : C::kN;
@@ -526,10 +553,12 @@ __global__ void __launch_bounds__(Short8::kThreads, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive(b_d_free + 8 * ds);
           if (all_visible(beta, two)) {
+            if constexpr (kTokScale) {
 #pragma unroll
-            for (int c = 0; c < 32; ++c) {
-              x0[c] *= sc0;
-              x1[c] *= sc1;
+              for (int c = 0; c < 32; ++c) {
+                x0[c] *= sc0;
+                x1[c] *= sc1;
+              }
             }
           } else {
             const int n0 = first_row(beta), n1 = two ? first_row(beta + 1) : C::kN;
@@ -640,10 +669,12 @@ __global__ void __launch_bounds__(Short8::kThreads, 1)
                                                                      fill_value(beta + 2), fill_value(beta + 3)));
       }
     }
-  } else if (warp >= C::kCvtW0 && warp < C::kCvtW0 + 4) {
-    // ----------------------------------------- int8 -> fp16 into TMEM --
-    // Warp q converts token rows 32q..32q+31 of both pages of every item.
+  } else if (warp >= C::kCvtW0 && warp < C::kCvtW0 + C::kCvtWarps) {
+    // ------------------------------ int8 or FP4 -> 16 bits into TMEM --
+    // Warp q of set s converts token rows 32q..32q+31 of pages s, s + kCvtSets,
+    // ... of every item (its TMEM lane quarter is q = warp % 4).
     const int quarter = warp & 3;
+    const int set = (warp - C::kCvtW0) >> 2;
     const int row = quarter * 32 + lane;                  // token row of the page
     const uint32_t t_lane = tmem_base + ((uint32_t)(quarter * 32) << 16);
     uint32_t ss = 0, sph = 0, it = 0;
@@ -659,45 +690,98 @@ __global__ void __launch_bounds__(Short8::kThreads, 1)
         const uint32_t rs = it % S, as = it % C::kA;
         const int npg = beta + 1 < d.b1 ? 2 : 1;
         if (!warp_wait(b_st_full + 8 * rs, (it / S) & 1u, ctl)) { ok = false; break; }
-        for (int jp = 0; jp < npg; ++jp) {
+        if (set >= npg) {                                 // no page of this item: the stage is read
+          __syncwarp();
+          if (lane == 0) mbar_arrive(b_st_empty + 8 * rs);
+        }
+        for (int jp = set; jp < npg; jp += C::kCvtSets) {
+          const bool last_read = jp + C::kCvtSets >= npg;
           const uint8_t* src = smem + C::k_off + rs * C::kStageBytes + (uint32_t)jp * C::kPageBytes;
           const int page = raw_page[2 * rs + jp];
-          float sv = 0.f;
-          if (p.layout == 2) {
-            const int64_t trow = (int64_t)page + row;     // page holds the first key row here
-            if (trow < (int64_t)d.kbase + d.L && trow < p.NP) sv = __ldg(p.scale + trow * p.H_kv + d.hk);
-          } else if (page >= 0 && (int64_t)page < p.NP) {
-            sv = reinterpret_cast<const float*>(src + kRawBytes)[row];
-          }
-          // row of the page: 8 chunks of 16 bytes, stored 128-byte swizzled
-          int4 raw[8];
-#pragma unroll
-          for (int c = 0; c < 8; ++c)
-            raw[c] = *reinterpret_cast<const int4*>(src + row * 128 + ((c ^ (row & 7)) << 4));
-          if (jp == npg - 1) {
-            __syncwarp();
-            if (lane == 0) mbar_arrive(b_st_empty + 8 * rs);
-          }
           uint32_t hv[64];
+          float sv = 0.f;
+          if constexpr (KF4 != 0) {
+            // this token's group scale bytes (8 NVFP4, 4 MXFP4): from the stage
+            // (paged) or from global memory (packed keys)
+            uint2 gs = make_uint2(0u, 0u);
+            const uint8_t* g = nullptr;
+            if (p.layout == 2) {
+              const int64_t trow = (int64_t)page + row;   // page holds the first key row here
+              if (trow < (int64_t)d.kbase + d.L && trow < p.NP)
+                g = p.k_scale8 + (trow * p.H_kv + d.hk) * (int64_t)p.fp4_ng;
+            } else if (page >= 0 && (int64_t)page < p.NP) {
+              g = src + kRawBytes + row * p.fp4_ng;
+            }
+            if (g) {
+              if constexpr (KF4 == 1) gs = *reinterpret_cast<const uint2*>(g);
+              else gs.x = *reinterpret_cast<const uint32_t*>(g);
+            }
+            // the 64-byte row of codes, 64-byte swizzled: chunk c at (c ^ ((row >> 1) & 3)) * 16
+            const int sw = (row >> 1) & 3;
+            uint4 in[4];
 #pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            int8x4_to_half4((uint32_t)raw[c].x, hv[8 * c + 0], hv[8 * c + 1]);
-            int8x4_to_half4((uint32_t)raw[c].y, hv[8 * c + 2], hv[8 * c + 3]);
-            int8x4_to_half4((uint32_t)raw[c].z, hv[8 * c + 4], hv[8 * c + 5]);
-            int8x4_to_half4((uint32_t)raw[c].w, hv[8 * c + 6], hv[8 * c + 7]);
+            for (int c = 0; c < 4; ++c)
+              in[c] = *reinterpret_cast<const uint4*>(src + row * 64 + ((c ^ sw) << 4));
+            if (last_read) {
+              __syncwarp();
+              if (lane == 0) mbar_arrive(b_st_empty + 8 * rs);
+            }
+            // word w = elements 8w .. 8w+7 (element 2i in the low nibble of byte i)
+#pragma unroll
+            for (int w = 0; w < 16; ++w) {
+              const uint4 v4 = in[w >> 2];
+              const uint32_t word = (w & 3) == 0 ? v4.x : (w & 3) == 1 ? v4.y : (w & 3) == 2 ? v4.z : v4.w;
+              uint4 o;
+              if constexpr (KF4 == 1) {
+                const int gi = w >> 1;                    // group of 16 elements
+                const uint32_t sb = ((gi < 4 ? gs.x : gs.y) >> (8 * (gi & 3))) & 0xffu;
+                o = fp4x8_to_f16(word, e4m3_scale2(sb));
+              } else {
+                const uint32_t sb = (gs.x >> (8 * (w >> 2))) & 0xffu;   // group of 32 elements
+                o = fp4x8_to_bf16(word, e8m0_scale(sb));
+              }
+              hv[4 * w + 0] = o.x;
+              hv[4 * w + 1] = o.y;
+              hv[4 * w + 2] = o.z;
+              hv[4 * w + 3] = o.w;
+            }
+          } else {
+            if (p.layout == 2) {
+              const int64_t trow = (int64_t)page + row;   // page holds the first key row here
+              if (trow < (int64_t)d.kbase + d.L && trow < p.NP) sv = __ldg(p.scale + trow * p.H_kv + d.hk);
+            } else if (page >= 0 && (int64_t)page < p.NP) {
+              sv = reinterpret_cast<const float*>(src + kRawBytes)[row];
+            }
+            // row of the page: 8 chunks of 16 bytes, stored 128-byte swizzled
+            int4 raw[8];
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+              raw[c] = *reinterpret_cast<const int4*>(src + row * 128 + ((c ^ (row & 7)) << 4));
+            if (last_read) {
+              __syncwarp();
+              if (lane == 0) mbar_arrive(b_st_empty + 8 * rs);
+            }
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+              int8x4_to_half4((uint32_t)raw[c].x, hv[8 * c + 0], hv[8 * c + 1]);
+              int8x4_to_half4((uint32_t)raw[c].y, hv[8 * c + 2], hv[8 * c + 3]);
+              int8x4_to_half4((uint32_t)raw[c].z, hv[8 * c + 4], hv[8 * c + 5]);
+              int8x4_to_half4((uint32_t)raw[c].w, hv[8 * c + 6], hv[8 * c + 7]);
+            }
           }
-          if (jp == 0) {
+          if (jp == set) {
             if (!warp_wait(b_a_free + 8 * as, ((it / C::kA) & 1u) ^ 1u, ctl)) { ok = false; break; }
             tc_fence_after();
           }
           tmem_st64(t_lane + as * 128u + 64u * jp, hv);
-          tmem_st1(t_lane + C::kScCol0 + (2u * it + jp) % C::kScCols, __float_as_uint(sv));
+          if constexpr (kTokScale) tmem_st1(t_lane + C::kScCol0 + (2u * it + jp) % C::kScCols, __float_as_uint(sv));
         }
         if (!ok) break;
         tmem_wait_st();
         // one warp also waits until the epilogue has read the accumulator pair
         // this item will use: the item is ready only after all four arrived
-        if (quarter == 0 && !warp_wait(b_d_free + 8 * (it % C::kD), ((it / C::kD) & 1u) ^ 1u, ctl)) {
+        if (quarter == 0 && set == 0 &&
+            !warp_wait(b_d_free + 8 * (it % C::kD), ((it / C::kD) & 1u) ^ 1u, ctl)) {
           ok = false;
           break;
         }
@@ -715,6 +799,30 @@ __global__ void __launch_bounds__(Short8::kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem_base, kTmemCols);
   }
+}
+
+// One persistent CTA per SM, launched as a programmatic dependent of the plan.
+template <bool BF16, int TOPK, int KF4>
+cudaError_t launch_short_kernel(const void* tq, const void* tk, const Params& p, cudaStream_t s) {
+  auto kern = short_kernel<BF16, TOPK, KF4>;
+  static std::atomic<uint64_t> configured[64];   // per device: context the limit was raised in
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  e = ensure_smem_limit(kern, (int)Short8::bytes, configured, dev);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)p.num_sms);
+  cfg.blockDim = dim3(Short8::kThreads);
+  cfg.dynamicSmemBytes = Short8::bytes;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, *static_cast<const CUtensorMap*>(tq),
+                            *static_cast<const CUtensorMap*>(tk), p);
 }
 
 }  // namespace msa

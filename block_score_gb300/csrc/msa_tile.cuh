@@ -865,7 +865,7 @@ __global__ void __launch_bounds__(TileCfg<tile_mode(KI8, KM)>::kThreads, 1)
                 } else {
                   // MXFP4: group (64x + 8i) / 32 = 2x + i / 4 of 4 scale bytes
                   const uint32_t sb = (gsc[j].x >> (8 * (2 * x + (i >> 2)))) & 0xffu;
-                  o = fp4x8_to_bf16(wv[i], e8m0_scale2(sb));
+                  o = fp4x8_to_bf16(wv[i], e8m0_scale(sb));
                 }
                 *reinterpret_cast<uint4*>(rowp + ((i ^ (row & 7)) << 4)) = o;
               }

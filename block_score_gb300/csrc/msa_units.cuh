@@ -5,6 +5,7 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_fp4.h>
 #include <cuda_fp8.h>
 
 #include "msa_common.cuh"
@@ -47,71 +48,41 @@ __device__ __forceinline__ void int8x4_to_half4(uint32_t w, uint32_t& lo, uint32
 
 // ------------------------------------------------------------- FP4 (E2M1) --
 // Codes c0..c7 of a 32-bit word sit in its nibbles 0..7 (element 2i in the
-// low nibble of byte i).  The 3 magnitude bits of four codes (one 16-bit half
-// of the word, masked with 0x7777) are exactly four byte selectors of a
-// byte permute, so one prmt looks four magnitudes up in an 8-entry table; the
-// sign bits (bits 4n+3) are the top bits of the bytes of w << 4 (even codes)
-// and of w (odd codes), which prmt's sign-replicating selectors spread into
-// whole bytes.
-
-// prmt with the default mode: a selector nibble with its top bit set
-// replicates the sign bit of the selected byte.
-__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
-  uint32_t r;
-  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
-  return r;
-}
-
-// 0x00 / 0xff per code: the signs of codes 4h .. 4h+3 of w
-__device__ __forceinline__ uint32_t fp4_sign_bytes(uint32_t w, int h) {
-  return prmt(w << 4, w, h ? 0xFBEAu : 0xD9C8u);
-}
+// low nibble of byte i); one byte is a pair of codes, which the hardware
+// conversion (cvt.rn.f16x2.e2m1x2, through cuda_fp4.h) turns into a binary16
+// pair with the low nibble in the low half.
 
 // 8 E2M1 codes times an NVFP4 group scale (E4M3, as binary16) -> 8 binary16
-// values: each code becomes the E4M3 byte of the same value (magnitudes 0,
-// 0.5, 1, 1.5, 2, 3, 4, 6 are 0x00 0x30 0x38 0x3c 0x40 0x44 0x48 0x4c), the
-// hardware converts E4M3 pairs to binary16, one multiplication applies the
-// scale.  Exact: every product of an E2M1 value and an E4M3 value is a
-// binary16 number.
+// values: the hardware converts each byte (a pair of codes, the low nibble
+// first) to a binary16 pair, one multiplication applies the scale.  Exact:
+// every product of an E2M1 value and an E4M3 value is a binary16 number.
 __device__ __forceinline__ uint4 fp4x8_to_f16(uint32_t w, __half2 scale2) {
   uint32_t r[4];
 #pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    const uint32_t mag = prmt(0x3C383000u, 0x4C484440u, (w >> (16 * h)) & 0x7777u);
-    const uint32_t e4 = mag | (fp4_sign_bytes(w, h) & 0x80808080u);
-#pragma unroll
-    for (int q = 0; q < 2; ++q) {
-      const __half2_raw hr =
-          __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(e4 >> (16 * q)), __NV_E4M3);
-      const __half2 v = __hmul2(__half2(hr), scale2);
-      r[2 * h + q] = *reinterpret_cast<const uint32_t*>(&v);
-    }
+  for (int q = 0; q < 4; ++q) {
+    const __half2_raw hr = __nv_cvt_fp4x2_to_halfraw2((__nv_fp4x2_storage_t)(w >> (8 * q)), __NV_E2M1);
+    const __half2 v = __hmul2(__half2(hr), scale2);
+    r[q] = *reinterpret_cast<const uint32_t*>(&v);
   }
   return make_uint4(r[0], r[1], r[2], r[3]);
 }
 
-// 8 E2M1 codes times an MXFP4 group scale 2^(e-127) (E8M0 code e, as a
-// bfloat16 power of two) -> 8 bfloat16 values: two table lookups give the
-// high and low bytes of each magnitude's bfloat16 pattern (0.5 0x3f00, 1
-// 0x3f80, 1.5 0x3fc0, 2 0x4000, 3 0x4040, 4 0x4080, 6 0x40c0), two permutes
-// interleave them into pairs, the sign goes to bit 15, one multiplication
-// applies the scale.  Exact while the products stay in bfloat16's normal
-// range (E8M0 codes 2 .. 252).
-__device__ __forceinline__ uint4 fp4x8_to_bf16(uint32_t w, __nv_bfloat162 scale2) {
+// 8 E2M1 codes times an MXFP4 group scale 2^(e-127) (E8M0 code e, as an fp32
+// power of two) -> 8 bfloat16 values: the hardware converts each byte (a pair
+// of codes, the low nibble first) to a binary16 pair, which widens exactly to
+// fp32; the scale multiplies in fp32 and the pair is rounded to bfloat16.
+// Exact for every code 0 .. 254: an E2M1 value has at most two significant
+// bits, and every product lies in fp32's (and bfloat16's) normal or
+// subnormal range at a multiple of 2^-128.  (Everything but the conversion
+// runs on the FMA pipe.)
+__device__ __forceinline__ uint4 fp4x8_to_bf16(uint32_t w, float scale) {
   uint32_t r[4];
 #pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    const uint32_t sel = (w >> (16 * h)) & 0x7777u;
-    const uint32_t hb = prmt(0x3F3F3F00u, 0x40404040u, sel);
-    const uint32_t lb = prmt(0xC0800000u, 0xC0804000u, sel);
-    const uint32_t sg = fp4_sign_bytes(w, h);
-#pragma unroll
-    for (int q = 0; q < 2; ++q) {
-      const uint32_t bits = prmt(lb, hb, q ? 0x7362u : 0x5140u) |
-                            (prmt(sg, sg, q ? 0x3020u : 0x1000u) & 0x80008000u);
-      const __nv_bfloat162 v = __hmul2(*reinterpret_cast<const __nv_bfloat162*>(&bits), scale2);
-      r[2 * h + q] = *reinterpret_cast<const uint32_t*>(&v);
-    }
+  for (int q = 0; q < 4; ++q) {
+    const __half2_raw hr = __nv_cvt_fp4x2_to_halfraw2((__nv_fp4x2_storage_t)(w >> (8 * q)), __NV_E2M1);
+    const float2 f = __half22float2(__half2(hr));
+    const __nv_bfloat162 v = __floats2bfloat162_rn(f.x * scale, f.y * scale);
+    r[q] = *reinterpret_cast<const uint32_t*>(&v);
   }
   return make_uint4(r[0], r[1], r[2], r[3]);
 }
@@ -121,11 +92,9 @@ __device__ __forceinline__ __half2 e4m3_scale2(uint32_t byte) {
   const __half h = __half(__nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)byte, __NV_E4M3));
   return __half2half2(h);
 }
-__device__ __forceinline__ __nv_bfloat162 e8m0_scale2(uint32_t byte) {
-  // 2^(e-127): the code is a bfloat16 exponent field; 0 is 2^-127 (subnormal), 255 NaN
-  const uint32_t b = byte == 0xffu ? 0x7fc0u : (byte ? (byte << 7) : 0x0040u);
-  const uint32_t b2 = b | (b << 16);
-  return *reinterpret_cast<const __nv_bfloat162*>(&b2);
+__device__ __forceinline__ float e8m0_scale(uint32_t byte) {
+  // 2^(e-127): the code is an fp32 exponent field; 0 is 2^-127 (subnormal), 255 NaN
+  return __uint_as_float(byte == 0xffu ? 0x7fc00000u : (byte ? (byte << 23) : 0x00400000u));
 }
 
 // K page tile load.  The tensor map's dimensions are ordered by increasing

@@ -303,9 +303,14 @@ msa_status_t msa_index_score_topk(const msa_index_score_args *args, int32_t k, i
  *   workspace msa_index_score_fp4_workspace_size() bytes (256-byte aligned,
  *             caller-owned): the plan and the dequantised query, and for a
  *             prefill-heavy call on paged keys (T * g >= 128 * B) a 16-bit copy
- *             of the dequantised key pages [NP, H_kv, P, D], which lets every
- *             page be dequantised once per call instead of once per query tile
- *             (a workspace without it is accepted: the slower route then).
+ *             of the dequantised key pages [NP, H_kv, P, D] of the query-tile
+ *             requests, which lets every page be dequantised once per call
+ *             instead of once per query tile (a workspace without it is
+ *             accepted: the slower route then).  Requests with Lq * g <= 32
+ *             query rows (decode) are scored by the short-query kernel, which
+ *             dequantises each page once into tensor memory; a positive
+ *             args->max_seqlen_q with max_seqlen_q * g <= 32 leaves the tile
+ *             kernel out of the call.
  *
  * Errors as msa_index_score, plus MSA_ERR_INVALID_ARG for a bad format or a
  * missing or misaligned scale array.  Asynchronous on `stream`.
@@ -318,7 +323,7 @@ msa_status_t msa_index_score_fp4(const msa_index_score_args *args, int32_t forma
 
 /* The two halves of msa_index_score_fp4, on the same stream and workspace:
  * _plan dequantises the query into the workspace and writes the work plan;
- * _run launches the tile kernel that reads the key cache and writes `out`. */
+ * _run launches the score kernels that read the key cache and write `out`. */
 msa_status_t msa_index_score_fp4_plan(const msa_index_score_args *args, int32_t format,
                                       const uint8_t *q_scale, void *workspace,
                                       size_t workspace_bytes, msa_stream_t stream);

@@ -113,6 +113,52 @@ def test_fp4_benchmark_workload_sampled(dev, n):
 
 
 @pytest.mark.parametrize("fmt", ["mx", "nv"])
+@pytest.mark.parametrize("layout", ["BBND", "BNBD", "TND"])
+@pytest.mark.parametrize("g,mode", [(1, 3), (8, 3), (8, 0), (32, 3)])
+def test_fp4_short_query_requests(dev, fmt, layout, g, mode):
+    # requests of at most 32 query rows (decode, speculative decode): the
+    # short-query kernel dequantises each FP4 page once into tensor memory.
+    # One-key and one-page requests, q_len 0, kv_len 0, a ragged tail and a
+    # long request; with the host length bound the tile kernel is left out.
+    import block_score_gb300 as bs
+    qmax = 32 // g
+    H_kv = 1 if g == 32 else 2
+    case = synth.make_fp4_case([1, qmax, 0, 1, max(1, qmax // 2), 1], [1, 300, 50, 0, 129, 9000],
+                               fmt=fmt, H_q=g * H_kv, H_kv=H_kv, layout=layout,
+                               MB=80 if layout != "TND" else None, sparse_mode=mode,
+                               init_blocks=1, local_blocks=2,
+                               seed=430 + g + 2 * mode + (fmt == "nv") + 5 * len(layout))
+    ref = oracle.oracle_full(case)
+    for bound in (None, qmax):
+        prep = bs.from_case(case, dev, max_seqlen_q=bound)
+        out = prep().cpu()
+        assert prep.device_error() == 0
+        assert_parity(out, ref, what=f"fp4 short {fmt} {layout} g={g} mode {mode} bound={bound}")
+
+
+@pytest.mark.parametrize("fmt,unit", [("mx", 127), ("nv", 0x38)])
+def test_fp4_short_query_unit_scales_bit_exact(dev, fmt, unit):
+    # decode only (g = 16, N = 16 rows, and q_len 2 -> 32 rows): bit-exact
+    case = synth.make_fp4_case([1, 2, 1, 1], [5000, 700, 128, 33], fmt=fmt, H_q=16, H_kv=1,
+                               layout="BNBD", MB=40, scale_codes=(unit, unit),
+                               init_blocks=0, local_blocks=0, seed=450 + (fmt == "nv"))
+    out, err = run(case, dev)
+    assert err == 0
+    assert_parity(out, oracle.oracle_full(case), exact=True, what=f"fp4 short {fmt} unit scales")
+
+
+def test_fp4_short_query_bad_block_table_entry_is_reported(dev):
+    case = synth.make_fp4_case([1, 2], [300, 500], fmt="nv", H_q=8, H_kv=1, layout="BBND",
+                               MB=4, seed=460)
+    case.block_table[0, 1] = 10_000          # beyond NP, inside the needed range
+    _, err = run(case, dev)
+    assert err & 0x08
+    case.block_table[0, 1] = -3
+    _, err = run(case, dev)
+    assert err & 0x08
+
+
+@pytest.mark.parametrize("fmt", ["mx", "nv"])
 @pytest.mark.parametrize("mirror", [True, False])
 def test_fp4_mirror_and_converter_paths(dev, fmt, mirror):
     # a prefill-heavy call: with the full workspace the key pages are
