@@ -71,10 +71,12 @@ __device__ __forceinline__ uint4 fp4x8_to_f16(uint32_t w, __half2 scale2) {
 // power of two) -> 8 bfloat16 values: the hardware converts each byte (a pair
 // of codes, the low nibble first) to a binary16 pair, which widens exactly to
 // fp32; the scale multiplies in fp32 and the pair is rounded to bfloat16.
-// Exact for every code 0 .. 254: an E2M1 value has at most two significant
+// Exact for every code 0 .. 252: an E2M1 value has at most two significant
 // bits, and every product lies in fp32's (and bfloat16's) normal or
-// subnormal range at a multiple of 2^-128.  (Everything but the conversion
-// runs on the FMA pipe.)
+// subnormal range at a multiple of 2^-128 (codes 253 and 254 put the largest
+// magnitudes beyond both types' range).  Everything but the conversion runs
+// on the FMA pipe, where the permute-table decode this replaces kept the
+// half-rate ALU pipe busy.
 __device__ __forceinline__ uint4 fp4x8_to_bf16(uint32_t w, float scale) {
   uint32_t r[4];
 #pragma unroll
