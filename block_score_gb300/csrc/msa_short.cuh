@@ -405,7 +405,8 @@ __global__ void __launch_bounds__(Short8::kThreads, 1)
       const uint32_t code = named_bar_popc(C::kMmaBar, 64, false);
       if (code == 0) break;
       tc_fence_after();
-      if (lane == 0) {
+      {
+        // the whole (converged) warp runs the issue, its elected lane issues
         const uint32_t as = it % C::kA, ds = it % C::kD;
         const uint32_t qsrc = sbase + C::q_off + qb * C::kQBytes;
         const uint32_t idesc = (code & C::kCodeNarrow) ? idesc16 : idesc32;   // N = 16 or 32 query rows
@@ -415,21 +416,24 @@ __global__ void __launch_bounds__(Short8::kThreads, 1)
           const uint32_t dt = tmem_base + C::kDCol0 + ds * (2u * C::kN) + (uint32_t)C::kN * j;
 #pragma unroll
           for (int k = 0; k < 8; ++k)
-            tc_mma_f16_ta(dt, at + 8u * k,
-                          smem_desc_sw128(qsrc + (uint32_t)(k >> 2) * C::kQHalf + (k & 3) * 32u),
-                          idesc, k > 0 ? 1u : 0u);
+            tc_mma_f16_ta_w(dt, at + 8u * k,
+                            smem_desc_sw128(qsrc + (uint32_t)(k >> 2) * C::kQHalf + (k & 3) * 32u),
+                            idesc, k > 0 ? 1u : 0u);
         }
-        tc_commit(b_a_free + 8 * as);
-        tc_commit(b_d_full + 8 * ds);
-        if (code & C::kCodeLast) tc_commit(b_q_empty + 8 * qb);
+        tc_commit_w(b_a_free + 8 * as);
+        tc_commit_w(b_d_full + 8 * ds);
+        if (code & C::kCodeLast) tc_commit_w(b_q_empty + 8 * qb);
       }
       if (code & C::kCodeLast) qb = qb + 1 == (uint32_t)C::kQBufs ? 0u : qb + 1;
       issued = true;
     }
-    if (lane == 0 && issued) {
-      tc_commit(b_drain);
-      const uint64_t t0 = global_timer_ns();
-      while (!mbar_try_wait(b_drain, 0) && global_timer_ns() - t0 < kDrainLimitNs) {
+    __syncwarp();
+    if (issued) {
+      tc_commit_w(b_drain);
+      if (lane == 0) {
+        const uint64_t t0 = global_timer_ns();
+        while (!mbar_try_wait(b_drain, 0) && global_timer_ns() - t0 < kDrainLimitNs) {
+        }
       }
     }
     __syncwarp();

@@ -471,7 +471,8 @@ __global__ void __launch_bounds__(TileCfg<tile_mode(KI8, KM)>::kThreads, 1)
       if (code == 0) break;
       tc_fence_after();
       if (code & kCodeFirst) x = 0;
-      if (lane == 0) {
+      {
+        // the whole (converged) warp runs the issue, its elected lane issues
         const uint32_t qsrc = sbase + L::q_off + qb * kTileBytes;
         const uint32_t dt = tmem_base + ab * 256u;
         const uint32_t idesc = (code & kCodeLone) ? idesc1 : idesc2;
@@ -479,14 +480,14 @@ __global__ void __launch_bounds__(TileCfg<tile_mode(KI8, KM)>::kThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
           if constexpr (kF8)
-            tc_mma_f8(dt, desc_at(qsrc, kk), smem_desc_sw128(ksrc + 32u * kk), idesc, kk ? 1u : 0u);
+            tc_mma_f8_w(dt, desc_at(qsrc, kk), smem_desc_sw128(ksrc + 32u * kk), idesc, kk ? 1u : 0u);
           else
-            tc_mma_f16(dt, desc_at(qsrc, 4 * (int)x + kk), smem_desc_sw128(ksrc + 32u * kk), idesc,
-                       (x | (uint32_t)kk) ? 1u : 0u);
+            tc_mma_f16_w(dt, desc_at(qsrc, 4 * (int)x + kk), smem_desc_sw128(ksrc + 32u * kk), idesc,
+                         (x | (uint32_t)kk) ? 1u : 0u);
         }
-        tc_commit(b_k_empty + 8 * ks);   // the slot is free once these four MMAs are done
-        if (code & kCodeLast) tc_commit(b_acc_full + 8 * ab);
-        if (code & kCodeUnitEnd) tc_commit(b_q_empty + 8 * qb);
+        tc_commit_w(b_k_empty + 8 * ks);   // the slot is free once these four MMAs are done
+        if (code & kCodeLast) tc_commit_w(b_acc_full + 8 * ab);
+        if (code & kCodeUnitEnd) tc_commit_w(b_q_empty + 8 * qb);
       }
       ++x;
       if (++ks == (uint32_t)PS) ks = 0;
@@ -494,11 +495,14 @@ __global__ void __launch_bounds__(TileCfg<tile_mode(KI8, KM)>::kThreads, 1)
       if ((code & kCodeUnitEnd) && ++qb == (uint32_t)L::kQBufs) qb = 0;
       issued = true;
     }
-    if (lane == 0 && issued) {
+    __syncwarp();
+    if (issued) {
       // every MMA of this CTA has landed before TMEM is released
-      tc_commit(b_drain);
-      const uint64_t t0 = global_timer_ns();
-      while (!mbar_try_wait(b_drain, 0) && global_timer_ns() - t0 < kDrainLimitNs) {
+      tc_commit_w(b_drain);
+      if (lane == 0) {
+        const uint64_t t0 = global_timer_ns();
+        while (!mbar_try_wait(b_drain, 0) && global_timer_ns() - t0 < kDrainLimitNs) {
+        }
       }
     }
     __syncwarp();
