@@ -500,14 +500,15 @@ __global__ void __launch_bounds__(kK1Threads, 1)
       if (!warp_wait(b_v_full + 8 * bj, phj, ctl)) return false;
       if (!warp_wait(b_o_empty + 8 * bj, phj ^ 1u, ctl)) return false;   // O(j-2) read
       tc_fence_after();
-      if (lane == 0) {
+      {
+        // the whole (converged) warp runs the issue, its elected lane issues
         const uint32_t buf = tmem_base + bj * kBufCols;
         const uint32_t vt = sbase + Lo::stage_off + bj * Lo::kStage + 2 * Lo::kTile;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          tc_mma_f16_ta(buf + kColO, buf + 8u * kk, v_desc_mn(vt, kk), idesc_o, kk ? 1u : 0u);
-        tc_commit(b_o_full + 8 * bj);
-        tc_commit(b_v_empty + 8 * bj);
+          tc_mma_f16_ta_w(buf + kColO, buf + 8u * kk, v_desc_mn(vt, kk), idesc_o, kk ? 1u : 0u);
+        tc_commit_w(b_o_full + 8 * bj);
+        tc_commit_w(b_v_empty + 8 * bj);
       }
       __syncwarp();
       return true;
@@ -523,25 +524,28 @@ __global__ void __launch_bounds__(kK1Threads, 1)
         break;
       }
       tc_fence_after();
-      if (lane == 0) {
+      {
         // S = Q K^T: rows = (query, head), columns = the block's 128 tokens
         const uint32_t st_base = sbase + Lo::stage_off + st * Lo::kStage;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          tc_mma_f16(tmem_base + st * kBufCols, desc_at(st_base, kk), desc_at(st_base + Lo::kTile, kk),
-                     idesc_s, kk ? 1u : 0u);
-        tc_commit(b_s_full + 8 * st);
-        tc_commit(b_kq_empty + 8 * st);
+          tc_mma_f16_w(tmem_base + st * kBufCols, desc_at(st_base, kk), desc_at(st_base + Lo::kTile, kk),
+                       idesc_s, kk ? 1u : 0u);
+        tc_commit_w(b_s_full + 8 * st);
+        tc_commit_w(b_kq_empty + 8 * st);
       }
       __syncwarp();
       issued = true;
       if (i > 0 && !pv(i - 1)) { ok = false; break; }
     }
     if (ok && i > 0) pv(i - 1);
-    if (lane == 0 && issued) {
-      tc_commit(b_drain);
-      const uint64_t t0 = global_timer_ns();
-      while (!mbar_try_wait(b_drain, 0) && global_timer_ns() - t0 < kDrainLimitNs) {
+    __syncwarp();
+    if (issued) {
+      tc_commit_w(b_drain);
+      if (lane == 0) {
+        const uint64_t t0 = global_timer_ns();
+        while (!mbar_try_wait(b_drain, 0) && global_timer_ns() - t0 < kDrainLimitNs) {
+        }
       }
     }
     __syncwarp();
