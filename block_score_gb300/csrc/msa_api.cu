@@ -750,7 +750,7 @@ namespace {
 
 // Workspace of a sparse-attention call, each array 256-byte aligned.
 struct SparseLayout {
-  size_t header, cnt, row_ptr, cursor, unit_ptr, qidx, units, o_part, lse_part, bytes;
+  size_t header, cnt, row_ptr, cursor, unit_ptr, qrec, units, o_part, lse_part, bytes;
   int64_t rows, entries;
 };
 
@@ -766,7 +766,7 @@ SparseLayout sparse_layout(const msa_index_score_args* a, int k) {
   l.row_ptr = off;  off += up256(4 * (size_t)(l.rows + 1));
   l.cursor = off;   off += up256(4 * (size_t)l.rows);
   l.unit_ptr = off; off += up256(4 * (size_t)(l.rows + 1));
-  l.qidx = off;     off += up256(4 * (size_t)l.entries);
+  l.qrec = off;     off += up256(8 * (size_t)l.entries);
   l.units = off;    off += up256(16 * (size_t)l.entries);
   l.o_part = off;   off += up256(2 * (size_t)a->T * a->H_q * k * a->D);   // 16-bit partials
   l.lse_part = off; off += up256(4 * (size_t)a->T * a->H_q * k);
@@ -781,6 +781,10 @@ msa_status_t validate_sparse(const msa_index_score_args* a, const msa_sparse_att
   if (a->q_dtype != MSA_F16 && a->q_dtype != MSA_BF16)
     return fail(MSA_ERR_INVALID_ARG, "sparse attention takes fp16 or bf16 query, keys and values");
   if (sa->k < 1 || sa->k > 32) return fail(MSA_ERR_INVALID_ARG, "k must be in [1, 32]");
+  // a unit descriptor keeps the kv head in 15 bits
+  if (a->H_kv > 32767) return fail(MSA_ERR_UNSUPPORTED, "sparse attention takes H_kv <= 32767");
+  // an entry record keeps token * 32 + slot in 32 bits
+  if (a->T >= (1ll << 27)) return fail(MSA_ERR_UNSUPPORTED, "sparse attention takes T < 2^27");
   if (!(sa->sm_scale >= 0.f)) return fail(MSA_ERR_INVALID_ARG, "sm_scale must be >= 0 (0: 1/sqrt(D))");
   if (a->T > 0 && a->B > 0) {
     if (!sa->value_cache || !sa->selection)
@@ -834,7 +838,7 @@ msa_status_t msa_sparse_attention(const msa_index_score_args* args,
   sp.row_ptr = reinterpret_cast<int32_t*>(w + lo.row_ptr);
   sp.cursor = reinterpret_cast<int32_t*>(w + lo.cursor);
   sp.unit_ptr = reinterpret_cast<int32_t*>(w + lo.unit_ptr);
-  sp.qidx = reinterpret_cast<int32_t*>(w + lo.qidx);
+  sp.qrec = reinterpret_cast<int2*>(w + lo.qrec);
   sp.units = reinterpret_cast<int4*>(w + lo.units);
   sp.o_part = reinterpret_cast<uint16_t*>(w + lo.o_part);
   sp.lse_part = reinterpret_cast<float*>(w + lo.lse_part);

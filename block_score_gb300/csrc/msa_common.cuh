@@ -189,7 +189,7 @@ struct SparseParams {
   int32_t* row_ptr;        // [rows + 1]
   int32_t* cursor;         // [rows] scatter positions
   int32_t* unit_ptr;       // [rows + 1] first unit of each list
-  int32_t* qidx;           // [T * H_kv * k] token * k + slot, grouped by list
+  int2* qrec;              // [T * H_kv * k] {token * 32 + slot, last visible key of the token}, grouped by list
   int4* units;             // [T * H_kv * k] {list, first entry, entries, 0}
   uint16_t* o_part;        // [T, H_q, k, D] per-block outputs, normalised, fp16 / bf16 as the input
   float* lse_part;         // [T, H_q, k] per-block natural log-sum-exp

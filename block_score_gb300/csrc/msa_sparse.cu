@@ -161,6 +161,11 @@ __global__ void scatter_kernel(const SparseParams sp) {
   const int64_t L = kv_length(sp, b);
   const int32_t* row = sp.sel + (t * p.H_kv + r) * sp.k;
   const int lane = threadIdx.x & 31;
+  // the last key the token sees (rightDownCausal and kv_len), or -1: what K1
+  // masks by, decided once per entry here rather than per unit and row there
+  int64_t lastk = L - 1;
+  if (live && p.sparse_mode == 3) lastk = min(lastk, L - ((int64_t)p.cu_q[b + 1] - p.cu_q[b]) + (t - p.cu_q[b]));
+  const int last = (int)max(lastk, (int64_t)-1);
   for (int s = 0; s < sp.k; ++s) {
     const int beta = live ? __ldg(row + s) : -1;
     const bool valid = live && entry_valid(beta, p.MB, L);
@@ -171,7 +176,7 @@ __global__ void scatter_kernel(const SparseParams sp) {
       int base = 0;
       if (lane == leader) base = atomicAdd(sp.cursor + list, __popc(peers));
       base = __shfl_sync(peers, base, leader);
-      sp.qidx[base + __popc(peers & ((1u << lane) - 1u))] = (int32_t)(t * sp.k + s);
+      sp.qrec[base + __popc(peers & ((1u << lane) - 1u))] = make_int2((int)(t * 32 + s), last);
     }
   }
 }
@@ -183,8 +188,14 @@ __global__ void units_kernel(const SparseParams sp) {
   const int c = sp.cnt[list];
   const int base = sp.row_ptr[list];
   int4* dst = sp.units + sp.unit_ptr[list];
+  // the list's (kv head, request, block), decoded once here: K1 reads a unit
+  // descriptor on its softmax warps' critical path, where 64-bit divisions by
+  // runtime values cost ~1 us per unit
+  const int beta = (int)(list % sp.p.MB);
+  const int64_t rb = list / sp.p.MB;
+  const int b = (int)(rb % sp.p.B), r = (int)(rb / sp.p.B);
   for (int u = 0; u * sp.qpu < c; ++u)
-    dst[u] = make_int4((int)list, base + u * sp.qpu, min(sp.qpu, c - u * sp.qpu), 0);
+    dst[u] = make_int4(beta, base + u * sp.qpu, min(sp.qpu, c - u * sp.qpu) | (r << 16), b);
 }
 
 // ------------------------------------------------------------------- K1 ----
@@ -249,15 +260,32 @@ struct UnitInfo {
   int r, b, beta, e0, ne;
 };
 
+// Read-only global loads issued where they stand in the program: the
+// compiler may not sink an asm volatile load down to the first use of its
+// value (it may sink an __ldg), so a prefetch issued early stays early and
+// only its consumer waits for it.
+__device__ __forceinline__ int2 ldg_now2(const int2* ptr) {
+  int2 v;
+  asm volatile("ld.global.nc.v2.b32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(ptr));
+  return v;
+}
+__device__ __forceinline__ int4 ldg_now4(const int4* ptr) {
+  int4 v;
+  asm volatile("ld.global.nc.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(ptr));
+  return v;
+}
+
+// A unit descriptor: {block, first entry, entries | kv head << 16, request}
+// (entries <= 128).
 __device__ __forceinline__ UnitInfo unit_of(const SparseParams& sp, int4 d) {
+  (void)sp;
   UnitInfo ui;
-  const int64_t list = d.x;
-  ui.beta = (int)(list % sp.p.MB);
-  const int64_t rb = list / sp.p.MB;
-  ui.b = (int)(rb % sp.p.B);
-  ui.r = (int)(rb / sp.p.B);
+  ui.beta = d.x;
   ui.e0 = d.y;
-  ui.ne = d.z;
+  ui.ne = d.z & 0xffff;
+  ui.r = d.z >> 16;
+  ui.b = d.w;
   return ui;
 }
 
@@ -268,7 +296,7 @@ __device__ __forceinline__ UnitInfo unit_info(const SparseParams& sp, int u) {
 // What one MMA row (query entry row / g, head r * g + row % g) needs of a unit.
 struct RowInfo {
   bool valid;
-  int64_t t;
+  int t;            // token (< 2^27)
   int s, h;
   int lim;          // last visible column of the block (-1: none)
 };
@@ -277,13 +305,12 @@ struct RowInfo {
 // RowInfo later (row_fin), so their latency hides under other work.
 struct RowPre {
   bool valid;
-  int entry, t0, t1, kv0, kv1;   // query entry; cu_q[b], cu_q[b+1]; the request's KV bounds
+  int2 rec;                      // the query entry's {token * 32 + slot, last visible key}
   int r, beta;
 };
 
-// The loads are unconditional, from indices clamped into range (a unit
-// descriptor of zeros reads entry 0 of request 0), so that no instruction
-// depends on a loaded value before row_fin.
+// The load is unconditional, from an index clamped into range, so that no
+// instruction depends on the loaded value before row_fin.
 __device__ __forceinline__ RowPre row_pre(const SparseParams& sp, const UnitInfo& ui, int row) {
   const Params& p = sp.p;
   RowPre q;
@@ -291,16 +318,7 @@ __device__ __forceinline__ RowPre row_pre(const SparseParams& sp, const UnitInfo
   q.r = ui.r;
   q.beta = ui.beta;
   const int e = ui.e0 + max(0, min(row / p.g, ui.ne - 1));
-  q.entry = __ldg(sp.qidx + e);
-  q.t0 = __ldg(p.cu_q + ui.b);
-  q.t1 = __ldg(p.cu_q + ui.b + 1);
-  if (p.layout == 2) {
-    q.kv0 = __ldg(p.cu_k + ui.b);
-    q.kv1 = __ldg(p.cu_k + ui.b + 1);
-  } else {
-    q.kv0 = 0;
-    q.kv1 = __ldg(p.kv_len + ui.b);
-  }
+  q.rec = ldg_now2(sp.qrec + e);
   return q;
 }
 
@@ -312,16 +330,11 @@ __device__ __forceinline__ RowInfo row_fin(const SparseParams& sp, const RowPre&
   ri.s = ri.h = 0;
   ri.lim = -1;
   if (ri.valid) {
-    ri.t = q.entry / sp.k;
-    ri.s = q.entry - (int)(ri.t * sp.k);
+    ri.t = (int)((uint32_t)q.rec.x >> 5);
+    ri.s = q.rec.x & 31;
     ri.h = q.r * p.g + row % p.g;
-    int64_t L = (int64_t)q.kv1 - q.kv0;
-    if (L < 0) L = 0;
-    const int64_t Lq = (int64_t)q.t1 - q.t0;
-    int64_t last = L - 1;
-    if (p.sparse_mode == 3) last = min(last, L - Lq + (ri.t - q.t0));
-    const int64_t c = last - (int64_t)q.beta * kP;
-    ri.lim = c < 0 ? -1 : (c > kP - 1 ? kP - 1 : (int)c);
+    const int c = q.rec.y - q.beta * kP;       // last visible column of the block
+    ri.lim = c < 0 ? -1 : (c > kP - 1 ? kP - 1 : c);
   }
   return ri;
 }
@@ -421,7 +434,7 @@ __global__ void __launch_bounds__(kK1Threads, 1)
       }
       // the unit's query tokens (entry / k), lane e holding entry e
       int qt = 0;
-      if (QTMA && lane < ui.ne) qt = __ldg(sp.qidx + ui.e0 + lane) / sp.k;
+      if (QTMA && lane < ui.ne) qt = __ldg(&sp.qrec[ui.e0 + lane].x) >> 5;
       const uint32_t st_base = sbase + Lo::stage_off + st * Lo::kStage;
       if (!warp_wait(b_kq_empty + 8 * st, ph ^ 1u, ctl)) break;
       if (lane == 0) {
@@ -452,7 +465,7 @@ __global__ void __launch_bounds__(kK1Threads, 1)
           for (int q = 0; q < 2; ++q) {
             const int row = (q0 + q) * 32 + lane;
             const bool have = row < ui.ne * g;
-            const int64_t t = have ? __ldg(sp.qidx + ui.e0 + row / g) / sp.k : 0;
+            const int64_t t = have ? __ldg(&sp.qrec[ui.e0 + row / g].x) >> 5 : 0;
             const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(sp.query) +
                                                               (t * p.H_q + ui.r * g + row % g) * (int64_t)kD);
 #pragma unroll
@@ -613,7 +626,7 @@ __global__ void __launch_bounds__(kK1Threads, 1)
       float inv = 0.f;
       if (prev.valid) {
         const bool any = prev.lim >= 0;
-        slot = (prev.t * p.H_q + prev.h) * (int64_t)sp.k + prev.s;
+        slot = ((int64_t)prev.t * p.H_q + prev.h) * sp.k + prev.s;
         inv = any ? 1.f / prev_l : 0.f;
         // natural-log LSE of the block's visible keys
         sp.lse_part[slot] = any ? (prev_m + __log2f(prev_l)) * 0.6931471805599453f : ninf;
@@ -669,7 +682,7 @@ __global__ void __launch_bounds__(kK1Threads, 1)
       // issued now and used after this unit's softmax and the previous store
       RowPre pre = row_pre(sp, unit_of(sp, d_next), row);
       pre.valid = pre.valid && u + ustep < n_units;
-      const int4 d_after = __ldg(sp.units + min(u + 2 * ustep, n_units - 1));
+      const int4 d_after = ldg_now4(sp.units + min(u + 2 * ustep, n_units - 1));
       if (!warp_wait(b_s_full + 8 * grp, (uint32_t)(i >> 1) & 1u, ctl)) { ok = false; break; }
       tc_fence_after();
       // pass 1: row max over the visible columns (eight independent chains)

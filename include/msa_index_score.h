@@ -365,7 +365,8 @@ msa_status_t msa_index_score_fp4_run(const msa_index_score_args *args, int32_t f
  *          type and T * H_q * k fp32 log-sum-exps).
  *
  * Errors: as msa_index_score, plus MSA_ERR_INVALID_ARG for a missing value
- * cache or selection, k outside [1, 32] or a dtype other than fp16 / bf16.
+ * cache or selection, k outside [1, 32] or a dtype other than fp16 / bf16,
+ * and MSA_ERR_UNSUPPORTED for H_kv > 32767 or T >= 2^27.
  * Selection rows that are out of range, repeated or not ascending set
  * MSA_DEVERR_SELECTION (their outputs are then unspecified); read the error
  * word with msa_get_device_error.  Asynchronous on `stream`.
