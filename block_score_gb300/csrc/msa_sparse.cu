@@ -685,6 +685,9 @@ __global__ void __launch_bounds__(kK1Threads, 1)
       const int4 d_after = ldg_now4(sp.units + min(u + 2 * ustep, n_units - 1));
       if (!warp_wait(b_s_full + 8 * grp, (uint32_t)(i >> 1) & 1u, ctl)) { ok = false; break; }
       tc_fence_after();
+      // every row of the warp sees the whole block (or has no entry): no
+      // per-element mask (blocks off the causal diagonal, most of them)
+      const bool full = __all_sync(0xffffffffu, cur.lim >= kP - 1 || !cur.valid);
       // pass 1: row max over the visible columns (eight independent chains)
       float mp[8];
 #pragma unroll
@@ -694,13 +697,21 @@ __global__ void __launch_bounds__(kK1Threads, 1)
         float x[64];
         tmem_ld64(t_s + 64 * hh, x);
         tmem_wait_ld();
+        if (full) {
 #pragma unroll
-        for (int c = 0; c < 64; ++c)
-          if (64 * hh + c <= cur.lim) mp[c & 7] = fmaxf(mp[c & 7], x[c]);
+          for (int c = 0; c < 64; c += 2) mp[(c >> 1) & 7] = fmax3(mp[(c >> 1) & 7], x[c], x[c + 1]);
+        } else {
+#pragma unroll
+          for (int c = 0; c < 64; ++c)
+            if (64 * hh + c <= cur.lim) mp[c & 7] = fmaxf(mp[c & 7], x[c]);
+        }
       }
       const float m = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
                             fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7]))) * kscale;
       const bool any = cur.lim >= 0;
+      // the unmasked exponentials' offset: +inf for a row with no visible key,
+      // so that each of its p is exactly 0
+      const float m_off = any ? m : __int_as_float(0x7f800000);
       // pass 2: p = 2^(s * scale - m) over each 32-column quarter; the 16
       // packed pairs of quarter hq go to P columns 16 hq .. 16 hq + 15 (S
       // columns this thread has already read)
@@ -713,13 +724,23 @@ __global__ void __launch_bounds__(kK1Threads, 1)
         tmem_ld32(t_s + 32 * hq, x);
         tmem_wait_ld();
         uint32_t pk[16];
+        if (full) {
 #pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          const int c0 = 32 * hq + 2 * c;
-          const float a0 = any && c0 <= cur.lim ? ex2(fmaf(x[2 * c], kscale, -m)) : 0.f;
-          const float a1 = any && c0 + 1 <= cur.lim ? ex2(fmaf(x[2 * c + 1], kscale, -m)) : 0.f;
-          lp[c & 7] += a0 + a1;
-          pk[c] = pack2(a0, a1, BF16);
+          for (int c = 0; c < 16; ++c) {
+            const float a0 = ex2(fmaf(x[2 * c], kscale, -m_off));
+            const float a1 = ex2(fmaf(x[2 * c + 1], kscale, -m_off));
+            lp[c & 7] += a0 + a1;
+            pk[c] = pack2(a0, a1, BF16);
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < 16; ++c) {
+            const int c0 = 32 * hq + 2 * c;
+            const float a0 = any && c0 <= cur.lim ? ex2(fmaf(x[2 * c], kscale, -m)) : 0.f;
+            const float a1 = any && c0 + 1 <= cur.lim ? ex2(fmaf(x[2 * c + 1], kscale, -m)) : 0.f;
+            lp[c & 7] += a0 + a1;
+            pk[c] = pack2(a0, a1, BF16);
+          }
         }
         tmem_st16(t_s + 16 * hq, pk);
       }
