@@ -653,8 +653,11 @@ __global__ void __launch_bounds__(kK1Threads, 1)
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               const int col = 32 * qh + 8 * c + 2 * e;
-              w[e] = pack2(fminf(fmaxf(x[col] * inv, -lim16), lim16), fminf(fmaxf(x[col + 1] * inv, -lim16), lim16),
-                           BF16);
+              if constexpr (BF16)   // bfloat16 has fp32's range: nothing to clamp
+                w[e] = pack2(x[col] * inv, x[col + 1] * inv, true);
+              else
+                w[e] = pack2(fminf(fmaxf(x[col] * inv, -lim16), lim16),
+                             fminf(fmaxf(x[col + 1] * inv, -lim16), lim16), false);
             }
             *reinterpret_cast<uint4*>(ostage + lane * Lo::kORow + 16 * c) = make_uint4(w[0], w[1], w[2], w[3]);
           }
