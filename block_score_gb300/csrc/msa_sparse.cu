@@ -445,14 +445,16 @@ __global__ void __launch_bounds__(kK1Threads, 1)
                 p.layout, pol);
       }
       if (QTMA) {
-        // entry e's g heads land in rows e*g .. e*g+g-1 of each half (1 KiB aligned: g % 8 == 0)
-        for (int e = 0; e < ui.ne; ++e) {
-          const int t = __shfl_sync(0xffffffffu, qt, e);
-          if (lane == 0)
-            for (int x = 0; x < 2; ++x)
-              tma_load_3d(st_base + x * kHalfBytes + (uint32_t)(e * g) * 128u, &tm_q, b_k_full + 8 * st,
-                          64 * x, ui.r * g, t);
-        }
+        // entry e's g heads land in rows e*g .. e*g+g-1 of each half (1 KiB
+        // aligned: g % 8 == 0).  Lane e issues entry e's two boxes (ne <= 128 / g
+        // <= 16): one lane issuing all of them took ~2 us a unit and held back
+        // the next QK (one box per lane instead gains nothing more: the copy
+        // engine's ~45 ns a box is then the limit).
+        __syncwarp();   // lane 0's expect_tx above first
+        if (lane < ui.ne)
+          for (int x = 0; x < 2; ++x)
+            tma_load_3d(st_base + x * kHalfBytes + (uint32_t)(lane * g) * 128u, &tm_q, b_k_full + 8 * st,
+                        64 * x, ui.r * g, qt);
       }
       if (!QTMA) {
         // the unit's query rows (query entry row / g, head r * g + row % g):
