@@ -842,16 +842,18 @@ msa_status_t msa_sparse_attention(const msa_index_score_args* args,
   sp.units = reinterpret_cast<int4*>(w + lo.units);
   sp.o_part = reinterpret_cast<uint16_t*>(w + lo.o_part);
   sp.lse_part = reinterpret_cast<float*>(w + lo.lse_part);
-  // K and V pages through the key cache's tensor-map recipe; the query map
-  // with a run of one position (a box is one query entry's g heads)
-  CUtensorMap tq, tk, tv, tq_unused;
+  // K and V pages through the key cache's tensor-map recipe; the query maps
+  // with a run of one position (a box is one query entry's g heads) and of
+  // 128 / g positions (a unit of consecutive query tokens in two boxes)
+  CUtensorMap tq, tk, tv, tq_unused, tqr;
   msa::Params p1 = sp.p;
   p1.np = 1;
   if ((st = make_maps(args, p1, &tq, &tk, nullptr, nullptr)) != MSA_OK) return st;
+  if ((st = make_maps(args, sp.p, &tqr, &tq_unused, nullptr, nullptr)) != MSA_OK) return st;
   msa_index_score_args va = *args;
   va.key_cache = sa->value_cache;
   if ((st = make_maps(&va, p1, &tq_unused, &tv, nullptr, nullptr)) != MSA_OK) return st;
-  cudaError_t e = msa::launch_sparse_attention(&tq, &tk, &tv, sp, args->q_dtype == MSA_BF16, out, lse,
+  cudaError_t e = msa::launch_sparse_attention(&tq, &tk, &tv, &tqr, sp, args->q_dtype == MSA_BF16, out, lse,
                                                reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "sparse attention launch");
   return MSA_OK;

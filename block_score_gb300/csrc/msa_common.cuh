@@ -197,7 +197,9 @@ struct SparseParams {
 
 // tm_q: the query map with a box of (64 columns, g heads, 1 position), read
 // when g is a multiple of 8; tm_k / tm_v: one 128-token page of one kv head.
-cudaError_t launch_sparse_attention(const void* tm_q, const void* tm_k, const void* tm_v,
+// tm_q: query boxes of one position (one query entry's g heads); tm_qr: of
+// 128 / g positions (a run of consecutive query tokens)
+cudaError_t launch_sparse_attention(const void* tm_q, const void* tm_k, const void* tm_v, const void* tm_qr,
                                     const SparseParams& sp, bool bf16, float* out, float* lse,
                                     cudaStream_t s);
 

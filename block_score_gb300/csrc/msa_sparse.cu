@@ -355,7 +355,8 @@ __device__ __forceinline__ RowInfo row_fin(const SparseParams& sp, const RowPre&
 template <bool BF16, bool QTMA>
 __global__ void __launch_bounds__(kK1Threads, 1)
     sparse_k1_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                     const __grid_constant__ CUtensorMap tm_v, const SparseParams sp) {
+                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_qr,
+                     const SparseParams sp) {
   using Lo = K1Layout;
   const Params& p = sp.p;
   extern __shared__ uint8_t smem_raw[];
@@ -393,7 +394,10 @@ __global__ void __launch_bounds__(kK1Threads, 1)
     mbar_init(b_drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
-    if (QTMA) prefetch_tmap(&tm_q);
+    if (QTMA) {
+      prefetch_tmap(&tm_q);
+      prefetch_tmap(&tm_qr);
+    }
     prefetch_tmap(&tm_k);
     prefetch_tmap(&tm_v);
   }
@@ -435,11 +439,16 @@ __global__ void __launch_bounds__(kK1Threads, 1)
       // the unit's query tokens (entry / k), lane e holding entry e
       int qt = 0;
       if (QTMA && lane < ui.ne) qt = __ldg(&sp.qrec[ui.e0 + lane].x) >> 5;
+      // entries of consecutive tokens t0, t0 + 1, ... (the blocks every token
+      // of a range selects): one box of 128 / g positions per half brings
+      // the whole tile (positions past the entries are rows the softmax skips)
+      const int t0 = __shfl_sync(0xffffffffu, qt, 0);
+      const bool run = QTMA && __all_sync(0xffffffffu, lane >= ui.ne || qt == t0 + lane);
+      const uint32_t q_bytes = !QTMA ? 0u : run ? 2u * (uint32_t)(sp.qpu * g) * 128u : (uint32_t)(ui.ne * g) * 2u * 128u;
       const uint32_t st_base = sbase + Lo::stage_off + st * Lo::kStage;
       if (!warp_wait(b_kq_empty + 8 * st, ph ^ 1u, ctl)) break;
       if (lane == 0) {
-        mbar_arrive_expect_tx(b_k_full + 8 * st,
-                              Lo::kTile + (QTMA ? (uint32_t)(ui.ne * g) * 2u * 128u : 0u));
+        mbar_arrive_expect_tx(b_k_full + 8 * st, Lo::kTile + q_bytes);
         for (int x = 0; x < 2; ++x)
           tma_k(st_base + Lo::kTile + x * kHalfBytes, &tm_k, b_k_full + 8 * st, 64 * x, tok, ui.r, page,
                 p.layout, pol);
@@ -451,10 +460,15 @@ __global__ void __launch_bounds__(kK1Threads, 1)
         // the next QK (one box per lane instead gains nothing more: the copy
         // engine's ~45 ns a box is then the limit).
         __syncwarp();   // lane 0's expect_tx above first
-        if (lane < ui.ne)
+        if (run) {
+          if (lane == 0)
+            for (int x = 0; x < 2; ++x)
+              tma_load_3d(st_base + x * kHalfBytes, &tm_qr, b_k_full + 8 * st, 64 * x, ui.r * g, t0);
+        } else if (lane < ui.ne) {
           for (int x = 0; x < 2; ++x)
             tma_load_3d(st_base + x * kHalfBytes + (uint32_t)(lane * g) * 128u, &tm_q, b_k_full + 8 * st,
                         64 * x, ui.r * g, qt);
+        }
       }
       if (!QTMA) {
         // the unit's query rows (query entry row / g, head r * g + row % g):
@@ -849,8 +863,8 @@ __global__ void combine_kernel(const SparseParams sp, float* __restrict__ out,
 
 }  // namespace
 
-cudaError_t launch_sparse_attention(const void* tm_q, const void* tm_k, const void* tm_v, const SparseParams& sp,
-                                    bool bf16, float* out, float* lse, cudaStream_t s) {
+cudaError_t launch_sparse_attention(const void* tm_q, const void* tm_k, const void* tm_v, const void* tm_qr,
+                                    const SparseParams& sp, bool bf16, float* out, float* lse, cudaStream_t s) {
   const Params& p = sp.p;
   const int64_t th = p.T * (int64_t)p.H_kv;
   cudaError_t e = cudaMemsetAsync(sp.p.ws, 0, sizeof(SparseHeader), s);
@@ -875,7 +889,8 @@ cudaError_t launch_sparse_attention(const void* tm_q, const void* tm_k, const vo
     return e;
   k1<<<(unsigned)p.num_sms, kK1Threads, K1Layout::bytes, s>>>(*static_cast<const CUtensorMap*>(tm_q),
                                                                *static_cast<const CUtensorMap*>(tm_k),
-                                                               *static_cast<const CUtensorMap*>(tm_v), sp);
+                                                               *static_cast<const CUtensorMap*>(tm_v),
+                                                               *static_cast<const CUtensorMap*>(tm_qr), sp);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   const int64_t rows = p.T * (int64_t)p.H_q;
   if (rows > 0) {
