@@ -635,7 +635,10 @@ __global__ void __launch_bounds__(kK1Threads, 1)
     // quarter of the warp's rows goes through the warp's staging area (each
     // thread writes its row's 64 bytes), then every store instruction writes
     // eight 64-byte row segments.
-    auto store_o = [&](int j) -> bool {
+    // the stored unit's row state comes by value: a by-reference capture of
+    // it kept it in local memory (a 40-byte stack frame), whose reloads from
+    // L2 showed as ~1 us per 64-column half of the store
+    auto store_o = [&](int j, const RowInfo prev, const float prev_l, const float prev_m) -> bool {
       if (!warp_wait(b_o_full + 8 * grp, (uint32_t)(j >> 1) & 1u, ctl)) return false;
       tc_fence_after();
       int64_t slot = -1;
@@ -768,14 +771,14 @@ __global__ void __launch_bounds__(kK1Threads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(b_p_full + 8 * grp);
-      if (i >= 2 && !store_o(i - 2)) { ok = false; break; }
+      if (i >= 2 && !store_o(i - 2, prev, prev_l, prev_m)) { ok = false; break; }
       prev = cur;
       prev_l = l;
       prev_m = m;
       cur = row_fin(sp, pre, row);
       d_next = d_after;
     }
-    if (ok && i > grp) store_o(i - 2);
+    if (ok && i > grp) store_o(i - 2, prev, prev_l, prev_m);
   }
 
   tc_fence_before();
