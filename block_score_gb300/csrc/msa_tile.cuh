@@ -12,12 +12,15 @@
 // Why two blocks per MMA: the issuing thread stalls on every mbarrier wait
 // until its queued MMAs have been dispatched, and a 64-cycle N=128 MMA cannot
 // cover that pause, so the tensor pipe idles for a few hundred cycles per block.
-// A 128-cycle N=256 MMA keeps the pipe busy across the wait.
+// A 128-cycle N=256 MMA keeps the pipe busy across the wait.  The whole MMA
+// warp runs the issue loop and its elected lane (elect.sync) issues: issued so,
+// back-to-back N=256 MMAs complete every ~134 cycles, against ~168 when one
+// lane issues them from a divergent branch.
 //
 // Roles (one CTA per SM, persistent over units fetched with an atomic counter):
 //   warp 0       scheduler: claims the next unit from the global counter a few
 //                blocks before the producer needs it and decodes it from the plan
-//   warp 1       TMEM owner + single-thread tcgen05.mma issuer
+//   warp 1       TMEM owner + tcgen05.mma issuer (converged warp, elected lane)
 //   warp 2       TMA producer (Q tiles, K pages through block_table)
 //   16-bit keys:
 //   warps 3..10  epilogue, two groups of four warps (one per TMEM lane
