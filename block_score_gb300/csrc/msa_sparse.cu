@@ -106,45 +106,65 @@ __global__ void count_kernel(const SparseParams sp) {
 }
 
 // One CTA: exclusive prefix sums of the list lengths (row_ptr) and of the
-// units per list (unit_ptr); the scatter cursors start at row_ptr.
+// units per list (unit_ptr); the scatter cursors start at row_ptr.  Tiles of
+// 1024 lists: one coalesced count per thread (the next tile's already in
+// flight), a shuffle scan in each warp, one pass over the 32 warp totals, and a
+// running carry from tile to tile.  (Every partial sum is at most the entry
+// count, below 2^31.)
 __global__ void __launch_bounds__(1024) scan_kernel(const SparseParams sp) {
-  __shared__ int64_t s_sum[2][1024];
-  const int tid = threadIdx.x;
+  __shared__ int s_w[2][32];
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const int64_t rows = sp.rows;
-  const int64_t per = (rows + 1023) / 1024;
-  const int64_t r0 = min(rows, tid * per), r1 = min(rows, r0 + per);
-  int64_t a = 0, u = 0;
-  for (int64_t i = r0; i < r1; ++i) {
-    const int c = sp.cnt[i];
-    a += c;
-    u += (c + sp.qpu - 1) / sp.qpu;
-  }
-  s_sum[0][tid] = a;
-  s_sum[1][tid] = u;
-  __syncthreads();
-  // Hillis-Steele inclusive scan of the per-thread totals
-  for (int off = 1; off < 1024; off <<= 1) {
-    int64_t xa = 0, xu = 0;
-    if (tid >= off) { xa = s_sum[0][tid - off]; xu = s_sum[1][tid - off]; }
+  int carry_a = 0, carry_u = 0;                     // lists and units before the tile
+  int c_next = tid < rows ? sp.cnt[tid] : 0;
+  for (int64_t base = 0; base < rows; base += 1024) {
+    const int64_t i = base + tid;
+    const int c = c_next;
+    c_next = i + 1024 < rows ? sp.cnt[i + 1024] : 0;
+    const int cu = (c + sp.qpu - 1) / sp.qpu;
+    int a = c, u = cu;                               // inclusive scans within the warp
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int na = __shfl_up_sync(0xffffffffu, a, o), nu = __shfl_up_sync(0xffffffffu, u, o);
+      if (lane >= o) {
+        a += na;
+        u += nu;
+      }
+    }
+    if (lane == 31) {
+      s_w[0][wid] = a;
+      s_w[1][wid] = u;
+    }
     __syncthreads();
-    s_sum[0][tid] += xa;
-    s_sum[1][tid] += xu;
+    if (wid == 0) {                                  // inclusive scan of the warp totals
+      int wa = s_w[0][lane], wu = s_w[1][lane];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int na = __shfl_up_sync(0xffffffffu, wa, o), nu = __shfl_up_sync(0xffffffffu, wu, o);
+        if (lane >= o) {
+          wa += na;
+          wu += nu;
+        }
+      }
+      s_w[0][lane] = wa;
+      s_w[1][lane] = wu;
+    }
     __syncthreads();
+    const int pa = carry_a + (wid ? s_w[0][wid - 1] : 0) + a - c;   // exclusive
+    const int pu = carry_u + (wid ? s_w[1][wid - 1] : 0) + u - cu;
+    if (i < rows) {
+      sp.row_ptr[i] = pa;
+      sp.cursor[i] = pa;
+      sp.unit_ptr[i] = pu;
+    }
+    carry_a += s_w[0][31];
+    carry_u += s_w[1][31];
+    __syncthreads();                                 // the totals are read before the next tile writes them
   }
-  a = tid ? s_sum[0][tid - 1] : 0;
-  u = tid ? s_sum[1][tid - 1] : 0;
-  for (int64_t i = r0; i < r1; ++i) {
-    const int c = sp.cnt[i];
-    sp.row_ptr[i] = (int32_t)a;
-    sp.cursor[i] = (int32_t)a;
-    sp.unit_ptr[i] = (int32_t)u;
-    a += c;
-    u += (c + sp.qpu - 1) / sp.qpu;
-  }
-  if (tid == 1023) {
-    sp.row_ptr[rows] = (int32_t)s_sum[0][1023];
-    sp.unit_ptr[rows] = (int32_t)s_sum[1][1023];
-    reinterpret_cast<SparseHeader*>(sp.p.ws)->n_units = (int32_t)s_sum[1][1023];
+  if (tid == 0) {
+    sp.row_ptr[rows] = carry_a;
+    sp.unit_ptr[rows] = carry_u;
+    reinterpret_cast<SparseHeader*>(sp.p.ws)->n_units = carry_u;
   }
 }
 
