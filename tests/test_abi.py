@@ -197,3 +197,42 @@ def test_fp4_host_rules(lib):
                  dict(fp4, page_stride=100)):
         assert lib.msa_index_score_fp4_workspace_size(ctypes.byref(_args(**over)), 0,
                                                       ctypes.byref(n)) == 1
+
+
+def _sparse(**over):
+    import block_score_gb300 as bs
+    sa = bs._SparseArgs()
+    base = dict(value_cache=16, selection=16, k=16, sm_scale=0.0)
+    base.update(over)
+    for k, v in base.items():
+        setattr(sa, k, v)
+    return sa
+
+
+def test_sparse_attention_host_rules(lib):
+    n = ctypes.c_size_t()
+    ok = _args()                                           # bf16 query and keys
+    assert lib.msa_sparse_attention_workspace_size(ctypes.byref(ok), ctypes.byref(_sparse()),
+                                                   ctypes.byref(n)) == 0
+    small = n.value
+    # the per-entry records (8 bytes) and unit descriptors (16) and the 16-bit
+    # partials grow with T * H_kv * k
+    big = _args(T=64)
+    assert lib.msa_sparse_attention_workspace_size(ctypes.byref(big), ctypes.byref(_sparse()),
+                                                   ctypes.byref(n)) == 0
+    assert n.value > small
+    cases = [
+        (ok, dict(k=0), 1), (ok, dict(k=33), 1), (ok, dict(sm_scale=-1.0), 1),
+        (ok, dict(value_cache=None), 1), (ok, dict(selection=None), 1),
+        (_args(q_dtype=0, k_dtype=0), {}, 0),              # fp16 is fine too
+        (_args(q_dtype=3, k_dtype=3), {}, 1),              # FP8: not for the sparse branch
+        # a unit descriptor keeps the kv head in 15 bits, an entry record the
+        # token in 27
+        (_args(H_q=40000, H_kv=40000, page_stride=40000 * 128 * 128), {}, 2),
+        (_args(T=1 << 27), {}, 2),
+        (_args(T=(1 << 27) - 1), {}, 0),
+    ]
+    for a, over, status in cases:
+        got = lib.msa_sparse_attention_workspace_size(ctypes.byref(a), ctypes.byref(_sparse(**over)),
+                                                      ctypes.byref(n))
+        assert got == status, (over, got, status)
