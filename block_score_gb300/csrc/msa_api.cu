@@ -45,7 +45,7 @@ int64_t row_elems(const msa_index_score_args* a) {
   return a->k_dtype == MSA_E2M1 ? a->D / 2 : a->D;
 }
 
-// Host-side checks; everything that can be judged without reading device memory.
+// Host-side checks; everything that can be decided without reading device memory.
 // `fp4`: the call is msa_index_score_fp4 (E2M1 query and key, scales given apart).
 msa_status_t validate(const msa_index_score_args* a, bool fp4 = false) {
   if (!a) return fail(MSA_ERR_INVALID_ARG, "args is NULL");

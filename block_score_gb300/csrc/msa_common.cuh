@@ -9,7 +9,7 @@
 
 namespace msa {
 
-constexpr int kD = 128;          // head dim handled by this build
+constexpr int kD = 128;          // head dim handled by this library
 constexpr int kP = 128;          // tokens per page (block_size)
 constexpr int kTileRows = 128;   // MMA rows per work unit: floor(128/g) positions x g heads
 

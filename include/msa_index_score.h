@@ -35,7 +35,7 @@
  * reference op's aclnn interface).  Two calls that share a workspace must be
  * ordered (same stream, or joined by events).
  *
- * Scope of this build: D == 128 and P == 128; g = H_q / H_kv <= 128.
+ * Scope of this library: D == 128 and P == 128; g = H_q / H_kv <= 128.
  */
 #ifndef MSA_INDEX_SCORE_H_
 #define MSA_INDEX_SCORE_H_
@@ -55,7 +55,7 @@ typedef struct CUstream_st *msa_stream_t;
 typedef enum {
     MSA_OK = 0,
     MSA_ERR_INVALID_ARG = 1,   /* argument violates the op's rules (layout, dtype, shapes) */
-    MSA_ERR_UNSUPPORTED = 2,   /* legal for the op, outside this build (D != 128, P != 128, g > 128) */
+    MSA_ERR_UNSUPPORTED = 2,   /* legal for the op, outside this library (D != 128, P != 128, g > 128) */
     MSA_ERR_CUDA = 3,          /* a CUDA runtime/driver call failed; see msa_last_error_message() */
     MSA_ERR_DEVICE_DATA = 4,   /* device-side data check failed; see msa_get_device_error() */
     MSA_ERR_WORKSPACE = 5      /* workspace NULL, too small or misaligned */
@@ -123,7 +123,7 @@ typedef struct {
     int32_t local_blocks;          /* default 1, <= MB */
 
     /* Optional host-side upper bound on every request's query length (0 = not
-     * known).  This build's own addition, not an argument of the op in the
+     * known).  An addition of this library, not an argument of the op in the
      * pages: like the max_seqlen_q of varlen attention calls, it lets the host
      * skip the query-tile kernel when every request is a short int8 request
      * (max_seqlen_q * H_q / H_kv <= 32).  A request longer than a nonzero bound

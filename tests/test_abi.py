@@ -102,7 +102,7 @@ def test_workspace_size_grows_with_batch(lib):
     (dict(layout=7), 1),                        # layout outside BBND/BNBD/TND
     (dict(sparse_mode=1), 1),                   # modes 0 and 3 only
     (dict(H_q=9, H_kv=2), 1),                   # H_q % H_kv
-    (dict(D=64), 2),                            # scope of this build
+    (dict(D=64), 2),                            # scope of this library
     (dict(P=64, page_stride=64 * 128), 2),
     (dict(k_dtype=2, q_dtype=1, scale=16), 1),  # int8 keys need an fp16 query
     (dict(k_dtype=2, q_dtype=0, scale=None), 1),  # int8 keys need a scale
