@@ -104,14 +104,41 @@ KERNEL_SOURCES = {
 }
 
 
+def code_only(text: str) -> str:
+    """C/CUDA source with its comments, trailing blanks and empty lines
+    removed (string and character literals kept as written), so that a
+    change to a comment alone leaves the hash of a kernel's sources as it was."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            out.append(" ")
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    lines = (line.rstrip() for line in "".join(out).split("\n"))
+    return "\n".join(line for line in lines if line)
+
+
 def kernel_source_hash(kernel: str) -> str:
-    """Hash of the CUDA sources of one kernel."""
+    """Hash of the code (comments left out) of the CUDA sources of one kernel."""
     import hashlib
     h = hashlib.sha256()
     d = os.path.join(ROOT, "block_score_gb300", "csrc")
     for name in KERNEL_SOURCES[kernel]:
-        with open(os.path.join(d, name), "rb") as f:
-            h.update(name.encode() + b"\0" + f.read())
+        with open(os.path.join(d, name), encoding="utf-8") as f:
+            h.update(name.encode() + b"\0" + code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 
