@@ -5,7 +5,8 @@ section 4.8 Equation (8) (softmax restricted to the selected blocks, GQA
 groups sharing one selection, section 4.3 Equation (3)).  It is checked
 against things other than itself:
   * torch's scaled_dot_product_attention (float64, explicit causal mask) when
-    every block is selected: the restricted softmax is then plain attention;
+    every block is selected: the restricted softmax is then plain attention
+    (paged and packed keys; the default scale against torch's default);
   * a hand-worked example (P = 2, D = 2) in tests/golden/;
   * closed forms: one visible key gives O = v_j and LSE = s_j;
   * invariants: keys and values of blocks that are not selected, or of
@@ -45,6 +46,9 @@ def _all_blocks(case, k):
 def _dense(case, value, b):
     """Keys and values of request b by logical position, float64 [L, H_kv, D]."""
     L, P = case.kv_lens[b], case.P
+    if case.layout == "TND":                               # packed rows from cu_seqlens_k[b]
+        lo = int(case.cu_seqlens_k[b])
+        return case.key[lo:lo + L].double(), value[lo:lo + L].double()
     ks, vs = [], []
     for j in range(L):
         page = int(case.block_table[b, j // P])
@@ -56,7 +60,7 @@ def _dense(case, value, b):
     return torch.stack(ks).double(), torch.stack(vs).double()
 
 
-@pytest.mark.parametrize("layout", ["BBND", "BNBD"])
+@pytest.mark.parametrize("layout", ["BBND", "BNBD", "TND"])
 @pytest.mark.parametrize("mode", [3, 0])
 def test_full_selection_is_plain_attention(layout, mode):
     case = make_case([5, 3, 1], [9, 20, 7], H_q=4, H_kv=2, P=4, D=8, layout=layout,
@@ -82,6 +86,26 @@ def test_full_selection_is_plain_attention(layout, mode):
         lse = torch.logsumexp(scores.masked_fill(~mask, -math.inf), dim=-1)   # [H_q, Lq]
         np.testing.assert_allclose(O[cu[b]:cu[b + 1]], ref.permute(1, 0, 2).numpy(), rtol=1e-12, atol=1e-12)
         np.testing.assert_allclose(LSE[cu[b]:cu[b + 1]], lse.T.numpy(), rtol=1e-12, atol=1e-12)
+
+
+def test_default_scale_is_torchs_default():
+    # sm_scale omitted: Equation (8)'s 1/sqrt(D), which is also the default of
+    # torch's scaled_dot_product_attention
+    case = make_case([4, 2], [11, 6], H_q=2, H_kv=1, P=4, D=16, layout="BBND",
+                     q_dtype=torch.bfloat16, MB=3, sparse_mode=3, seed=78)
+    value = _value_like(case, 79)
+    O, _ = sparse_attention(case, value, _all_blocks(case, 3))
+    cu = case.cu_seqlens_q.tolist()
+    for b in range(case.B):
+        k, v = _dense(case, value, b)
+        q = case.query[cu[b]:cu[b + 1]].double().permute(1, 0, 2)   # [H_q, Lq, D]
+        Lq, L = q.shape[1], k.shape[0]
+        mask = torch.arange(L)[None, :] <= (L - Lq + torch.arange(Lq)[:, None])
+        ref = torch.nn.functional.scaled_dot_product_attention(
+            q, k.permute(1, 0, 2).expand(2, L, 16), v.permute(1, 0, 2).expand(2, L, 16),
+            attn_mask=mask)
+        np.testing.assert_allclose(O[cu[b]:cu[b + 1]], ref.permute(1, 0, 2).numpy(),
+                                   rtol=1e-12, atol=1e-12)
 
 
 def test_hand_example():
@@ -152,3 +176,20 @@ def test_empty_selection_gives_zero_and_minus_inf():
     value = _value_like(case, 77)
     O, LSE = sparse_attention(case, value, torch.full((2, 1, 4), -1, dtype=torch.int32))
     assert np.all(O == 0) and np.all(np.isneginf(LSE))
+
+
+def test_row_subset_computes_the_listed_rows_only():
+    # rows = flat t * H_q + h: those rows equal the full call's, the others stay O = 0, LSE = nan
+    case = make_case([5, 3], [30, 12], H_q=4, H_kv=2, P=4, D=8, layout="BBND",
+                     q_dtype=torch.bfloat16, MB=8, seed=80)
+    value = _value_like(case, 81)
+    sel = _all_blocks(case, 8)
+    O, LSE = sparse_attention(case, value, sel)
+    rows = [1, 14, 30]                                   # (t, h) = (0, 1), (3, 2), (7, 2)
+    O2, LSE2 = sparse_attention(case, value, sel, rows=rows)
+    for flat in range(case.T * case.H_q):
+        t, h = divmod(flat, case.H_q)
+        if flat in rows:
+            assert np.array_equal(O2[t, h], O[t, h]) and LSE2[t, h] == LSE[t, h]
+        else:
+            assert np.all(O2[t, h] == 0) and np.isnan(LSE2[t, h])

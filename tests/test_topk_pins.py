@@ -208,3 +208,25 @@ def test_own_block_of_each_query_token():
     # request 0: q_pos 297, 298, 299 -> block 2; request 1: q_pos 128 -> block 1;
     # request 3: q_pos -1 (no key at or before it) and 0 -> none, block 0
     assert loc == [2, 2, 2, 1, -1, 0]
+
+
+def test_row_subsets_select_the_listed_rows_only():
+    # rows = flat h * T + t (block_topk) and r * T + t (group_topk); a subset
+    # gives the full call's selections there and -1 everywhere else
+    rng = np.random.default_rng(7)
+    H, T, MB, k, g = 4, 6, 20, 5, 2
+    score = rng.standard_normal((H, T, 32)).astype(np.float32)
+    full = otk.block_topk(score, MB, k)
+    rows = [1, 8, 23]                                    # (h, t) = (0, 1), (1, 2), (3, 5)
+    part = otk.block_topk(score, MB, k, rows=rows)
+    for r in range(H * T):
+        h, t = divmod(r, T)
+        want = full[t, h] if r in rows else np.full(k, -1)
+        assert np.array_equal(part[t, h], want), (h, t)
+    gfull = otk.group_topk(score, g, MB, k)
+    grows = [2, 7]                                       # (r, t) = (0, 2), (1, 1)
+    gpart = otk.group_topk(score, g, MB, k, rows=grows)
+    for flat in range((H // g) * T):
+        r, t = divmod(flat, T)
+        want = gfull[t, r] if flat in grows else np.full(k, -1)
+        assert np.array_equal(gpart[t, r], want), (r, t)
