@@ -84,7 +84,8 @@ typedef enum { MSA_FP4_MX = 0, MSA_FP4_NV = 1 } msa_fp4_format_t;
 #define MSA_DEVERR_SELECTION   0x20  /* sparse attention: a selection entry >= MB, repeated, or not ascending */
 
 typedef struct {
-    /* query: [T, H_q, D] contiguous, fp16 or bf16 ("TND" query of the guide, sec. 4). */
+    /* query: [T, H_q, D] contiguous ("TND" query of the guide, sec. 4); fp16, bf16 or
+     * FP8 (see msa_dtype_t); E2M1 codes only through msa_index_score_fp4. */
     const void *query;
     msa_dtype_t q_dtype;
     int64_t T;                  /* total query tokens = cu_seqlens_q[B] */
@@ -230,8 +231,8 @@ msa_status_t msa_noalloc_device_error(int32_t *bits, msa_stream_t stream);
  * visible key; a NaN score is never selected).  Equal scores rank the smaller
  * block index first.  The local mask's forced blocks (1e30 / 1e29) therefore
  * always make the selection when k covers them.  When H_q > H_kv the
- * selection is per index head; a caller that wants one selection per GQA group
- * (section 4.3, Equation (3)) passes one representative head per group.
+ * selection is per index head; one selection per GQA group (section 4.3,
+ * Equation (3)) is what msa_index_score_topk computes, fused into the scores.
  *
  * Asynchronous on `stream`; no workspace, no allocation.  Returns
  * MSA_ERR_INVALID_ARG for null pointers with work to do, negative sizes,
