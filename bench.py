@@ -440,21 +440,34 @@ def config_block(case, workload):
                     "inputs fit in L2 (no flush; launch- or latency-bound case)"))}
 
 
+def is_fp8(case) -> bool:
+    """FP8 query and keys (FP4 codes are bytes too, but they are multiplied on
+    the 16-bit tensor path)."""
+    return case.query.element_size() == 1 and not getattr(case, "fp4", None)
+
+
+def tensor_peak(case, peaks) -> float:
+    """Dense tensor peak (TFLOP/s) of the case's operand type: the measured bf16
+    burst peak, times the nominal dense ratio 4.5 / 2.25 for FP8 operands."""
+    return peaks["bf16_tflops"] * (2.0 if is_fp8(case) else 1.0)
+
+
 def roofline_of(case, work, kern_ms, peaks, traffic):
     """Roofline record of the dominant kernel from its per-launch duration."""
     kern_s = kern_ms / 1e3
     hbm_gbs_kernel = work["bytes"] / kern_s / 1e9
     tflops_kernel = work["flops"] / kern_s / 1e12
+    fp8 = is_fp8(case)
+    tensor_peak_tf = tensor_peak(case, peaks)
+    # the binding roof: the longer of the two roofline times, each at its own peak
     bound = "hbm" if work["bytes"] / (peaks["hbm_gbs"] * 1e9) >= \
-        work["flops"] / (peaks["bf16_tflops"] * 1e12) else "tensor"
+        work["flops"] / (tensor_peak_tf * 1e12) else "tensor"
     if bound == "hbm":
         roof = {"bound": "hbm", "achieved": hbm_gbs_kernel, "peak": peaks["hbm_gbs"],
                 "unit": "GB/s", "frac": hbm_gbs_kernel / peaks["hbm_gbs"],
                 "traffic": traffic, "peak_source": peaks["source"] + " hbm_gbs"}
-    elif case.query.element_size() == 1 and not getattr(case, "fp4", None):
-        # FP8 operands: the measured bf16 peak times the nominal dense ratio 4.5 / 2.25
-        # (FP4 codes are bytes too, but they are multiplied on the 16-bit path)
-        pk = peaks["bf16_tflops"] * 2.0
+    elif fp8:
+        pk = tensor_peak_tf
         roof = {"bound": "tensor", "achieved": tflops_kernel, "peak": pk, "unit": "TFLOP/s",
                 "frac": tflops_kernel / pk, "traffic": traffic,
                 "peak_source": peaks["source"] + " bf16_tflops (burst) x 2 (nominal fp8 / bf16)"}
@@ -538,8 +551,7 @@ def measure(case, key, steps, warmup, device, stream, peaks, ws, traffic=None):
         "tflops": work["flops"] / call_s / 1e12,
         "k_cache_gbs": work["k_bytes"] / call_s / 1e9,
         "frac_hbm": (work["bytes"] / call_s / 1e9) / peaks["hbm_gbs"],
-        "frac_tensor": work["flops"] / call_s / 1e12 /
-        (peaks["bf16_tflops"] * (2.0 if case.query.element_size() == 1 else 1.0)),
+        "frac_tensor": work["flops"] / call_s / 1e12 / tensor_peak(case, peaks),
         "roofline": roof,
         "gpu_launches": launches_per_call(case) * steps,
         "clocks": sampler.summary(),
