@@ -9,7 +9,8 @@ given beside each) and must pass.
 
     python tests/oracle_mutants.py [--dst DIR] [--only I ...]
 
-The source tree itself is never modified.
+The source tree itself is never modified; the copy lives in DIR/oracle_mutants_copy
+(DIR defaults to a new temporary directory) and is removed at the end.
 """
 from __future__ import annotations
 
@@ -310,10 +311,15 @@ def run_one(dst: str, mutant) -> bool:
 
 def main() -> int:
     ap = argparse.ArgumentParser()
-    ap.add_argument("--dst", default=None, help="scratch directory for the mutated copy")
+    ap.add_argument("--dst", default=None,
+                    help="directory under which the mutated copy is made (default: a new "
+                         "temporary directory); only its subdirectory oracle_mutants_copy "
+                         "is written and removed")
     ap.add_argument("--only", type=int, nargs="*", default=None, help="mutant numbers to run")
     args = ap.parse_args()
-    scratch = args.dst or os.path.join(tempfile.mkdtemp(prefix="oracle_mutants_"), "repo")
+    parent = args.dst or tempfile.mkdtemp(prefix="oracle_mutants_")
+    os.makedirs(parent, exist_ok=True)
+    scratch = os.path.join(parent, "oracle_mutants_copy")
     bad = 0
     for i, m in enumerate(MUTANTS):
         if args.only is not None and i not in args.only:
@@ -327,6 +333,8 @@ def main() -> int:
         print(f"{i:3d} {m[0]:28s} {m[3]:34s} {state}{note}{'' if ok else '  <-- UNEXPECTED'}",
               flush=True)
     shutil.rmtree(scratch, ignore_errors=True)
+    if args.dst is None:
+        shutil.rmtree(parent, ignore_errors=True)
     print("all as expected" if not bad else f"{bad} unexpected")
     return 1 if bad else 0
 
