@@ -499,13 +499,23 @@ class Prepared:
         shape, dtype and strides; ``selection`` is int32 ``[T, H_kv, k]``.
         Returns ``(out [T, H_q, D] fp32, lse [T, H_q] fp32)``."""
         key = self.call.key
+        T, H_q = int(self.call.args.T), int(self.call.args.H_q)
+        H_kv, D = int(self.call.args.H_kv), int(self.call.args.D)
+        # every array the kernels index must have the shape they index it with
+        if (selection.dtype != torch.int32 or selection.dim() != 3 or not selection.is_contiguous()
+                or tuple(selection.shape[:2]) != (T, H_kv)):
+            raise ValueError(f"selection must be a contiguous int32 tensor [T, H_kv, k] = "
+                             f"[{T}, {H_kv}, k]")
+        for name, t, shape in (("out", out, (T, H_q, D)), ("lse", lse, (T, H_q))):
+            if t is not None and (tuple(t.shape) != shape or t.dtype != torch.float32
+                                  or not t.is_contiguous()):
+                raise ValueError(f"{name} must be a contiguous float32 tensor of shape {shape}")
         if (tuple(value.shape) != tuple(key.shape) or value.stride() != key.stride()
                 or value.dtype != key.dtype or not value.is_cuda):
             raise ValueError("value must match the key cache's shape, strides and dtype")
-        if selection.dtype != torch.int32 or selection.dim() != 3 or not selection.is_contiguous():
-            raise ValueError("selection must be a contiguous int32 tensor [T, H_kv, k]")
-        T, H_q = int(self.call.args.T), int(self.call.args.H_q)
-        D = int(self.call.args.D)
+        for name, t in (("selection", selection), ("out", out), ("lse", lse)):
+            if t is not None and t.device != value.device:
+                raise ValueError(f"{name} must be on the value cache's device {value.device}")
         sa = _SparseArgs()
         sa.value_cache = value.data_ptr()
         sa.selection = selection.data_ptr()

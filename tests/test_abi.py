@@ -236,3 +236,27 @@ def test_sparse_attention_host_rules(lib):
         got = lib.msa_sparse_attention_workspace_size(ctypes.byref(a), ctypes.byref(_sparse(**over)),
                                                       ctypes.byref(n))
         assert got == status, (over, got, status)
+
+
+def test_sparse_attention_binding_checks_the_arrays_it_indexes():
+    # a selection, out or lse of another shape would make the kernels read or
+    # write out of bounds: the binding refuses them before anything runs
+    import block_score_gb300 as bs
+    import synth
+    case = synth.make_case([3, 2], [300, 40], H_q=4, H_kv=2, layout="BBND",
+                           q_dtype=torch.bfloat16, MB=3, seed=1)
+    prep = bs.from_case(case, torch.device("cpu"))
+    value = torch.zeros_like(prep.call.key)
+    good = torch.full((5, 2, 4), -1, dtype=torch.int32)
+    for sel in (torch.full((4, 2, 4), -1, dtype=torch.int32),     # fewer tokens
+                torch.full((5, 1, 4), -1, dtype=torch.int32),     # fewer groups
+                good.to(torch.int64),                             # wrong dtype
+                good.transpose(0, 1).contiguous().transpose(0, 1)):   # not contiguous
+        with pytest.raises(ValueError, match="selection"):
+            prep.sparse_attention(value, sel)
+    with pytest.raises(ValueError, match="out"):
+        prep.sparse_attention(value, good, out=torch.empty(5, 4, 64))
+    with pytest.raises(ValueError, match="lse"):
+        prep.sparse_attention(value, good, lse=torch.empty(5, 4, dtype=torch.float64))
+    with pytest.raises(ValueError, match="value"):                # a CPU value cache
+        prep.sparse_attention(value, good)
