@@ -209,6 +209,13 @@ class _Call:
         self.scale = None if scale is None else scale.contiguous()
         if self.scale is not None and self.scale.dtype != torch.float32:
             raise ValueError("scale must be float32")
+        # the kernels dereference every array on the query's device
+        for name, t in (("key", key), ("start_loc", self.start_loc), ("block_table", block_table),
+                        ("scale", self.scale), ("actual_seq_qlen", self.cu_q),
+                        ("actual_seq_klen", klen)):
+            if t is not None and t.device != query.device:
+                raise ValueError(f"{name} is on {t.device}, the query on {query.device}: "
+                                 "all arrays must be on one device")
         if layout == "TND":
             self.block_table, self.kv_len, self.cu_k = None, None, klen
             if max_blocks is None:
@@ -406,6 +413,8 @@ class Prepared:
                 raise ValueError("FP4 inputs need q_scale and k_scale")
             if q_scale.dtype != torch.uint8 or k_scale.dtype != torch.uint8:
                 raise ValueError("q_scale and k_scale are uint8 scale bytes")
+            if q_scale.device != query.device or k_scale.device != query.device:
+                raise ValueError("q_scale and k_scale must be on the query's device")
             self.q_scale, self.k_scale = q_scale.contiguous(), k_scale.contiguous()
         self.shape = self.call.out_shape()
         if fp4 is not None:

@@ -260,3 +260,21 @@ def test_sparse_attention_binding_checks_the_arrays_it_indexes():
         prep.sparse_attention(value, good, lse=torch.empty(5, 4, dtype=torch.float64))
     with pytest.raises(ValueError, match="value"):                # a CPU value cache
         prep.sparse_attention(value, good)
+
+
+def test_binding_refuses_arrays_on_another_device():
+    # a pointer of another device (or of host memory) would be dereferenced by
+    # the kernels: every array must be on the query's device
+    import block_score_gb300 as bs
+    q = torch.zeros(4, 2, 128, dtype=torch.float16)
+    k = torch.zeros(2, 128, 1, 128, dtype=torch.float16)
+    args = dict(layout_key="BBND", actual_seq_qlen=torch.tensor([0, 4], dtype=torch.int32),
+                actual_seq_klen=torch.tensor([10], dtype=torch.int32),
+                block_table=torch.zeros(1, 1, dtype=torch.int32))
+    assert bs.msa_index_score_out_shape(q, k, torch.zeros(1, dtype=torch.int32), **args)
+    for name in ("block_table", "actual_seq_klen"):
+        bad = dict(args, **{name: args[name].to("meta")})
+        with pytest.raises(ValueError, match=name):
+            bs.msa_index_score_out_shape(q, k, torch.zeros(1, dtype=torch.int32), **bad)
+    with pytest.raises(ValueError, match="key"):
+        bs.msa_index_score_out_shape(q, k.to("meta"), torch.zeros(1, dtype=torch.int32), **args)
