@@ -278,3 +278,19 @@ def test_binding_refuses_arrays_on_another_device():
             bs.msa_index_score_out_shape(q, k, torch.zeros(1, dtype=torch.int32), **bad)
     with pytest.raises(ValueError, match="key"):
         bs.msa_index_score_out_shape(q, k.to("meta"), torch.zeros(1, dtype=torch.int32), **args)
+
+
+@pytest.mark.parametrize("T,H_q,H_kv,k", [(32, 8, 1, 16), (1000, 16, 2, 3), (4096, 64, 8, 32)])
+def test_workspaces_hold_what_the_kernels_write(lib, T, H_q, H_kv, k):
+    # lower bounds from the header's description of each workspace: the sparse
+    # branch's partials (T * H_q * k outputs of D 16-bit values and as many fp32
+    # log-sum-exps) and the fused selection's partial lists (at least one part
+    # per epilogue group: T * H_kv * 2 * k 64-bit keys)
+    n = ctypes.c_size_t()
+    a = _args(T=T, H_q=H_q, H_kv=H_kv, page_stride=128 * H_kv * 128)
+    assert lib.msa_sparse_attention_workspace_size(ctypes.byref(a), ctypes.byref(_sparse(k=k)),
+                                                   ctypes.byref(n)) == 0
+    assert n.value >= T * H_q * k * (128 * 2 + 4)
+    if 32 % (H_q // H_kv) == 0 and k <= 16:
+        assert lib.msa_index_score_topk_workspace_size(ctypes.byref(a), k, ctypes.byref(n)) == 0
+        assert n.value >= T * H_kv * 2 * k * 8
